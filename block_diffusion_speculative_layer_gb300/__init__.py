@@ -1,0 +1,328 @@
+"""Python binding of the GB300 DFlash draft-and-verify engine (libdflash.so).
+
+Argument marshalling only: every step of the cycle runs in the library's
+CUDA kernels.  PyTorch provides device memory and the stream.  There is no
+CPU path; if the library has not been built, every entry point raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Iterable, List, Optional, Sequence, Tuple, Union
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libdflash.so")
+
+DF_OK, DF_EINVAL, DF_ENOMEM, DF_ECUDA, DF_ETIMEOUT, DF_ESTATE = range(6)
+DF_FP32, DF_BF16 = 0, 1
+DF_DBG_TAPS, DF_DBG_LOGITS, DF_DBG_DRAFT_LOGITS, DF_DBG_DRAFT_HIDDEN, DF_DBG_CTX, DF_DBG_HIDDEN = 1, 2, 3, 4, 5, 6
+STATUS_NAMES = {0: "DF_OK", 1: "DF_EINVAL", 2: "DF_ENOMEM", 3: "DF_ECUDA", 4: "DF_ETIMEOUT", 5: "DF_ESTATE"}
+
+EXPORTED = [
+    "df_default_feat_layers", "df_num_weights", "df_weight_info", "df_init", "df_prefill", "df_draft_block",
+    "df_verify_accept", "df_generate", "df_greedy_reference", "df_reset_seq", "df_get_stats", "df_reset_stats",
+    "df_seq_info", "df_destroy", "df_last_error", "df_debug_enable", "df_debug_read", "df_debug_weight_ptr",
+    "df_op_gemm_bf16", "df_op_lmhead_argmax_bf16",
+]
+
+
+class DfError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class DfConfig(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32), ("d_model", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("d_ffn", ctypes.c_int32),
+        ("vocab", ctypes.c_int32), ("draft_layers", ctypes.c_int32), ("block_size", ctypes.c_int32),
+        ("feat_layers", ctypes.c_int32 * 5), ("max_batch", ctypes.c_int32), ("max_ctx", ctypes.c_int32),
+        ("page_tokens", ctypes.c_int32), ("dtype", ctypes.c_int32), ("mask_token_id", ctypes.c_int32),
+        ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
+    ]
+
+
+class DfStats(ctypes.Structure):
+    _fields_ = [
+        ("cycles", ctypes.c_int64), ("accepted_drafts", ctypes.c_int64), ("emitted_tokens", ctypes.c_int64),
+        ("accept_hist", ctypes.c_int64 * 65), ("draft_us", ctypes.c_double), ("verify_us", ctypes.c_double),
+        ("prefill_us", ctypes.c_double),
+    ]
+
+    def as_dict(self) -> dict:
+        return {
+            "cycles": self.cycles, "accepted_drafts": self.accepted_drafts, "emitted_tokens": self.emitted_tokens,
+            "accept_hist": list(self.accept_hist), "draft_us": self.draft_us, "verify_us": self.verify_us,
+            "prefill_us": self.prefill_us,
+        }
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_IP = ctypes.POINTER(ctypes.c_int32)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library.  Raises if it has not been built: there is no fallback."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libdflash.so is missing ({LIB_PATH}); build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB_PATH)
+    L.df_default_feat_layers.argtypes = [_I, _IP]
+    L.df_num_weights.argtypes = [ctypes.POINTER(DfConfig)]
+    L.df_num_weights.restype = _I
+    L.df_weight_info.argtypes = [ctypes.POINTER(DfConfig), _I, ctypes.c_char_p, _IP, ctypes.POINTER(ctypes.c_int64)]
+    L.df_init.argtypes = [ctypes.POINTER(DfConfig), ctypes.POINTER(_P), _I, _P, ctypes.POINTER(_P)]
+    L.df_prefill.argtypes = [_P, _I, _IP, _I, _IP]
+    L.df_draft_block.argtypes = [_P, _IP, _I, _IP]
+    L.df_verify_accept.argtypes = [_P, _IP, _I, _IP, _IP, _IP]
+    L.df_generate.argtypes = [_P, _IP, _IP, _I, _I, _IP, ctypes.POINTER(DfStats)]
+    L.df_greedy_reference.argtypes = [_P, _IP, _IP, _I, _I, _IP]
+    L.df_reset_seq.argtypes = [_P, _I]
+    L.df_get_stats.argtypes = [_P, ctypes.POINTER(DfStats)]
+    L.df_reset_stats.argtypes = [_P]
+    L.df_seq_info.argtypes = [_P, _I, _IP, _IP]
+    L.df_destroy.argtypes = [_P]
+    L.df_destroy.restype = None
+    L.df_last_error.argtypes = [_P]
+    L.df_last_error.restype = ctypes.c_char_p
+    L.df_debug_enable.argtypes = [_P, _I]
+    L.df_debug_read.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_float), ctypes.c_int64, _IP]
+    L.df_debug_weight_ptr.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_uint64)]
+    L.df_op_gemm_bf16.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P]
+    L.df_op_lmhead_argmax_bf16.argtypes = [_P, _P, _P, _I, _I, _I, _P]
+    for name in EXPORTED:
+        fn = getattr(L, name)
+        if fn.restype is ctypes.c_int:  # default restype: the df_status enum
+            fn.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _ip(a: np.ndarray):
+    return a.ctypes.data_as(_IP)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def default_feat_layers(n_layers: int) -> List[int]:
+    out = (ctypes.c_int32 * 5)()
+    st = lib().df_default_feat_layers(n_layers, out)
+    if st != DF_OK:
+        raise DfError(st, f"no feature layers for {n_layers} layers")
+    return list(out)
+
+
+def make_config(shape, max_batch: int, max_ctx: int, page_tokens: int = 16,
+                feat_layers: Optional[Sequence[int]] = None) -> DfConfig:
+    c = DfConfig()
+    c.n_layers, c.d_model, c.n_q_heads = shape.n_layers, shape.d_model, shape.n_q_heads
+    c.n_kv_heads, c.head_dim, c.d_ffn, c.vocab = shape.n_kv_heads, shape.head_dim, shape.d_ffn, shape.vocab
+    c.draft_layers, c.block_size = shape.draft_layers, shape.block_size
+    fl = list(feat_layers) if feat_layers is not None else default_feat_layers(shape.n_layers)
+    for i in range(5):
+        c.feat_layers[i] = fl[i]
+    c.max_batch, c.max_ctx, c.page_tokens = max_batch, max_ctx, page_tokens
+    c.dtype = DF_BF16 if shape.dtype == "bf16" else DF_FP32
+    c.mask_token_id = shape.vocab - 1
+    c.rms_eps, c.rope_theta = shape.rms_eps, shape.rope_theta
+    return c
+
+
+def weight_info(cfg: DfConfig) -> List[Tuple[str, Tuple[int, ...]]]:
+    L = lib()
+    n = L.df_num_weights(ctypes.byref(cfg))
+    out = []
+    name = ctypes.create_string_buffer(32)
+    nd = ctypes.c_int32()
+    shp = (ctypes.c_int64 * 2)()
+    for i in range(n):
+        st = L.df_weight_info(ctypes.byref(cfg), i, name, ctypes.byref(nd), shp)
+        if st != DF_OK:
+            raise DfError(st, "df_weight_info")
+        out.append((name.value.decode(), tuple(shp[: nd.value])))
+    return out
+
+
+def _to_device(arr, torch):
+    if isinstance(arr, torch.Tensor):
+        return arr.contiguous().cuda()
+    a = np.ascontiguousarray(arr)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).cuda()
+
+
+class Engine:
+    """One DFlash engine (target + drafter) on the current CUDA device."""
+
+    def __init__(self, shape, weights: Union[Dict[str, np.ndarray], Iterable[Tuple[str, np.ndarray]]],
+                 max_batch: int = 1, max_ctx: int = 1024, page_tokens: int = 16,
+                 feat_layers: Optional[Sequence[int]] = None, stream=None):
+        import torch
+        self.L = lib()
+        self.shape = shape
+        self.cfg = make_config(shape, max_batch, max_ctx, page_tokens, feat_layers)
+        self.B = shape.block_size
+        self.V = shape.vocab
+        self.d = shape.d_model
+        specs = weight_info(self.cfg)
+        items = weights.items() if isinstance(weights, dict) else weights
+        dev = {}
+        for name, arr in items:
+            dev[name] = _to_device(arr, torch)
+        missing = [n for n, _ in specs if n not in dev]
+        if missing:
+            raise ValueError(f"missing weights: {missing[:5]}")
+        for n, shp in specs:
+            if tuple(dev[n].shape) != shp:
+                raise ValueError(f"weight {n}: shape {tuple(dev[n].shape)} != {shp}")
+        ptrs = (_P * len(specs))(*[dev[n].data_ptr() for n, _ in specs])
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        h = _P()
+        torch.cuda.synchronize()
+        st = self.L.df_init(ctypes.byref(self.cfg), ptrs, len(specs), _P(self.stream.cuda_stream), ctypes.byref(h))
+        del dev
+        if st != DF_OK:
+            raise DfError(st, "df_init failed (shape, memory or device)")
+        self.h = h
+
+    # -------------------------------------------------------------- helpers
+    def _check(self, st: int, what: str):
+        if st != DF_OK:
+            msg = self.L.df_last_error(self.h)
+            raise DfError(st, f"{what}: {msg.decode() if msg else ''}")
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.L.df_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+    # -------------------------------------------------------------- cycle
+    def prefill(self, seq: int, prompt: Sequence[int]) -> int:
+        p = _i32(prompt)
+        bonus = ctypes.c_int32()
+        self._check(self.L.df_prefill(self.h, seq, _ip(p), len(p), ctypes.byref(bonus)), "df_prefill")
+        return bonus.value
+
+    def draft_block(self, seqs: Sequence[int]) -> np.ndarray:
+        s = _i32(seqs)
+        out = np.zeros((len(s), self.B - 1), np.int32)
+        self._check(self.L.df_draft_block(self.h, _ip(s), len(s), _ip(out)), "df_draft_block")
+        return out
+
+    def verify_accept(self, seqs: Sequence[int], drafts: Optional[np.ndarray] = None):
+        s = _i32(seqs)
+        acc = np.zeros((len(s), self.B), np.int32)
+        n = np.zeros(len(s), np.int32)
+        dp = None
+        keep = None  # holds the draft buffer alive across the call
+        if drafts is not None:
+            keep = _i32(drafts).reshape(len(s), self.B - 1)
+            dp = _ip(keep)
+        self._check(self.L.df_verify_accept(self.h, _ip(s), len(s), dp, _ip(acc), _ip(n)), "df_verify_accept")
+        return acc, n
+
+    def generate(self, prompts: Sequence[Sequence[int]], n_new: int):
+        lens = _i32([len(p) for p in prompts])
+        flat = _i32(np.concatenate([_i32(p) for p in prompts]))
+        out = np.zeros((len(prompts), n_new), np.int32)
+        stats = DfStats()
+        self._check(self.L.df_generate(self.h, _ip(flat), _ip(lens), len(prompts), n_new, _ip(out),
+                                       ctypes.byref(stats)), "df_generate")
+        return out, stats.as_dict()
+
+    def greedy_reference(self, prompts: Sequence[Sequence[int]], n_new: int) -> np.ndarray:
+        lens = _i32([len(p) for p in prompts])
+        flat = _i32(np.concatenate([_i32(p) for p in prompts]))
+        out = np.zeros((len(prompts), n_new), np.int32)
+        self._check(self.L.df_greedy_reference(self.h, _ip(flat), _ip(lens), len(prompts), n_new, _ip(out)),
+                    "df_greedy_reference")
+        return out
+
+    def reset_seq(self, seq: int):
+        self._check(self.L.df_reset_seq(self.h, seq), "df_reset_seq")
+
+    def seq_info(self, seq: int) -> Tuple[int, int]:
+        ln, b = ctypes.c_int32(), ctypes.c_int32()
+        self._check(self.L.df_seq_info(self.h, seq, ctypes.byref(ln), ctypes.byref(b)), "df_seq_info")
+        return ln.value, b.value
+
+    def stats(self) -> dict:
+        s = DfStats()
+        self._check(self.L.df_get_stats(self.h, ctypes.byref(s)), "df_get_stats")
+        return s.as_dict()
+
+    def reset_stats(self):
+        self._check(self.L.df_reset_stats(self.h), "df_reset_stats")
+
+    # -------------------------------------------------------------- inspection
+    def debug(self, on: bool = True):
+        self._check(self.L.df_debug_enable(self.h, 1 if on else 0), "df_debug_enable")
+
+    def debug_read(self, what: int) -> np.ndarray:
+        cols = {DF_DBG_TAPS: 5 * self.d, DF_DBG_LOGITS: self.V, DF_DBG_DRAFT_LOGITS: self.V,
+                DF_DBG_DRAFT_HIDDEN: self.d, DF_DBG_CTX: self.d, DF_DBG_HIDDEN: self.d}[what]
+        cap = max(512, self.cfg.max_batch * self.B) * cols
+        buf = np.zeros(cap, np.float32)
+        rows = ctypes.c_int32()
+        self._check(self.L.df_debug_read(self.h, what, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), cap,
+                                         ctypes.byref(rows)), "df_debug_read")
+        return buf[: rows.value * cols].reshape(rows.value, cols)
+
+    def weight_ptr(self, which: int) -> int:
+        a = ctypes.c_uint64()
+        self._check(self.L.df_debug_weight_ptr(self.h, which, ctypes.byref(a)), "df_debug_weight_ptr")
+        return a.value
+
+
+# ------------------------------------------------------------------ single ops
+def gemm_bf16(x, w, splits: int = 0, token_tile: int = 0, stream=None):
+    """y = x @ w.T (bf16 in, fp32 out) on the tcgen05 GEMM.  x: [M, K], w: [N, K] (torch, cuda)."""
+    import torch
+    assert x.dtype == torch.bfloat16 and w.dtype == torch.bfloat16 and x.is_cuda and w.is_cuda
+    M, K = x.shape
+    N = w.shape[0]
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = lib().df_op_gemm_bf16(_P(x.data_ptr()), _P(w.data_ptr()), _P(y.data_ptr()), M, N, K, splits, token_tile,
+                               _P(s.cuda_stream))
+    if st != DF_OK:
+        raise DfError(st, "df_op_gemm_bf16")
+    return y
+
+
+def lmhead_argmax_bf16(x, w, stream=None):
+    """ids[m] = argmax_v x[m] . w[v] (fp32 logits, lowest index on ties)."""
+    import torch
+    M, K = x.shape
+    V = w.shape[0]
+    ids = torch.empty(M, dtype=torch.int32, device=x.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = lib().df_op_lmhead_argmax_bf16(_P(x.data_ptr()), _P(w.data_ptr()), _P(ids.data_ptr()), M, V, K,
+                                        _P(s.cuda_stream))
+    if st != DF_OK:
+        raise DfError(st, "df_op_lmhead_argmax_bf16")
+    return ids

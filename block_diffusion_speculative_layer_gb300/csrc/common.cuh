@@ -1,0 +1,208 @@
+// Shared device-side definitions of the DFlash engine (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dfk {
+
+// Bits of the sticky device error word.
+enum : int {
+  ERR_TIMEOUT = 1,     // a bounded mbarrier wait ran out
+  ERR_BOUNDS = 2,      // an index fell outside its buffer; the access was skipped
+  ERR_TMEM = 4,        // tensor-memory allocation returned an unexpected address
+};
+
+__device__ __forceinline__ void flag_error(int* err, int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+template <typename T> struct Cvt;
+template <> struct Cvt<float> {
+  static __device__ __forceinline__ float to_f(float v) { return v; }
+  static __device__ __forceinline__ float from_f(float v) { return v; }
+};
+template <> struct Cvt<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+// Monotonic map of an fp32 value to uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// Packed (value, index) key: max picks the largest value, then the lowest index.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+  return ((unsigned long long)ordered_bits(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
+}
+__device__ __forceinline__ int argmax_key_index(unsigned long long key) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+}
+
+// What a GEMM does with its fp32 result tile.
+enum EpiKind : int {
+  EPI_STORE = 0,   // out[m][n] = acc (out type = T)
+  EPI_STORE_F32,   // out_f32[m][n] = acc
+  EPI_RESID,       // resid[m][n] += acc (fp32 residual stream)
+  EPI_SWIGLU,      // tiles hold 64 gate rows then the 64 matching up rows:
+                   // out[m][n/2 + f] = silu(gate) * up
+  EPI_QKV,         // rotary embedding + scatter of q / k / v
+  EPI_ARGMAX,      // per-row packed max over the tile's logits (+ optional store)
+};
+
+// Where K/V rows of EPI_QKV go.
+enum KvDest : int {
+  KV_PAGED = 0,  // paged cache: [layer][page][k|v][head][page_tokens][hd]
+  KV_ROWS = 1,   // row buffer:  [k|v][head][row][hd] (drafter block keys/values)
+};
+
+struct EpiParams {
+  int kind;
+  void* out;          // EPI_STORE / EPI_SWIGLU / EPI_QKV (q) / EPI_ARGMAX (debug logits, fp32)
+  int ldo;            // row stride of out (elements)
+  float* resid;       // EPI_RESID
+  int ldr;
+  // EPI_QKV
+  int q_dim;          // features [0, q_dim) are queries (0 for pure K/V injection)
+  int kv_dim;         // features per K (and per V) block
+  int head_dim;
+  int n_kv_heads;
+  int kv_dest;        // KvDest
+  void* kv_base;      // cache base (KV_PAGED) or row buffer (KV_ROWS)
+  long long layer_stride;   // elements between layers of the paged cache
+  int layer0;         // first cache layer written (injection spans several)
+  const int* page_table;    // [seq][pt_stride]
+  int pt_stride;
+  int page_tokens;
+  int n_pages;        // bounds check on page ids
+  int rows_cap;       // KV_ROWS: rows per (k|v, head) plane
+  const int* row_pos; // [M] absolute position of row m; < 0 = row is inactive
+  const int* row_seq; // [M] sequence slot of row m
+  const float2* rope; // [pos][hd/2] (cos, sin)
+  int rope_rows;      // positions in the table (bounds check)
+  // EPI_ARGMAX
+  unsigned long long* amax;  // [M]
+  int* err;
+};
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Apply the epilogue to one result tile held in shared memory.
+//   tile[r * ld + f] = acc for row m0 + r, feature n0 + f, f in [0, 128),
+//   r in [0, rows).  Called by exactly 128 threads (one per feature column).
+template <typename T>
+__device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, int n0, int m0, int rows, int M) {
+  const int f = threadIdx.x & 127;
+  const int n = n0 + f;
+  switch (ep.kind) {
+    case EPI_STORE: {
+      T* out = reinterpret_cast<T*>(ep.out);
+      for (int r = 0; r < rows; ++r) {
+        int m = m0 + r;
+        if (m >= M) break;
+        out[(size_t)m * ep.ldo + n] = Cvt<T>::from_f(tile[r * ld + f]);
+      }
+    } break;
+    case EPI_STORE_F32: {
+      float* out = reinterpret_cast<float*>(ep.out);
+      for (int r = 0; r < rows; ++r) {
+        int m = m0 + r;
+        if (m >= M) break;
+        out[(size_t)m * ep.ldo + n] = tile[r * ld + f];
+      }
+    } break;
+    case EPI_RESID: {
+      for (int r = 0; r < rows; ++r) {
+        int m = m0 + r;
+        if (m >= M) break;
+        if (ep.row_pos && ep.row_pos[m] < 0) continue;
+        ep.resid[(size_t)m * ep.ldr + n] += tile[r * ld + f];
+      }
+    } break;
+    case EPI_SWIGLU: {
+      // 128 threads handle (row, gate feature) pairs: 64 features x 2 rows per pass.
+      T* out = reinterpret_cast<T*>(ep.out);
+      const int g = f & 63;
+      const int rsub = f >> 6;
+      for (int r = rsub; r < rows; r += 2) {
+        int m = m0 + r;
+        if (m >= M) break;
+        float gate = tile[r * ld + g];
+        float up = tile[r * ld + 64 + g];
+        out[(size_t)m * ep.ldo + (n0 >> 1) + g] = Cvt<T>::from_f(silu_f(gate) * up);
+      }
+    } break;
+    case EPI_QKV: {
+      const int hd = ep.head_dim;
+      const int half = hd >> 1;
+      const int dim = n & (hd - 1);
+      const int partner = f ^ half;
+      int kind;          // 0 = q, 1 = k, 2 = v
+      int layer = 0, head = 0;
+      if (n < ep.q_dim) {
+        kind = 0;
+      } else {
+        int r2 = n - ep.q_dim;
+        int per_layer = 2 * ep.kv_dim;
+        layer = r2 / per_layer;
+        r2 -= layer * per_layer;
+        kind = 1 + r2 / ep.kv_dim;
+        head = (r2 % ep.kv_dim) / hd;
+      }
+      for (int r = 0; r < rows; ++r) {
+        int m = m0 + r;
+        if (m >= M) break;
+        int pos = ep.row_pos[m];
+        if (pos < 0) continue;
+        float v = tile[r * ld + f];
+        if (kind < 2) {
+          if (pos >= ep.rope_rows) { flag_error(ep.err, ERR_BOUNDS); continue; }
+          float p = tile[r * ld + partner];
+          float2 cs = ep.rope[(size_t)pos * half + (dim & (half - 1))];
+          v = (dim < half) ? (v * cs.x - p * cs.y) : (v * cs.x + p * cs.y);
+        }
+        if (kind == 0) {
+          T* q = reinterpret_cast<T*>(ep.out);
+          q[(size_t)m * ep.ldo + n] = Cvt<T>::from_f(v);
+        } else {
+          T* base = reinterpret_cast<T*>(ep.kv_base);
+          const int kv = kind - 1;
+          size_t off;
+          if (ep.kv_dest == KV_PAGED) {
+            int seq = ep.row_seq[m];
+            int page = ep.page_table[(size_t)seq * ep.pt_stride + pos / ep.page_tokens];
+            if (page < 0 || page >= ep.n_pages) { flag_error(ep.err, ERR_BOUNDS); continue; }
+            size_t page_elems = (size_t)2 * ep.n_kv_heads * ep.page_tokens * hd;
+            off = (size_t)(ep.layer0 + layer) * ep.layer_stride + (size_t)page * page_elems +
+                  ((size_t)(kv * ep.n_kv_heads + head) * ep.page_tokens + (pos % ep.page_tokens)) * hd + dim;
+          } else {
+            if (m >= ep.rows_cap) { flag_error(ep.err, ERR_BOUNDS); continue; }
+            off = ((size_t)(kv * ep.n_kv_heads + head) * ep.rows_cap + m) * hd + dim;
+          }
+          base[off] = Cvt<T>::from_f(v);
+        }
+      }
+    } break;
+    case EPI_ARGMAX: {
+      // One warp reduces 32 features of a row; four keys per row meet in one atomicMax each.
+      float* dbg = reinterpret_cast<float*>(ep.out);
+      for (int r = 0; r < rows; ++r) {
+        int m = m0 + r;
+        if (m >= M) break;
+        float v = tile[r * ld + f];
+        if (dbg) dbg[(size_t)m * ep.ldo + n] = v;
+        unsigned long long key = argmax_key(v, n);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+          key = other > key ? other : key;
+        }
+        if ((threadIdx.x & 31) == 0) atomicMax(ep.amax + m, key);
+      }
+    } break;
+  }
+}
+
+}  // namespace dfk

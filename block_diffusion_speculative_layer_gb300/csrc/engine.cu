@@ -1,0 +1,1208 @@
+// Host engine of the DFlash draft-and-verify cycle and its C ABI.
+//
+// One handle holds one model on one GPU: a weight arena (target, drafter,
+// one shared embedding and LM head), a paged target KV cache, a paged drafter
+// context cache filled by KV injection, pre-allocated activation buffers,
+// split-K and split-KV workspaces, and the per-sequence state (bonus token and
+// its position) on the device.  A cycle launches only this library's kernels
+// on the caller's stream and reads back one small result per cycle (accepted
+// tokens and their count).
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "dflash.h"
+#include "internal.h"
+
+using namespace dfk;
+
+namespace {
+
+constexpr int ATTN_CHUNK = 64;
+constexpr int PREFILL_CHUNK = 512;
+
+struct Tmap {
+  alignas(64) uint8_t b[TMAP_BYTES];
+};
+
+struct Linear {
+  void* ptr = nullptr;  // [N][K] row-major
+  int N = 0, K = 0;
+  Tmap tm;              // bf16 only: TMA map with 128-row boxes
+};
+
+struct Layer {
+  float* attn_norm = nullptr;
+  Linear qkv, wo;
+  float* mlp_norm = nullptr;
+  Linear gu, down;  // gu: 64 gate rows then the 64 matching up rows, per 128-row tile
+};
+
+struct SeqHost {
+  bool active = false;
+  int len = 0;    // verified positions = position of the bonus token
+  int bonus = -1;
+  std::vector<int> pages;  // page ids in position order
+};
+
+}  // namespace
+
+struct df_handle {
+  df_config cfg{};
+  cudaStream_t st = nullptr;
+  bool bf16 = false;
+  size_t esz = 4;
+  int d = 0, hd = 0, Hq = 0, Hkv = 0, F = 0, V = 0, L = 0, Ld = 0, B = 0, qdim = 0, kvdim = 0, qkv_n = 0;
+  int sm_count = 152;
+  int tap_of_layer[1024];  // zero-based layer index -> tap slot (or -1)
+  int Mmax = 0;
+
+  std::vector<void*> allocs;
+  void* arena = nullptr;
+  std::vector<Layer> tl, dl;
+  void* embed = nullptr;
+  Linear lm_head, fc, inj;
+  float *final_norm = nullptr, *fc_norm = nullptr, *d_final_norm = nullptr;
+
+  int PT = 16, pages_per_seq = 0, n_pages = 0;
+  void *kv_t = nullptr, *kv_d = nullptr;
+  long long layer_stride = 0;
+  int* d_pt = nullptr;
+  std::vector<int> free_pages;
+  std::vector<SeqHost> seqs;
+
+  int *d_bonus = nullptr, *d_bonus_pos = nullptr;
+  int *d_row_tok = nullptr, *d_row_pos = nullptr, *d_row_seq = nullptr, *d_inj_pos = nullptr, *d_ids = nullptr;
+  int *d_slots = nullptr, *d_drafts = nullptr, *d_acc = nullptr, *d_n = nullptr, *d_gen = nullptr;
+  unsigned long long* d_amax = nullptr;
+
+  float* h = nullptr;
+  void *xb = nullptr, *q = nullptr, *attn = nullptr, *act = nullptr, *taps = nullptr, *ctx = nullptr, *blk = nullptr;
+  float* fcout = nullptr;
+  float* tmp = nullptr;
+  float *dbg_logits = nullptr, *dbg_dlogits = nullptr, *dbg_dh = nullptr, *dbg_th = nullptr;
+  float* ws = nullptr;
+  int* counters = nullptr;
+  float* part_acc = nullptr;
+  float2* part_ml = nullptr;
+  int n_chunk_slots = 0;
+  float2* rope = nullptr;
+  int* d_err = nullptr;
+  int* h_pin = nullptr;  // pinned host staging for per-cycle results
+  size_t h_pin_ints = 0;
+
+  std::map<std::tuple<uintptr_t, int, int>, Tmap> xmaps;
+  df_stats stats{};
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  std::string err;
+  bool debug = false;
+  bool failed = false;
+  int rows_last_target = 0, rows_last_draft = 0, rows_last_ctx = 0, rows_last_logits = 0;
+};
+
+namespace {
+
+df_status fail(df_handle* h, df_status s, const std::string& msg) {
+  if (h) h->err = msg;
+  return s;
+}
+
+#define CK(expr)                                                                               \
+  do {                                                                                         \
+    cudaError_t e_ = (expr);                                                                   \
+    if (e_ != cudaSuccess) {                                                                   \
+      H->failed = true;                                                                        \
+      return fail(H, DF_ECUDA, std::string(#expr) + ": " + cudaGetErrorString(e_));            \
+    }                                                                                          \
+  } while (0)
+
+#define CKS(expr)                \
+  do {                           \
+    df_status s_ = (expr);       \
+    if (s_ != DF_OK) return s_;  \
+  } while (0)
+
+df_status dalloc(df_handle* H, void** p, size_t bytes) {
+  if (bytes == 0) bytes = 256;
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    *p = nullptr;
+    (void)cudaGetLastError();
+    return fail(H, DF_ENOMEM, "cudaMalloc of " + std::to_string(bytes) + " bytes failed");
+  }
+  H->allocs.push_back(*p);
+  return DF_OK;
+}
+template <typename P>
+df_status dalloc_t(df_handle* H, P** p, size_t bytes) {
+  void* v = nullptr;
+  df_status s = dalloc(H, &v, bytes);
+  *p = reinterpret_cast<P*>(v);
+  return s;
+}
+
+int feat_default(int L, int i) { return 2 + (i * (L - 4) + 2) / 4; }
+
+// ---------------------------------------------------------------- weight list
+struct WSpec {
+  std::string name;
+  int ndim;
+  long long s0, s1;
+};
+
+std::vector<WSpec> weight_specs(const df_config& c) {
+  std::vector<WSpec> w;
+  const long long d = c.d_model, F = c.d_ffn, V = c.vocab, qd = (long long)c.n_q_heads * c.head_dim,
+                  kd = (long long)c.n_kv_heads * c.head_dim;
+  auto layer = [&](const std::string& p) {
+    w.push_back({p + ".attn_norm", 1, d, 0});
+    w.push_back({p + ".wq", 2, qd, d});
+    w.push_back({p + ".wk", 2, kd, d});
+    w.push_back({p + ".wv", 2, kd, d});
+    w.push_back({p + ".wo", 2, d, qd});
+    w.push_back({p + ".mlp_norm", 1, d, 0});
+    w.push_back({p + ".w_gate", 2, F, d});
+    w.push_back({p + ".w_up", 2, F, d});
+    w.push_back({p + ".w_down", 2, d, F});
+  };
+  w.push_back({"embed", 2, V, d});
+  for (int l = 0; l < c.n_layers; ++l) layer("t" + std::to_string(l));
+  w.push_back({"final_norm", 1, d, 0});
+  w.push_back({"lm_head", 2, V, d});
+  w.push_back({"fc", 2, d, 5 * d});
+  w.push_back({"fc_norm", 1, d, 0});
+  for (int l = 0; l < c.draft_layers; ++l) layer("d" + std::to_string(l));
+  w.push_back({"d_final_norm", 1, d, 0});
+  return w;
+}
+
+df_status validate(const df_config* c, std::string& why) {
+  auto bad = [&](const char* m) {
+    why = m;
+    return DF_EINVAL;
+  };
+  if (!c) return bad("null config");
+  if (c->n_layers < 8 || c->n_layers > 1000) return bad("n_layers must be in [8, 1000]");
+  if (c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 64 or 128");
+  if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->n_q_heads % c->n_kv_heads) return bad("bad head counts");
+  if (c->n_q_heads / c->n_kv_heads > 8) return bad("query heads per KV head must be <= 8");
+  if (c->d_model % 128 || c->d_model <= 0) return bad("d_model must be a multiple of 128");
+  if ((c->n_q_heads * c->head_dim) % 128 || (c->n_kv_heads * c->head_dim) % 128)
+    return bad("query and KV widths must be multiples of 128");
+  if (c->d_ffn % 64 || c->d_ffn <= 0) return bad("d_ffn must be a multiple of 64");
+  if (c->vocab % 128 || c->vocab <= 0) return bad("vocab must be a multiple of 128");
+  if (c->draft_layers < 1) return bad("draft_layers must be >= 1");
+  if (c->block_size < 2 || c->block_size > 32) return bad("block_size must be in [2, 32]");
+  if (c->max_batch < 1 || c->max_ctx < c->block_size + 1) return bad("bad max_batch / max_ctx");
+  if (c->page_tokens < 1) return bad("page_tokens must be >= 1");
+  if (c->dtype != DF_FP32 && c->dtype != DF_BF16) return bad("dtype must be DF_FP32 or DF_BF16");
+  if (c->mask_token_id < 0 || c->mask_token_id >= c->vocab) return bad("mask_token_id out of range");
+  for (int i = 0; i < 5; ++i) {
+    if (c->feat_layers[i] < 1 || c->feat_layers[i] > c->n_layers - 1)
+      return bad("feat_layers must be 1-based layers in [1, n_layers-1]");
+    if (i && c->feat_layers[i] <= c->feat_layers[i - 1]) return bad("feat_layers must increase");
+  }
+  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.f)) return bad("bad rms_eps / rope_theta");
+  return DF_OK;
+}
+
+// ---------------------------------------------------------------- GEMM dispatch
+df_status xmap(df_handle* H, const void* ptr, int K, int nt, const void** out) {
+  auto key = std::make_tuple(reinterpret_cast<uintptr_t>(ptr), K, nt);
+  auto it = H->xmaps.find(key);
+  if (it == H->xmaps.end()) {
+    Tmap t;
+    if (!make_tmap_bf16(t.b, ptr, H->Mmax, K, nt)) return fail(H, DF_ECUDA, "tensor map encode failed (activations)");
+    it = H->xmaps.emplace(key, t).first;
+  }
+  *out = it->second.b;
+  return DF_OK;
+}
+
+EpiParams epi(df_handle* H, int kind) {
+  EpiParams e{};
+  e.kind = kind;
+  e.err = H->d_err;
+  e.head_dim = H->hd;
+  e.n_kv_heads = H->Hkv;
+  e.kv_dim = H->kvdim;
+  e.page_table = H->d_pt;
+  e.pt_stride = H->pages_per_seq;
+  e.page_tokens = H->PT;
+  e.n_pages = H->n_pages;
+  e.rope = H->rope;
+  e.rope_rows = H->cfg.max_ctx;
+  e.layer_stride = H->layer_stride;
+  e.rows_cap = H->Mmax;
+  return e;
+}
+
+df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiParams& ep) {
+  if (M <= 0) return DF_OK;
+  if (H->bf16) {
+    const int nt = tc_token_tile(M);
+    const void* tmX = nullptr;
+    CKS(xmap(H, X, W.K, nt, &tmX));
+    const int splits = tc_splits(W.N, W.K, H->sm_count);
+    CK(launch_gemm_tc(W.tm.b, tmX, nt, M, W.N, W.K, splits, H->ws, H->counters, ep, H->st));
+  } else {
+    CK(launch_gemm_f32(reinterpret_cast<const float*>(X), reinterpret_cast<const float*>(W.ptr), H->tmp, M, W.N, W.K,
+                       ep, H->st));
+  }
+  return DF_OK;
+}
+
+// ---------------------------------------------------------------- passes
+void* row_ptr(df_handle* H, void* base, int row, int ld) {
+  return reinterpret_cast<uint8_t*>(base) + (size_t)row * ld * H->esz;
+}
+
+// LM head with fused argmax over rows [row0, row0 + M) of xb -> d_ids[0..M).
+df_status lm_head_argmax(df_handle* H, int M, float* dbg) {
+  CK(launch_fill_u64(H->d_amax, 0ull, M, H->st));
+  EpiParams e = epi(H, EPI_ARGMAX);
+  e.amax = H->d_amax;
+  e.out = dbg;
+  e.ldo = H->V;
+  CKS(gemm(H, H->lm_head, H->xb, M, e));
+  CK(launch_argmax_finalize(H->d_amax, H->d_ids, M, H->st));
+  return DF_OK;
+}
+
+df_status attention(df_handle* H, int M, int R, int nseq, bool causal, const void* cache_layer, int max_len) {
+  AttnParams p{};
+  p.q = H->q;
+  p.out = H->attn;
+  p.M = M;
+  p.rows_per_seq = R;
+  p.n_seqs = nseq;
+  p.Hq = H->Hq;
+  p.Hkv = H->Hkv;
+  p.hd = H->hd;
+  p.row_pos = H->d_row_pos;
+  p.row_seq = H->d_row_seq;
+  p.causal = causal ? 1 : 0;
+  p.cache = cache_layer;
+  p.page_table = H->d_pt;
+  p.pt_stride = H->pages_per_seq;
+  p.page_tokens = H->PT;
+  p.n_pages = H->n_pages;
+  p.blk = H->blk;
+  p.rows_cap = H->Mmax;
+  p.chunk = ATTN_CHUNK;
+  p.n_chunk_slots = H->n_chunk_slots;
+  p.grid_chunks = std::max(1, (max_len + ATTN_CHUNK - 1) / ATTN_CHUNK);
+  if (p.grid_chunks > H->n_chunk_slots - 1) return fail(H, DF_EINVAL, "context longer than max_ctx");
+  p.part_acc = H->part_acc;
+  p.part_ml = H->part_ml;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)H->hd));
+  p.err = H->d_err;
+  CK(launch_attention(p, H->bf16, H->st));
+  return DF_OK;
+}
+
+void* kv_layer(df_handle* H, void* base, int l) {
+  return reinterpret_cast<uint8_t*>(base) + (size_t)l * H->layer_stride * H->esz;
+}
+
+// One decoder layer over M rows.  causal: target (K/V into the paged target
+// cache); otherwise drafter (K/V into the block row buffer, attention over the
+// injected context + block).
+df_status layer_pass(df_handle* H, const Layer& Lw, int M, int R, int nseq, bool causal, int cache_layer, int max_len,
+                     int tap) {
+  const float eps = H->cfg.rms_eps;
+  CK(launch_rmsnorm(H->h, H->d, Lw.attn_norm, H->xb, H->d, H->bf16, M, H->d, eps, tap >= 0 ? H->taps : nullptr,
+                    tap, nullptr, H->st));
+  EpiParams e = epi(H, EPI_QKV);
+  e.out = H->q;
+  e.ldo = H->qdim;
+  e.q_dim = H->qdim;
+  e.row_pos = H->d_row_pos;
+  e.row_seq = H->d_row_seq;
+  if (causal) {
+    e.kv_dest = KV_PAGED;
+    e.kv_base = H->kv_t;
+    e.layer0 = cache_layer;
+  } else {
+    e.kv_dest = KV_ROWS;
+    e.kv_base = H->blk;
+  }
+  CKS(gemm(H, Lw.qkv, H->xb, M, e));
+  CKS(attention(H, M, R, nseq, causal, kv_layer(H, causal ? H->kv_t : H->kv_d, cache_layer), max_len));
+  EpiParams r = epi(H, EPI_RESID);
+  r.resid = H->h;
+  r.ldr = H->d;
+  CKS(gemm(H, Lw.wo, H->attn, M, r));
+  CK(launch_rmsnorm(H->h, H->d, Lw.mlp_norm, H->xb, H->d, H->bf16, M, H->d, eps, nullptr, 0, nullptr, H->st));
+  EpiParams s = epi(H, EPI_SWIGLU);
+  s.out = H->act;
+  s.ldo = H->F;
+  CKS(gemm(H, Lw.gu, H->xb, M, s));
+  CKS(gemm(H, Lw.down, H->act, M, r));
+  return DF_OK;
+}
+
+// Target over M rows (row_tok / row_pos / row_seq already set).  head_rows:
+// 0 = no LM head; -1 = every row; else only the last row (prefill).
+df_status target_pass(df_handle* H, int M, int R, int nseq, int max_len, bool want_taps, int head_mode) {
+  CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, M, H->d, H->V, H->d_err, H->st));
+  for (int l = 0; l < H->L; ++l) {
+    const int tap = want_taps ? H->tap_of_layer[l] : -1;
+    CKS(layer_pass(H, H->tl[l], M, R, nseq, true, l, max_len, tap));
+  }
+  H->rows_last_target = M;
+  if (H->debug) CK(cudaMemcpyAsync(H->dbg_th, H->h, (size_t)M * H->d * 4, cudaMemcpyDeviceToDevice, H->st));
+  if (head_mode == 0) return DF_OK;
+  const int first = head_mode < 0 ? 0 : M - 1;
+  const int rows = head_mode < 0 ? M : 1;
+  H->rows_last_logits = rows;
+  CK(launch_rmsnorm(H->h + (size_t)first * H->d, H->d, H->final_norm, H->xb, H->d, H->bf16, rows, H->d,
+                    H->cfg.rms_eps, nullptr, 0, nullptr, H->st));
+  return lm_head_argmax(H, rows, H->debug ? H->dbg_logits : nullptr);
+}
+
+// Fuse the taps of rows [0, M) and inject K/V of every drafter layer at the
+// rows' positions (row_pos < 0: inactive row).
+df_status fuse_inject(df_handle* H, int M, const int* row_pos) {
+  EpiParams e = epi(H, EPI_STORE_F32);
+  e.out = H->fcout;
+  e.ldo = H->d;
+  CKS(gemm(H, H->fc, H->taps, M, e));
+  CK(launch_rmsnorm(H->fcout, H->d, H->fc_norm, H->ctx, H->d, H->bf16, M, H->d, H->cfg.rms_eps, nullptr, 0, row_pos,
+                    H->st));
+  EpiParams k = epi(H, EPI_QKV);
+  k.q_dim = 0;
+  k.kv_dest = KV_PAGED;
+  k.kv_base = H->kv_d;
+  k.layer0 = 0;
+  k.row_pos = row_pos;
+  k.row_seq = H->d_row_seq;
+  CKS(gemm(H, H->inj, H->ctx, M, k));
+  H->rows_last_ctx = M;
+  return DF_OK;
+}
+
+df_status drafter_pass(df_handle* H, int nseq, int max_ctx_len) {
+  const int B = H->B, M = nseq * B;
+  CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, M, H->d, H->V, H->d_err, H->st));
+  for (int l = 0; l < H->Ld; ++l) CKS(layer_pass(H, H->dl[l], M, B, nseq, false, l, max_ctx_len, -1));
+  if (H->debug) CK(cudaMemcpyAsync(H->dbg_dh, H->h, (size_t)M * H->d * 4, cudaMemcpyDeviceToDevice, H->st));
+  CK(launch_rmsnorm(H->h, H->d, H->d_final_norm, H->xb, H->d, H->bf16, M, H->d, H->cfg.rms_eps, nullptr, 0, nullptr,
+                    H->st));
+  CKS(lm_head_argmax(H, M, H->debug ? H->dbg_dlogits : nullptr));
+  H->rows_last_draft = M;
+  return DF_OK;
+}
+
+// ---------------------------------------------------------------- pages
+df_status ensure_pages(df_handle* H, int slot, int npos) {
+  SeqHost& s = H->seqs[slot];
+  const int need = (npos + H->PT - 1) / H->PT;
+  if (need > H->pages_per_seq) return fail(H, DF_EINVAL, "sequence would exceed max_ctx");
+  bool changed = false;
+  while ((int)s.pages.size() < need) {
+    if (H->free_pages.empty()) return fail(H, DF_ENOMEM, "KV page pool exhausted");
+    s.pages.push_back(H->free_pages.back());
+    H->free_pages.pop_back();
+    changed = true;
+  }
+  if (changed) {
+    std::vector<int> row(H->pages_per_seq, -1);
+    std::copy(s.pages.begin(), s.pages.end(), row.begin());
+    CK(cudaMemcpyAsync(H->d_pt + (size_t)slot * H->pages_per_seq, row.data(), row.size() * 4, cudaMemcpyHostToDevice,
+                       H->st));
+  }
+  return DF_OK;
+}
+
+// Return pages wholly past `keep` positions (rollback after acceptance).
+df_status trim_pages(df_handle* H, int slot, int keep) {
+  SeqHost& s = H->seqs[slot];
+  const int need = (keep + H->PT - 1) / H->PT;
+  bool changed = false;
+  while ((int)s.pages.size() > need) {
+    H->free_pages.push_back(s.pages.back());
+    s.pages.pop_back();
+    changed = true;
+  }
+  if (changed) {
+    std::vector<int> row(H->pages_per_seq, -1);
+    std::copy(s.pages.begin(), s.pages.end(), row.begin());
+    CK(cudaMemcpyAsync(H->d_pt + (size_t)slot * H->pages_per_seq, row.data(), row.size() * 4, cudaMemcpyHostToDevice,
+                       H->st));
+  }
+  return DF_OK;
+}
+
+df_status check_device_error(df_handle* H) {
+  int e = 0;
+  CK(cudaMemcpy(&e, H->d_err, 4, cudaMemcpyDeviceToHost));
+  if (e) {
+    H->failed = true;
+    if (e & ERR_TIMEOUT) return fail(H, DF_ETIMEOUT, "a bounded device wait ran out (error word " + std::to_string(e) + ")");
+    return fail(H, DF_ECUDA, "device error word " + std::to_string(e));
+  }
+  return DF_OK;
+}
+
+df_status sync(df_handle* H) {
+  CK(cudaStreamSynchronize(H->st));
+  return check_device_error(H);
+}
+
+df_status check_slots(df_handle* H, const int32_t* slots, int nseq) {
+  if (nseq < 1 || nseq > H->cfg.max_batch || !slots) return fail(H, DF_EINVAL, "bad sequence list");
+  for (int i = 0; i < nseq; ++i) {
+    if (slots[i] < 0 || slots[i] >= H->cfg.max_batch) return fail(H, DF_EINVAL, "sequence slot out of range");
+    if (!H->seqs[slots[i]].active) return fail(H, DF_ESTATE, "sequence slot not prefilled");
+    for (int j = 0; j < i; ++j)
+      if (slots[j] == slots[i]) return fail(H, DF_EINVAL, "sequence listed twice");
+  }
+  return DF_OK;
+}
+
+df_status prefill_impl(df_handle* H, int seq, const int32_t* prompt, int len, bool inject, int* bonus_out) {
+  if (seq < 0 || seq >= H->cfg.max_batch) return fail(H, DF_EINVAL, "sequence slot out of range");
+  if (!prompt || len < 1) return fail(H, DF_EINVAL, "empty prompt");
+  if (len + H->B > H->cfg.max_ctx) return fail(H, DF_EINVAL, "prompt too long for max_ctx");
+  if (H->seqs[seq].active) return fail(H, DF_ESTATE, "sequence slot already in use");
+  for (int i = 0; i < len; ++i)
+    if (prompt[i] < 0 || prompt[i] >= H->V) return fail(H, DF_EINVAL, "prompt token out of range");
+  SeqHost& s = H->seqs[seq];
+  s.active = true;
+  s.len = 0;
+  s.pages.clear();
+  CKS(ensure_pages(H, seq, len));
+  const int chunk = std::min(PREFILL_CHUNK, H->Mmax);
+  std::vector<int> tok(chunk), pos(chunk), sq(chunk, seq);
+  for (int c0 = 0; c0 < len; c0 += chunk) {
+    const int rows = std::min(chunk, len - c0);
+    for (int i = 0; i < rows; ++i) {
+      tok[i] = prompt[c0 + i];
+      pos[i] = c0 + i;
+    }
+    CK(cudaMemcpyAsync(H->d_row_tok, tok.data(), rows * 4, cudaMemcpyHostToDevice, H->st));
+    CK(cudaMemcpyAsync(H->d_row_pos, pos.data(), rows * 4, cudaMemcpyHostToDevice, H->st));
+    CK(cudaMemcpyAsync(H->d_row_seq, sq.data(), rows * 4, cudaMemcpyHostToDevice, H->st));
+    const bool last = c0 + rows == len;
+    CKS(target_pass(H, rows, rows, 1, c0 + rows, inject, last ? 1 : 0));
+    if (inject) CKS(fuse_inject(H, rows, H->d_row_pos));
+  }
+  // bonus token = argmax at the last prompt position; it sits at position len
+  CK(cudaMemcpyAsync(H->d_bonus + seq, H->d_ids, 4, cudaMemcpyDeviceToDevice, H->st));
+  CK(cudaMemcpyAsync(H->d_bonus_pos + seq, &len, 4, cudaMemcpyHostToDevice, H->st));
+  CK(cudaMemcpyAsync(H->h_pin, H->d_ids, 4, cudaMemcpyDeviceToHost, H->st));
+  CKS(sync(H));
+  s.len = len;
+  s.bonus = H->h_pin[0];
+  if (bonus_out) *bonus_out = s.bonus;
+  return DF_OK;
+}
+
+df_status draft_impl(df_handle* H, const int32_t* slots, int nseq, int32_t* drafts_host) {
+  CKS(check_slots(H, slots, nseq));
+  const int B = H->B;
+  CK(cudaMemcpyAsync(H->d_slots, slots, nseq * 4, cudaMemcpyHostToDevice, H->st));
+  int max_len = 0;
+  for (int i = 0; i < nseq; ++i) max_len = std::max(max_len, H->seqs[slots[i]].len);
+  CK(cudaEventRecord(H->ev[0], H->st));
+  CK(launch_prep_block(H->d_slots, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 0,
+                       H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st));
+  CKS(drafter_pass(H, nseq, max_len));
+  CK(launch_collect_drafts(H->d_ids, nseq, B, H->d_slots, H->d_drafts, H->st));
+  CK(cudaEventRecord(H->ev[1], H->st));
+  if (drafts_host) {
+    CK(cudaMemcpyAsync(H->h_pin, H->d_drafts, (size_t)H->cfg.max_batch * (B - 1) * 4, cudaMemcpyDeviceToHost, H->st));
+    CKS(sync(H));
+    for (int i = 0; i < nseq; ++i)
+      std::memcpy(drafts_host + (size_t)i * (B - 1), H->h_pin + (size_t)slots[i] * (B - 1), (B - 1) * 4);
+  }
+  return DF_OK;
+}
+
+df_status verify_impl(df_handle* H, const int32_t* slots, int nseq, const int32_t* drafts_host, int32_t* acc_host,
+                      int32_t* n_host, bool timed) {
+  CKS(check_slots(H, slots, nseq));
+  const int B = H->B;
+  int max_len = 0;
+  for (int i = 0; i < nseq; ++i) {
+    SeqHost& s = H->seqs[slots[i]];
+    if (s.len + B > H->cfg.max_ctx) return fail(H, DF_EINVAL, "sequence would exceed max_ctx");
+    CKS(ensure_pages(H, slots[i], s.len + B));
+    max_len = std::max(max_len, s.len + B);
+  }
+  CK(cudaMemcpyAsync(H->d_slots, slots, nseq * 4, cudaMemcpyHostToDevice, H->st));
+  if (drafts_host) {
+    for (int i = 0; i < nseq; ++i) {
+      for (int j = 0; j < B - 1; ++j) {
+        const int t = drafts_host[(size_t)i * (B - 1) + j];
+        if (t < 0 || t >= H->V) return fail(H, DF_EINVAL, "draft token out of range");
+      }
+      CK(cudaMemcpyAsync(H->d_drafts + (size_t)slots[i] * (B - 1), drafts_host + (size_t)i * (B - 1), (B - 1) * 4,
+                         cudaMemcpyHostToDevice, H->st));
+    }
+  }
+  CK(cudaEventRecord(H->ev[2], H->st));
+  CK(launch_prep_block(H->d_slots, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 1,
+                       H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st));
+  const int M = nseq * B;
+  CKS(target_pass(H, M, B, nseq, max_len, true, -1));
+  CK(launch_accept(H->d_slots, nseq, B, H->d_row_tok, H->d_ids, H->d_bonus, H->d_bonus_pos, H->d_acc, H->d_n,
+                   H->d_inj_pos, H->st));
+  CKS(fuse_inject(H, M, H->d_inj_pos));
+  CK(cudaEventRecord(H->ev[3], H->st));
+  CK(cudaMemcpyAsync(H->h_pin, H->d_acc, (size_t)nseq * B * 4, cudaMemcpyDeviceToHost, H->st));
+  CK(cudaMemcpyAsync(H->h_pin + (size_t)nseq * B, H->d_n, (size_t)nseq * 4, cudaMemcpyDeviceToHost, H->st));
+  CKS(sync(H));
+  const int* acc = H->h_pin;
+  const int* n = H->h_pin + (size_t)nseq * B;
+  for (int i = 0; i < nseq; ++i) {
+    SeqHost& s = H->seqs[slots[i]];
+    const int k = n[i] - 1;
+    if (k < 0 || k > B - 1) return fail(H, DF_ECUDA, "accept kernel produced an invalid count");
+    s.len += k + 1;
+    s.bonus = acc[(size_t)i * B + k];
+    CKS(trim_pages(H, slots[i], s.len + B));
+    H->stats.cycles += 1;
+    H->stats.accepted_drafts += k;
+    H->stats.accept_hist[std::min(k, 64)] += 1;
+  }
+  if (timed) {
+    float a = 0.f, b = 0.f;
+    if (cudaEventElapsedTime(&a, H->ev[0], H->ev[1]) == cudaSuccess) H->stats.draft_us += 1000.0 * a;
+    if (cudaEventElapsedTime(&b, H->ev[2], H->ev[3]) == cudaSuccess) H->stats.verify_us += 1000.0 * b;
+  }
+  if (acc_host) std::memcpy(acc_host, acc, (size_t)nseq * B * 4);
+  if (n_host) std::memcpy(n_host, n, (size_t)nseq * 4);
+  return DF_OK;
+}
+
+df_status release(df_handle* H, int slot) {
+  SeqHost& s = H->seqs[slot];
+  for (int p : s.pages) H->free_pages.push_back(p);
+  s.pages.clear();
+  s.active = false;
+  s.len = 0;
+  s.bonus = -1;
+  std::vector<int> row(H->pages_per_seq, -1);
+  CK(cudaMemcpyAsync(H->d_pt + (size_t)slot * H->pages_per_seq, row.data(), row.size() * 4, cudaMemcpyHostToDevice,
+                     H->st));
+  CK(cudaStreamSynchronize(H->st));
+  return DF_OK;
+}
+
+df_status check_batch_args(df_handle* H, const int32_t* prompts, const int32_t* lens, int nseq, int n_new, void* out) {
+  if (!prompts || !lens || !out || nseq < 1 || nseq > H->cfg.max_batch || n_new < 1)
+    return fail(H, DF_EINVAL, "bad batch arguments");
+  for (int i = 0; i < nseq; ++i) {
+    if (H->seqs[i].active) return fail(H, DF_ESTATE, "slots 0..nseq-1 must be free");
+    if (lens[i] < 1 || (long long)lens[i] + n_new + H->B > H->cfg.max_ctx)
+      return fail(H, DF_EINVAL, "prompt length + n_new + block exceeds max_ctx");
+  }
+  return DF_OK;
+}
+
+// ---------------------------------------------------------------- init helpers
+df_status pack_weights(df_handle* H, const void* const* w, int nw) {
+  const df_config& c = H->cfg;
+  const size_t es = H->esz;
+  const int d = H->d;
+  std::vector<WSpec> specs = weight_specs(c);
+  if ((int)specs.size() != nw) return fail(H, DF_EINVAL, "wrong number of weights");
+  for (int i = 0; i < nw; ++i)
+    if (!w[i]) return fail(H, DF_EINVAL, "null weight pointer: " + specs[i].name);
+
+  // Arena layout: every matrix 256-byte aligned; norm gains stored as fp32.
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += (bytes + 255) & ~size_t(255);
+    return o;
+  };
+  struct Slot {
+    size_t off;
+  };
+  const long long V = H->V, F = H->F, qd = H->qdim, kd = H->kvdim;
+  size_t o_embed = take(V * d * es), o_lm = take(V * d * es), o_fc = take((size_t)d * 5 * d * es);
+  size_t o_inj = take((size_t)H->Ld * 2 * kd * d * es);
+  size_t o_fn = take(d * 4), o_fcn = take(d * 4), o_dfn = take(d * 4);
+  struct LOff {
+    size_t an, qkv, wo, mn, gu, down;
+  };
+  std::vector<LOff> lo(H->L + H->Ld);
+  for (auto& x : lo) {
+    x.an = take(d * 4);
+    x.qkv = take((size_t)H->qkv_n * d * es);
+    x.wo = take((size_t)d * qd * es);
+    x.mn = take(d * 4);
+    x.gu = take((size_t)2 * F * d * es);
+    x.down = take((size_t)d * F * es);
+  }
+  CKS(dalloc(H, &H->arena, off));
+  uint8_t* A = reinterpret_cast<uint8_t*>(H->arena);
+  cudaStream_t st = H->st;
+  auto cp = [&](size_t dst, const void* src, size_t bytes) {
+    return cudaMemcpyAsync(A + dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+  };
+  // gains: device -> host -> fp32 -> device
+  auto gain = [&](size_t dst, const void* src) -> df_status {
+    std::vector<float> g(d);
+    if (H->bf16) {
+      std::vector<uint16_t> b(d);
+      CK(cudaMemcpy(b.data(), src, d * 2, cudaMemcpyDeviceToHost));
+      for (int i = 0; i < d; ++i) {
+        uint32_t u = (uint32_t)b[i] << 16;
+        std::memcpy(&g[i], &u, 4);
+      }
+    } else {
+      CK(cudaMemcpy(g.data(), src, d * 4, cudaMemcpyDeviceToHost));
+    }
+    CK(cudaMemcpy(A + dst, g.data(), d * 4, cudaMemcpyHostToDevice));
+    return DF_OK;
+  };
+
+  int i = 0;
+  CK(cp(o_embed, w[i++], V * d * es));
+  H->embed = A + o_embed;
+  auto layer = [&](int li, Layer& Lw) -> df_status {
+    const LOff& x = lo[li];
+    CKS(gain(x.an, w[i++]));
+    CK(cp(x.qkv, w[i++], qd * d * es));
+    CK(cp(x.qkv + qd * d * es, w[i++], kd * d * es));
+    CK(cp(x.qkv + (qd + kd) * d * es, w[i++], kd * d * es));
+    CK(cp(x.wo, w[i++], (size_t)d * qd * es));
+    CKS(gain(x.mn, w[i++]));
+    const void* gate = w[i++];
+    const void* up = w[i++];
+    const size_t blk = (size_t)64 * d * es;
+    CK(cudaMemcpy2DAsync(A + x.gu, 2 * blk, gate, blk, blk, F / 64, cudaMemcpyDeviceToDevice, st));
+    CK(cudaMemcpy2DAsync(A + x.gu + blk, 2 * blk, up, blk, blk, F / 64, cudaMemcpyDeviceToDevice, st));
+    CK(cp(x.down, w[i++], (size_t)d * F * es));
+    Lw.attn_norm = reinterpret_cast<float*>(A + x.an);
+    Lw.mlp_norm = reinterpret_cast<float*>(A + x.mn);
+    Lw.qkv = Linear{A + x.qkv, H->qkv_n, d, {}};
+    Lw.wo = Linear{A + x.wo, d, (int)qd, {}};
+    Lw.gu = Linear{A + x.gu, (int)(2 * F), d, {}};
+    Lw.down = Linear{A + x.down, d, (int)F, {}};
+    return DF_OK;
+  };
+  H->tl.resize(H->L);
+  H->dl.resize(H->Ld);
+  for (int l = 0; l < H->L; ++l) CKS(layer(l, H->tl[l]));
+  CKS(gain(o_fn, w[i++]));
+  H->final_norm = reinterpret_cast<float*>(A + o_fn);
+  CK(cp(o_lm, w[i++], V * d * es));
+  H->lm_head = Linear{A + o_lm, (int)V, d, {}};
+  CK(cp(o_fc, w[i++], (size_t)d * 5 * d * es));
+  H->fc = Linear{A + o_fc, d, 5 * d, {}};
+  CKS(gain(o_fcn, w[i++]));
+  H->fc_norm = reinterpret_cast<float*>(A + o_fcn);
+  // the drafter layers; their W_k/W_v also feed the injection matrix
+  for (int l = 0; l < H->Ld; ++l) {
+    const int base = i;
+    CKS(layer(H->L + l, H->dl[l]));
+    const size_t kv_bytes = (size_t)kd * d * es;
+    CK(cp(o_inj + (size_t)l * 2 * kv_bytes, w[base + 2], kv_bytes));
+    CK(cp(o_inj + (size_t)l * 2 * kv_bytes + kv_bytes, w[base + 3], kv_bytes));
+  }
+  H->inj = Linear{A + o_inj, (int)(H->Ld * 2 * kd), d, {}};
+  CKS(gain(o_dfn, w[i++]));
+  H->d_final_norm = reinterpret_cast<float*>(A + o_dfn);
+  CK(cudaStreamSynchronize(st));
+
+  if (H->bf16) {
+    std::vector<Linear*> all = {&H->lm_head, &H->fc, &H->inj};
+    for (auto& Lw : H->tl) all.insert(all.end(), {&Lw.qkv, &Lw.wo, &Lw.gu, &Lw.down});
+    for (auto& Lw : H->dl) all.insert(all.end(), {&Lw.qkv, &Lw.wo, &Lw.gu, &Lw.down});
+    for (Linear* Lp : all)
+      if (!make_tmap_bf16(Lp->tm.b, Lp->ptr, Lp->N, Lp->K, 128))
+        return fail(H, DF_ECUDA, "tensor map encode failed (weights)");
+  }
+  return DF_OK;
+}
+
+df_status alloc_state(df_handle* H) {
+  const df_config& c = H->cfg;
+  const size_t es = H->esz;
+  const int d = H->d, M = H->Mmax;
+  H->PT = c.page_tokens;
+  H->pages_per_seq = (c.max_ctx + H->PT - 1) / H->PT;
+  H->n_pages = H->pages_per_seq * c.max_batch;
+  const size_t page_elems = (size_t)2 * H->Hkv * H->PT * H->hd;
+  H->layer_stride = (long long)(page_elems * H->n_pages);
+  CKS(dalloc(H, &H->kv_t, (size_t)H->layer_stride * H->L * es));
+  CKS(dalloc(H, &H->kv_d, (size_t)H->layer_stride * H->Ld * es));
+  CKS(dalloc_t(H, &H->d_pt, (size_t)c.max_batch * H->pages_per_seq * 4));
+  CK(cudaMemset(H->d_pt, 0xFF, (size_t)c.max_batch * H->pages_per_seq * 4));
+  for (int p = H->n_pages - 1; p >= 0; --p) H->free_pages.push_back(p);
+  H->seqs.assign(c.max_batch, SeqHost{});
+
+  CKS(dalloc_t(H, &H->d_bonus, c.max_batch * 4));
+  CKS(dalloc_t(H, &H->d_bonus_pos, c.max_batch * 4));
+  CKS(dalloc_t(H, &H->d_row_tok, M * 4));
+  CKS(dalloc_t(H, &H->d_row_pos, M * 4));
+  CKS(dalloc_t(H, &H->d_row_seq, M * 4));
+  CKS(dalloc_t(H, &H->d_inj_pos, M * 4));
+  CKS(dalloc_t(H, &H->d_ids, M * 4));
+  CKS(dalloc_t(H, &H->d_slots, c.max_batch * 4));
+  CKS(dalloc_t(H, &H->d_drafts, (size_t)c.max_batch * H->B * 4));
+  CKS(dalloc_t(H, &H->d_acc, (size_t)c.max_batch * H->B * 4));
+  CKS(dalloc_t(H, &H->d_n, c.max_batch * 4));
+  CKS(dalloc_t(H, &H->d_amax, M * 8));
+  CKS(dalloc_t(H, &H->d_err, 4));
+  CK(cudaMemset(H->d_err, 0, 4));
+  CK(cudaMemset(H->d_drafts, 0, (size_t)c.max_batch * H->B * 4));
+
+  CKS(dalloc_t(H, &H->h, (size_t)M * d * 4));
+  CKS(dalloc(H, &H->xb, (size_t)M * d * es));
+  CKS(dalloc(H, &H->q, (size_t)M * H->qdim * es));
+  CKS(dalloc(H, &H->attn, (size_t)M * H->qdim * es));
+  CKS(dalloc(H, &H->act, (size_t)M * H->F * es));
+  CKS(dalloc(H, &H->taps, (size_t)M * 5 * d * es));
+  CKS(dalloc_t(H, &H->fcout, (size_t)M * d * 4));
+  CKS(dalloc(H, &H->ctx, (size_t)M * d * es));
+  CKS(dalloc(H, &H->blk, (size_t)2 * H->Hkv * M * H->hd * es));
+  // zero the activation buffers once so rows a pass does not write are finite
+  CK(cudaMemset(H->xb, 0, (size_t)M * d * es));
+  CK(cudaMemset(H->attn, 0, (size_t)M * H->qdim * es));
+  CK(cudaMemset(H->act, 0, (size_t)M * H->F * es));
+  CK(cudaMemset(H->taps, 0, (size_t)M * 5 * d * es));
+  CK(cudaMemset(H->ctx, 0, (size_t)M * d * es));
+
+  // GEMM shapes: split-K workspace and tile tickets
+  std::vector<std::pair<int, int>> shapes = {{H->qkv_n, d}, {d, H->qdim}, {2 * H->F, d}, {d, H->F},
+                                             {H->V, d},     {d, 5 * d},   {H->inj.N, d}};
+  size_t ws = 0, cnt = 0;
+  if (H->bf16) {
+    for (auto& s : shapes) {
+      const int splits = tc_splits(s.first, s.second, H->sm_count);
+      for (int nt : {16, 32, 64, 128, 256}) {
+        ws = std::max(ws, tc_workspace_floats(M, s.first, splits, nt));
+        cnt = std::max(cnt, tc_counter_ints(M, s.first, nt));
+      }
+    }
+  } else {
+    size_t maxN = 0;
+    for (auto& s : shapes) maxN = std::max(maxN, (size_t)s.first);
+    CKS(dalloc_t(H, &H->tmp, (size_t)M * maxN * 4));
+  }
+  CKS(dalloc_t(H, &H->ws, std::max<size_t>(ws, 64) * 4));
+  CKS(dalloc_t(H, &H->counters, std::max<size_t>(cnt, 64) * 4));
+  CK(cudaMemset(H->counters, 0, std::max<size_t>(cnt, 64) * 4));
+
+  H->n_chunk_slots = (c.max_ctx + ATTN_CHUNK - 1) / ATTN_CHUNK + 1;
+  CKS(dalloc_t(H, &H->part_acc, (size_t)M * H->Hq * H->n_chunk_slots * H->hd * 4));
+  CKS(dalloc_t(H, &H->part_ml, (size_t)M * H->Hq * H->n_chunk_slots * 8));
+
+  // rotary table in double precision on the host: angle = pos * theta^(-2j/hd)
+  const int half = H->hd / 2;
+  std::vector<float2> rope((size_t)c.max_ctx * half);
+  for (int pos = 0; pos < c.max_ctx; ++pos)
+    for (int j = 0; j < half; ++j) {
+      const double inv = std::pow((double)c.rope_theta, -2.0 * j / H->hd);
+      const double a = (double)pos * inv;
+      rope[(size_t)pos * half + j] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
+  CKS(dalloc_t(H, &H->rope, rope.size() * sizeof(float2)));
+  CK(cudaMemcpy(H->rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice));
+
+  H->h_pin_ints = std::max<size_t>((size_t)c.max_batch * (H->B + 2) * 2, 64);
+  CK(cudaMallocHost(&H->h_pin, H->h_pin_ints * 4));
+  for (auto& e : H->ev) CK(cudaEventCreate(&e));
+  return DF_OK;
+}
+
+df_status ensure_debug_buffers(df_handle* H) {
+  if (H->dbg_logits) return DF_OK;
+  const size_t M = H->Mmax;
+  CKS(dalloc_t(H, &H->dbg_logits, M * H->V * 4));
+  CKS(dalloc_t(H, &H->dbg_dlogits, M * H->V * 4));
+  CKS(dalloc_t(H, &H->dbg_dh, M * H->d * 4));
+  CKS(dalloc_t(H, &H->dbg_th, M * H->d * 4));
+  return DF_OK;
+}
+
+}  // namespace
+
+// =============================================================================
+// C ABI
+// =============================================================================
+extern "C" {
+
+df_status df_default_feat_layers(int32_t n_layers, int32_t out[5]) {
+  if (!out || n_layers < 8) return DF_EINVAL;
+  for (int i = 0; i < 5; ++i) out[i] = feat_default(n_layers, i);
+  return DF_OK;
+}
+
+int32_t df_num_weights(const df_config* cfg) {
+  if (!cfg || cfg->n_layers < 0 || cfg->draft_layers < 0) return -1;
+  return (int32_t)weight_specs(*cfg).size();
+}
+
+df_status df_weight_info(const df_config* cfg, int32_t index, char name[32], int32_t* ndim, int64_t shape[2]) {
+  if (!cfg) return DF_EINVAL;
+  std::vector<WSpec> s = weight_specs(*cfg);
+  if (index < 0 || index >= (int)s.size()) return DF_EINVAL;
+  if (name) {
+    std::memset(name, 0, 32);
+    std::strncpy(name, s[index].name.c_str(), 31);
+  }
+  if (ndim) *ndim = s[index].ndim;
+  if (shape) {
+    shape[0] = s[index].s0;
+    shape[1] = s[index].s1;
+  }
+  return DF_OK;
+}
+
+df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_weights, void* stream,
+                  df_handle** out) {
+  if (!out) return DF_EINVAL;
+  *out = nullptr;
+  std::string why;
+  if (validate(cfg, why) != DF_OK) return DF_EINVAL;
+  if (!weights) return DF_EINVAL;
+  df_handle* H = new df_handle();
+  H->cfg = *cfg;
+  H->st = reinterpret_cast<cudaStream_t>(stream);
+  H->bf16 = cfg->dtype == DF_BF16;
+  H->esz = H->bf16 ? 2 : 4;
+  H->d = cfg->d_model;
+  H->hd = cfg->head_dim;
+  H->Hq = cfg->n_q_heads;
+  H->Hkv = cfg->n_kv_heads;
+  H->F = cfg->d_ffn;
+  H->V = cfg->vocab;
+  H->L = cfg->n_layers;
+  H->Ld = cfg->draft_layers;
+  H->B = cfg->block_size;
+  H->qdim = H->Hq * H->hd;
+  H->kvdim = H->Hkv * H->hd;
+  H->qkv_n = H->qdim + 2 * H->kvdim;
+  H->Mmax = std::max(std::min(PREFILL_CHUNK, cfg->max_ctx), cfg->max_batch * cfg->block_size);
+  for (int l = 0; l < 1024; ++l) H->tap_of_layer[l] = -1;
+  for (int i = 0; i < 5; ++i) H->tap_of_layer[cfg->feat_layers[i]] = i;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&H->sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    delete H;
+    (void)cudaGetLastError();
+    return DF_ECUDA;
+  }
+  if (H->bf16) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10) {
+      delete H;
+      return DF_ECUDA;
+    }
+  }
+  df_status s = pack_weights(H, weights, n_weights);
+  if (s == DF_OK) s = alloc_state(H);
+  if (s != DF_OK) {
+    df_destroy(H);
+    return s;
+  }
+  *out = H;
+  return DF_OK;
+}
+
+#define GUARD(H)                                                              \
+  do {                                                                        \
+    if (!(H)) return DF_EINVAL;                                               \
+    if ((H)->failed) return fail(H, DF_ECUDA, "handle is in a failed state"); \
+  } while (0)
+
+df_status df_prefill(df_handle* H, int32_t seq, const int32_t* prompt_host, int32_t len, int32_t* bonus_out) {
+  GUARD(H);
+  cudaEvent_t a = H->ev[0], b = H->ev[1];
+  cudaEventRecord(a, H->st);
+  df_status s = prefill_impl(H, seq, prompt_host, len, true, bonus_out);
+  if (s != DF_OK) {
+    if (seq >= 0 && seq < H->cfg.max_batch && H->seqs[seq].active && H->seqs[seq].len == 0) release(H, seq);
+    return s;
+  }
+  cudaEventRecord(b, H->st);
+  cudaEventSynchronize(b);
+  float ms = 0.f;
+  if (cudaEventElapsedTime(&ms, a, b) == cudaSuccess) H->stats.prefill_us += 1000.0 * ms;
+  return DF_OK;
+}
+
+df_status df_draft_block(df_handle* H, const int32_t* seqs_host, int32_t nseq, int32_t* drafts_host) {
+  GUARD(H);
+  return draft_impl(H, seqs_host, nseq, drafts_host);
+}
+
+df_status df_verify_accept(df_handle* H, const int32_t* seqs_host, int32_t nseq, const int32_t* drafts_host,
+                           int32_t* accepted_host, int32_t* n_host) {
+  GUARD(H);
+  return verify_impl(H, seqs_host, nseq, drafts_host, accepted_host, n_host, false);
+}
+
+df_status df_generate(df_handle* H, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,
+                      int32_t n_new, int32_t* out_host, df_stats* stats) {
+  GUARD(H);
+  CKS(check_batch_args(H, prompts_host, lens_host, nseq, n_new, out_host));
+  const df_stats before = H->stats;
+  const int B = H->B;
+  std::vector<int> count(nseq, 0);
+  size_t off = 0;
+  df_status s = DF_OK;
+  for (int i = 0; i < nseq && s == DF_OK; ++i) {
+    int bonus = 0;
+    s = df_prefill(H, i, prompts_host + off, lens_host[i], &bonus);
+    off += lens_host[i];
+    if (s == DF_OK) out_host[(size_t)i * n_new] = bonus, count[i] = 1;
+  }
+  std::vector<int> active, acc((size_t)nseq * B), n(nseq);
+  while (s == DF_OK) {
+    active.clear();
+    for (int i = 0; i < nseq; ++i)
+      if (count[i] < n_new) active.push_back(i);
+    if (active.empty()) break;
+    s = draft_impl(H, active.data(), (int)active.size(), nullptr);
+    if (s != DF_OK) break;
+    s = verify_impl(H, active.data(), (int)active.size(), nullptr, acc.data(), n.data(), true);
+    if (s != DF_OK) break;
+    for (size_t j = 0; j < active.size(); ++j) {
+      const int i = active[j];
+      for (int t = 0; t < n[j] && count[i] < n_new; ++t) out_host[(size_t)i * n_new + count[i]++] = acc[j * B + t];
+    }
+  }
+  for (int i = 0; i < nseq; ++i)
+    if (H->seqs[i].active) release(H, i);
+  if (s != DF_OK) return s;
+  for (int i = 0; i < nseq; ++i) H->stats.emitted_tokens += count[i];
+  if (stats) {
+    df_stats d{};
+    d.cycles = H->stats.cycles - before.cycles;
+    d.accepted_drafts = H->stats.accepted_drafts - before.accepted_drafts;
+    d.emitted_tokens = H->stats.emitted_tokens - before.emitted_tokens;
+    for (int k = 0; k < 65; ++k) d.accept_hist[k] = H->stats.accept_hist[k] - before.accept_hist[k];
+    d.draft_us = H->stats.draft_us - before.draft_us;
+    d.verify_us = H->stats.verify_us - before.verify_us;
+    d.prefill_us = H->stats.prefill_us - before.prefill_us;
+    *stats = d;
+  }
+  return DF_OK;
+}
+
+df_status df_greedy_reference(df_handle* H, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,
+                              int32_t n_new, int32_t* out_host) {
+  GUARD(H);
+  CKS(check_batch_args(H, prompts_host, lens_host, nseq, n_new, out_host));
+  std::vector<int> bonus(nseq), pos(nseq), sq(nseq);
+  size_t off = 0;
+  df_status s = DF_OK;
+  for (int i = 0; i < nseq && s == DF_OK; ++i) {
+    s = prefill_impl(H, i, prompts_host + off, lens_host[i], false, &bonus[i]);
+    off += lens_host[i];
+    pos[i] = lens_host[i];
+    sq[i] = i;
+  }
+  int* d_gen = nullptr;
+  if (s == DF_OK) {
+    if (cudaMalloc(&d_gen, (size_t)nseq * n_new * 4) != cudaSuccess) s = fail(H, DF_ENOMEM, "output buffer");
+  }
+  auto body = [&]() -> df_status {
+    CK(cudaMemcpyAsync(H->d_row_tok, bonus.data(), nseq * 4, cudaMemcpyHostToDevice, H->st));
+    CK(cudaMemcpyAsync(H->d_row_pos, pos.data(), nseq * 4, cudaMemcpyHostToDevice, H->st));
+    CK(cudaMemcpyAsync(H->d_row_seq, sq.data(), nseq * 4, cudaMemcpyHostToDevice, H->st));
+    CK(cudaMemcpyAsync(H->d_ids, bonus.data(), nseq * 4, cudaMemcpyHostToDevice, H->st));
+    CK(launch_greedy_step(H->d_ids, nseq, 0, n_new, d_gen, H->d_row_tok, H->d_row_pos, H->st));
+    // greedy_step advanced the positions; undo that for step 0's inputs
+    CK(cudaMemcpyAsync(H->d_row_pos, pos.data(), nseq * 4, cudaMemcpyHostToDevice, H->st));
+    for (int t = 1; t < n_new; ++t) {
+      int max_len = 0;
+      for (int i = 0; i < nseq; ++i) {
+        const int p = lens_host[i] + t - 1;  // position of this step's input token
+        CKS(ensure_pages(H, i, p + 1));
+        max_len = std::max(max_len, p + 1);
+      }
+      CKS(target_pass(H, nseq, 1, nseq, max_len, false, -1));
+      CK(launch_greedy_step(H->d_ids, nseq, t, n_new, d_gen, H->d_row_tok, H->d_row_pos, H->st));
+    }
+    CK(cudaMemcpyAsync(out_host, d_gen, (size_t)nseq * n_new * 4, cudaMemcpyDeviceToHost, H->st));
+    return sync(H);
+  };
+  if (s == DF_OK) s = body();
+  if (d_gen) cudaFree(d_gen);
+  for (int i = 0; i < nseq; ++i)
+    if (H->seqs[i].active) release(H, i);
+  return s;
+}
+
+df_status df_reset_seq(df_handle* H, int32_t seq) {
+  if (!H) return DF_EINVAL;
+  if (seq < 0 || seq >= H->cfg.max_batch) return fail(H, DF_EINVAL, "sequence slot out of range");
+  return release(H, seq);
+}
+
+df_status df_get_stats(const df_handle* H, df_stats* out) {
+  if (!H || !out) return DF_EINVAL;
+  *out = H->stats;
+  return DF_OK;
+}
+
+df_status df_reset_stats(df_handle* H) {
+  if (!H) return DF_EINVAL;
+  H->stats = df_stats{};
+  return DF_OK;
+}
+
+df_status df_seq_info(const df_handle* H, int32_t seq, int32_t* length, int32_t* bonus) {
+  if (!H || seq < 0 || seq >= H->cfg.max_batch) return DF_EINVAL;
+  if (length) *length = H->seqs[seq].len;
+  if (bonus) *bonus = H->seqs[seq].bonus;
+  return DF_OK;
+}
+
+void df_destroy(df_handle* H) {
+  if (!H) return;
+  if (H->st) cudaStreamSynchronize(H->st);
+  else cudaDeviceSynchronize();
+  for (void* p : H->allocs) cudaFree(p);
+  if (H->h_pin) cudaFreeHost(H->h_pin);
+  for (auto& e : H->ev)
+    if (e) cudaEventDestroy(e);
+  delete H;
+}
+
+const char* df_last_error(const df_handle* H) {
+  if (!H) return "null handle";
+  return H->err.c_str();
+}
+
+df_status df_debug_enable(df_handle* H, int32_t on) {
+  if (!H) return DF_EINVAL;
+  if (on) CKS(ensure_debug_buffers(H));
+  H->debug = on != 0;
+  return DF_OK;
+}
+
+df_status df_debug_read(df_handle* H, int32_t what, float* out_host, int64_t max_floats, int32_t* rows_out) {
+  if (!H || !out_host) return DF_EINVAL;
+  CK(cudaStreamSynchronize(H->st));
+  const void* src = nullptr;
+  bool typed = false;  // stored in the model dtype (else fp32)
+  int rows = 0;
+  size_t cols = 0;
+  switch (what) {
+    case DF_DBG_TAPS: src = H->taps; typed = true; rows = H->rows_last_target; cols = (size_t)5 * H->d; break;
+    case DF_DBG_LOGITS: src = H->dbg_logits; rows = H->rows_last_logits; cols = H->V; break;
+    case DF_DBG_DRAFT_LOGITS: src = H->dbg_dlogits; rows = H->rows_last_draft; cols = H->V; break;
+    case DF_DBG_DRAFT_HIDDEN: src = H->dbg_dh; rows = H->rows_last_draft; cols = H->d; break;
+    case DF_DBG_CTX: src = H->ctx; typed = true; rows = H->rows_last_ctx; cols = H->d; break;
+    case DF_DBG_HIDDEN: src = H->dbg_th; rows = H->rows_last_target; cols = H->d; break;
+    default: return fail(H, DF_EINVAL, "unknown debug buffer");
+  }
+  if (!src) return fail(H, DF_ESTATE, "debug buffers are off (df_debug_enable)");
+  const size_t n = (size_t)rows * cols;
+  if ((int64_t)n > max_floats) return fail(H, DF_EINVAL, "output buffer too small");
+  if (typed && H->bf16) {
+    std::vector<uint16_t> b(n);
+    CK(cudaMemcpy(b.data(), src, n * 2, cudaMemcpyDeviceToHost));
+    for (size_t i = 0; i < n; ++i) {
+      uint32_t u = (uint32_t)b[i] << 16;
+      std::memcpy(out_host + i, &u, 4);
+    }
+  } else {
+    CK(cudaMemcpy(out_host, src, n * 4, cudaMemcpyDeviceToHost));
+  }
+  if (rows_out) *rows_out = rows;
+  return DF_OK;
+}
+
+df_status df_debug_weight_ptr(const df_handle* H, int32_t which, uint64_t* addr) {
+  if (!H || !addr) return DF_EINVAL;
+  switch (which) {
+    case 0:  // target embedding
+    case 1:  // drafter embedding: the same table
+      *addr = reinterpret_cast<uint64_t>(H->embed);
+      return DF_OK;
+    case 2:  // target LM head
+    case 3:  // drafter LM head: the same matrix
+      *addr = reinterpret_cast<uint64_t>(H->lm_head.ptr);
+      return DF_OK;
+    default: return DF_EINVAL;
+  }
+}
+
+// ---------------------------------------------------------------- single ops
+df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, int32_t M, int32_t N, int32_t K,
+                          int32_t splits, int32_t token_tile, void* stream) {
+  if (!x_dev || !w_dev || !y_dev || M < 1 || N % 128 || K % 64 || N <= 0 || K <= 0) return DF_EINVAL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int nt = token_tile ? token_tile : tc_token_tile(M);
+  if (nt != 16 && nt != 32 && nt != 64 && nt != 128 && nt != 256) return DF_EINVAL;
+  const int sp = splits ? splits : tc_splits(N, K, sms);
+  if (sp < 1 || sp > K / 64) return DF_EINVAL;
+  Tmap tw, tx;
+  if (!make_tmap_bf16(tw.b, w_dev, N, K, 128) || !make_tmap_bf16(tx.b, x_dev, M, K, nt)) return DF_EINVAL;
+  float* ws = nullptr;
+  int* cnt = nullptr;
+  const size_t wsf = tc_workspace_floats(M, N, sp, nt), cn = tc_counter_ints(M, N, nt);
+  if (cudaMallocAsync(reinterpret_cast<void**>(&ws), std::max<size_t>(wsf, 1) * 4, st) != cudaSuccess) return DF_ENOMEM;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&cnt), cn * 4, st) != cudaSuccess) {
+    cudaFreeAsync(ws, st);
+    return DF_ENOMEM;
+  }
+  cudaMemsetAsync(cnt, 0, cn * 4, st);
+  EpiParams e{};
+  e.kind = EPI_STORE_F32;
+  e.out = y_dev;
+  e.ldo = N;
+  cudaError_t r = launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st);
+  cudaFreeAsync(ws, st);
+  cudaFreeAsync(cnt, st);
+  return r == cudaSuccess ? DF_OK : DF_ECUDA;
+}
+
+df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32_t* ids_dev, int32_t M, int32_t V,
+                                   int32_t K, void* stream) {
+  if (!x_dev || !wlm_dev || !ids_dev || M < 1 || V % 128 || K % 64 || V <= 0 || K <= 0) return DF_EINVAL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int nt = tc_token_tile(M);
+  const int sp = tc_splits(V, K, sms);
+  Tmap tw, tx;
+  if (!make_tmap_bf16(tw.b, wlm_dev, V, K, 128) || !make_tmap_bf16(tx.b, x_dev, M, K, nt)) return DF_EINVAL;
+  float* ws = nullptr;
+  int* cnt = nullptr;
+  unsigned long long* amax = nullptr;
+  const size_t wsf = tc_workspace_floats(M, V, sp, nt), cn = tc_counter_ints(M, V, nt);
+  if (cudaMallocAsync(reinterpret_cast<void**>(&ws), std::max<size_t>(wsf, 1) * 4, st) != cudaSuccess) return DF_ENOMEM;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&cnt), cn * 4, st) != cudaSuccess ||
+      cudaMallocAsync(reinterpret_cast<void**>(&amax), (size_t)M * 8, st) != cudaSuccess) {
+    cudaFreeAsync(ws, st);
+    if (cnt) cudaFreeAsync(cnt, st);
+    return DF_ENOMEM;
+  }
+  cudaMemsetAsync(cnt, 0, cn * 4, st);
+  cudaMemsetAsync(amax, 0, (size_t)M * 8, st);
+  EpiParams e{};
+  e.kind = EPI_ARGMAX;
+  e.amax = amax;
+  cudaError_t r = launch_gemm_tc(tw.b, tx.b, nt, M, V, K, sp, ws, cnt, e, st);
+  if (r == cudaSuccess) r = launch_argmax_finalize(amax, ids_dev, M, st);
+  cudaFreeAsync(ws, st);
+  cudaFreeAsync(cnt, st);
+  cudaFreeAsync(amax, st);
+  return r == cudaSuccess ? DF_OK : DF_ECUDA;
+}
+
+}  // extern "C"

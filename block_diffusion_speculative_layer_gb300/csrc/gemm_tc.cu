@@ -1,0 +1,395 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// Computes acc[m][n] = sum_k X[m][k] * W[n][k] for a weight matrix W
+// [N][K] (a linear layer's [out, in] layout) and activations X [M][K], both
+// bf16 and K-contiguous, accumulating in fp32.  Decode-shaped calls have few
+// token rows (M = block size x batch), so the roles are swapped: 128 weight
+// rows form the MMA's M side and the token rows its N side (16..256).  Each
+// CTA owns one 128-row weight tile, one token tile and one K range (split-K);
+// the weight stream is what bounds the kernel, so the pipeline only has to
+// keep enough TMA loads in flight.
+//
+// Roles (128 threads): warp 0 lane 0 issues TMA loads into a STAGES-deep ring
+// of shared-memory stages; warp 1 lane 0 issues tcgen05.mma (kind::f16, bf16 in,
+// fp32 accumulate in tensor memory) and releases stages with tcgen05.commit;
+// warp 2 owns the TMEM allocation; all four warps drain the accumulator with
+// tcgen05.ld (thread t holds weight row n0+t for every token) into a shared
+// tile on which the fused epilogue runs.
+//
+// Split-K partials go to a workspace; the CTA that finishes a tile last (an
+// atomic ticket, no waiting) adds the partials in split order 0,1,2,... and
+// runs the epilogue.  The split count depends only on (N, K), and the MMA
+// sequence of one output does not depend on M, so every output is bitwise
+// the same whatever the number of token rows.
+//
+// Every mbarrier wait is bounded (about two seconds); on expiry the kernel
+// records ERR_TIMEOUT, waits (bounded) for the TMA loads it issued, frees its
+// tensor memory and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dfk {
+
+constexpr int BM = 128;  // weight rows per tile (MMA M)
+constexpr int BK = 64;   // K elements per stage: 128 bytes, one swizzle row
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait on an mbarrier phase.  Returns false (and flags the error word)
+// when the phase has not completed within the limit.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 1023u) == 0 && global_ns() - t0 > kWaitLimitNs) break;
+  }
+  flag_error(err, ERR_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);   // start address
+  d |= (uint64_t)1 << 16;                     // leading-dimension offset (unused with this swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;           // stride between 8-row groups
+  d |= (uint64_t)1 << 46;                     // descriptor version
+  d |= (uint64_t)2 << 61;                     // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int NT>
+struct TcCfg {
+  static constexpr int STAGES = NT <= 16 ? 6 : NT <= 32 ? 5 : 4;
+  static constexpr int W_BYTES = BM * BK * 2;
+  static constexpr int X_BYTES = NT * BK * 2;
+  static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+  static constexpr int TMEM_COLS = NT < 32 ? 32 : NT;
+  static constexpr int TLD = BM + 4;  // epilogue tile row stride (floats)
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+  static_assert(NT * TLD * 4 <= STAGES * STAGE_BYTES, "epilogue tile must fit in the stage ring");
+};
+
+template <int NT>
+__global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                      const __grid_constant__ CUtensorMap tmX, int M, int N, int K,
+                                                      int splits, float* __restrict__ ws, int* __restrict__ counters,
+                                                      EpiParams ep) {
+  using C = TcCfg<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sW = smem;
+  uint8_t* sX = smem + C::STAGES * C::W_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 1);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // 0 last-CTA, 1 consumed, 2 failed, 3 issued
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
+  const int n0 = tile_n * BM, m0 = tile_m * NT;
+  const int nkb = K / BK;
+  const int kb0 = (int)((long long)nkb * split / splits);
+  const int kb1 = (int)((long long)nkb * (split + 1) / splits);
+  const int nk = kb1 - kb0;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + C::STAGES);
+  const uint32_t accum_bar = smem_u32(bars + 2 * C::STAGES);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(accum_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    flags[0] = 0; flags[1] = 0; flags[2] = 0; flags[3] = 0;
+  }
+  if (threadIdx.x == 32) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+  }
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer
+    const uint64_t pol_w = policy_evict_first();  // weights are read once per launch
+    const uint64_t pol_x = policy_evict_last();   // activations are re-read by every weight tile
+    int i = 0;
+    for (; i < nk; ++i) {
+      const int s = i % C::STAGES;
+      const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
+      if (i >= C::STAGES && !mbar_wait(empty0 + 8 * s, ph ^ 1u, ep.err)) {
+        flags[2] = 1;
+        break;
+      }
+      mbar_expect_tx(full0 + 8 * s, C::STAGE_BYTES);
+      const int kc = (kb0 + i) * BK;
+      tma_load_2d(smem_u32(sW + s * C::W_BYTES), &tmW, full0 + 8 * s, kc, n0, pol_w);
+      tma_load_2d(smem_u32(sX + s * C::X_BYTES), &tmX, full0 + 8 * s, kc, m0, pol_x);
+    }
+    flags[3] = i;
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(BM, NT);
+    int i = 0;
+    for (; i < nk; ++i) {
+      const int s = i % C::STAGES;
+      const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
+      if (!mbar_wait(full0 + 8 * s, ph, ep.err)) {
+        flags[2] = 1;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t aw = smem_u32(sW + s * C::W_BYTES);
+      const uint32_t ax = smem_u32(sX + s * C::X_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        mma_bf16(tmem, desc_sw128(aw + kk * 32), desc_sw128(ax + kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(empty0 + 8 * s);
+    }
+    flags[1] = i;
+    mma_commit(accum_bar);  // arrives once every MMA issued above has completed
+  }
+  __syncwarp();
+
+  // ---- drain the accumulator: thread t holds weight row n0 + t for all NT tokens
+  if (!mbar_wait(accum_bar, 0, ep.err)) flags[2] = 1;
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  __syncthreads();
+  float* tile = reinterpret_cast<float*>(smem);
+  const int f = threadIdx.x;
+  const bool failed = flags[2] != 0;
+  if (!failed) {
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+#pragma unroll 1
+    for (int c = 0; c < NT; c += 16) {
+      float v[16];
+      tmem_ld16(tmem + lane_base + (uint32_t)c, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) tile[(c + j) * C::TLD + f] = v[j];
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 2) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
+  }
+  if (failed) {
+    // Wait (bounded) for loads that were issued but never consumed, then leave.
+    if (threadIdx.x == 0) {
+      const int consumed = flags[1], issued = flags[3];
+      for (int i = consumed; i < issued; ++i) {
+        if (!mbar_wait(full0 + 8 * (i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u, ep.err)) break;
+      }
+    }
+    __syncthreads();
+    return;
+  }
+
+  const int rows = min(NT, M - m0);
+  if (splits > 1) {
+    const int tile_id = tile_m * gridDim.x + tile_n;
+    float* part = ws + (size_t)tile_id * splits * NT * BM;
+    float* mine = part + (size_t)split * NT * BM;
+    for (int r = 0; r < rows; ++r) mine[r * BM + f] = tile[r * C::TLD + f];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int prev = atomicAdd(counters + tile_id, 1);
+      flags[0] = (prev == splits - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!flags[0]) return;
+    __threadfence();
+    for (int r = 0; r < rows; ++r) {
+      float s = 0.f;
+      for (int q = 0; q < splits; ++q) {
+        const float p = (q == split) ? tile[r * C::TLD + f] : __ldcg(part + (size_t)q * NT * BM + r * BM + f);
+        s = (q == 0) ? p : s + p;
+      }
+      tile[r * C::TLD + f] = s;
+    }
+    if (threadIdx.x == 0) counters[tile_id] = 0;
+    __syncthreads();
+  }
+  epilogue_tile<__nv_bfloat16>(ep, tile, C::TLD, n0, m0, rows, M);
+}
+
+// ----------------------------------------------------------------------------
+// Host side
+// ----------------------------------------------------------------------------
+
+typedef CUresult (*PFN_encodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                      const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                      CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static PFN_encodeTiled_t encode_fn() {
+  static PFN_encodeTiled_t fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiled_t>(p);
+  }
+  return fn;
+}
+
+bool make_tmap_bf16(void* map_out, const void* ptr, long long rows, long long cols, int box_rows) {
+  PFN_encodeTiled_t enc = encode_fn();
+  if (!enc) return false;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (cols * 2) % 16 || cols % BK || box_rows > 256) return false;
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(reinterpret_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
+                   gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static_assert(sizeof(CUtensorMap) == TMAP_BYTES, "tensor map size");
+
+int tc_token_tile(int M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  if (M <= 128) return 128;
+  return 256;
+}
+
+int tc_splits(int N, int K, int sm_count) {
+  const int tiles = N / BM;
+  const int nkb = K / BK;
+  int s = (sm_count + tiles / 2) / tiles;
+  if (s < 1) s = 1;
+  if (s > 8) s = 8;
+  if (s > nkb / 4) s = nkb / 4 > 0 ? nkb / 4 : 1;
+  return s;
+}
+
+size_t tc_workspace_floats(int M, int N, int splits, int nt) {
+  if (splits <= 1) return 0;
+  const size_t tiles = (size_t)(N / BM) * ((M + nt - 1) / nt);
+  return tiles * splits * nt * BM;
+}
+size_t tc_counter_ints(int M, int N, int nt) { return (size_t)(N / BM) * ((M + nt - 1) / nt); }
+
+template <int NT>
+static cudaError_t launch_nt(const void* tmW, const void* tmX, int M, int N, int K, int splits, float* ws,
+                             int* counters, const EpiParams& ep, cudaStream_t st) {
+  using C = TcCfg<NT>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(N / BM, (M + NT - 1) / NT, splits);
+  gemm_tc_kernel<NT><<<grid, 128, C::SMEM, st>>>(*reinterpret_cast<const CUtensorMap*>(tmW),
+                                                  *reinterpret_cast<const CUtensorMap*>(tmX), M, N, K, splits, ws,
+                                                  counters, ep);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(const void* tmW, const void* tmX, int nt, int M, int N, int K, int splits, float* ws,
+                           int* counters, const EpiParams& ep, cudaStream_t st) {
+  if (N % BM || K % BK || M < 1 || splits < 1 || splits > K / BK) return cudaErrorInvalidValue;
+  switch (nt) {
+    case 16: return launch_nt<16>(tmW, tmX, M, N, K, splits, ws, counters, ep, st);
+    case 32: return launch_nt<32>(tmW, tmX, M, N, K, splits, ws, counters, ep, st);
+    case 64: return launch_nt<64>(tmW, tmX, M, N, K, splits, ws, counters, ep, st);
+    case 128: return launch_nt<128>(tmW, tmX, M, N, K, splits, ws, counters, ep, st);
+    case 256: return launch_nt<256>(tmW, tmX, M, N, K, splits, ws, counters, ep, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dfk

@@ -1,0 +1,78 @@
+// Internal launch interface between the engine and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dfk {
+
+constexpr int TMAP_BYTES = 128;  // sizeof(CUtensorMap)
+
+// ---- tcgen05 GEMM (gemm_tc.cu)
+bool make_tmap_bf16(void* map_out, const void* ptr, long long rows, long long cols, int box_rows);
+int tc_token_tile(int M);
+int tc_splits(int N, int K, int sm_count);
+size_t tc_workspace_floats(int M, int N, int splits, int nt);
+size_t tc_counter_ints(int M, int N, int nt);
+cudaError_t launch_gemm_tc(const void* tmW, const void* tmX, int nt, int M, int N, int K, int splits, float* ws,
+                           int* counters, const EpiParams& ep, cudaStream_t st);
+
+// ---- fp32 SIMT GEMM + epilogue (gemm_simt.cu)
+cudaError_t launch_gemm_f32(const float* x, const float* w, float* tmp, int M, int N, int K, const EpiParams& ep,
+                            cudaStream_t st);
+
+// ---- attention (attention.cu)
+struct AttnParams {
+  const void* q;          // [M][Hq*hd]
+  void* out;              // [M][Hq*hd]
+  int M;                  // rows
+  int rows_per_seq;       // rows of one sequence (block size, or a prefill chunk)
+  int n_seqs;             // sequences in this pass (rows are sequence-major)
+  int Hq, Hkv, hd;
+  const int* row_pos;     // [M] absolute positions
+  const int* row_seq;     // [M] sequence slots
+  int causal;             // 1: keys [0, pos]; 0: context [0, pos - slot) plus the whole block
+  const void* cache;      // paged cache of this layer: [page][k|v][Hkv][page_tokens][hd]
+  const int* page_table;  // [slot][pt_stride]
+  int pt_stride, page_tokens, n_pages;
+  const void* blk;        // block rows [k|v][Hkv][rows_cap][hd] (causal == 0)
+  int rows_cap;
+  int chunk;              // keys per split-KV chunk
+  int n_chunk_slots;      // chunk slots per (row, head) in the partial buffers
+  int grid_chunks;        // context chunks launched
+  float* part_acc;        // [M][Hq][n_chunk_slots][hd]
+  float2* part_ml;        // [M][Hq][n_chunk_slots]
+  float scale_log2;       // log2(e) / sqrt(hd)
+  int* err;
+};
+cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st);
+
+// ---- small kernels (misc.cu)
+cudaError_t launch_embed(const void* embed, bool bf16, const int* tok, float* h, int M, int d, int vocab, int* err,
+                         cudaStream_t st);
+// out[m] = T(h[m] * rsqrt(mean(h[m]^2) + eps) * gain); optionally taps[m][tap][:] = T(h[m]).
+// rows with row_pos[m] < 0 (if row_pos given) are skipped.
+cudaError_t launch_rmsnorm(const float* h, int ldh, const float* gain, void* out, int ldo, bool bf16, int M, int d,
+                           float eps, void* taps, int tap_index, const int* row_pos, cudaStream_t st);
+cudaError_t launch_fill_u64(unsigned long long* p, unsigned long long v, int n, cudaStream_t st);
+cudaError_t launch_argmax_finalize(const unsigned long long* amax, int* ids, int M, cudaStream_t st);
+// Block rows for drafting (verify = 0: [bonus, MASK...]) or verification (verify = 1: [bonus, drafts...]);
+// drafts are per slot: drafts[slot][B-1].
+cudaError_t launch_prep_block(const int* batch_slots, int nseq, int B, const int* bonus, const int* bonus_pos,
+                              const int* drafts, int mask_id, int verify, int* row_tok, int* row_pos, int* row_seq,
+                              cudaStream_t st);
+// Greedy acceptance: one warp per sequence.
+cudaError_t launch_accept(const int* batch_slots, int nseq, int B, const int* row_tok, const int* ids, int* bonus,
+                          int* bonus_pos, int* acc_out, int* n_out, int* inj_pos, cudaStream_t st);
+// Drafts for the next verification, per slot: drafts[slot_b][i] = ids[b*B + 1 + i].
+cudaError_t launch_collect_drafts(const int* ids, int nseq, int B, const int* batch_slots, int* drafts,
+                                  cudaStream_t st);
+// One greedy decode step: out[b][t] = ids[b]; row_tok[b] = ids[b]; row_pos[b] += 1.
+cudaError_t launch_greedy_step(const int* ids, int nseq, int t, int n_new, int* out, int* row_tok, int* row_pos,
+                               cudaStream_t st);
+cudaError_t launch_copy_row_f32(const float* src, int lds, float* dst, int ldd, int rows, int cols, cudaStream_t st);
+
+}  // namespace dfk

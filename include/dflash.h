@@ -1,0 +1,229 @@
+/*
+ * dflash.h - C ABI of the GB300 DFlash draft-and-verify engine.
+ *
+ * The engine runs DFlash speculative decoding on one GPU: a target decoder
+ * (RMSNorm, RoPE, grouped-query attention, SwiGLU) verifies blocks that a
+ * small block-diffusion drafter proposes in one forward pass.  The drafter
+ * is conditioned on hidden states of five target layers, fused by a light FC
+ * + RMSNorm and injected as K/V into every drafter layer.
+ *
+ * Sources (web pages, by title and section):
+ *   [ARCH]  "DFlash 的架构密码——扩散模型如何「寄生」在自回归模型上"
+ *           (zhichai.net): 第一层 Feature Fusion, 第二层 KV Injection,
+ *           第三层 Block Diffusion, 训练策略 (bonus-token anchors, shared
+ *           embedding & LM head), 技术细节补充 (提取层数, 投影层, 稀疏注意力训练).
+ *   [ABS]   "DFlash：基于块扩散的闪存推测解码方法" (ai-stack.site): 摘要
+ *           (single forward pass, feature conditioning, lossless);
+ *           实践 2 (block verification, keep up to the last correct token);
+ *           实践 3 (the drafter never modifies the target's KV cache);
+ *           实践 5 (pre-allocated activation pool, verification fused on the GPU).
+ *   [PRESS] DFlash press repost (zaocj.com): a single forward pass with
+ *           bidirectional attention fills the 8-16 slots after the verified token.
+ *
+ * Conventions shared by every call
+ *   - All sizes are explicit int32/int64.  Token ids are int32.
+ *   - Weights are passed as DEVICE pointers in the canonical order given by
+ *     df_weight_info(); df_init copies them into a library-owned arena, so the
+ *     caller may free its copies once df_init returns.
+ *   - Every other pointer named *_host is caller-owned HOST memory; pointers
+ *     named *_dev are caller-owned DEVICE memory.
+ *   - All GPU work is ordered on the stream passed to df_init (a cudaStream_t,
+ *     or NULL for the legacy default stream).  Calls that return host-visible
+ *     results synchronise that stream before returning.
+ *   - Errors: every call returns a df_status; df_last_error() gives a message.
+ *     Kernels report device-side failures (a bounded wait that ran out, an
+ *     index outside its buffer) in a sticky error word; once set, later calls
+ *     on the handle return DF_ECUDA or DF_ETIMEOUT.
+ *   - The library never prints, never aborts and never falls back to the CPU.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct df_handle df_handle; /* opaque; owned by the library */
+
+typedef enum {
+  DF_OK = 0,
+  DF_EINVAL = 1,   /* bad argument or unsupported shape */
+  DF_ENOMEM = 2,   /* device allocation or page pool exhausted */
+  DF_ECUDA = 3,    /* a CUDA call failed or a kernel flagged an error */
+  DF_ETIMEOUT = 4, /* a bounded device-side wait ran out */
+  DF_ESTATE = 5    /* call made in the wrong sequence state */
+} df_status;
+
+typedef enum { DF_FP32 = 0, DF_BF16 = 1 } df_dtype;
+
+/* Model and capacity description.
+ *   n_layers .. vocab : target decoder shape (head_dim 64 or 128).
+ *   draft_layers      : drafter depth (same width as the target).
+ *   block_size B      : slots per draft block, the bonus slot included, so a
+ *                       cycle proposes B-1 drafts ([PRESS]: 8-16 slots).
+ *   feat_layers[5]    : 1-based target layers whose outputs are fused; fill
+ *                       with df_default_feat_layers() ([ARCH] 提取层数).
+ *   max_batch         : sequences held at once; max_ctx: positions per sequence.
+ *   page_tokens       : tokens per KV page (16).
+ *   dtype             : DF_FP32 (plain fp32 FMA everywhere) or DF_BF16 (bf16
+ *                       weights and GEMM operands, fp32 accumulation,
+ *                       fp32 residual stream).
+ *   mask_token_id     : id embedded into the drafter's masked slots (vocab-1).
+ */
+typedef struct {
+  int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim, d_ffn, vocab;
+  int32_t draft_layers, block_size;
+  int32_t feat_layers[5];
+  int32_t max_batch, max_ctx, page_tokens;
+  int32_t dtype;
+  int32_t mask_token_id;
+  float rms_eps, rope_theta;
+} df_config;
+
+/* Per-handle counters.  k = accepted drafts in a cycle; a cycle emits k+1
+ * tokens, so the mean accepted length is (accepted_drafts + cycles) / cycles. */
+typedef struct {
+  int64_t cycles;
+  int64_t accepted_drafts;
+  int64_t emitted_tokens;
+  int64_t accept_hist[65]; /* histogram of k, k <= 64 */
+  double draft_us;         /* summed device time of draft passes (CUDA events) */
+  double verify_us;        /* summed device time of verify+accept+inject */
+  double prefill_us;
+} df_stats;
+
+/* Five feature layers sampled uniformly from layer 2 to the third-from-last
+ * ([ARCH] 技术细节补充, 提取层数): s_i = 2 + round_half_up(i (L-4) / 4), 1-based.
+ * DF_EINVAL if n_layers < 8 (five distinct layers need L >= 8). */
+df_status df_default_feat_layers(int32_t n_layers, int32_t out[5]);
+
+/* Number of weight tensors df_init expects for cfg. */
+int32_t df_num_weights(const df_config* cfg);
+
+/* Canonical weight list.  For index i fills a NUL-terminated name (<= 31
+ * chars), the number of dims (1 or 2) and the shape.  Matrices are
+ * [out_features, in_features] row-major; vectors are RMSNorm gains.  Order:
+ * embed[V,d]; per target layer: attn_norm, wq, wk, wv, wo, mlp_norm, w_gate,
+ * w_up, w_down; final_norm; lm_head[V,d]; fc[d,5d]; fc_norm; per drafter
+ * layer the same nine; d_final_norm.  The drafter has no embedding or LM head
+ * of its own: it reuses the target's ([ARCH] Shared Embedding & LM Head). */
+df_status df_weight_info(const df_config* cfg, int32_t index, char name[32], int32_t* ndim, int64_t shape[2]);
+
+/* Create an engine.  weights: n_weights DEVICE pointers in canonical order,
+ * each dense row-major in cfg->dtype (fp32, or bf16 bit patterns).  stream: a
+ * cudaStream_t (may be NULL).  Allocates the weight arena, both paged KV caches
+ * (target, and the drafter's injected context cache, kept apart per [ABS]
+ * 实践 3) and every activation buffer up front ([ABS] 实践 5).  *out receives
+ * the handle; on failure *out is NULL and the status says why. */
+df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_weights, void* stream,
+                  df_handle** out);
+
+/* Prefill sequence slot seq (0 <= seq < max_batch, slot must be empty):
+ * run the target over prompt_host[0..len), write its KV pages, take the argmax
+ * at the last position as the first bonus token (*bonus_out), fuse the prompt's
+ * feature-layer states and inject them into the drafter's context cache
+ * ([ARCH] 第一层: after the target's prefill). */
+df_status df_prefill(df_handle* h, int32_t seq, const int32_t* prompt_host, int32_t len, int32_t* bonus_out);
+
+/* Draft one block for each listed sequence: one drafter forward pass over
+ * [bonus, MASK x (B-1)] at the bonus position, attending to the injected
+ * context and bidirectionally inside the block, nothing across blocks
+ * ([ARCH] 第三层, 稀疏注意力训练).  Slot i (1..B-1) gives draft i by argmax
+ * through the shared LM head.  drafts_host: [nseq][B-1] (may be NULL). */
+df_status df_draft_block(df_handle* h, const int32_t* seqs_host, int32_t nseq, int32_t* drafts_host);
+
+/* Verify and accept.  The target runs once over [bonus, d_1..d_{B-1}] for each
+ * sequence; k = the longest prefix with d_i equal to the target's greedy token
+ * before it; the cycle emits d_1..d_k and the target's token after them (the
+ * next bonus), rolls the target KV cache back to the verified length and
+ * injects the fused features of the k+1 verified positions into the drafter's
+ * context cache ([ABS] 实践 2; [ARCH] bonus-token anchors).
+ * drafts_host: [nseq][B-1] drafts to verify, or NULL to verify the drafts of
+ * the last df_draft_block for these sequences.
+ * accepted_host: [nseq][B] emitted tokens (first n_host[i] valid);
+ * n_host: [nseq] = k+1.  Either output may be NULL. */
+df_status df_verify_accept(df_handle* h, const int32_t* seqs_host, int32_t nseq, const int32_t* drafts_host,
+                           int32_t* accepted_host, int32_t* n_host);
+
+/* Whole speculative generation for nseq prompts (packed back to back in
+ * prompts_host, lengths lens_host): prefill each into slots 0..nseq-1, then
+ * draft/verify cycles until n_new tokens per sequence; the last cycle is
+ * truncated.  out_host: [nseq][n_new].  stats (may be NULL) receives this
+ * call's counters.  Slots are released at the end. */
+df_status df_generate(df_handle* h, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,
+                      int32_t n_new, int32_t* out_host, df_stats* stats);
+
+/* Plain token-by-token greedy decoding of the target on the GPU, with the
+ * same kernels as verification: the lossless reference the speculative
+ * output must equal bit for bit.  Same arguments as df_generate. */
+df_status df_greedy_reference(df_handle* h, const int32_t* prompts_host, const int32_t* lens_host,
+                              int32_t nseq, int32_t n_new, int32_t* out_host);
+
+/* Release a sequence slot (its pages return to the pool). */
+df_status df_reset_seq(df_handle* h, int32_t seq);
+
+/* Counters accumulated since df_init or the last df_reset_stats. */
+df_status df_get_stats(const df_handle* h, df_stats* out);
+df_status df_reset_stats(df_handle* h);
+
+/* Current verified length and bonus token of a slot (host mirror). */
+df_status df_seq_info(const df_handle* h, int32_t seq, int32_t* length, int32_t* bonus);
+
+void df_destroy(df_handle* h);
+const char* df_last_error(const df_handle* h);
+
+/* ------------------------------------------------------------------------
+ * Inspection (tests).  df_debug_read copies a buffer of the last pass to
+ * host memory as float32 (bf16 widened exactly):
+ *   DF_DBG_TAPS          [rows][5][d]  feature-layer outputs of the last target pass
+ *   DF_DBG_LOGITS        [rows][V]     logits of the last target pass (needs debug on)
+ *   DF_DBG_DRAFT_LOGITS  [rows][V]     logits of the last drafter pass (needs debug on)
+ *   DF_DBG_DRAFT_HIDDEN  [rows][d]     drafter output before its final norm
+ *   DF_DBG_CTX           [rows][d]     fused context features of the last injection
+ *   DF_DBG_HIDDEN        [rows][d]     target output before the final norm
+ * rows is the row count of that pass (*rows_out).  With debug on, the fused
+ * LM-head argmax also stores the logits it reduces; off by default.
+ * ------------------------------------------------------------------------ */
+enum {
+  DF_DBG_TAPS = 1,
+  DF_DBG_LOGITS = 2,
+  DF_DBG_DRAFT_LOGITS = 3,
+  DF_DBG_DRAFT_HIDDEN = 4,
+  DF_DBG_CTX = 5,
+  DF_DBG_HIDDEN = 6
+};
+df_status df_debug_enable(df_handle* h, int32_t on);
+df_status df_debug_read(df_handle* h, int32_t what, float* out_host, int64_t max_floats, int32_t* rows_out);
+
+/* Device address of a weight as the engine holds it (embed, lm_head, ...):
+ * lets a test confirm that the drafter and the target share one embedding
+ * and one LM head.  which: 0 target embedding, 1 drafter embedding, 2 target
+ * LM head, 3 drafter LM head. */
+df_status df_debug_weight_ptr(const df_handle* h, int32_t which, uint64_t* addr);
+
+/* ------------------------------------------------------------------------
+ * Single operations on caller device buffers (per-kernel tests, microbench).
+ * All pointers are *_dev DEVICE pointers; dtype follows the argument's type.
+ * Each call is stream-ordered on `stream` and does not synchronise.
+ * ------------------------------------------------------------------------ */
+
+/* y[M][N] = x[M][K] . w[N][K]^T, bf16 operands, fp32 accumulation and output
+ * (the tcgen05 GEMM the engine uses; fixed K order, so each output does not
+ * depend on M).  N % 128 == 0, K % 64 == 0, M >= 1, 16-byte aligned pointers.
+ * splits: 0 = the engine's choice for (N, K), else the split-K count.
+ * token_tile: 0 = the engine's choice for M, else one of 16,32,64,128,256. */
+df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, int32_t M, int32_t N, int32_t K,
+                          int32_t splits, int32_t token_tile, void* stream);
+
+/* ids[m] = argmax_v (x[m] . w_lm[v]) over V rows of w_lm (bf16 [V][K]),
+ * fp32 logits, lowest index on ties; logits are never written.  V % 128 == 0. */
+df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32_t* ids_dev, int32_t M, int32_t V,
+                                   int32_t K, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

@@ -205,3 +205,23 @@ def make_hidden(rows: int, cols: int, seed: int = HIDDEN_SEED, stream: int = 0) 
     """N(0, 1) float32 rows (stand-ins for tapped hidden states)."""
     g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, stream])))
     return g.standard_normal((rows, cols), dtype=np.float32)
+
+
+def make_normal(shape: Tuple[int, ...], std: float, seed: int, stream: int = 0,
+                threads: int | None = None) -> np.ndarray:
+    """N(0, std) float32 array drawn in BLOCK-sized pieces, block b from
+    PCG64(SeedSequence([seed, stream, b])); the result does not depend on threads."""
+    n = int(np.prod(shape))
+    nblk = (n + BLOCK - 1) // BLOCK
+    sizes = [min(BLOCK, n - b * BLOCK) for b in range(nblk)]
+
+    def one(b):
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, stream, b])))
+        out = g.standard_normal(sizes[b], dtype=np.float32)
+        out *= np.float32(std)
+        return out
+
+    threads = threads or min(16, os.cpu_count() or 1)
+    with ThreadPoolExecutor(threads) as pool:
+        parts = list(pool.map(one, range(nblk)))
+    return np.concatenate(parts).reshape(shape) if nblk > 1 else parts[0].reshape(shape)

@@ -1,0 +1,90 @@
+"""The C ABI library: builds, loads, exports every declared symbol, and its
+host-only calls agree with the pages' closed forms.  No GPU is touched."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synthetic as syn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dflash.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__ as g
+    g.build()
+    import block_diffusion_speculative_layer_gb300 as dfl
+    return dfl.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(df_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_cycle_calls():
+    syms = declared_symbols()
+    for s in ["df_init", "df_prefill", "df_draft_block", "df_verify_accept", "df_generate", "df_greedy_reference",
+              "df_reset_seq", "df_destroy", "df_last_error", "df_default_feat_layers"]:
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [s for s in declared_symbols() if not hasattr(L, s)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    import block_diffusion_speculative_layer_gb300 as dfl
+    assert sorted(dfl.EXPORTED) == declared_symbols()
+
+
+def test_feature_layers_from_library(L):
+    import block_diffusion_speculative_layer_gb300 as dfl
+    golden = os.path.join(ROOT, "tests", "golden", "feature_layers.txt")
+    for line in open(golden):
+        if line.strip() and not line.startswith("#"):
+            v = [int(x) for x in line.split()]
+            assert dfl.default_feat_layers(v[0]) == v[1:]
+    out = (ctypes.c_int32 * 5)()
+    assert L.df_default_feat_layers(7, out) == dfl.DF_EINVAL
+
+
+@pytest.mark.parametrize("shape", [syn.TINY, syn.QWEN3_8B, syn.DENSE_27B])
+def test_weight_list_matches_generator(L, shape):
+    import block_diffusion_speculative_layer_gb300 as dfl
+    cfg = dfl.make_config(shape, 1, 1024)
+    assert dfl.weight_info(cfg) == syn.weight_specs(shape)
+
+
+def test_init_rejects_bad_config_without_gpu(L):
+    import block_diffusion_speculative_layer_gb300 as dfl
+    cfg = dfl.make_config(syn.TINY, 1, 256)
+    cfg.head_dim = 96
+    h = ctypes.c_void_p()
+    ptrs = (ctypes.c_void_p * 1)()
+    assert L.df_init(ctypes.byref(cfg), ptrs, 1, None, ctypes.byref(h)) == dfl.DF_EINVAL
+    assert not h.value
+    cfg = dfl.make_config(syn.TINY, 1, 256)
+    cfg.block_size = 1
+    assert L.df_init(ctypes.byref(cfg), ptrs, 1, None, ctypes.byref(h)) == dfl.DF_EINVAL
+
+
+def test_null_handle_calls_fail_cleanly(L):
+    import block_diffusion_speculative_layer_gb300 as dfl
+    assert L.df_prefill(None, 0, None, 0, None) == dfl.DF_EINVAL
+    assert L.df_last_error(None) == b"null handle"
+    L.df_destroy(None)
+
+
+def test_parameter_counts_match_pages_sizing():
+    # The 27B-class drafter (5 layers of width 5120, no own embedding/LM head)
+    # has about 1.78B parameters: the "about 2B drafter" sizing of the pages.
+    s = syn.DENSE_27B
+    n = sum(int(np.prod(shp)) for name, shp in syn.weight_specs(s) if name.startswith("d") or name.startswith("fc"))
+    assert 1.7e9 < n < 2.0e9

@@ -1,0 +1,154 @@
+"""bf16 engine (tcgen05 GEMMs) through the C ABI.
+
+Two bars: (1) losslessness: the speculative stream equals the GPU's own
+token-by-token greedy decode bit for bit; (2) parity with the float64 oracle
+under teacher forcing (the oracle is fed the GPU's token stream): for each
+tensor, max|gpu - oracle| / max|oracle| <= 2e-2.
+"""
+import numpy as np
+import pytest
+
+import synthetic as syn
+from oracle import dflash_oracle as O
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+TOL = 2e-2
+
+# Small grouped-query model: 4 query heads per KV head as in the Qwen3-8B shape.
+SMALL = syn.ModelShape("small-bf16", n_layers=8, d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                       d_ffn=2048, vocab=4096, draft_layers=2, block_size=16, dtype="bf16")
+# Qwen3-8B width, vocabulary and heads at reduced depth (8 target layers, 1 drafter layer).
+WIDE = syn.QWEN3_8B.replace(name="qwen3-8b-width-8-layers", n_layers=8, draft_layers=1)
+
+
+def rel_err(gpu, ref):
+    return float(np.abs(gpu.astype(np.float64) - ref).max() / np.abs(ref).max())
+
+
+@pytest.fixture(scope="module")
+def dfl():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import __graft_entry__ as g
+    g.build()
+    import block_diffusion_speculative_layer_gb300 as m
+    return m
+
+
+class Setup:
+    def __init__(self, dfl, shape, gain_std, max_batch, max_ctx):
+        self.shape = shape
+        self.w = syn.make_weights(shape, gain_std=gain_std)
+        self.model = O.Model(O.Weights(self.w, cache=True), shape)
+        self.eng = dfl.Engine(shape, self.w, max_batch=max_batch, max_ctx=max_ctx)
+
+
+@pytest.fixture(scope="module")
+def small(dfl):
+    s = Setup(dfl, SMALL, 0.1, 4, 512)
+    yield s
+    s.eng.close()
+
+
+@pytest.fixture(scope="module")
+def wide(dfl):
+    s = Setup(dfl, WIDE, 0.0, 1, 256)
+    yield s
+    s.eng.close()
+
+
+# ---------------------------------------------------------------- losslessness
+
+def test_lossless_single(small):
+    p = syn.make_prompt(SMALL, 64)
+    spec, stats = small.eng.generate([p], 96)
+    greedy = small.eng.greedy_reference([p], 96)
+    np.testing.assert_array_equal(spec, greedy)
+    assert stats["cycles"] >= 1
+
+
+def test_lossless_batch_ragged_prompts(small):
+    prompts = [syn.make_prompt(SMALL, L, stream=s) for s, L in [(1, 17), (2, 64), (3, 5), (4, 100)]]
+    spec, _ = small.eng.generate(prompts, 50)
+    greedy = small.eng.greedy_reference(prompts, 50)
+    np.testing.assert_array_equal(spec, greedy)
+    # and each sequence alone gives the same stream as in the batch
+    for i, p in enumerate(prompts[:2]):
+        alone, _ = small.eng.generate([p], 50)
+        np.testing.assert_array_equal(alone[0], spec[i])
+
+
+def test_forced_acceptance_accepts_whole_blocks(small):
+    p = syn.make_prompt(SMALL, 40, stream=7)
+    B = SMALL.block_size
+    g = small.eng.greedy_reference([p], 4 * B + 1)[0]
+    small.eng.prefill(0, p)
+    try:
+        for c in range(4):
+            acc, n = small.eng.verify_accept([0], g[c * B + 1:(c + 1) * B])
+            assert n[0] == B
+            np.testing.assert_array_equal(acc[0], g[c * B + 1:(c + 1) * B + 1])
+    finally:
+        small.eng.reset_seq(0)
+
+
+# ---------------------------------------------------------------- parity under teacher forcing
+
+def _verify_parity(dfl, s, prompt):
+    eng, model, shape = s.eng, s.model, s.shape
+    B = shape.block_size
+    g = eng.greedy_reference([prompt], B + 1)[0]
+    eng.debug(True)
+    try:
+        bonus = eng.prefill(0, prompt)
+        assert bonus == g[0]
+        ctx_gpu = eng.debug_read(dfl.DF_DBG_CTX)           # last prefill chunk's fused context rows
+        eng.draft_block([0])
+        dh_gpu = eng.debug_read(dfl.DF_DBG_DRAFT_HIDDEN)
+        dl_gpu = eng.debug_read(dfl.DF_DBG_DRAFT_LOGITS)
+        acc, n = eng.verify_accept([0], g[1:B])             # teacher-forced block
+        assert n[0] == B
+        taps_gpu = eng.debug_read(dfl.DF_DBG_TAPS)
+        logits_gpu = eng.debug_read(dfl.DF_DBG_LOGITS)
+        hid_gpu = eng.debug_read(dfl.DF_DBG_HIDDEN)
+    finally:
+        eng.reset_seq(0)
+        eng.debug(False)
+
+    P = len(prompt)
+    tokens = np.concatenate([prompt, g[:B]])
+    cache = O.KVCache(shape.n_layers, shape.n_kv_heads, shape.head_dim)
+    pre = O.target_forward(model.W, shape, prompt, cache)
+    ver = O.target_forward(model.W, shape, tokens[P:], cache)
+    # fused context of the prompt
+    ctx = O.fuse_features(model.W, shape, pre.taps)
+    assert rel_err(ctx_gpu, ctx[-len(ctx_gpu):]) <= TOL
+    # drafter pass at the first bonus token
+    cc = O.ContextCache(shape.draft_layers, shape.n_kv_heads, shape.head_dim)
+    O.inject_kv(model.W, shape, cc, ctx)
+    dp = O.draft_blocks(model.W, shape, cc, [(int(g[0]), P)])
+    assert rel_err(dh_gpu, dp.hidden) <= TOL
+    assert rel_err(dl_gpu, dp.logits) <= TOL
+    # verification pass
+    assert rel_err(taps_gpu.reshape(B, 5, -1), ver.taps) <= TOL
+    assert rel_err(hid_gpu, ver.hidden[-1]) <= TOL
+    assert rel_err(logits_gpu, ver.logits) <= TOL
+    return dp
+
+
+def test_small_parity_teacher_forced(dfl, small):
+    _verify_parity(dfl, small, syn.make_prompt(SMALL, 48, stream=3))
+
+
+def test_wide_parity_teacher_forced(dfl, wide):
+    # full width, full vocabulary (151936), GQA 32/8 x 128: every kernel at the
+    # Qwen3-8B shape, against the oracle
+    _verify_parity(dfl, wide, syn.make_prompt(WIDE, 40, stream=4))
+
+
+def test_wide_lossless(wide):
+    p = syn.make_prompt(WIDE, 64, stream=5)
+    spec, _ = wide.eng.generate([p], 40)
+    np.testing.assert_array_equal(spec, wide.eng.greedy_reference([p], 40))
