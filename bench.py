@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Decoded tokens/s of the DFlash draft-and-verify cycle on one GB300.
+
+Workload: the Qwen3-8B-shaped bf16 target (36 layers, d=4096, GQA 32/8 x 128,
+SwiGLU 12288, vocab 151936) with a 5-layer drafter of the same width sharing
+the embedding and LM head; block 16; batch 1; a 512-token uniform-random
+prompt; 512 new tokens, greedy.  Weights are random N(0, 0.02) (seeded,
+synthetic): the drafter is untrained, so the measured mean accepted length
+is about 1; a second, labelled run forces the drafts to the target's own
+greedy continuation (accepted length = block size) to show the engine's
+ceiling.
+
+One step = one whole generation through the C ABI (df_generate): prefill,
+then draft -> verify -> accept -> inject cycles until 512 new tokens.  The
+weights (18.5 GB) are larger than L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (float64 numpy) on the host cores on a
+bounded sample of the same workload (one decode cycle's worth of layers,
+scaled to a cycle).  Under torchrun each rank runs an independent replica
+(the cycle is one serial chain per sequence: replicas only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decoded tokens/s (Qwen3-8B shape, bs1) & draft+verify cycle us vs roofline"
+UNIT = "tokens/s"
+WORKLOAD = "qwen3-8b-shape bf16, drafter 5 layers, block 16, bs1, prompt 512, 512 new tokens, greedy"
+
+# DRAM bytes per launch of the decode GEMM class measured by ncu on a given
+# kernel source; reported only while the source hash still matches.
+NCU_TRAFFIC = {"source_sha": None, "bytes_per_gemm_launch_avg": None}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "block_diffusion_speculative_layer_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- CPU oracle sample
+
+_SAMPLE_WEIGHTS = {}
+
+
+def oracle_cycle_sample(shape, prompt_len: int, tau: float, repeats: int = 1):
+    """Time the float64 oracle on one decode cycle's worth of work, on a sample of layers.
+
+    Measured: one target layer over a 16-row block with a 512+16 key cache,
+    one drafter layer over a 16-row block with 512 context keys, the shared LM
+    head over 31 rows (16 verify + 15 draft), fusion of one row and injection
+    of one row into one drafter layer.  Scaled: cycle = 36 x target layer +
+    5 x (drafter layer + injection into one layer) + LM head + fusion;
+    tokens/s = tau / cycle.
+    """
+    import numpy as np
+
+    import synthetic as syn
+    from oracle import dflash_oracle as O
+
+    key = shape.name
+    if key not in _SAMPLE_WEIGHTS:
+        specs = syn.weight_specs(shape)
+        need = {"t0.", "d0.", "fc", "fc_norm", "lm_head", "final_norm", "d_final_norm"}
+        raw = {}
+        for i, (name, shp) in enumerate(specs):
+            if any(name.startswith(p) for p in need):
+                raw[name] = syn.draw_weight(shape, i, name, shp)
+        W = O.Weights(raw, cache=True)
+        for name in list(raw):
+            W[name]  # widen once, outside the timed part
+        _SAMPLE_WEIGHTS[key] = W
+    W = _SAMPLE_WEIGHTS[key]
+    B = shape.block_size
+    rng = np.random.default_rng(0)
+    C = prompt_len
+    h = rng.standard_normal((B, shape.d_model)) * 0.02
+    kc = rng.standard_normal((C, shape.n_kv_heads, shape.head_dim))
+    vc = rng.standard_normal((C, shape.n_kv_heads, shape.head_dim))
+    pos = np.arange(C, C + B)
+
+    def target_layer():
+        def kv(k, v):
+            keys = np.concatenate([kc, k])
+            vals = np.concatenate([vc, v])
+            vis = np.arange(C + B)[None, :] <= pos[:, None]
+            return keys, vals, vis
+        return O.decoder_layer(W, "t0", shape, h, pos, kv)
+
+    def drafter_layer():
+        def kv(k, v):
+            keys = np.concatenate([kc, k])
+            vals = np.concatenate([vc, v])
+            return keys, vals, np.ones((B, C + B), bool)
+        return O.decoder_layer(W, "d0", shape, h, pos, kv)
+
+    def lm_head():
+        hf = O.rms_norm(np.concatenate([h, h[1:]]), W["final_norm"], shape.rms_eps)
+        return O.argmax_lowest(hf @ W["lm_head"].T)
+
+    ctx1 = O.fuse_features(W, shape, rng.standard_normal((1, 5, shape.d_model)))
+
+    def fuse():
+        return O.fuse_features(W, shape, rng.standard_normal((1, 5, shape.d_model)))
+
+    def inject_one_layer():
+        cc = O.ContextCache(1, shape.n_kv_heads, shape.head_dim)
+        O.inject_kv(W, shape.replace(draft_layers=1), cc, ctx1)
+        return cc
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        for _ in range(repeats):
+            fn()
+        return (time.perf_counter() - t0) / repeats
+
+    tl, dl, lm = timed(target_layer), timed(drafter_layer), timed(lm_head)
+    fu, ij = timed(fuse), timed(inject_one_layer)
+    cycle = shape.n_layers * tl + shape.draft_layers * (dl + ij) + lm + fu
+    return {"value": tau / cycle, "cycle_s": cycle, "target_layer_s": tl, "drafter_layer_s": dl, "lm_head_s": lm,
+            "fuse_s": fu, "inject_layer_s": ij, "cores": os.cpu_count()}
+
+
+# ---------------------------------------------------------------------------- arms
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    import synthetic as syn
+    shape = syn.QWEN3_8B
+    tau = 1.0
+    for _ in range(args.warmup):
+        oracle_cycle_sample(shape, args.prompt_len, tau)
+    vals, samples = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = oracle_cycle_sample(shape, args.prompt_len, tau)
+        samples.append(r)
+        vals.append(r["value"])
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    sample = ("one decode cycle sampled: 1 of 36 target layers (16-row block, 512-key cache), 1 of 5 drafter "
+              "layers, the LM head over 31 rows, one fusion row and one injection layer; scaled to 36+5 layers; "
+              "tau=1")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wall / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "oracle": "float64 numpy, CPU",
+                   "cycle_s": statistics.mean([s["cycle_s"] for s in samples])},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    import block_diffusion_speculative_layer_gb300 as dfl
+    import synthetic as syn
+    from block_diffusion_speculative_layer_gb300 import build as _b
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    _b.build()
+
+    shape = syn.QWEN3_8B
+    B, P, n_new = shape.block_size, args.prompt_len, args.new_tokens
+    max_ctx = ((P + n_new + 2 * B + 63) // 64) * 64
+    t0 = time.time()
+    eng = dfl.Engine(shape, syn.iter_weights(shape), max_batch=1, max_ctx=max_ctx)
+    torch.cuda.empty_cache()
+    setup_s = time.time() - t0
+    stream = eng.stream
+    prompt_t = torch.from_numpy(syn.make_prompt(shape, P, stream=rank)).pin_memory()
+    prompt = prompt_t.numpy()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        eng.generate([prompt], n_new)
+
+    # ---- timed region: K whole generations, device time from CUDA events on the engine's stream
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    eng.reset_stats()
+    e0.record(stream)
+    for _ in range(args.steps):
+        eng.generate([prompt], n_new)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    st = eng.stats()
+    secs = e0.elapsed_time(e1) / 1000.0
+    if dist is not None:
+        t = torch.tensor([secs], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        secs = float(t.item())
+    value = world * args.steps * n_new / secs
+    cycles = max(st["cycles"], 1)
+    tau = (st["accepted_drafts"] + st["cycles"]) / cycles
+
+    # ---- end to end: the same call with host buffers, wall clock, copies inside
+    out_pinned = torch.empty((1, n_new), dtype=torch.int32).pin_memory()
+    eng.reset_stats()
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for _ in range(args.steps):
+        out, _ = eng.generate([prompt], n_new)
+        out_pinned.numpy()[:] = out
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - w0
+    st_e2e = eng.stats()
+
+    # ---- kernel-class device times (events around every launch) for the roofline
+    eng.profile(True)
+    eng.generate([prompt], n_new)
+    prof = eng.profile_read()
+    eng.profile(False)
+    peaks = measured_peaks()
+    g = prof["gemm"]
+    gemm_gbs = g["bytes"] / (g["us"] * 1e-6) / 1e9 if g["us"] > 0 else None
+    traffic = None
+    if NCU_TRAFFIC["source_sha"] == kernel_source_sha() and NCU_TRAFFIC["bytes_per_gemm_launch_avg"]:
+        traffic = NCU_TRAFFIC["bytes_per_gemm_launch_avg"]
+    roofline = {
+        "bound": "hbm", "kernel": "gemm_tc_kernel (tcgen05, weight-streaming; every GEMM launch of one generation)",
+        "achieved": gemm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": (gemm_gbs / peaks["hbm_gbs"]) if gemm_gbs else None, "traffic": traffic,
+        "peak_source": peaks["source"], "algorithmic_bytes_per_launch": g["bytes"] / max(g["launches"], 1),
+        "avg_launch_us": g["us"] / max(g["launches"], 1),
+    }
+    breakdown = {k: {"launches": v["launches"], "ms": v["us"] / 1000.0,
+                     "GB/s": (v["bytes"] / (v["us"] * 1e-6) / 1e9) if v["us"] > 0 and v["bytes"] > 0 else None}
+                 for k, v in prof.items()}
+
+    # ---- forced acceptance: drafts replaced by the target's greedy continuation (tau = B)
+    forced = None
+    if not args.no_forced:
+        g_stream = eng.greedy_reference([prompt], n_new + B)[0]
+        eng.reset_stats()
+        torch.cuda.synchronize()
+        f0 = time.perf_counter()
+        eng.prefill(0, prompt)
+        made = 1
+        while made < n_new:
+            eng.draft_block([0])
+            _, n = eng.verify_accept([0], g_stream[made:made + B - 1])
+            made += int(n[0])
+        torch.cuda.synchronize()
+        fs = time.perf_counter() - f0
+        eng.reset_seq(0)
+        fst = eng.stats()
+        fc = max(fst["cycles"], 1)
+        forced = {"tokens_per_s": made / fs, "mean_accept_len": (fst["accepted_drafts"] + fst["cycles"]) / fc,
+                  "cycles": fst["cycles"], "wall_s": fs,
+                  "note": "drafts forced to the target's greedy continuation; includes the draft pass; wall clock"}
+
+    # ---- per-cycle latency and the cycle's roofline floor
+    draft_us = st["draft_us"] / cycles
+    verify_us = st["verify_us"] / cycles
+    d, F, V, L, Ld = shape.d_model, shape.d_ffn, shape.vocab, shape.n_layers, shape.draft_layers
+    layer_w = 2 * (d * (shape.q_dim + 2 * shape.kv_dim) + shape.q_dim * d + 3 * d * F)
+    cycle_bytes = (L + Ld) * layer_w + 2 * 2 * V * d + 2 * (5 * d * d + Ld * 2 * shape.kv_dim * d)
+    floor_us = cycle_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = oracle_cycle_sample(shape, P, tau)
+        cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+               "sample": "float64 numpy oracle, one decode cycle sampled (1 of 36 target layers, 1 of 5 drafter "
+                         "layers, LM head over 31 rows, one fusion row, one injection layer), scaled to the full "
+                         f"cycle at the measured tau={tau:.3f}; cycle {r['cycle_s']:.2f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * secs / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": P + n_new, "parallelism": "replicas",
+                       "l2": "inputs larger than L2 (18.5 GB of weights streamed per cycle)"},
+            "cycle": {"draft_us": draft_us, "verify_us": verify_us, "cycle_us": draft_us + verify_us,
+                      "mean_accept_len": tau, "cycles_per_step": st["cycles"] / args.steps,
+                      "floor_us": floor_us, "floor_frac": floor_us / (draft_us + verify_us),
+                      "cycle_algorithmic_bytes": cycle_bytes},
+            "roofline": roofline,
+            "kernels": breakdown,
+            "forced_acceptance": forced,
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * args.steps * n_new / e2e_s, "unit": UNIT,
+                    "h2d_bytes_per_step": st_e2e["h2d_bytes"] / args.steps,
+                    "d2h_bytes_per_step": st_e2e["d2h_bytes"] / args.steps},
+            "gpu_launches": st["kernel_launches"],
+            "clocks": clk,
+            "setup_s": setup_s,
+        }
+        print(json.dumps(line))
+    eng.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--prompt-len", type=int, default=512)
+    ap.add_argument("--new-tokens", type=int, default=512)
+    ap.add_argument("--no-forced", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return run_reference(args) if args.impl == "reference" else run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

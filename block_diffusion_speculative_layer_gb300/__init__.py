@@ -24,7 +24,8 @@ EXPORTED = [
     "df_default_feat_layers", "df_num_weights", "df_weight_info", "df_init", "df_prefill", "df_draft_block",
     "df_verify_accept", "df_generate", "df_greedy_reference", "df_reset_seq", "df_get_stats", "df_reset_stats",
     "df_seq_info", "df_destroy", "df_last_error", "df_debug_enable", "df_debug_read", "df_debug_weight_ptr",
-    "df_op_gemm_bf16", "df_op_lmhead_argmax_bf16",
+    "df_op_gemm_bf16", "df_op_lmhead_argmax_bf16", "df_profile_enable", "df_profile_read",
+    "df_op_bench_gemm_bf16",
 ]
 
 
@@ -49,15 +50,22 @@ class DfStats(ctypes.Structure):
     _fields_ = [
         ("cycles", ctypes.c_int64), ("accepted_drafts", ctypes.c_int64), ("emitted_tokens", ctypes.c_int64),
         ("accept_hist", ctypes.c_int64 * 65), ("draft_us", ctypes.c_double), ("verify_us", ctypes.c_double),
-        ("prefill_us", ctypes.c_double),
+        ("prefill_us", ctypes.c_double), ("kernel_launches", ctypes.c_int64),
+        ("h2d_bytes", ctypes.c_int64), ("d2h_bytes", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:
         return {
             "cycles": self.cycles, "accepted_drafts": self.accepted_drafts, "emitted_tokens": self.emitted_tokens,
             "accept_hist": list(self.accept_hist), "draft_us": self.draft_us, "verify_us": self.verify_us,
-            "prefill_us": self.prefill_us,
+            "prefill_us": self.prefill_us, "kernel_launches": self.kernel_launches,
+            "h2d_bytes": self.h2d_bytes, "d2h_bytes": self.d2h_bytes,
         }
+
+
+class DfKernelStat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64), ("total_us", ctypes.c_double),
+                ("bytes", ctypes.c_double), ("flops", ctypes.c_double)]
 
 
 _lib = None
@@ -99,6 +107,9 @@ def lib() -> ctypes.CDLL:
     L.df_debug_weight_ptr.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_uint64)]
     L.df_op_gemm_bf16.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P]
     L.df_op_lmhead_argmax_bf16.argtypes = [_P, _P, _P, _I, _I, _I, _P]
+    L.df_op_bench_gemm_bf16.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, ctypes.POINTER(ctypes.c_float)]
+    L.df_profile_enable.argtypes = [_P, _I]
+    L.df_profile_read.argtypes = [_P, ctypes.POINTER(DfKernelStat), _I, _IP]
     for name in EXPORTED:
         fn = getattr(L, name)
         if fn.restype is ctypes.c_int:  # default restype: the df_status enum
@@ -292,6 +303,17 @@ class Engine:
                                          ctypes.byref(rows)), "df_debug_read")
         return buf[: rows.value * cols].reshape(rows.value, cols)
 
+    def profile(self, on: bool = True):
+        self._check(self.L.df_profile_enable(self.h, 1 if on else 0), "df_profile_enable")
+
+    def profile_read(self) -> Dict[str, dict]:
+        """Per kernel class: launches, device microseconds, algorithmic bytes and flops (then cleared)."""
+        arr = (DfKernelStat * 8)()
+        n = ctypes.c_int32()
+        self._check(self.L.df_profile_read(self.h, arr, 8, ctypes.byref(n)), "df_profile_read")
+        return {arr[i].name.decode(): {"launches": arr[i].launches, "us": arr[i].total_us, "bytes": arr[i].bytes,
+                                       "flops": arr[i].flops} for i in range(n.value)}
+
     def weight_ptr(self, which: int) -> int:
         a = ctypes.c_uint64()
         self._check(self.L.df_debug_weight_ptr(self.h, which, ctypes.byref(a)), "df_debug_weight_ptr")
@@ -312,6 +334,21 @@ def gemm_bf16(x, w, splits: int = 0, token_tile: int = 0, stream=None):
     if st != DF_OK:
         raise DfError(st, "df_op_gemm_bf16")
     return y
+
+
+def bench_gemm_bf16(x, w, iters: int = 20, splits: int = 0, token_tile: int = 0, stream=None) -> float:
+    """Mean device microseconds of the tcgen05 GEMM over `iters` back-to-back launches."""
+    import torch
+    M, K = x.shape
+    N = w.shape[0]
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    us = ctypes.c_float()
+    st = lib().df_op_bench_gemm_bf16(_P(x.data_ptr()), _P(w.data_ptr()), _P(y.data_ptr()), M, N, K, splits,
+                                     token_tile, iters, _P(s.cuda_stream), ctypes.byref(us))
+    if st != DF_OK:
+        raise DfError(st, "df_op_bench_gemm_bf16")
+    return us.value
 
 
 def lmhead_argmax_bf16(x, w, stream=None):

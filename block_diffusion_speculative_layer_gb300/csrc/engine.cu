@@ -102,6 +102,16 @@ struct df_handle {
   std::string err;
   bool debug = false;
   bool failed = false;
+  // kernel-class profiling
+  bool profiling = false;
+  std::vector<cudaEvent_t> evpool;
+  size_t ev_used = 0;
+  struct Pending {
+    int cls, e0, e1, n;
+    double bytes, flops;
+  };
+  std::vector<Pending> pending;
+  df_kernel_stat prof[5];
   int rows_last_target = 0, rows_last_draft = 0, rows_last_ctx = 0, rows_last_logits = 0;
 };
 
@@ -126,6 +136,70 @@ df_status fail(df_handle* h, df_status s, const std::string& msg) {
     df_status s_ = (expr);       \
     if (s_ != DF_OK) return s_;  \
   } while (0)
+
+
+enum { PC_GEMM = 0, PC_ATTN, PC_NORM, PC_EMBED, PC_CTRL, PC_N };
+const char* const PC_NAMES[PC_N] = {"gemm", "attention", "rmsnorm", "embed", "control"};
+constexpr size_t EV_POOL = 4096;
+
+// Read every pending event pair (the stream is synchronised first).
+void prof_resolve(df_handle* H) {
+  if (H->pending.empty()) {
+    H->ev_used = 0;
+    return;
+  }
+  cudaStreamSynchronize(H->st);
+  for (const auto& p : H->pending) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, H->evpool[p.e0], H->evpool[p.e1]) == cudaSuccess) {
+      df_kernel_stat& k = H->prof[p.cls];
+      k.launches += p.n;
+      k.total_us += 1000.0 * ms;
+      k.bytes += p.bytes;
+      k.flops += p.flops;
+    }
+  }
+  H->pending.clear();
+  H->ev_used = 0;
+}
+
+int ev_take(df_handle* H) {
+  if (H->ev_used >= H->evpool.size()) prof_resolve(H);
+  if (H->ev_used >= H->evpool.size()) return -1;
+  return (int)H->ev_used++;
+}
+
+// Counts this library's launches; with profiling on, brackets them with events.
+struct ProfScope {
+  df_handle* H;
+  int cls, n, e0 = -1;
+  double bytes, flops;
+  ProfScope(df_handle* h, int c, int nlaunch, double b = 0.0, double f = 0.0)
+      : H(h), cls(c), n(nlaunch), bytes(b), flops(f) {
+    H->stats.kernel_launches += n;
+    if (H->profiling) {
+      e0 = ev_take(H);
+      if (e0 >= 0) cudaEventRecord(H->evpool[e0], H->st);
+    }
+  }
+  ~ProfScope() {
+    if (!H->profiling || e0 < 0) return;
+    const int e1 = ev_take(H);
+    if (e1 < 0) return;
+    cudaEventRecord(H->evpool[e1], H->st);
+    H->pending.push_back({cls, e0, e1, n, bytes, flops});
+  }
+};
+
+// Host<->device copies on the engine's stream, counted for the end-to-end byte totals.
+cudaError_t h2d(df_handle* H, void* dst, const void* src, size_t bytes) {
+  H->stats.h2d_bytes += (int64_t)bytes;
+  return h2d(H, dst, src, bytes);
+}
+cudaError_t d2h(df_handle* H, void* dst, const void* src, size_t bytes) {
+  H->stats.d2h_bytes += (int64_t)bytes;
+  return d2h(H, dst, src, bytes);
+}
 
 df_status dalloc(df_handle* H, void** p, size_t bytes) {
   if (bytes == 0) bytes = 256;
@@ -242,8 +316,23 @@ EpiParams epi(df_handle* H, int kind) {
   return e;
 }
 
+// Algorithmic bytes of a GEMM launch: weights, inputs and outputs once each.
+double gemm_bytes(const df_handle* H, const Linear& W, int M, const EpiParams& ep) {
+  const double es = (double)H->esz;
+  double out = 0.0;
+  switch (ep.kind) {
+    case EPI_STORE: case EPI_QKV: out = (double)M * W.N * es; break;
+    case EPI_STORE_F32: out = (double)M * W.N * 4; break;
+    case EPI_RESID: out = (double)M * W.N * 8; break;
+    case EPI_SWIGLU: out = (double)M * (W.N / 2) * es; break;
+    case EPI_ARGMAX: out = (double)M * 8; break;
+  }
+  return (double)W.N * W.K * es + (double)M * W.K * es + out;
+}
+
 df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiParams& ep) {
   if (M <= 0) return DF_OK;
+  ProfScope ps(H, PC_GEMM, H->bf16 ? 1 : 2, gemm_bytes(H, W, M, ep), 2.0 * M * W.N * W.K);
   if (H->bf16) {
     const int nt = tc_token_tile(M);
     const void* tmX = nullptr;
@@ -264,12 +353,16 @@ void* row_ptr(df_handle* H, void* base, int row, int ld) {
 
 // LM head with fused argmax over rows [row0, row0 + M) of xb -> d_ids[0..M).
 df_status lm_head_argmax(df_handle* H, int M, float* dbg) {
-  CK(launch_fill_u64(H->d_amax, 0ull, M, H->st));
+  {
+    ProfScope ps(H, PC_CTRL, 1);
+    CK(launch_fill_u64(H->d_amax, 0ull, M, H->st));
+  }
   EpiParams e = epi(H, EPI_ARGMAX);
   e.amax = H->d_amax;
   e.out = dbg;
   e.ldo = H->V;
   CKS(gemm(H, H->lm_head, H->xb, M, e));
+  ProfScope ps(H, PC_CTRL, 1);
   CK(launch_argmax_finalize(H->d_amax, H->d_ids, M, H->st));
   return DF_OK;
 }
@@ -302,6 +395,10 @@ df_status attention(df_handle* H, int M, int R, int nseq, bool causal, const voi
   p.part_ml = H->part_ml;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)H->hd));
   p.err = H->d_err;
+  // algorithmic bytes: the visible keys/values of every sequence, queries and outputs
+  const double kv_bytes = (double)nseq * (double)(max_len + (causal ? 0 : R)) * 2.0 * H->kvdim * H->esz;
+  const double qo_bytes = 2.0 * M * H->qdim * H->esz;
+  ProfScope ps(H, PC_ATTN, 2, kv_bytes + qo_bytes, 4.0 * M * H->qdim * (double)max_len);
   CK(launch_attention(p, H->bf16, H->st));
   return DF_OK;
 }
@@ -316,8 +413,8 @@ void* kv_layer(df_handle* H, void* base, int l) {
 df_status layer_pass(df_handle* H, const Layer& Lw, int M, int R, int nseq, bool causal, int cache_layer, int max_len,
                      int tap) {
   const float eps = H->cfg.rms_eps;
-  CK(launch_rmsnorm(H->h, H->d, Lw.attn_norm, H->xb, H->d, H->bf16, M, H->d, eps, tap >= 0 ? H->taps : nullptr,
-                    tap, nullptr, H->st));
+  { ProfScope ps_(H, PC_NORM, 1); CK(launch_rmsnorm(H->h, H->d, Lw.attn_norm, H->xb, H->d, H->bf16, M, H->d, eps, tap >= 0 ? H->taps : nullptr,
+                    tap, nullptr, H->st)); }
   EpiParams e = epi(H, EPI_QKV);
   e.out = H->q;
   e.ldo = H->qdim;
@@ -338,7 +435,7 @@ df_status layer_pass(df_handle* H, const Layer& Lw, int M, int R, int nseq, bool
   r.resid = H->h;
   r.ldr = H->d;
   CKS(gemm(H, Lw.wo, H->attn, M, r));
-  CK(launch_rmsnorm(H->h, H->d, Lw.mlp_norm, H->xb, H->d, H->bf16, M, H->d, eps, nullptr, 0, nullptr, H->st));
+  { ProfScope ps_(H, PC_NORM, 1); CK(launch_rmsnorm(H->h, H->d, Lw.mlp_norm, H->xb, H->d, H->bf16, M, H->d, eps, nullptr, 0, nullptr, H->st)); }
   EpiParams s = epi(H, EPI_SWIGLU);
   s.out = H->act;
   s.ldo = H->F;
@@ -350,7 +447,7 @@ df_status layer_pass(df_handle* H, const Layer& Lw, int M, int R, int nseq, bool
 // Target over M rows (row_tok / row_pos / row_seq already set).  head_rows:
 // 0 = no LM head; -1 = every row; else only the last row (prefill).
 df_status target_pass(df_handle* H, int M, int R, int nseq, int max_len, bool want_taps, int head_mode) {
-  CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, M, H->d, H->V, H->d_err, H->st));
+  { ProfScope ps_(H, PC_EMBED, 1); CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, M, H->d, H->V, H->d_err, H->st)); }
   for (int l = 0; l < H->L; ++l) {
     const int tap = want_taps ? H->tap_of_layer[l] : -1;
     CKS(layer_pass(H, H->tl[l], M, R, nseq, true, l, max_len, tap));
@@ -361,8 +458,9 @@ df_status target_pass(df_handle* H, int M, int R, int nseq, int max_len, bool wa
   const int first = head_mode < 0 ? 0 : M - 1;
   const int rows = head_mode < 0 ? M : 1;
   H->rows_last_logits = rows;
-  CK(launch_rmsnorm(H->h + (size_t)first * H->d, H->d, H->final_norm, H->xb, H->d, H->bf16, rows, H->d,
-                    H->cfg.rms_eps, nullptr, 0, nullptr, H->st));
+  H->rows_last_logits = rows;
+  { ProfScope ps_(H, PC_NORM, 1); CK(launch_rmsnorm(H->h + (size_t)first * H->d, H->d, H->final_norm, H->xb, H->d, H->bf16, rows, H->d,
+                    H->cfg.rms_eps, nullptr, 0, nullptr, H->st)); }
   return lm_head_argmax(H, rows, H->debug ? H->dbg_logits : nullptr);
 }
 
@@ -373,8 +471,8 @@ df_status fuse_inject(df_handle* H, int M, const int* row_pos) {
   e.out = H->fcout;
   e.ldo = H->d;
   CKS(gemm(H, H->fc, H->taps, M, e));
-  CK(launch_rmsnorm(H->fcout, H->d, H->fc_norm, H->ctx, H->d, H->bf16, M, H->d, H->cfg.rms_eps, nullptr, 0, row_pos,
-                    H->st));
+  { ProfScope ps_(H, PC_NORM, 1); CK(launch_rmsnorm(H->fcout, H->d, H->fc_norm, H->ctx, H->d, H->bf16, M, H->d, H->cfg.rms_eps, nullptr, 0, row_pos,
+                    H->st)); }
   EpiParams k = epi(H, EPI_QKV);
   k.q_dim = 0;
   k.kv_dest = KV_PAGED;
@@ -389,11 +487,11 @@ df_status fuse_inject(df_handle* H, int M, const int* row_pos) {
 
 df_status drafter_pass(df_handle* H, int nseq, int max_ctx_len) {
   const int B = H->B, M = nseq * B;
-  CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, M, H->d, H->V, H->d_err, H->st));
+  { ProfScope ps_(H, PC_EMBED, 1); CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, M, H->d, H->V, H->d_err, H->st)); }
   for (int l = 0; l < H->Ld; ++l) CKS(layer_pass(H, H->dl[l], M, B, nseq, false, l, max_ctx_len, -1));
   if (H->debug) CK(cudaMemcpyAsync(H->dbg_dh, H->h, (size_t)M * H->d * 4, cudaMemcpyDeviceToDevice, H->st));
-  CK(launch_rmsnorm(H->h, H->d, H->d_final_norm, H->xb, H->d, H->bf16, M, H->d, H->cfg.rms_eps, nullptr, 0, nullptr,
-                    H->st));
+  { ProfScope ps_(H, PC_NORM, 1); CK(launch_rmsnorm(H->h, H->d, H->d_final_norm, H->xb, H->d, H->bf16, M, H->d, H->cfg.rms_eps, nullptr, 0, nullptr,
+                    H->st)); }
   CKS(lm_head_argmax(H, M, H->debug ? H->dbg_dlogits : nullptr));
   H->rows_last_draft = M;
   return DF_OK;
@@ -414,8 +512,7 @@ df_status ensure_pages(df_handle* H, int slot, int npos) {
   if (changed) {
     std::vector<int> row(H->pages_per_seq, -1);
     std::copy(s.pages.begin(), s.pages.end(), row.begin());
-    CK(cudaMemcpyAsync(H->d_pt + (size_t)slot * H->pages_per_seq, row.data(), row.size() * 4, cudaMemcpyHostToDevice,
-                       H->st));
+    CK(h2d(H, H->d_pt + (size_t)slot * H->pages_per_seq, row.data(), row.size() * 4));
   }
   return DF_OK;
 }
@@ -433,15 +530,15 @@ df_status trim_pages(df_handle* H, int slot, int keep) {
   if (changed) {
     std::vector<int> row(H->pages_per_seq, -1);
     std::copy(s.pages.begin(), s.pages.end(), row.begin());
-    CK(cudaMemcpyAsync(H->d_pt + (size_t)slot * H->pages_per_seq, row.data(), row.size() * 4, cudaMemcpyHostToDevice,
-                       H->st));
+    CK(h2d(H, H->d_pt + (size_t)slot * H->pages_per_seq, row.data(), row.size() * 4));
   }
   return DF_OK;
 }
 
 df_status check_device_error(df_handle* H) {
   int e = 0;
-  CK(cudaMemcpy(&e, H->d_err, 4, cudaMemcpyDeviceToHost));
+  CK(d2h(H, &e, H->d_err, 4));
+  CK(cudaStreamSynchronize(H->st));
   if (e) {
     H->failed = true;
     if (e & ERR_TIMEOUT) return fail(H, DF_ETIMEOUT, "a bounded device wait ran out (error word " + std::to_string(e) + ")");
@@ -452,6 +549,7 @@ df_status check_device_error(df_handle* H) {
 
 df_status sync(df_handle* H) {
   CK(cudaStreamSynchronize(H->st));
+  if (H->profiling) prof_resolve(H);
   return check_device_error(H);
 }
 
@@ -486,17 +584,17 @@ df_status prefill_impl(df_handle* H, int seq, const int32_t* prompt, int len, bo
       tok[i] = prompt[c0 + i];
       pos[i] = c0 + i;
     }
-    CK(cudaMemcpyAsync(H->d_row_tok, tok.data(), rows * 4, cudaMemcpyHostToDevice, H->st));
-    CK(cudaMemcpyAsync(H->d_row_pos, pos.data(), rows * 4, cudaMemcpyHostToDevice, H->st));
-    CK(cudaMemcpyAsync(H->d_row_seq, sq.data(), rows * 4, cudaMemcpyHostToDevice, H->st));
+    CK(h2d(H, H->d_row_tok, tok.data(), rows * 4));
+    CK(h2d(H, H->d_row_pos, pos.data(), rows * 4));
+    CK(h2d(H, H->d_row_seq, sq.data(), rows * 4));
     const bool last = c0 + rows == len;
     CKS(target_pass(H, rows, rows, 1, c0 + rows, inject, last ? 1 : 0));
     if (inject) CKS(fuse_inject(H, rows, H->d_row_pos));
   }
   // bonus token = argmax at the last prompt position; it sits at position len
   CK(cudaMemcpyAsync(H->d_bonus + seq, H->d_ids, 4, cudaMemcpyDeviceToDevice, H->st));
-  CK(cudaMemcpyAsync(H->d_bonus_pos + seq, &len, 4, cudaMemcpyHostToDevice, H->st));
-  CK(cudaMemcpyAsync(H->h_pin, H->d_ids, 4, cudaMemcpyDeviceToHost, H->st));
+  CK(h2d(H, H->d_bonus_pos + seq, &len, 4));
+  CK(d2h(H, H->h_pin, H->d_ids, 4));
   CKS(sync(H));
   s.len = len;
   s.bonus = H->h_pin[0];
@@ -507,17 +605,17 @@ df_status prefill_impl(df_handle* H, int seq, const int32_t* prompt, int len, bo
 df_status draft_impl(df_handle* H, const int32_t* slots, int nseq, int32_t* drafts_host) {
   CKS(check_slots(H, slots, nseq));
   const int B = H->B;
-  CK(cudaMemcpyAsync(H->d_slots, slots, nseq * 4, cudaMemcpyHostToDevice, H->st));
+  CK(h2d(H, H->d_slots, slots, nseq * 4));
   int max_len = 0;
   for (int i = 0; i < nseq; ++i) max_len = std::max(max_len, H->seqs[slots[i]].len);
   CK(cudaEventRecord(H->ev[0], H->st));
-  CK(launch_prep_block(H->d_slots, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 0,
-                       H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st));
+  { ProfScope ps_(H, PC_CTRL, 1); CK(launch_prep_block(H->d_slots, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 0,
+                       H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st)); }
   CKS(drafter_pass(H, nseq, max_len));
-  CK(launch_collect_drafts(H->d_ids, nseq, B, H->d_slots, H->d_drafts, H->st));
+  { ProfScope ps_(H, PC_CTRL, 1); CK(launch_collect_drafts(H->d_ids, nseq, B, H->d_slots, H->d_drafts, H->st)); }
   CK(cudaEventRecord(H->ev[1], H->st));
   if (drafts_host) {
-    CK(cudaMemcpyAsync(H->h_pin, H->d_drafts, (size_t)H->cfg.max_batch * (B - 1) * 4, cudaMemcpyDeviceToHost, H->st));
+    CK(d2h(H, H->h_pin, H->d_drafts, (size_t)H->cfg.max_batch * (B - 1) * 4));
     CKS(sync(H));
     for (int i = 0; i < nseq; ++i)
       std::memcpy(drafts_host + (size_t)i * (B - 1), H->h_pin + (size_t)slots[i] * (B - 1), (B - 1) * 4);
@@ -536,28 +634,27 @@ df_status verify_impl(df_handle* H, const int32_t* slots, int nseq, const int32_
     CKS(ensure_pages(H, slots[i], s.len + B));
     max_len = std::max(max_len, s.len + B);
   }
-  CK(cudaMemcpyAsync(H->d_slots, slots, nseq * 4, cudaMemcpyHostToDevice, H->st));
+  CK(h2d(H, H->d_slots, slots, nseq * 4));
   if (drafts_host) {
     for (int i = 0; i < nseq; ++i) {
       for (int j = 0; j < B - 1; ++j) {
         const int t = drafts_host[(size_t)i * (B - 1) + j];
         if (t < 0 || t >= H->V) return fail(H, DF_EINVAL, "draft token out of range");
       }
-      CK(cudaMemcpyAsync(H->d_drafts + (size_t)slots[i] * (B - 1), drafts_host + (size_t)i * (B - 1), (B - 1) * 4,
-                         cudaMemcpyHostToDevice, H->st));
+      CK(h2d(H, H->d_drafts + (size_t)slots[i] * (B - 1), drafts_host + (size_t)i * (B - 1), (B - 1) * 4));
     }
   }
   CK(cudaEventRecord(H->ev[2], H->st));
-  CK(launch_prep_block(H->d_slots, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 1,
-                       H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st));
+  { ProfScope ps_(H, PC_CTRL, 1); CK(launch_prep_block(H->d_slots, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 1,
+                       H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st)); }
   const int M = nseq * B;
   CKS(target_pass(H, M, B, nseq, max_len, true, -1));
-  CK(launch_accept(H->d_slots, nseq, B, H->d_row_tok, H->d_ids, H->d_bonus, H->d_bonus_pos, H->d_acc, H->d_n,
-                   H->d_inj_pos, H->st));
+  { ProfScope ps_(H, PC_CTRL, 1); CK(launch_accept(H->d_slots, nseq, B, H->d_row_tok, H->d_ids, H->d_bonus, H->d_bonus_pos, H->d_acc, H->d_n,
+                   H->d_inj_pos, H->st)); }
   CKS(fuse_inject(H, M, H->d_inj_pos));
   CK(cudaEventRecord(H->ev[3], H->st));
-  CK(cudaMemcpyAsync(H->h_pin, H->d_acc, (size_t)nseq * B * 4, cudaMemcpyDeviceToHost, H->st));
-  CK(cudaMemcpyAsync(H->h_pin + (size_t)nseq * B, H->d_n, (size_t)nseq * 4, cudaMemcpyDeviceToHost, H->st));
+  CK(d2h(H, H->h_pin, H->d_acc, (size_t)nseq * B * 4));
+  CK(d2h(H, H->h_pin + (size_t)nseq * B, H->d_n, (size_t)nseq * 4));
   CKS(sync(H));
   const int* acc = H->h_pin;
   const int* n = H->h_pin + (size_t)nseq * B;
@@ -590,8 +687,7 @@ df_status release(df_handle* H, int slot) {
   s.len = 0;
   s.bonus = -1;
   std::vector<int> row(H->pages_per_seq, -1);
-  CK(cudaMemcpyAsync(H->d_pt + (size_t)slot * H->pages_per_seq, row.data(), row.size() * 4, cudaMemcpyHostToDevice,
-                     H->st));
+  CK(h2d(H, H->d_pt + (size_t)slot * H->pages_per_seq, row.data(), row.size() * 4));
   CK(cudaStreamSynchronize(H->st));
   return DF_OK;
 }
@@ -991,6 +1087,9 @@ df_status df_generate(df_handle* H, const int32_t* prompts_host, const int32_t* 
     d.draft_us = H->stats.draft_us - before.draft_us;
     d.verify_us = H->stats.verify_us - before.verify_us;
     d.prefill_us = H->stats.prefill_us - before.prefill_us;
+    d.kernel_launches = H->stats.kernel_launches - before.kernel_launches;
+    d.h2d_bytes = H->stats.h2d_bytes - before.h2d_bytes;
+    d.d2h_bytes = H->stats.d2h_bytes - before.d2h_bytes;
     *stats = d;
   }
   return DF_OK;
@@ -1014,13 +1113,13 @@ df_status df_greedy_reference(df_handle* H, const int32_t* prompts_host, const i
     if (cudaMalloc(&d_gen, (size_t)nseq * n_new * 4) != cudaSuccess) s = fail(H, DF_ENOMEM, "output buffer");
   }
   auto body = [&]() -> df_status {
-    CK(cudaMemcpyAsync(H->d_row_tok, bonus.data(), nseq * 4, cudaMemcpyHostToDevice, H->st));
-    CK(cudaMemcpyAsync(H->d_row_pos, pos.data(), nseq * 4, cudaMemcpyHostToDevice, H->st));
-    CK(cudaMemcpyAsync(H->d_row_seq, sq.data(), nseq * 4, cudaMemcpyHostToDevice, H->st));
-    CK(cudaMemcpyAsync(H->d_ids, bonus.data(), nseq * 4, cudaMemcpyHostToDevice, H->st));
-    CK(launch_greedy_step(H->d_ids, nseq, 0, n_new, d_gen, H->d_row_tok, H->d_row_pos, H->st));
+    CK(h2d(H, H->d_row_tok, bonus.data(), nseq * 4));
+    CK(h2d(H, H->d_row_pos, pos.data(), nseq * 4));
+    CK(h2d(H, H->d_row_seq, sq.data(), nseq * 4));
+    CK(h2d(H, H->d_ids, bonus.data(), nseq * 4));
+    { ProfScope ps_(H, PC_CTRL, 1); CK(launch_greedy_step(H->d_ids, nseq, 0, n_new, d_gen, H->d_row_tok, H->d_row_pos, H->st)); }
     // greedy_step advanced the positions; undo that for step 0's inputs
-    CK(cudaMemcpyAsync(H->d_row_pos, pos.data(), nseq * 4, cudaMemcpyHostToDevice, H->st));
+    CK(h2d(H, H->d_row_pos, pos.data(), nseq * 4));
     for (int t = 1; t < n_new; ++t) {
       int max_len = 0;
       for (int i = 0; i < nseq; ++i) {
@@ -1029,9 +1128,9 @@ df_status df_greedy_reference(df_handle* H, const int32_t* prompts_host, const i
         max_len = std::max(max_len, p + 1);
       }
       CKS(target_pass(H, nseq, 1, nseq, max_len, false, -1));
-      CK(launch_greedy_step(H->d_ids, nseq, t, n_new, d_gen, H->d_row_tok, H->d_row_pos, H->st));
+      { ProfScope ps_(H, PC_CTRL, 1); CK(launch_greedy_step(H->d_ids, nseq, t, n_new, d_gen, H->d_row_tok, H->d_row_pos, H->st)); }
     }
-    CK(cudaMemcpyAsync(out_host, d_gen, (size_t)nseq * n_new * 4, cudaMemcpyDeviceToHost, H->st));
+    CK(d2h(H, out_host, d_gen, (size_t)nseq * n_new * 4));
     return sync(H);
   };
   if (s == DF_OK) s = body();
@@ -1074,6 +1173,7 @@ void df_destroy(df_handle* H) {
   if (H->h_pin) cudaFreeHost(H->h_pin);
   for (auto& e : H->ev)
     if (e) cudaEventDestroy(e);
+  for (auto& e : H->evpool) cudaEventDestroy(e);
   delete H;
 }
 
@@ -1135,6 +1235,38 @@ df_status df_debug_weight_ptr(const df_handle* H, int32_t which, uint64_t* addr)
       return DF_OK;
     default: return DF_EINVAL;
   }
+}
+
+df_status df_profile_enable(df_handle* H, int32_t on) {
+  if (!H) return DF_EINVAL;
+  if (on && H->evpool.empty()) {
+    H->evpool.resize(EV_POOL, nullptr);
+    for (auto& e : H->evpool) CK(cudaEventCreate(&e));
+  }
+  if (!on) prof_resolve(H);
+  H->profiling = on != 0;
+  for (int c = 0; c < PC_N; ++c) {
+    std::memset(H->prof[c].name, 0, 32);
+    std::strncpy(H->prof[c].name, PC_NAMES[c], 31);
+  }
+  return DF_OK;
+}
+
+df_status df_profile_read(df_handle* H, df_kernel_stat* out, int32_t max, int32_t* n) {
+  if (!H || !out || max < 0) return DF_EINVAL;
+  prof_resolve(H);
+  const int k = std::min<int>(max, PC_N);
+  for (int c = 0; c < k; ++c) {
+    out[c] = H->prof[c];
+    std::memset(out[c].name, 0, 32);
+    std::strncpy(out[c].name, PC_NAMES[c], 31);
+  }
+  for (int c = 0; c < PC_N; ++c) {
+    H->prof[c].launches = 0;
+    H->prof[c].total_us = H->prof[c].bytes = H->prof[c].flops = 0.0;
+  }
+  if (n) *n = k;
+  return DF_OK;
 }
 
 // ---------------------------------------------------------------- single ops
@@ -1202,6 +1334,51 @@ df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32
   cudaFreeAsync(ws, st);
   cudaFreeAsync(cnt, st);
   cudaFreeAsync(amax, st);
+  return r == cudaSuccess ? DF_OK : DF_ECUDA;
+}
+
+df_status df_op_bench_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, int32_t M, int32_t N, int32_t K,
+                                int32_t splits, int32_t token_tile, int32_t iters, void* stream, float* us_per_launch) {
+  if (!x_dev || !w_dev || !y_dev || !us_per_launch || M < 1 || N % 128 || K % 64 || N <= 0 || K <= 0 || iters < 1)
+    return DF_EINVAL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int nt = token_tile ? token_tile : tc_token_tile(M);
+  if (nt != 16 && nt != 32 && nt != 64 && nt != 128 && nt != 256) return DF_EINVAL;
+  const int sp = splits ? splits : tc_splits(N, K, sms);
+  if (sp < 1 || sp > K / 64) return DF_EINVAL;
+  Tmap tw, tx;
+  if (!make_tmap_bf16(tw.b, w_dev, N, K, 128) || !make_tmap_bf16(tx.b, x_dev, M, K, nt)) return DF_EINVAL;
+  float* ws = nullptr;
+  int* cnt = nullptr;
+  const size_t wsf = tc_workspace_floats(M, N, sp, nt), cn = tc_counter_ints(M, N, nt);
+  if (cudaMalloc(reinterpret_cast<void**>(&ws), std::max<size_t>(wsf, 1) * 4) != cudaSuccess) return DF_ENOMEM;
+  if (cudaMalloc(reinterpret_cast<void**>(&cnt), cn * 4) != cudaSuccess) {
+    cudaFree(ws);
+    return DF_ENOMEM;
+  }
+  cudaMemsetAsync(cnt, 0, cn * 4, st);
+  EpiParams e{};
+  e.kind = EPI_STORE_F32;
+  e.out = y_dev;
+  e.ldo = N;
+  cudaEvent_t a, b;
+  cudaEventCreate(&a);
+  cudaEventCreate(&b);
+  cudaError_t r = launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st);  // warm-up
+  cudaEventRecord(a, st);
+  for (int i = 0; i < iters && r == cudaSuccess; ++i) r = launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st);
+  cudaEventRecord(b, st);
+  cudaStreamSynchronize(st);
+  float ms = 0.f;
+  cudaEventElapsedTime(&ms, a, b);
+  *us_per_launch = 1000.f * ms / iters;
+  cudaEventDestroy(a);
+  cudaEventDestroy(b);
+  cudaFree(ws);
+  cudaFree(cnt);
   return r == cudaSuccess ? DF_OK : DF_ECUDA;
 }
 

@@ -93,7 +93,23 @@ typedef struct {
   double draft_us;         /* summed device time of draft passes (CUDA events) */
   double verify_us;        /* summed device time of verify+accept+inject */
   double prefill_us;
+  int64_t kernel_launches; /* this library's kernels launched */
+  int64_t h2d_bytes;       /* host-to-device bytes copied by the engine */
+  int64_t d2h_bytes;       /* device-to-host bytes copied by the engine */
 } df_stats;
+
+/* Device time per kernel class, from CUDA events recorded on the engine's
+ * stream around every launch while profiling is on (df_profile_enable).
+ * bytes / flops are ALGORITHMIC: weights + inputs + outputs each counted once
+ * (for a GEMM: N*K weights, M*K inputs, M*N outputs; for attention: the
+ * visible keys and values plus queries and outputs), not measured traffic. */
+typedef struct {
+  char name[32];
+  int64_t launches;
+  double total_us;
+  double bytes;
+  double flops;
+} df_kernel_stat;
 
 /* Five feature layers sampled uniformly from layer 2 to the third-from-last
  * ([ARCH] 技术细节补充, 提取层数): s_i = 2 + round_half_up(i (L-4) / 4), 1-based.
@@ -175,6 +191,13 @@ df_status df_seq_info(const df_handle* h, int32_t seq, int32_t* length, int32_t*
 void df_destroy(df_handle* h);
 const char* df_last_error(const df_handle* h);
 
+/* Kernel-class profiling (off by default).  While on, every launch is
+ * bracketed by two CUDA events on the engine's stream; the events are read
+ * at the next synchronising call.  df_profile_read fills up to max entries
+ * (classes: gemm, attention, rmsnorm, embed, control) and clears them. */
+df_status df_profile_enable(df_handle* h, int32_t on);
+df_status df_profile_read(df_handle* h, df_kernel_stat* out, int32_t max, int32_t* n);
+
 /* ------------------------------------------------------------------------
  * Inspection (tests).  df_debug_read copies a buffer of the last pass to
  * host memory as float32 (bf16 widened exactly):
@@ -222,6 +245,13 @@ df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, in
  * fp32 logits, lowest index on ties; logits are never written.  V % 128 == 0. */
 df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32_t* ids_dev, int32_t M, int32_t V,
                                    int32_t K, void* stream);
+
+/* Device time of the tcgen05 GEMM alone: y = x . w^T launched `iters` times
+ * back to back on `stream` (tensor maps and split-K workspace made once),
+ * timed with CUDA events around the whole run; *us_per_launch receives the
+ * mean.  Same shape rules as df_op_gemm_bf16.  Synchronises `stream`. */
+df_status df_op_bench_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, int32_t M, int32_t N, int32_t K,
+                                int32_t splits, int32_t token_tile, int32_t iters, void* stream, float* us_per_launch);
 
 #ifdef __cplusplus
 }

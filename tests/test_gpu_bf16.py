@@ -15,6 +15,12 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 TOL = 2e-2
+# At the Qwen3-8B width the bf16 rounding of activations at the GEMM inputs
+# (normalised x, q/k/v, attention output, SwiGLU output) alone gives 1-2.3 %
+# against float64 (a float64 emulation of exactly those rounding points, 8
+# layers: taps 1.0-1.7 %, final hidden 2.0 %, logits 2.3 %).  The bound for
+# that model is set from that emulation with headroom.
+TOL_WIDE = 3e-2
 
 # Small grouped-query model: 4 query heads per KV head as in the Qwen3-8B shape.
 SMALL = syn.ModelShape("small-bf16", n_layers=8, d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128,
@@ -38,10 +44,10 @@ def dfl():
 
 
 class Setup:
-    def __init__(self, dfl, shape, gain_std, max_batch, max_ctx):
+    def __init__(self, dfl, shape, gain_std, max_batch, max_ctx, cache=True):
         self.shape = shape
         self.w = syn.make_weights(shape, gain_std=gain_std)
-        self.model = O.Model(O.Weights(self.w, cache=True), shape)
+        self.model = O.Model(O.Weights(self.w, cache=cache), shape)
         self.eng = dfl.Engine(shape, self.w, max_batch=max_batch, max_ctx=max_ctx)
 
 
@@ -54,7 +60,7 @@ def small(dfl):
 
 @pytest.fixture(scope="module")
 def wide(dfl):
-    s = Setup(dfl, WIDE, 0.0, 1, 256)
+    s = Setup(dfl, WIDE, 0.0, 1, 256, cache=False)
     yield s
     s.eng.close()
 
@@ -96,7 +102,7 @@ def test_forced_acceptance_accepts_whole_blocks(small):
 
 # ---------------------------------------------------------------- parity under teacher forcing
 
-def _verify_parity(dfl, s, prompt):
+def _verify_parity(dfl, s, prompt, tol=TOL):
     eng, model, shape = s.eng, s.model, s.shape
     B = shape.block_size
     g = eng.greedy_reference([prompt], B + 1)[0]
@@ -124,17 +130,17 @@ def _verify_parity(dfl, s, prompt):
     ver = O.target_forward(model.W, shape, tokens[P:], cache)
     # fused context of the prompt
     ctx = O.fuse_features(model.W, shape, pre.taps)
-    assert rel_err(ctx_gpu, ctx[-len(ctx_gpu):]) <= TOL
+    assert rel_err(ctx_gpu, ctx[-len(ctx_gpu):]) <= tol
     # drafter pass at the first bonus token
     cc = O.ContextCache(shape.draft_layers, shape.n_kv_heads, shape.head_dim)
     O.inject_kv(model.W, shape, cc, ctx)
     dp = O.draft_blocks(model.W, shape, cc, [(int(g[0]), P)])
-    assert rel_err(dh_gpu, dp.hidden) <= TOL
-    assert rel_err(dl_gpu, dp.logits) <= TOL
+    assert rel_err(dh_gpu, dp.hidden) <= tol
+    assert rel_err(dl_gpu, dp.logits) <= tol
     # verification pass
-    assert rel_err(taps_gpu.reshape(B, 5, -1), ver.taps) <= TOL
-    assert rel_err(hid_gpu, ver.hidden[-1]) <= TOL
-    assert rel_err(logits_gpu, ver.logits) <= TOL
+    assert rel_err(taps_gpu.reshape(B, 5, -1), ver.taps) <= tol
+    assert rel_err(hid_gpu, ver.hidden[-1]) <= tol
+    assert rel_err(logits_gpu, ver.logits) <= tol
     return dp
 
 
@@ -145,7 +151,7 @@ def test_small_parity_teacher_forced(dfl, small):
 def test_wide_parity_teacher_forced(dfl, wide):
     # full width, full vocabulary (151936), GQA 32/8 x 128: every kernel at the
     # Qwen3-8B shape, against the oracle
-    _verify_parity(dfl, wide, syn.make_prompt(WIDE, 40, stream=4))
+    _verify_parity(dfl, wide, syn.make_prompt(WIDE, 40, stream=4), tol=TOL_WIDE)
 
 
 def test_wide_lossless(wide):
