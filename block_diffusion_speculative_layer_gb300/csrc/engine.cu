@@ -194,11 +194,11 @@ struct ProfScope {
 // Host<->device copies on the engine's stream, counted for the end-to-end byte totals.
 cudaError_t h2d(df_handle* H, void* dst, const void* src, size_t bytes) {
   H->stats.h2d_bytes += (int64_t)bytes;
-  return h2d(H, dst, src, bytes);
+  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, H->st);
 }
 cudaError_t d2h(df_handle* H, void* dst, const void* src, size_t bytes) {
   H->stats.d2h_bytes += (int64_t)bytes;
-  return d2h(H, dst, src, bytes);
+  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, H->st);
 }
 
 df_status dalloc(df_handle* H, void** p, size_t bytes) {
