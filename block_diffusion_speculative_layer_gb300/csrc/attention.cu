@@ -246,6 +246,13 @@ static cudaError_t launch_t(const AttnParams& p, cudaStream_t st) {
 
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st) {
   if (p.Hq % p.Hkv || p.Hq / p.Hkv > 8 || p.M != p.rows_per_seq * p.n_seqs) return cudaErrorInvalidValue;
+  if (bf16 && p.hd == 128) {
+    // tensor-core partials (attention_mma.cu), then the same ordered merge
+    cudaError_t e = launch_attention_mma(p, st);
+    if (e != cudaSuccess) return e;
+    attn_combine_kernel<__nv_bfloat16, 128><<<dim3(p.M, p.Hq), 128, 0, st>>>(p);
+    return cudaGetLastError();
+  }
   if (p.hd == 128) return bf16 ? launch_t<__nv_bfloat16, 128>(p, st) : launch_t<float, 128>(p, st);
   if (p.hd == 64) return bf16 ? launch_t<__nv_bfloat16, 64>(p, st) : launch_t<float, 64>(p, st);
   return cudaErrorInvalidValue;

@@ -89,36 +89,63 @@ struct EpiParams {
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// Per-row facts an epilogue needs, staged in shared memory once per tile so
+// that the element loops never wait on a chain of dependent global loads.
+struct RowMeta {
+  int pos;   // absolute position (< 0: inactive row)
+  int page;  // KV page of that position (paged K/V destinations), else -1
+};
+
+constexpr int EPI_BATCH = 8;  // rows whose global loads are issued together
+
 // Apply the epilogue to one result tile held in shared memory.
 //   tile[r * ld + f] = acc for row m0 + r, feature n0 + f, f in [0, 128),
-//   r in [0, rows).  Called by exactly 128 threads (one per feature column).
+//   r in [0, rows), rows <= M - m0.  Called by exactly 128 threads (one per
+//   feature column); meta has room for `rows` entries.  Contains
+//   __syncthreads(), so all 128 threads must call it.
 template <typename T>
-__device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, int n0, int m0, int rows, int M) {
+__device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, int n0, int m0, int rows, int M,
+                              RowMeta* meta) {
   const int f = threadIdx.x & 127;
   const int n = n0 + f;
+  rows = min(rows, M - m0);
+  if (ep.kind == EPI_QKV || (ep.kind == EPI_RESID && ep.row_pos)) {
+    for (int r = threadIdx.x; r < rows; r += 128) {
+      const int m = m0 + r;
+      RowMeta mt;
+      mt.pos = ep.row_pos[m];
+      mt.page = -1;
+      if (ep.kind == EPI_QKV && ep.kv_dest == KV_PAGED && mt.pos >= 0)
+        mt.page = ep.page_table[(size_t)ep.row_seq[m] * ep.pt_stride + mt.pos / ep.page_tokens];
+      meta[r] = mt;
+    }
+    __syncthreads();
+  }
   switch (ep.kind) {
     case EPI_STORE: {
       T* out = reinterpret_cast<T*>(ep.out);
-      for (int r = 0; r < rows; ++r) {
-        int m = m0 + r;
-        if (m >= M) break;
-        out[(size_t)m * ep.ldo + n] = Cvt<T>::from_f(tile[r * ld + f]);
-      }
+      for (int r = 0; r < rows; ++r) out[(size_t)(m0 + r) * ep.ldo + n] = Cvt<T>::from_f(tile[r * ld + f]);
     } break;
     case EPI_STORE_F32: {
       float* out = reinterpret_cast<float*>(ep.out);
-      for (int r = 0; r < rows; ++r) {
-        int m = m0 + r;
-        if (m >= M) break;
-        out[(size_t)m * ep.ldo + n] = tile[r * ld + f];
-      }
+      for (int r = 0; r < rows; ++r) out[(size_t)(m0 + r) * ep.ldo + n] = tile[r * ld + f];
     } break;
     case EPI_RESID: {
-      for (int r = 0; r < rows; ++r) {
-        int m = m0 + r;
-        if (m >= M) break;
-        if (ep.row_pos && ep.row_pos[m] < 0) continue;
-        ep.resid[(size_t)m * ep.ldr + n] += tile[r * ld + f];
+      // Load EPI_BATCH residual values, then add and store them.
+      for (int rb = 0; rb < rows; rb += EPI_BATCH) {
+        float old[EPI_BATCH];
+#pragma unroll
+        for (int i = 0; i < EPI_BATCH; ++i) {
+          const int r = rb + i;
+          old[i] = (r < rows) ? ep.resid[(size_t)(m0 + r) * ep.ldr + n] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < EPI_BATCH; ++i) {
+          const int r = rb + i;
+          if (r >= rows) break;
+          if (ep.row_pos && meta[r].pos < 0) continue;
+          ep.resid[(size_t)(m0 + r) * ep.ldr + n] = old[i] + tile[r * ld + f];
+        }
       }
     } break;
     case EPI_SWIGLU: {
@@ -127,11 +154,9 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
       const int g = f & 63;
       const int rsub = f >> 6;
       for (int r = rsub; r < rows; r += 2) {
-        int m = m0 + r;
-        if (m >= M) break;
-        float gate = tile[r * ld + g];
-        float up = tile[r * ld + 64 + g];
-        out[(size_t)m * ep.ldo + (n0 >> 1) + g] = Cvt<T>::from_f(silu_f(gate) * up);
+        const float gate = tile[r * ld + g];
+        const float up = tile[r * ld + 64 + g];
+        out[(size_t)(m0 + r) * ep.ldo + (n0 >> 1) + g] = Cvt<T>::from_f(silu_f(gate) * up);
       }
     } break;
     case EPI_QKV: {
@@ -139,49 +164,71 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
       const int half = hd >> 1;
       const int dim = n & (hd - 1);
       const int partner = f ^ half;
-      int kind;          // 0 = q, 1 = k, 2 = v
+      int kind;  // 0 = q, 1 = k, 2 = v
       int layer = 0, head = 0;
       if (n < ep.q_dim) {
         kind = 0;
       } else {
         int r2 = n - ep.q_dim;
-        int per_layer = 2 * ep.kv_dim;
+        const int per_layer = 2 * ep.kv_dim;
         layer = r2 / per_layer;
         r2 -= layer * per_layer;
         kind = 1 + r2 / ep.kv_dim;
         head = (r2 % ep.kv_dim) / hd;
       }
-      for (int r = 0; r < rows; ++r) {
-        int m = m0 + r;
-        if (m >= M) break;
-        int pos = ep.row_pos[m];
-        if (pos < 0) continue;
-        float v = tile[r * ld + f];
-        if (kind < 2) {
-          if (pos >= ep.rope_rows) { flag_error(ep.err, ERR_BOUNDS); continue; }
-          float p = tile[r * ld + partner];
-          float2 cs = ep.rope[(size_t)pos * half + (dim & (half - 1))];
-          v = (dim < half) ? (v * cs.x - p * cs.y) : (v * cs.x + p * cs.y);
-        }
-        if (kind == 0) {
-          T* q = reinterpret_cast<T*>(ep.out);
-          q[(size_t)m * ep.ldo + n] = Cvt<T>::from_f(v);
-        } else {
-          T* base = reinterpret_cast<T*>(ep.kv_base);
-          const int kv = kind - 1;
-          size_t off;
-          if (ep.kv_dest == KV_PAGED) {
-            int seq = ep.row_seq[m];
-            int page = ep.page_table[(size_t)seq * ep.pt_stride + pos / ep.page_tokens];
-            if (page < 0 || page >= ep.n_pages) { flag_error(ep.err, ERR_BOUNDS); continue; }
-            size_t page_elems = (size_t)2 * ep.n_kv_heads * ep.page_tokens * hd;
-            off = (size_t)(ep.layer0 + layer) * ep.layer_stride + (size_t)page * page_elems +
-                  ((size_t)(kv * ep.n_kv_heads + head) * ep.page_tokens + (pos % ep.page_tokens)) * hd + dim;
-          } else {
-            if (m >= ep.rows_cap) { flag_error(ep.err, ERR_BOUNDS); continue; }
-            off = ((size_t)(kv * ep.n_kv_heads + head) * ep.rows_cap + m) * hd + dim;
+      const size_t page_elems = (size_t)2 * ep.n_kv_heads * ep.page_tokens * hd;
+      for (int rb = 0; rb < rows; rb += EPI_BATCH) {
+        float val[EPI_BATCH];
+        // rotary tables for the batch's rows (independent read-only loads)
+#pragma unroll
+        for (int i = 0; i < EPI_BATCH; ++i) {
+          const int r = rb + i;
+          val[i] = 0.f;
+          if (r >= rows) continue;
+          const int pos = meta[r].pos;
+          if (pos < 0) continue;
+          float v = tile[r * ld + f];
+          if (kind < 2 && pos < ep.rope_rows) {
+            const float p = tile[r * ld + partner];
+            const float2 cs = __ldg(ep.rope + (size_t)pos * half + (dim & (half - 1)));
+            v = (dim < half) ? (v * cs.x - p * cs.y) : (v * cs.x + p * cs.y);
           }
-          base[off] = Cvt<T>::from_f(v);
+          val[i] = v;
+        }
+#pragma unroll
+        for (int i = 0; i < EPI_BATCH; ++i) {
+          const int r = rb + i;
+          if (r >= rows) break;
+          const int m = m0 + r;
+          const int pos = meta[r].pos;
+          if (pos < 0) continue;
+          if (kind < 2 && pos >= ep.rope_rows) {
+            flag_error(ep.err, ERR_BOUNDS);
+            continue;
+          }
+          if (kind == 0) {
+            reinterpret_cast<T*>(ep.out)[(size_t)m * ep.ldo + n] = Cvt<T>::from_f(val[i]);
+          } else {
+            T* base = reinterpret_cast<T*>(ep.kv_base);
+            const int kv = kind - 1;
+            size_t off;
+            if (ep.kv_dest == KV_PAGED) {
+              const int page = meta[r].page;
+              if (page < 0 || page >= ep.n_pages) {
+                flag_error(ep.err, ERR_BOUNDS);
+                continue;
+              }
+              off = (size_t)(ep.layer0 + layer) * ep.layer_stride + (size_t)page * page_elems +
+                    ((size_t)(kv * ep.n_kv_heads + head) * ep.page_tokens + (pos % ep.page_tokens)) * hd + dim;
+            } else {
+              if (m >= ep.rows_cap) {
+                flag_error(ep.err, ERR_BOUNDS);
+                continue;
+              }
+              off = ((size_t)(kv * ep.n_kv_heads + head) * ep.rows_cap + m) * hd + dim;
+            }
+            base[off] = Cvt<T>::from_f(val[i]);
+          }
         }
       }
     } break;
@@ -189,14 +236,13 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
       // One warp reduces 32 features of a row; four keys per row meet in one atomicMax each.
       float* dbg = reinterpret_cast<float*>(ep.out);
       for (int r = 0; r < rows; ++r) {
-        int m = m0 + r;
-        if (m >= M) break;
-        float v = tile[r * ld + f];
+        const int m = m0 + r;
+        const float v = tile[r * ld + f];
         if (dbg) dbg[(size_t)m * ep.ldo + n] = v;
         unsigned long long key = argmax_key(v, n);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-          unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+          const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
           key = other > key ? other : key;
         }
         if ((threadIdx.x & 31) == 0) atomicMax(ep.amax + m, key);

@@ -143,7 +143,7 @@ struct TcCfg {
   static constexpr int TMEM_COLS = NT < 32 ? 32 : NT;
   static constexpr int TLD = BM + 4;  // epilogue tile row stride (floats)
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
-  static_assert(NT * TLD * 4 <= STAGES * STAGE_BYTES, "epilogue tile must fit in the stage ring");
+  static_assert(NT * TLD * 4 + NT * 8 <= STAGES * STAGE_BYTES, "epilogue tile and row facts must fit in the ring");
 };
 
 template <int NT>
@@ -286,18 +286,35 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
     __syncthreads();
     if (!flags[0]) return;
     __threadfence();
-    for (int r = 0; r < rows; ++r) {
-      float s = 0.f;
-      for (int q = 0; q < splits; ++q) {
-        const float p = (q == split) ? tile[r * C::TLD + f] : __ldcg(part + (size_t)q * NT * BM + r * BM + f);
-        s = (q == 0) ? p : s + p;
+    // Sum the partials in split order 0, 1, 2, ... (a fixed order, whoever
+    // arrives last); the loads of a batch of rows are issued together.
+    for (int rb = 0; rb < rows; rb += 16) {
+      float acc[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int r = rb + i;
+        acc[i] = (r < rows) ? ((split == 0) ? tile[r * C::TLD + f] : __ldcg(part + r * BM + f)) : 0.f;
       }
-      tile[r * C::TLD + f] = s;
+      for (int q = 1; q < splits; ++q) {
+        float pv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = rb + i;
+          pv[i] = (r < rows) ? ((q == split) ? tile[r * C::TLD + f] : __ldcg(part + (size_t)q * NT * BM + r * BM + f))
+                             : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] += pv[i];
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (rb + i < rows) tile[(rb + i) * C::TLD + f] = acc[i];
     }
     if (threadIdx.x == 0) counters[tile_id] = 0;
     __syncthreads();
   }
-  epilogue_tile<__nv_bfloat16>(ep, tile, C::TLD, n0, m0, rows, M);
+  epilogue_tile<__nv_bfloat16>(ep, tile, C::TLD, n0, m0, rows, M,
+                               reinterpret_cast<RowMeta*>(smem + (size_t)NT * C::TLD * 4));
 }
 
 // ----------------------------------------------------------------------------

@@ -49,6 +49,8 @@ struct AttnParams {
   int* err;
 };
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st);
+// bf16, head_dim 128: tensor-core partials (attention_mma.cu); merged by launch_attention.
+cudaError_t launch_attention_mma(const AttnParams& p, cudaStream_t st);
 
 // ---- small kernels (misc.cu)
 cudaError_t launch_embed(const void* embed, bool bf16, const int* tok, float* h, int M, int d, int vocab, int* err,
