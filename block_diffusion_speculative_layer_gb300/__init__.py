@@ -25,7 +25,7 @@ EXPORTED = [
     "df_verify_accept", "df_generate", "df_greedy_reference", "df_reset_seq", "df_get_stats", "df_reset_stats",
     "df_seq_info", "df_destroy", "df_last_error", "df_debug_enable", "df_debug_read", "df_debug_weight_ptr",
     "df_op_gemm_bf16", "df_op_lmhead_argmax_bf16", "df_profile_enable", "df_profile_read",
-    "df_op_bench_gemm_bf16",
+    "df_op_bench_gemm_bf16", "df_op_gemm_bf16_noalloc",
 ]
 
 
@@ -107,6 +107,7 @@ def lib() -> ctypes.CDLL:
     L.df_debug_weight_ptr.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_uint64)]
     L.df_op_gemm_bf16.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P]
     L.df_op_lmhead_argmax_bf16.argtypes = [_P, _P, _P, _I, _I, _I, _P]
+    L.df_op_gemm_bf16_noalloc.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P]
     L.df_op_bench_gemm_bf16.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, ctypes.POINTER(ctypes.c_float)]
     L.df_profile_enable.argtypes = [_P, _I]
     L.df_profile_read.argtypes = [_P, ctypes.POINTER(DfKernelStat), _I, _IP]

@@ -246,6 +246,28 @@ df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, in
 df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32_t* ids_dev, int32_t M, int32_t V,
                                    int32_t K, void* stream);
 
+/* The GEMM of df_op_gemm_bf16 without any device allocation.  The pages
+ * have no counterpart of this call: it serves callers that may not allocate
+ * device memory while they run (a process whose memory is reserved up front
+ * by its own pool, a latency-critical loop that cannot afford the
+ * synchronisation of an allocation and its release).  Instead of a
+ * cudaMallocAsync'd workspace it uses fixed scratch compiled into the library:
+ * DF_NOALLOC_WS_FLOATS floats of split-K partial sums and DF_NOALLOC_TICKETS
+ * tile tickets, held by every GPU that loads the library until the process
+ * exits.  Arguments and result as df_op_gemm_bf16; returns DF_EINVAL, before
+ * launching anything, when the shape's split-K scratch (tiles x splits x
+ * token tile x 128 floats) or its ticket count exceeds those limits.
+ * The first call on a device looks up the scratch's device address with that
+ * device current; make that first call before any stream capture.  All calls
+ * on a device share the one scratch, which keeps the last call's contents
+ * (the tickets a call uses are cleared on its stream first): calls that can
+ * overlap on the GPU (different streams without ordering) race and must not
+ * be issued. */
+#define DF_NOALLOC_WS_FLOATS (1 << 20)
+#define DF_NOALLOC_TICKETS 4096
+df_status df_op_gemm_bf16_noalloc(const void* x_dev, const void* w_dev, float* y_dev, int32_t M, int32_t N,
+                                  int32_t K, int32_t splits, int32_t token_tile, void* stream);
+
 /* Device time of the tcgen05 GEMM alone: y = x . w^T launched `iters` times
  * back to back on `stream` (tensor maps and split-K workspace made once),
  * timed with CUDA events around the whole run; *us_per_launch receives the
