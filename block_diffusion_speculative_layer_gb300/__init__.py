@@ -25,7 +25,7 @@ EXPORTED = [
     "df_verify_accept", "df_generate", "df_greedy_reference", "df_reset_seq", "df_get_stats", "df_reset_stats",
     "df_seq_info", "df_destroy", "df_last_error", "df_debug_enable", "df_debug_read", "df_debug_weight_ptr",
     "df_op_gemm_bf16", "df_op_lmhead_argmax_bf16", "df_profile_enable", "df_profile_read",
-    "df_op_bench_gemm_bf16", "df_op_gemm_bf16_noalloc",
+    "df_op_bench_gemm_bf16", "df_op_gemm_bf16_noalloc", "df_bench_drafter_step",
 ]
 
 
@@ -107,6 +107,8 @@ def lib() -> ctypes.CDLL:
     L.df_debug_weight_ptr.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_uint64)]
     L.df_op_gemm_bf16.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P]
     L.df_op_lmhead_argmax_bf16.argtypes = [_P, _P, _P, _I, _I, _I, _P]
+    L.df_bench_drafter_step.argtypes = [_P, _I, _I, ctypes.POINTER(ctypes.c_float), _I, _I,
+                                         ctypes.POINTER(ctypes.c_double)]
     L.df_op_gemm_bf16_noalloc.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P]
     L.df_op_bench_gemm_bf16.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, ctypes.POINTER(ctypes.c_float)]
     L.df_profile_enable.argtypes = [_P, _I]
@@ -314,6 +316,15 @@ class Engine:
         self._check(self.L.df_profile_read(self.h, arr, 8, ctypes.byref(n)), "df_profile_read")
         return {arr[i].name.decode(): {"launches": arr[i].launches, "us": arr[i].total_us, "bytes": arr[i].bytes,
                                        "flops": arr[i].flops} for i in range(n.value)}
+
+    def bench_drafter_step(self, nseq: int, ctx_len: int, taps: np.ndarray, iters: int = 5) -> Dict[str, float]:
+        """Device microseconds per drafter step: fusion, injection, block attention, LM-head argmax."""
+        t = np.ascontiguousarray(taps, dtype=np.float32).reshape(-1, 5 * self.d)
+        out = (ctypes.c_double * 4)()
+        self._check(self.L.df_bench_drafter_step(self.h, nseq, ctx_len,
+                                                 t.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), t.shape[0],
+                                                 iters, out), "df_bench_drafter_step")
+        return {"fuse_us": out[0], "inject_us": out[1], "block_attention_us": out[2], "lm_head_us": out[3]}
 
     def weight_ptr(self, which: int) -> int:
         a = ctypes.c_uint64()

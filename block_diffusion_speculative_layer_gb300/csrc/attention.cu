@@ -47,6 +47,8 @@ __device__ __forceinline__ int ctx_len_of(const AttnParams& p, int m) {
 
 template <typename T, int HD, int MAXQ>
 __global__ void __launch_bounds__(ATT_THREADS) attn_partial_kernel(AttnParams p) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int DPL = HD / 32;  // head dims per lane
   // MAXQ: query vectors per warp (16 rows x group size / 8 warps, rounded up)
   extern __shared__ float sm[];
@@ -188,6 +190,8 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial_kernel(AttnParams p)
 // Merge chunk partials in chunk order: out = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
 template <typename T, int HD>
 __global__ void attn_combine_kernel(AttnParams p) {
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x, head = blockIdx.y, d = threadIdx.x;
   if (p.row_pos[m] < 0) return;
   const int len = ctx_len_of(p, m);
@@ -224,8 +228,7 @@ static cudaError_t launch_partial(const AttnParams& p, dim3 grid, size_t smem, c
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  attn_partial_kernel<T, HD, MAXQ><<<grid, ATT_THREADS, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_k(attn_partial_kernel<T, HD, MAXQ>, grid, dim3(ATT_THREADS), smem, st, p);
 }
 
 template <typename T, int HD>
@@ -240,8 +243,7 @@ static cudaError_t launch_t(const AttnParams& p, cudaStream_t st) {
   else if (G <= 4) e = launch_partial<T, HD, 8>(p, grid, smem, st);
   else e = launch_partial<T, HD, 16>(p, grid, smem, st);
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<T, HD><<<dim3(p.M, p.Hq), HD, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_k(attn_combine_kernel<T, HD>, dim3(p.M, p.Hq), dim3(HD), 0, st, p);
 }
 
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st) {
@@ -250,8 +252,7 @@ cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st) {
     // tensor-core partials (attention_mma.cu), then the same ordered merge
     cudaError_t e = launch_attention_mma(p, st);
     if (e != cudaSuccess) return e;
-    attn_combine_kernel<__nv_bfloat16, 128><<<dim3(p.M, p.Hq), 128, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_k(attn_combine_kernel<__nv_bfloat16, 128>, dim3(p.M, p.Hq), dim3(128), 0, st, p);
   }
   if (p.hd == 128) return bf16 ? launch_t<__nv_bfloat16, 128>(p, st) : launch_t<float, 128>(p, st);
   if (p.hd == 64) return bf16 ? launch_t<__nv_bfloat16, 64>(p, st) : launch_t<float, 64>(p, st);

@@ -59,6 +59,8 @@ __device__ __forceinline__ int ctx_len_rows(const AttnParams& p, int m) {
 }
 
 __global__ void __launch_bounds__(256) attn_mma_kernel(AttnParams p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ __align__(128) uint8_t sK[MC * ROWB];
   __shared__ __align__(128) uint8_t sV[MC * ROWB];
   const int G = p.Hq / p.Hkv;
@@ -249,8 +251,7 @@ cudaError_t launch_attention_mma(const AttnParams& p, cudaStream_t st) {
   const int qtiles = (p.rows_per_seq + 15) / 16;
   dim3 grid(p.grid_chunks + (p.causal ? 0 : 1), p.Hkv, p.n_seqs * qtiles);
   const int threads = ((G * 32 + 127) / 128) * 128;  // at least 128 threads stage the chunk
-  attn_mma_kernel<<<grid, threads, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_k(attn_mma_kernel, grid, dim3(threads), 0, st, p);
 }
 
 }  // namespace dfk

@@ -18,6 +18,13 @@ __device__ __forceinline__ void flag_error(int* err, int bit) {
   if (err) atomicOr(err, bit);
 }
 
+// Programmatic dependent launch.  Every kernel of the engine is launched so
+// that it may start while the kernel before it drains: pdl_wait() blocks until
+// that kernel has finished and its writes are visible (a no-op when launched
+// normally); pdl_trigger() lets the next kernel start its own prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 template <typename T> struct Cvt;
 template <> struct Cvt<float> {
   static __device__ __forceinline__ float to_f(float v) { return v; }

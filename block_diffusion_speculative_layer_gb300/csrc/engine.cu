@@ -111,7 +111,7 @@ struct df_handle {
     double bytes, flops;
   };
   std::vector<Pending> pending;
-  df_kernel_stat prof[5];
+  df_kernel_stat prof[8];
   int rows_last_target = 0, rows_last_draft = 0, rows_last_ctx = 0, rows_last_logits = 0;
 };
 
@@ -138,8 +138,11 @@ df_status fail(df_handle* h, df_status s, const std::string& msg) {
   } while (0)
 
 
-enum { PC_GEMM = 0, PC_ATTN, PC_NORM, PC_EMBED, PC_CTRL, PC_N };
-const char* const PC_NAMES[PC_N] = {"gemm", "attention", "rmsnorm", "embed", "control"};
+// Kernel classes for profiling: the layer GEMMs, the LM-head GEMM (fused
+// argmax), the fusion GEMM with its norm, the injection GEMM, attention, the
+// layer norms, the embedding gather and the small control kernels.
+enum { PC_GEMM = 0, PC_LMHEAD, PC_FUSE, PC_INJECT, PC_ATTN, PC_NORM, PC_EMBED, PC_CTRL, PC_N };
+const char* const PC_NAMES[PC_N] = {"gemm", "lm_head", "fuse", "inject", "attention", "rmsnorm", "embed", "control"};
 constexpr size_t EV_POOL = 4096;
 
 // Read every pending event pair (the stream is synchronised first).
@@ -330,9 +333,9 @@ double gemm_bytes(const df_handle* H, const Linear& W, int M, const EpiParams& e
   return (double)W.N * W.K * es + (double)M * W.K * es + out;
 }
 
-df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiParams& ep) {
+df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiParams& ep, int cls = PC_GEMM) {
   if (M <= 0) return DF_OK;
-  ProfScope ps(H, PC_GEMM, H->bf16 ? 1 : 2, gemm_bytes(H, W, M, ep), 2.0 * M * W.N * W.K);
+  ProfScope ps(H, cls, H->bf16 ? 1 : 2, gemm_bytes(H, W, M, ep), 2.0 * M * W.N * W.K);
   if (H->bf16) {
     const int nt = tc_token_tile(M);
     const void* tmX = nullptr;
@@ -361,7 +364,7 @@ df_status lm_head_argmax(df_handle* H, int M, float* dbg) {
   e.amax = H->d_amax;
   e.out = dbg;
   e.ldo = H->V;
-  CKS(gemm(H, H->lm_head, H->xb, M, e));
+  CKS(gemm(H, H->lm_head, H->xb, M, e, PC_LMHEAD));
   ProfScope ps(H, PC_CTRL, 1);
   CK(launch_argmax_finalize(H->d_amax, H->d_ids, M, H->st));
   return DF_OK;
@@ -470,8 +473,8 @@ df_status fuse_inject(df_handle* H, int M, const int* row_pos) {
   EpiParams e = epi(H, EPI_STORE_F32);
   e.out = H->fcout;
   e.ldo = H->d;
-  CKS(gemm(H, H->fc, H->taps, M, e));
-  { ProfScope ps_(H, PC_NORM, 1); CK(launch_rmsnorm(H->fcout, H->d, H->fc_norm, H->ctx, H->d, H->bf16, M, H->d, H->cfg.rms_eps, nullptr, 0, row_pos,
+  CKS(gemm(H, H->fc, H->taps, M, e, PC_FUSE));
+  { ProfScope ps_(H, PC_FUSE, 1); CK(launch_rmsnorm(H->fcout, H->d, H->fc_norm, H->ctx, H->d, H->bf16, M, H->d, H->cfg.rms_eps, nullptr, 0, row_pos,
                     H->st)); }
   EpiParams k = epi(H, EPI_QKV);
   k.q_dim = 0;
@@ -480,7 +483,7 @@ df_status fuse_inject(df_handle* H, int M, const int* row_pos) {
   k.layer0 = 0;
   k.row_pos = row_pos;
   k.row_seq = H->d_row_seq;
-  CKS(gemm(H, H->inj, H->ctx, M, k));
+  CKS(gemm(H, H->inj, H->ctx, M, k, PC_INJECT));
   H->rows_last_ctx = M;
   return DF_OK;
 }
@@ -1267,6 +1270,84 @@ df_status df_profile_read(df_handle* H, df_kernel_stat* out, int32_t max, int32_
   }
   if (n) *n = k;
   return DF_OK;
+}
+
+df_status df_bench_drafter_step(df_handle* H, int32_t nseq, int32_t ctx_len, const float* taps_host,
+                                 int32_t taps_rows, int32_t iters, double us_out[4]) {
+  GUARD(H);
+  const int B = H->B, d = H->d;
+  if (nseq < 1 || nseq > H->cfg.max_batch || ctx_len < 1 || ctx_len + B > H->cfg.max_ctx || iters < 1 || !us_out ||
+      !taps_host || taps_rows < nseq * B || taps_rows > H->Mmax)
+    return fail(H, DF_EINVAL, "bad drafter-step benchmark arguments");
+  for (int i = 0; i < nseq; ++i)
+    if (H->seqs[i].active) return fail(H, DF_ESTATE, "slots 0..nseq-1 must be free");
+  // taps rows in the model dtype
+  {
+    const size_t n = (size_t)taps_rows * 5 * d;
+    if (H->bf16) {
+      std::vector<uint16_t> b(n);
+      for (size_t i = 0; i < n; ++i) {
+        uint32_t u;
+        std::memcpy(&u, taps_host + i, 4);
+        u = (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+        b[i] = (uint16_t)u;
+      }
+      CK(cudaMemcpy(H->taps, b.data(), n * 2, cudaMemcpyHostToDevice));
+    } else {
+      CK(cudaMemcpy(H->taps, taps_host, n * 4, cudaMemcpyHostToDevice));
+    }
+  }
+  auto body = [&]() -> df_status {
+    // context: every position of every sequence gets an injected feature row
+    for (int sq = 0; sq < nseq; ++sq) {
+      SeqHost& s = H->seqs[sq];
+      s.active = true;
+      s.len = ctx_len;
+      s.bonus = 0;
+      CKS(ensure_pages(H, sq, ctx_len + B));
+      std::vector<int> pos(taps_rows), seqv(taps_rows, sq);
+      for (int c0 = 0; c0 < ctx_len; c0 += taps_rows) {
+        const int rows = std::min(taps_rows, ctx_len - c0);
+        for (int i = 0; i < rows; ++i) pos[i] = c0 + i;
+        CK(h2d(H, H->d_row_pos, pos.data(), rows * 4));
+        CK(h2d(H, H->d_row_seq, seqv.data(), rows * 4));
+        CKS(fuse_inject(H, rows, H->d_row_pos));
+      }
+      const int zero = 0;
+      CK(h2d(H, H->d_bonus + sq, &zero, 4));
+      CK(h2d(H, H->d_bonus_pos + sq, &ctx_len, 4));
+    }
+    std::vector<int> slots(nseq);
+    for (int i = 0; i < nseq; ++i) slots[i] = i;
+    CK(h2d(H, H->d_slots, slots.data(), nseq * 4));
+    CKS(sync(H));
+    const bool was = H->profiling;
+    CKS(df_profile_enable(H, 1));
+    df_kernel_stat junk[PC_N];
+    int32_t nj = 0;
+    CKS(df_profile_read(H, junk, PC_N, &nj));  // start from zero
+    const int M = nseq * B;
+    for (int it = 0; it < iters; ++it) {
+      { ProfScope ps_(H, PC_CTRL, 1); CK(launch_prep_block(H->d_slots, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 0, H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st)); }
+      // K1 fusion and K2 injection of one block of feature rows per sequence
+      // (written at the block's positions, past the context the drafter reads)
+      CKS(fuse_inject(H, M, H->d_row_pos));
+      // K3 block attention (inside the drafter pass) and K5 LM-head argmax
+      CKS(drafter_pass(H, nseq, ctx_len));
+    }
+    df_kernel_stat st[PC_N];
+    CKS(df_profile_read(H, st, PC_N, &nj));
+    if (!was) CKS(df_profile_enable(H, 0));
+    us_out[0] = st[PC_FUSE].total_us / iters;
+    us_out[1] = st[PC_INJECT].total_us / iters;
+    us_out[2] = st[PC_ATTN].total_us / iters;
+    us_out[3] = st[PC_LMHEAD].total_us / iters;
+    return DF_OK;
+  };
+  df_status s = body();
+  for (int i = 0; i < nseq; ++i)
+    if (H->seqs[i].active) release(H, i);
+  return s;
 }
 
 // ---------------------------------------------------------------- single ops

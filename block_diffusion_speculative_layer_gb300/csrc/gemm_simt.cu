@@ -10,6 +10,8 @@ namespace dfk {
 
 __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                        float* __restrict__ y, int M, int N, int K) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + warp;
   const int m = blockIdx.y;
@@ -27,6 +29,8 @@ constexpr int EPI_ROWS = 16;
 constexpr int EPI_LD = 129;
 
 __global__ void __launch_bounds__(128) epilogue_f32_kernel(const float* __restrict__ y, int N, int M, EpiParams ep) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float tile[EPI_ROWS * EPI_LD];
   __shared__ RowMeta meta[EPI_ROWS];
   const int n0 = blockIdx.x * 128, m0 = blockIdx.y * EPI_ROWS;
@@ -39,11 +43,9 @@ __global__ void __launch_bounds__(128) epilogue_f32_kernel(const float* __restri
 cudaError_t launch_gemm_f32(const float* x, const float* w, float* tmp, int M, int N, int K, const EpiParams& ep,
                             cudaStream_t st) {
   if (N % 128 || M < 1) return cudaErrorInvalidValue;
-  gemm_f32_kernel<<<dim3((N + 7) / 8, M), 256, 0, st>>>(x, w, tmp, M, N, K);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_k(gemm_f32_kernel, dim3((N + 7) / 8, M), dim3(256), 0, st, x, w, tmp, M, N, K);
   if (e != cudaSuccess) return e;
-  epilogue_f32_kernel<<<dim3(N / 128, (M + EPI_ROWS - 1) / EPI_ROWS), 128, 0, st>>>(tmp, N, M, ep);
-  return cudaGetLastError();
+  return launch_k(epilogue_f32_kernel, dim3(N / 128, (M + EPI_ROWS - 1) / EPI_ROWS), dim3(128), 0, st, tmp, N, M, ep);
 }
 
 }  // namespace dfk

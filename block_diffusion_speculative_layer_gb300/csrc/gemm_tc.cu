@@ -22,6 +22,9 @@
 // sequence of one output does not depend on M, so every output is bitwise
 // the same whatever the number of token rows.
 //
+// Launched with programmatic dependent launch: the producer streams the first
+// STAGES weight tiles before waiting for the previous kernel's outputs.
+//
 // Every mbarrier wait is bounded (about two seconds); on expiry the kernel
 // records ERR_TIMEOUT, waits (bounded) for the TMA loads it issued, frees its
 // tensor memory and returns.
@@ -194,11 +197,22 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
+  pdl_trigger();
   if (warp == 0 && lane == 0) {
     // ---- TMA producer
     const uint64_t pol_w = policy_evict_first();  // weights are read once per launch
     const uint64_t pol_x = policy_evict_last();   // activations are re-read by every weight tile
-    int i = 0;
+    // The weights do not depend on the kernel before this one: fill the first
+    // stages with weight tiles while it drains, then wait for its outputs.
+    const int pre = nk < C::STAGES ? nk : C::STAGES;
+    for (int i = 0; i < pre; ++i) {
+      mbar_expect_tx(full0 + 8 * i, C::STAGE_BYTES);
+      tma_load_2d(smem_u32(sW + i * C::W_BYTES), &tmW, full0 + 8 * i, (kb0 + i) * BK, n0, pol_w);
+    }
+    pdl_wait();
+    for (int i = 0; i < pre; ++i)
+      tma_load_2d(smem_u32(sX + i * C::X_BYTES), &tmX, full0 + 8 * i, (kb0 + i) * BK, m0, pol_x);
+    int i = pre;
     for (; i < nk; ++i) {
       const int s = i % C::STAGES;
       const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
@@ -212,7 +226,10 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
       tma_load_2d(smem_u32(sX + s * C::X_BYTES), &tmX, full0 + 8 * s, kc, m0, pol_x);
     }
     flags[3] = i;
-  } else if (warp == 1 && lane == 0) {
+  } else {
+    pdl_wait();
+  }
+  if (warp == 1 && lane == 0) {
     // ---- MMA issuer
     constexpr uint32_t idesc = idesc_bf16(BM, NT);
     int i = 0;
@@ -390,10 +407,8 @@ static cudaError_t launch_nt(const void* tmW, const void* tmX, int M, int N, int
     attr_set = true;
   }
   dim3 grid(N / BM, (M + NT - 1) / NT, splits);
-  gemm_tc_kernel<NT><<<grid, 128, C::SMEM, st>>>(*reinterpret_cast<const CUtensorMap*>(tmW),
-                                                  *reinterpret_cast<const CUtensorMap*>(tmX), M, N, K, splits, ws,
-                                                  counters, ep);
-  return cudaGetLastError();
+  return launch_k(gemm_tc_kernel<NT>, grid, dim3(128), (size_t)C::SMEM, st, *reinterpret_cast<const CUtensorMap*>(tmW),
+                  *reinterpret_cast<const CUtensorMap*>(tmX), M, N, K, splits, ws, counters, ep);
 }
 
 cudaError_t launch_gemm_tc(const void* tmW, const void* tmX, int nt, int M, int N, int K, int splits, float* ws,

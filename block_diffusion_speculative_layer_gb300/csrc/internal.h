@@ -11,6 +11,26 @@ namespace dfk {
 
 constexpr int TMAP_BYTES = 128;  // sizeof(CUtensorMap)
 
+// Whether launches carry the programmatic-stream-serialization attribute
+// (on by default; DF_NO_PDL=1 in the environment turns it off).
+bool pdl_enabled();
+
+// Launch a kernel with programmatic dependent launch allowed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t c = {};
+  c.gridDim = grid;
+  c.blockDim = block;
+  c.dynamicSmemBytes = smem;
+  c.stream = st;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  c.attrs = a;
+  c.numAttrs = 1;
+  return cudaLaunchKernelEx(&c, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- tcgen05 GEMM (gemm_tc.cu)
 bool make_tmap_bf16(void* map_out, const void* ptr, long long rows, long long cols, int box_rows);
 int tc_token_tile(int M);

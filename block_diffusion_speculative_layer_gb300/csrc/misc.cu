@@ -4,11 +4,24 @@
 #include "common.cuh"
 #include "internal.h"
 
+#include <stdlib.h>
+
 namespace dfk {
+
+bool pdl_enabled() {
+  static int on = -1;
+  if (on < 0) {
+    const char* e = getenv("DF_NO_PDL");
+    on = (e && e[0] == '1') ? 0 : 1;
+  }
+  return on != 0;
+}
 
 template <typename T>
 __global__ void embed_kernel(const T* __restrict__ embed, const int* __restrict__ tok, float* __restrict__ h, int d,
                              int vocab, int* err) {
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x;
   const int t = tok[m];
   if (t < 0 || t >= vocab) {
@@ -22,10 +35,9 @@ __global__ void embed_kernel(const T* __restrict__ embed, const int* __restrict_
 cudaError_t launch_embed(const void* embed, bool bf16, const int* tok, float* h, int M, int d, int vocab, int* err,
                          cudaStream_t st) {
   if (bf16)
-    embed_kernel<__nv_bfloat16><<<M, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(embed), tok, h, d, vocab, err);
+    return launch_k(embed_kernel<__nv_bfloat16>, dim3(M), dim3(256), 0, st, reinterpret_cast<const __nv_bfloat16*>(embed), tok, h, d, vocab, err);
   else
-    embed_kernel<float><<<M, 256, 0, st>>>(reinterpret_cast<const float*>(embed), tok, h, d, vocab, err);
-  return cudaGetLastError();
+    return launch_k(embed_kernel<float>, dim3(M), dim3(256), 0, st, reinterpret_cast<const float*>(embed), tok, h, d, vocab, err);
 }
 
 // One block per row; the sum of squares is reduced in a fixed order
@@ -36,6 +48,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
                                                       const float* __restrict__ gain, T* __restrict__ out, int ldo,
                                                       int d, float eps, T* __restrict__ taps, int tap_index,
                                                       const int* __restrict__ row_pos) {
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x;
   if (row_pos && row_pos[m] < 0) return;
   const float* x = h + (size_t)m * ldh;
@@ -60,31 +74,32 @@ cudaError_t launch_rmsnorm(const float* h, int ldh, const float* gain, void* out
                            float eps, void* taps, int tap_index, const int* row_pos, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
   if (bf16)
-    rmsnorm_kernel<__nv_bfloat16><<<M, 256, 0, st>>>(h, ldh, gain, reinterpret_cast<__nv_bfloat16*>(out), ldo, d, eps,
+    return launch_k(rmsnorm_kernel<__nv_bfloat16>, dim3(M), dim3(256), 0, st, h, ldh, gain, reinterpret_cast<__nv_bfloat16*>(out), ldo, d, eps,
                                                      reinterpret_cast<__nv_bfloat16*>(taps), tap_index, row_pos);
   else
-    rmsnorm_kernel<float><<<M, 256, 0, st>>>(h, ldh, gain, reinterpret_cast<float*>(out), ldo, d, eps,
+    return launch_k(rmsnorm_kernel<float>, dim3(M), dim3(256), 0, st, h, ldh, gain, reinterpret_cast<float*>(out), ldo, d, eps,
                                              reinterpret_cast<float*>(taps), tap_index, row_pos);
-  return cudaGetLastError();
 }
 
 __global__ void fill_u64_kernel(unsigned long long* p, unsigned long long v, int n) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) p[i] = v;
 }
 cudaError_t launch_fill_u64(unsigned long long* p, unsigned long long v, int n, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  fill_u64_kernel<<<(n + 255) / 256, 256, 0, st>>>(p, v, n);
-  return cudaGetLastError();
+  return launch_k(fill_u64_kernel, dim3((n + 255) / 256), dim3(256), 0, st, p, v, n);
 }
 
 __global__ void argmax_finalize_kernel(const unsigned long long* amax, int* ids, int M) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < M) ids[i] = argmax_key_index(amax[i]);
 }
 cudaError_t launch_argmax_finalize(const unsigned long long* amax, int* ids, int M, cudaStream_t st) {
-  argmax_finalize_kernel<<<(M + 127) / 128, 128, 0, st>>>(amax, ids, M);
-  return cudaGetLastError();
+  return launch_k(argmax_finalize_kernel, dim3((M + 127) / 128), dim3(128), 0, st, amax, ids, M);
 }
 
 // Row b*B + i of a block: token (bonus, then MASK or draft i), absolute
@@ -92,6 +107,8 @@ cudaError_t launch_argmax_finalize(const unsigned long long* amax, int* ids, int
 // the last verification produced.
 __global__ void prep_block_kernel(const int* slots, int B, const int* bonus, const int* bonus_pos, const int* drafts,
                                   int mask_id, int verify, int* row_tok, int* row_pos, int* row_seq) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x, i = threadIdx.x;
   if (i >= B) return;
   const int s = slots[b];
@@ -106,9 +123,8 @@ __global__ void prep_block_kernel(const int* slots, int B, const int* bonus, con
 cudaError_t launch_prep_block(const int* batch_slots, int nseq, int B, const int* bonus, const int* bonus_pos,
                               const int* drafts, int mask_id, int verify, int* row_tok, int* row_pos, int* row_seq,
                               cudaStream_t st) {
-  prep_block_kernel<<<nseq, ((B + 31) / 32) * 32, 0, st>>>(batch_slots, B, bonus, bonus_pos, drafts, mask_id, verify,
+  return launch_k(prep_block_kernel, dim3(nseq), dim3(((B + 31) / 32) * 32), 0, st, batch_slots, B, bonus, bonus_pos, drafts, mask_id, verify,
                                                             row_tok, row_pos, row_seq);
-  return cudaGetLastError();
 }
 
 // Greedy acceptance for one sequence per warp.  Slot i of the block holds
@@ -118,6 +134,8 @@ cudaError_t launch_prep_block(const int* batch_slots, int nseq, int B, const int
 // 0..k become context positions p..p+k for injection, the rest are inactive.
 __global__ void accept_kernel(const int* slots, int B, const int* row_tok, const int* ids, int* bonus, int* bonus_pos,
                               int* acc_out, int* n_out, int* inj_pos) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int lane = threadIdx.x;  // one warp; B <= 32
   const int s = slots[b];
@@ -144,21 +162,23 @@ __global__ void accept_kernel(const int* slots, int B, const int* row_tok, const
 cudaError_t launch_accept(const int* batch_slots, int nseq, int B, const int* row_tok, const int* ids, int* bonus,
                           int* bonus_pos, int* acc_out, int* n_out, int* inj_pos, cudaStream_t st) {
   if (B > 32) return cudaErrorInvalidValue;
-  accept_kernel<<<nseq, 32, 0, st>>>(batch_slots, B, row_tok, ids, bonus, bonus_pos, acc_out, n_out, inj_pos);
-  return cudaGetLastError();
+  return launch_k(accept_kernel, dim3(nseq), dim3(32), 0, st, batch_slots, B, row_tok, ids, bonus, bonus_pos, acc_out, n_out, inj_pos);
 }
 
 __global__ void collect_drafts_kernel(const int* ids, int B, const int* slots, int* drafts) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x, i = threadIdx.x;
   if (i < B - 1) drafts[slots[b] * (B - 1) + i] = ids[b * B + 1 + i];
 }
 cudaError_t launch_collect_drafts(const int* ids, int nseq, int B, const int* batch_slots, int* drafts,
                                   cudaStream_t st) {
-  collect_drafts_kernel<<<nseq, 32, 0, st>>>(ids, B, batch_slots, drafts);
-  return cudaGetLastError();
+  return launch_k(collect_drafts_kernel, dim3(nseq), dim3(32), 0, st, ids, B, batch_slots, drafts);
 }
 
 __global__ void greedy_step_kernel(const int* ids, int nseq, int t, int n_new, int* out, int* row_tok, int* row_pos) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= nseq) return;
   const int tok = ids[b];
@@ -168,17 +188,17 @@ __global__ void greedy_step_kernel(const int* ids, int nseq, int t, int n_new, i
 }
 cudaError_t launch_greedy_step(const int* ids, int nseq, int t, int n_new, int* out, int* row_tok, int* row_pos,
                                cudaStream_t st) {
-  greedy_step_kernel<<<(nseq + 127) / 128, 128, 0, st>>>(ids, nseq, t, n_new, out, row_tok, row_pos);
-  return cudaGetLastError();
+  return launch_k(greedy_step_kernel, dim3((nseq + 127) / 128), dim3(128), 0, st, ids, nseq, t, n_new, out, row_tok, row_pos);
 }
 
 __global__ void copy_rows_kernel(const float* src, int lds, float* dst, int ldd, int cols) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   for (int i = threadIdx.x; i < cols; i += blockDim.x) dst[(size_t)r * ldd + i] = src[(size_t)r * lds + i];
 }
 cudaError_t launch_copy_row_f32(const float* src, int lds, float* dst, int ldd, int rows, int cols, cudaStream_t st) {
-  copy_rows_kernel<<<rows, 256, 0, st>>>(src, lds, dst, ldd, cols);
-  return cudaGetLastError();
+  return launch_k(copy_rows_kernel, dim3(rows), dim3(256), 0, st, src, lds, dst, ldd, cols);
 }
 
 }  // namespace dfk

@@ -2,6 +2,8 @@
 
   python -m block_diffusion_speculative_layer_gb300.microbench gemm --M 16 --N 24576 --K 4096 --iters 20
   python -m block_diffusion_speculative_layer_gb300.microbench lmhead --M 16 --N 151936 --K 4096
+  python -m block_diffusion_speculative_layer_gb300.microbench drafter [--blocks 8,16] [--ctx 1024,4096,16384,32768]
+                                                                       [--batch 1,4,16,32]
 
 Inputs are seeded synthetic bf16 (N(0,1) activations, N(0,0.02) weights)
 drawn on the GPU by torch.  For small shapes several weight copies are used
@@ -18,6 +20,43 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def drafter(a):
+    """Drafter step alone on the Qwen3-8B width: fusion, injection, block attention, LM-head argmax."""
+    import numpy as np
+
+    import block_diffusion_speculative_layer_gb300 as dfl
+    import synthetic as syn
+
+    blocks = [int(x) for x in a.blocks.split(",")]
+    ctxs = [int(x) for x in a.ctx.split(",")]
+    batches = [int(x) for x in a.batch.split(",")]
+    for B in blocks:
+        # the target is not used by the drafter step: its minimum depth keeps memory low
+        shape = syn.QWEN3_8B.replace(name=f"drafter-step-B{B}", n_layers=8, block_size=B)
+        d, kvd = shape.d_model, shape.kv_dim
+        max_b = max(batches)
+        eng = dfl.Engine(shape, syn.iter_weights(shape), max_batch=max_b, max_ctx=max(ctxs) + 2 * B)
+        taps = syn.make_hidden(512, 5 * d).reshape(512, 5, d)   # N(0, 1) feature rows
+        for C in ctxs:
+            for nb in batches:
+                r = eng.bench_drafter_step(nb, C, taps, iters=a.iters)
+                M = nb * B
+                byts = {
+                    "fuse": 2 * d * 5 * d + M * 5 * d * 2 + M * d * 2,
+                    "inject": 2 * shape.draft_layers * 2 * kvd * d + M * d * 2 + M * shape.draft_layers * 2 * kvd * 2,
+                    "block_attention": shape.draft_layers * (nb * (C + B) * 2 * kvd * 2 + 2 * M * shape.q_dim * 2),
+                    "lm_head": 2 * shape.vocab * d + M * d * 2 + M * 8,
+                }
+                us = {"fuse": r["fuse_us"], "inject": r["inject_us"], "block_attention": r["block_attention_us"],
+                      "lm_head": r["lm_head_us"]}
+                print(json.dumps({"op": "drafter_step", "block": B, "ctx": C, "batch": nb,
+                                  "us": {k: round(v, 2) for k, v in us.items()},
+                                  "total_us": round(sum(us.values()), 2),
+                                  "GB/s": {k: round(byts[k] / (us[k] * 1e-6) / 1e9, 1) for k in us if us[k] > 0}}),
+                      flush=True)
+        eng.close()
+
+
 def main():
     import torch
 
@@ -25,7 +64,10 @@ def main():
     from block_diffusion_speculative_layer_gb300 import build
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["gemm", "lmhead"])
+    ap.add_argument("op", choices=["gemm", "lmhead", "drafter"])
+    ap.add_argument("--blocks", default="8,16")
+    ap.add_argument("--ctx", default="1024,4096,16384,32768")
+    ap.add_argument("--batch", default="1,4,16,32")
     ap.add_argument("--M", type=int, default=16)
     ap.add_argument("--N", type=int, default=24576)
     ap.add_argument("--K", type=int, default=4096)
@@ -35,6 +77,10 @@ def main():
     ap.add_argument("--token-tile", type=int, default=0)
     a = ap.parse_args()
     build.build()
+    if a.op == "drafter":
+        a.iters = min(a.iters, 5)
+        drafter(a)
+        return
     g = torch.Generator(device="cuda").manual_seed(0)
     x = torch.randn(a.M, a.K, device="cuda", generator=g).to(torch.bfloat16)
     nw = max(1, min(4, int(512e6 // (a.N * a.K * 2)) + 1))

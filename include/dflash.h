@@ -194,7 +194,8 @@ const char* df_last_error(const df_handle* h);
 /* Kernel-class profiling (off by default).  While on, every launch is
  * bracketed by two CUDA events on the engine's stream; the events are read
  * at the next synchronising call.  df_profile_read fills up to max entries
- * (classes: gemm, attention, rmsnorm, embed, control) and clears them. */
+ * (classes: gemm (layer GEMMs), lm_head, fuse, inject, attention, rmsnorm,
+ * embed, control) and clears them. */
 df_status df_profile_enable(df_handle* h, int32_t on);
 df_status df_profile_read(df_handle* h, df_kernel_stat* out, int32_t max, int32_t* n);
 
@@ -267,6 +268,20 @@ df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32
 #define DF_NOALLOC_TICKETS 4096
 df_status df_op_gemm_bf16_noalloc(const void* x_dev, const void* w_dev, float* y_dev, int32_t M, int32_t N,
                                   int32_t K, int32_t splits, int32_t token_tile, void* stream);
+
+/* Drafter-step microbenchmark (the drafter's own kernels alone, at a chosen
+ * context length and batch).  Uses free slots 0..nseq-1 and releases them:
+ * fills the drafter's context cache for positions [0, ctx_len) of each
+ * sequence by fusing and injecting the caller's feature rows (taps_host:
+ * [taps_rows][5][d] float32, reused cyclically; nseq*B <= taps_rows <= 512),
+ * then runs `iters` times: fusion and injection of one block of feature rows
+ * per sequence, and one drafter pass over [bonus, MASK x (B-1)] at position
+ * ctx_len.  us_out receives the mean device microseconds per iteration of
+ * [0] the fusion GEMM + its RMSNorm, [1] the injection GEMM, [2] block
+ * attention summed over the drafter layers, [3] the LM-head argmax (CUDA
+ * events around each launch; [ARCH] 第一层/第二层/第三层 and Shared LM Head). */
+df_status df_bench_drafter_step(df_handle* h, int32_t nseq, int32_t ctx_len, const float* taps_host,
+                                int32_t taps_rows, int32_t iters, double us_out[4]);
 
 /* Device time of the tcgen05 GEMM alone: y = x . w^T launched `iters` times
  * back to back on `stream` (tensor maps and split-K workspace made once),
