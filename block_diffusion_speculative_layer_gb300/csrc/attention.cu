@@ -68,14 +68,19 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial_kernel(AttnParams p)
   const bool blk_chunk = (!p.causal && c == p.grid_chunks);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Key range of this chunk and the largest visible length among the rows.
+  // Key range of this chunk and the largest visible length among the rows
+  // (one row per lane of the first warp).
   int key0, key1;
-  int max_len = 0;
-  for (int r = 0; r < nrows; ++r) {
-    const int m = r0 + r;
-    if (p.row_pos[m] < 0) continue;
-    max_len = max(max_len, ctx_len_of(p, m));
+  __shared__ int s_max_len;
+  if (warp == 0) {
+    int l = 0;
+    if (lane < nrows && p.row_pos[r0 + lane] >= 0) l = ctx_len_of(p, r0 + lane);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l = max(l, __shfl_xor_sync(0xffffffffu, l, o));
+    if (lane == 0) s_max_len = l;
   }
+  __syncthreads();
+  const int max_len = s_max_len;
   if (blk_chunk) {
     key0 = 0;
     key1 = p.rows_per_seq;
@@ -188,32 +193,45 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial_kernel(AttnParams p)
 }
 
 // Merge chunk partials in chunk order: out = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
+// Loads are issued eight chunks at a time; the sums still run in chunk order.
 template <typename T, int HD>
 __global__ void attn_combine_kernel(AttnParams p) {
   pdl_wait();
   pdl_trigger();
+  constexpr int CB = 8;
   const int m = blockIdx.x, head = blockIdx.y, d = threadIdx.x;
   if (p.row_pos[m] < 0) return;
   const int len = ctx_len_of(p, m);
   const int nA = (len + p.chunk - 1) / p.chunk;
   const size_t base = ((size_t)m * p.Hq + head) * p.n_chunk_slots;
   const bool has_blk = !p.causal;
+  const int nc = nA + (has_blk ? 1 : 0);  // partial c: context chunk c, or the block slot last
+  auto slot = [&](int c) { return (c < nA) ? base + c : base + p.n_chunk_slots - 1; };
   float M_ = -INFINITY;
-  for (int c = 0; c < nA; ++c) M_ = fmaxf(M_, p.part_ml[base + c].x);
-  if (has_blk) M_ = fmaxf(M_, p.part_ml[base + p.n_chunk_slots - 1].x);
-  float L = 0.f, a = 0.f;
-  for (int c = 0; c < nA; ++c) {
-    const float2 ml = p.part_ml[base + c];
-    const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M_);
-    L = fmaf(ml.y, w, L);
-    a = fmaf(p.part_acc[(base + c) * HD + d], w, a);
+  for (int c0 = 0; c0 < nc; c0 += CB) {
+    float mv[CB];
+#pragma unroll
+    for (int i = 0; i < CB; ++i) mv[i] = (c0 + i < nc) ? __ldcg(&p.part_ml[slot(c0 + i)].x) : -INFINITY;
+#pragma unroll
+    for (int i = 0; i < CB; ++i) M_ = fmaxf(M_, mv[i]);
   }
-  if (has_blk) {
-    const size_t c = p.n_chunk_slots - 1;
-    const float2 ml = p.part_ml[base + c];
-    const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M_);
-    L = fmaf(ml.y, w, L);
-    a = fmaf(p.part_acc[(base + c) * HD + d], w, a);
+  float L = 0.f, a = 0.f;
+  for (int c0 = 0; c0 < nc; c0 += CB) {
+    float2 ml[CB];
+    float av[CB];
+#pragma unroll
+    for (int i = 0; i < CB; ++i) {
+      const bool ok = c0 + i < nc;
+      ml[i] = ok ? __ldcg(&p.part_ml[slot(c0 + i)]) : make_float2(-INFINITY, 0.f);
+      av[i] = ok ? __ldcg(&p.part_acc[slot(c0 + i) * HD + d]) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < CB; ++i) {
+      if (c0 + i >= nc) break;
+      const float w = (ml[i].x == -INFINITY) ? 0.f : exp2f(ml[i].x - M_);
+      L = fmaf(ml[i].y, w, L);
+      a = fmaf(av[i], w, a);
+    }
   }
   T* out = reinterpret_cast<T*>(p.out);
   out[(size_t)m * p.Hq * HD + (size_t)head * HD + d] = Cvt<T>::from_f(L > 0.f ? a / L : 0.f);
@@ -229,6 +247,26 @@ static cudaError_t launch_partial(const AttnParams& p, dim3 grid, size_t smem, c
     attr_set = true;
   }
   return launch_k(attn_partial_kernel<T, HD, MAXQ>, grid, dim3(ATT_THREADS), smem, st, p);
+}
+
+template <typename T, int HD, int MAXQ>
+static cudaError_t set_attn_attr() {
+  return cudaFuncSetAttribute(attn_partial_kernel<T, HD, MAXQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              112 * 1024);
+}
+
+// Set the CUDA-core attention kernels' shared-memory limits up front (before
+// any stream capture).
+cudaError_t attention_prepare() {
+  cudaError_t e = cudaSuccess;
+#define DF_ATTR(T, HD, Q) \
+  if ((e = set_attn_attr<T, HD, Q>()) != cudaSuccess) return e;
+  DF_ATTR(float, 64, 2) DF_ATTR(float, 64, 4) DF_ATTR(float, 64, 8) DF_ATTR(float, 64, 16)
+  DF_ATTR(float, 128, 2) DF_ATTR(float, 128, 4) DF_ATTR(float, 128, 8) DF_ATTR(float, 128, 16)
+  DF_ATTR(__nv_bfloat16, 64, 2) DF_ATTR(__nv_bfloat16, 64, 4) DF_ATTR(__nv_bfloat16, 64, 8)
+  DF_ATTR(__nv_bfloat16, 64, 16)
+#undef DF_ATTR
+  return e;
 }
 
 template <typename T, int HD>

@@ -75,11 +75,17 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(AttnParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
 
-  int max_len = 0;
-  for (int r = 0; r < nrows; ++r) {
-    const int m = r0 + r;
-    if (p.row_pos[m] >= 0) max_len = max(max_len, ctx_len_rows(p, m));
+  // the tile's longest visible length: one row per lane of the first warp
+  __shared__ int s_max_len;
+  if (warp == 0) {
+    int l = 0;
+    if (lane < nrows && p.row_pos[r0 + lane] >= 0) l = ctx_len_rows(p, r0 + lane);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l = max(l, __shfl_xor_sync(0xffffffffu, l, o));
+    if (lane == 0) s_max_len = l;
   }
+  __syncthreads();
+  const int max_len = s_max_len;
   int key0, nkeys;
   if (blk_chunk) {
     key0 = 0;
@@ -95,6 +101,15 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(AttnParams p) {
   const __nv_bfloat16* blk = reinterpret_cast<const __nv_bfloat16*>(p.blk);
   const size_t page_elems = (size_t)2 * p.Hkv * p.page_tokens * MHD;
   const int seq_slot = p.row_seq[r0];
+  // The chunk's page ids, one per key, looked up in parallel first so the
+  // copies below never wait on a dependent load.
+  __shared__ int s_page[MC];
+  if (!blk_chunk && threadIdx.x < MC) {
+    const int kabs = key0 + threadIdx.x;
+    s_page[threadIdx.x] =
+        (threadIdx.x < nkeys) ? p.page_table[(size_t)seq_slot * p.pt_stride + kabs / p.page_tokens] : -1;
+  }
+  __syncthreads();
   for (int idx = threadIdx.x; idx < MC * (MHD / 8); idx += blockDim.x) {
     const int key = idx >> 4, b = idx & 15;
     bool ok = key < nkeys;
@@ -106,7 +121,7 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(AttnParams p) {
         srcv = blk + ((size_t)(1 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8;
       } else {
         const int kabs = key0 + key;
-        const int page = p.page_table[(size_t)seq_slot * p.pt_stride + kabs / p.page_tokens];
+        const int page = s_page[key];
         if (page >= 0 && page < p.n_pages) {
           const size_t base = (size_t)page * page_elems + (size_t)(kabs % p.page_tokens) * MHD + b * 8;
           srck = cache + base + (size_t)(0 * p.Hkv + h) * p.page_tokens * MHD;

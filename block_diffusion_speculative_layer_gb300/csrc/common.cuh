@@ -57,6 +57,7 @@ enum EpiKind : int {
                    // out[m][n/2 + f] = silu(gate) * up
   EPI_QKV,         // rotary embedding + scatter of q / k / v
   EPI_ARGMAX,      // per-row packed max over the tile's logits (+ optional store)
+  EPI_STORE_SS,    // out[m][n] = acc (type T) and this tile's partial sum of acc^2 per row
 };
 
 // Where K/V rows of EPI_QKV go.
@@ -91,6 +92,19 @@ struct EpiParams {
   int rope_rows;      // positions in the table (bounds check)
   // EPI_ARGMAX
   unsigned long long* amax;  // [M]
+  // RMSNorm folded into the GEMM: the input rows were not normalised; each
+  // output row is scaled by rsqrt(sum(ss_in[m][:]) / d + eps) (the norm's
+  // gain is folded into the weight's columns).
+  const float* ss_in;        // [M][ss_tiles] partial sums of squares of the input rows; null: no scaling
+  int ss_tiles;
+  float inv_d;
+  float eps;
+  // EPI_RESID / EPI_STORE_SS: what the next (normalising) GEMM reads
+  void* xraw;                // [M][ldx] the new rows in the model dtype; null: none
+  int ldx;
+  float* ss_out;             // [M][ss_tiles] this tile's partial sum of squares; null: none
+  void* tap;                 // [M][5][N] feature-layer tap of the new rows; null: none
+  int tap_index;
   int* err;
 };
 
@@ -99,9 +113,19 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 // Per-row facts an epilogue needs, staged in shared memory once per tile so
 // that the element loops never wait on a chain of dependent global loads.
 struct RowMeta {
-  int pos;   // absolute position (< 0: inactive row)
-  int page;  // KV page of that position (paged K/V destinations), else -1
+  int pos;      // absolute position (< 0: inactive row)
+  int page;     // KV page of that position (paged K/V destinations), else -1
+  float scale;  // 1/rms of the input row (folded RMSNorm), else unused
 };
+
+// Partial sum of squares of one row's 128 tile values: each warp reduces its
+// 32 lanes in a fixed xor tree, then the four warp sums add in warp order.
+__device__ __forceinline__ void row_sumsq(float v, int r, float* red) {
+  float q = v * v;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+  if ((threadIdx.x & 31) == 0) red[r * 4 + (threadIdx.x >> 5)] = q;
+}
 
 constexpr int EPI_BATCH = 8;  // rows whose global loads are issued together
 
@@ -112,22 +136,39 @@ constexpr int EPI_BATCH = 8;  // rows whose global loads are issued together
 //   __syncthreads(), so all 128 threads must call it.
 template <typename T>
 __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, int n0, int m0, int rows, int M,
-                              RowMeta* meta) {
+                              RowMeta* meta, float* red) {
   const int f = threadIdx.x & 127;
   const int n = n0 + f;
   rows = min(rows, M - m0);
-  if (ep.kind == EPI_QKV || (ep.kind == EPI_RESID && ep.row_pos)) {
+  const bool need_meta = ep.kind == EPI_QKV || (ep.kind == EPI_RESID && ep.row_pos);
+  if (need_meta) {
     for (int r = threadIdx.x; r < rows; r += 128) {
       const int m = m0 + r;
-      RowMeta mt;
-      mt.pos = ep.row_pos[m];
-      mt.page = -1;
-      if (ep.kind == EPI_QKV && ep.kv_dest == KV_PAGED && mt.pos >= 0)
-        mt.page = ep.page_table[(size_t)ep.row_seq[m] * ep.pt_stride + mt.pos / ep.page_tokens];
-      meta[r] = mt;
+      const int pos = ep.row_pos[m];
+      meta[r].pos = pos;
+      meta[r].page = (ep.kind == EPI_QKV && ep.kv_dest == KV_PAGED && pos >= 0)
+                         ? ep.page_table[(size_t)ep.row_seq[m] * ep.pt_stride + pos / ep.page_tokens]
+                         : -1;
     }
-    __syncthreads();
   }
+  if (ep.ss_in) {
+    // 1/rms per row: 8 threads per row each add every 8th tile partial, then a
+    // fixed xor tree joins them (the same order for every row and batch).
+    for (int rb = 0; rb < rows; rb += 16) {
+      const int r = rb + (threadIdx.x >> 3), j = threadIdx.x & 7;
+      float part = 0.f;
+      if (r < rows) {
+        const float* sp = ep.ss_in + (size_t)(m0 + r) * ep.ss_tiles;
+        for (int t = j; t < ep.ss_tiles; t += 8) part += sp[t];
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 4);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      if (r < rows && j == 0) meta[r].scale = rsqrtf(part * ep.inv_d + ep.eps);
+    }
+  }
+  if (need_meta || ep.ss_in) __syncthreads();
+  const bool scaled = ep.ss_in != nullptr;
   switch (ep.kind) {
     case EPI_STORE: {
       T* out = reinterpret_cast<T*>(ep.out);
@@ -138,7 +179,8 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
       for (int r = 0; r < rows; ++r) out[(size_t)(m0 + r) * ep.ldo + n] = tile[r * ld + f];
     } break;
     case EPI_RESID: {
-      // Load EPI_BATCH residual values, then add and store them.
+      // Load EPI_BATCH residual values, then add and store them; also write the
+      // new rows for the next normalising GEMM (model dtype, tap, sum of squares).
       for (int rb = 0; rb < rows; rb += EPI_BATCH) {
         float old[EPI_BATCH];
 #pragma unroll
@@ -150,10 +192,33 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
         for (int i = 0; i < EPI_BATCH; ++i) {
           const int r = rb + i;
           if (r >= rows) break;
-          if (ep.row_pos && meta[r].pos < 0) continue;
-          ep.resid[(size_t)(m0 + r) * ep.ldr + n] = old[i] + tile[r * ld + f];
+          const int m = m0 + r;
+          const bool live = !(ep.row_pos && meta[r].pos < 0);
+          const float nv = live ? old[i] + tile[r * ld + f] : old[i];
+          if (live) ep.resid[(size_t)m * ep.ldr + n] = nv;
+          if (ep.xraw) reinterpret_cast<T*>(ep.xraw)[(size_t)m * ep.ldx + n] = Cvt<T>::from_f(nv);
+          if (ep.tap) reinterpret_cast<T*>(ep.tap)[((size_t)m * 5 + ep.tap_index) * ep.ldr + n] = Cvt<T>::from_f(nv);
+          if (ep.ss_out) row_sumsq(nv, r, red);
         }
       }
+      if (ep.ss_out) {
+        __syncthreads();
+        for (int r = threadIdx.x; r < rows; r += 128)
+          ep.ss_out[(size_t)(m0 + r) * ep.ss_tiles + (n0 >> 7)] =
+              ((red[r * 4 + 0] + red[r * 4 + 1]) + red[r * 4 + 2]) + red[r * 4 + 3];
+      }
+    } break;
+    case EPI_STORE_SS: {
+      T* out = reinterpret_cast<T*>(ep.out);
+      for (int r = 0; r < rows; ++r) {
+        const float v = tile[r * ld + f];
+        out[(size_t)(m0 + r) * ep.ldo + n] = Cvt<T>::from_f(v);
+        row_sumsq(v, r, red);
+      }
+      __syncthreads();
+      for (int r = threadIdx.x; r < rows; r += 128)
+        ep.ss_out[(size_t)(m0 + r) * ep.ss_tiles + (n0 >> 7)] =
+            ((red[r * 4 + 0] + red[r * 4 + 1]) + red[r * 4 + 2]) + red[r * 4 + 3];
     } break;
     case EPI_SWIGLU: {
       // 128 threads handle (row, gate feature) pairs: 64 features x 2 rows per pass.
@@ -161,8 +226,9 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
       const int g = f & 63;
       const int rsub = f >> 6;
       for (int r = rsub; r < rows; r += 2) {
-        const float gate = tile[r * ld + g];
-        const float up = tile[r * ld + 64 + g];
+        const float sc = scaled ? meta[r].scale : 1.f;
+        const float gate = tile[r * ld + g] * sc;
+        const float up = tile[r * ld + 64 + g] * sc;
         out[(size_t)(m0 + r) * ep.ldo + (n0 >> 1) + g] = Cvt<T>::from_f(silu_f(gate) * up);
       }
     } break;
@@ -194,9 +260,10 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
           if (r >= rows) continue;
           const int pos = meta[r].pos;
           if (pos < 0) continue;
-          float v = tile[r * ld + f];
+          const float sc = scaled ? meta[r].scale : 1.f;
+          float v = tile[r * ld + f] * sc;
           if (kind < 2 && pos < ep.rope_rows) {
-            const float p = tile[r * ld + partner];
+            const float p = tile[r * ld + partner] * sc;
             const float2 cs = __ldg(ep.rope + (size_t)pos * half + (dim & (half - 1)));
             v = (dim < half) ? (v * cs.x - p * cs.y) : (v * cs.x + p * cs.y);
           }

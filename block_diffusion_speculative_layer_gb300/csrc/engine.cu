@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <string>
@@ -83,7 +84,8 @@ struct df_handle {
 
   float* h = nullptr;
   void *xb = nullptr, *q = nullptr, *attn = nullptr, *act = nullptr, *taps = nullptr, *ctx = nullptr, *blk = nullptr;
-  float* fcout = nullptr;
+  void* xraw = nullptr;          // GEMM input rows, not normalised (model dtype)
+  float *ss = nullptr, *ss_ctx = nullptr;  // per-row, per-128-feature-tile sums of squares
   float* tmp = nullptr;
   float *dbg_logits = nullptr, *dbg_dlogits = nullptr, *dbg_dh = nullptr, *dbg_th = nullptr;
   float* ws = nullptr;
@@ -102,6 +104,15 @@ struct df_handle {
   std::string err;
   bool debug = false;
   bool failed = false;
+  // graph replay of the decode cycle (df_generate)
+  bool use_graphs = true;
+  int graph_ready_cycles = 0;        // eager cycles run by this handle (the first sets kernel attributes)
+  cudaGraphExec_t gexec = nullptr;
+  std::vector<int> gkey;             // slots + chunk counts the graph was captured for
+  int64_t g_launches = 0, g_h2d = 0, g_d2h = 0;
+  int* d_gslots = nullptr;
+  cudaStream_t gstream = nullptr;    // capture/replay stream, joined to the caller's stream by events
+  cudaEvent_t gjoin[2] = {nullptr, nullptr};
   // kernel-class profiling
   bool profiling = false;
   std::vector<cudaEvent_t> evpool;
@@ -413,17 +424,31 @@ void* kv_layer(df_handle* H, void* base, int l) {
 // One decoder layer over M rows.  causal: target (K/V into the paged target
 // cache); otherwise drafter (K/V into the block row buffer, attention over the
 // injected context + block).
+// Fill in the folded-RMSNorm fields: the GEMM reads unnormalised rows and
+// scales each output row by 1/rms from the per-tile sums of squares.
+void fold_norm(df_handle* H, EpiParams& e, const float* ss) {
+  e.ss_in = ss;
+  e.ss_tiles = H->d / 128;
+  e.inv_d = 1.0f / (float)H->d;
+  e.eps = H->cfg.rms_eps;
+}
+
+// One decoder layer over M rows.  Its RMSNorms are folded into the QKV and
+// gate/up GEMMs (gains in the weights, 1/rms in the epilogues); the residual
+// epilogues of the O and down GEMMs write the next GEMM's input rows and their
+// sums of squares.  causal: target (K/V into the paged target cache);
+// otherwise drafter (K/V into the block row buffer, attention over the
+// injected context + block).  next_tap: feature slot of the next layer's
+// input (the output of this layer), or -1.
 df_status layer_pass(df_handle* H, const Layer& Lw, int M, int R, int nseq, bool causal, int cache_layer, int max_len,
-                     int tap) {
-  const float eps = H->cfg.rms_eps;
-  { ProfScope ps_(H, PC_NORM, 1); CK(launch_rmsnorm(H->h, H->d, Lw.attn_norm, H->xb, H->d, H->bf16, M, H->d, eps, tap >= 0 ? H->taps : nullptr,
-                    tap, nullptr, H->st)); }
+                     int next_tap) {
   EpiParams e = epi(H, EPI_QKV);
   e.out = H->q;
   e.ldo = H->qdim;
   e.q_dim = H->qdim;
   e.row_pos = H->d_row_pos;
   e.row_seq = H->d_row_seq;
+  fold_norm(H, e, H->ss);
   if (causal) {
     e.kv_dest = KV_PAGED;
     e.kv_base = H->kv_t;
@@ -432,17 +457,25 @@ df_status layer_pass(df_handle* H, const Layer& Lw, int M, int R, int nseq, bool
     e.kv_dest = KV_ROWS;
     e.kv_base = H->blk;
   }
-  CKS(gemm(H, Lw.qkv, H->xb, M, e));
+  CKS(gemm(H, Lw.qkv, H->xraw, M, e));
   CKS(attention(H, M, R, nseq, causal, kv_layer(H, causal ? H->kv_t : H->kv_d, cache_layer), max_len));
   EpiParams r = epi(H, EPI_RESID);
   r.resid = H->h;
   r.ldr = H->d;
+  r.xraw = H->xraw;
+  r.ldx = H->d;
+  r.ss_out = H->ss;
+  r.ss_tiles = H->d / 128;
   CKS(gemm(H, Lw.wo, H->attn, M, r));
-  { ProfScope ps_(H, PC_NORM, 1); CK(launch_rmsnorm(H->h, H->d, Lw.mlp_norm, H->xb, H->d, H->bf16, M, H->d, eps, nullptr, 0, nullptr, H->st)); }
   EpiParams s = epi(H, EPI_SWIGLU);
   s.out = H->act;
   s.ldo = H->F;
-  CKS(gemm(H, Lw.gu, H->xb, M, s));
+  fold_norm(H, s, H->ss);
+  CKS(gemm(H, Lw.gu, H->xraw, M, s));
+  if (next_tap >= 0) {
+    r.tap = H->taps;
+    r.tap_index = next_tap;
+  }
   CKS(gemm(H, Lw.down, H->act, M, r));
   return DF_OK;
 }
@@ -450,9 +483,10 @@ df_status layer_pass(df_handle* H, const Layer& Lw, int M, int R, int nseq, bool
 // Target over M rows (row_tok / row_pos / row_seq already set).  head_rows:
 // 0 = no LM head; -1 = every row; else only the last row (prefill).
 df_status target_pass(df_handle* H, int M, int R, int nseq, int max_len, bool want_taps, int head_mode) {
-  { ProfScope ps_(H, PC_EMBED, 1); CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, M, H->d, H->V, H->d_err, H->st)); }
+  { ProfScope ps_(H, PC_EMBED, 1); CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, H->xraw, H->ss, M, H->d, H->V, H->d_err, H->st)); }
   for (int l = 0; l < H->L; ++l) {
-    const int tap = want_taps ? H->tap_of_layer[l] : -1;
+    // the output of layer l is the input of layer l+1: tap it if selected
+    const int tap = (want_taps && l + 1 < H->L) ? H->tap_of_layer[l + 1] : -1;
     CKS(layer_pass(H, H->tl[l], M, R, nseq, true, l, max_len, tap));
   }
   H->rows_last_target = M;
@@ -469,13 +503,18 @@ df_status target_pass(df_handle* H, int M, int R, int nseq, int max_len, bool wa
 
 // Fuse the taps of rows [0, M) and inject K/V of every drafter layer at the
 // rows' positions (row_pos < 0: inactive row).
+// Fuse the taps of rows [0, M) and inject K/V of every drafter layer at the
+// rows' positions (row_pos < 0: inactive row).  The fusion GEMM writes the FC
+// output in the model dtype with its per-tile sums of squares; the RMSNorm
+// after the FC is folded into the injection GEMM (fc_norm gain in its
+// weights, 1/rms in its epilogue).
 df_status fuse_inject(df_handle* H, int M, const int* row_pos) {
-  EpiParams e = epi(H, EPI_STORE_F32);
-  e.out = H->fcout;
+  EpiParams e = epi(H, EPI_STORE_SS);
+  e.out = H->ctx;
   e.ldo = H->d;
+  e.ss_out = H->ss_ctx;
+  e.ss_tiles = H->d / 128;
   CKS(gemm(H, H->fc, H->taps, M, e, PC_FUSE));
-  { ProfScope ps_(H, PC_FUSE, 1); CK(launch_rmsnorm(H->fcout, H->d, H->fc_norm, H->ctx, H->d, H->bf16, M, H->d, H->cfg.rms_eps, nullptr, 0, row_pos,
-                    H->st)); }
   EpiParams k = epi(H, EPI_QKV);
   k.q_dim = 0;
   k.kv_dest = KV_PAGED;
@@ -483,6 +522,7 @@ df_status fuse_inject(df_handle* H, int M, const int* row_pos) {
   k.layer0 = 0;
   k.row_pos = row_pos;
   k.row_seq = H->d_row_seq;
+  fold_norm(H, k, H->ss_ctx);
   CKS(gemm(H, H->inj, H->ctx, M, k, PC_INJECT));
   H->rows_last_ctx = M;
   return DF_OK;
@@ -490,7 +530,7 @@ df_status fuse_inject(df_handle* H, int M, const int* row_pos) {
 
 df_status drafter_pass(df_handle* H, int nseq, int max_ctx_len) {
   const int B = H->B, M = nseq * B;
-  { ProfScope ps_(H, PC_EMBED, 1); CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, M, H->d, H->V, H->d_err, H->st)); }
+  { ProfScope ps_(H, PC_EMBED, 1); CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, H->xraw, H->ss, M, H->d, H->V, H->d_err, H->st)); }
   for (int l = 0; l < H->Ld; ++l) CKS(layer_pass(H, H->dl[l], M, B, nseq, false, l, max_ctx_len, -1));
   if (H->debug) CK(cudaMemcpyAsync(H->dbg_dh, H->h, (size_t)M * H->d * 4, cudaMemcpyDeviceToDevice, H->st));
   { ProfScope ps_(H, PC_NORM, 1); CK(launch_rmsnorm(H->h, H->d, H->d_final_norm, H->xb, H->d, H->bf16, M, H->d, H->cfg.rms_eps, nullptr, 0, nullptr,
@@ -682,6 +722,137 @@ df_status verify_impl(df_handle* H, const int32_t* slots, int nseq, const int32_
   return DF_OK;
 }
 
+// The device work of one draft + verify cycle for the sequences in d_slots_dev
+// (stream-ordered, nothing read back): draft pass, verification, acceptance,
+// fusion and injection, then the accepted tokens and counts copied to h_pin.
+// ext_events: record the timing events as graph-visible event nodes.
+df_status cycle_work(df_handle* H, const int* d_slots_dev, int nseq, int max_len_d, int max_len_t, bool ext_events) {
+  const int B = H->B;
+  auto rec = [&](cudaEvent_t e) {
+    return ext_events ? cudaEventRecordWithFlags(e, H->st, cudaEventRecordExternal) : cudaEventRecord(e, H->st);
+  };
+  CK(rec(H->ev[0]));
+  { ProfScope ps_(H, PC_CTRL, 1); CK(launch_prep_block(d_slots_dev, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 0, H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st)); }
+  CKS(drafter_pass(H, nseq, max_len_d));
+  { ProfScope ps_(H, PC_CTRL, 1); CK(launch_collect_drafts(H->d_ids, nseq, B, d_slots_dev, H->d_drafts, H->st)); }
+  CK(rec(H->ev[1]));
+  CK(rec(H->ev[2]));
+  { ProfScope ps_(H, PC_CTRL, 1); CK(launch_prep_block(d_slots_dev, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 1, H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st)); }
+  const int M = nseq * B;
+  CKS(target_pass(H, M, B, nseq, max_len_t, true, -1));
+  { ProfScope ps_(H, PC_CTRL, 1); CK(launch_accept(d_slots_dev, nseq, B, H->d_row_tok, H->d_ids, H->d_bonus, H->d_bonus_pos, H->d_acc, H->d_n, H->d_inj_pos, H->st)); }
+  CKS(fuse_inject(H, M, H->d_inj_pos));
+  CK(rec(H->ev[3]));
+  CK(d2h(H, H->h_pin, H->d_acc, (size_t)nseq * B * 4));
+  CK(d2h(H, H->h_pin + (size_t)nseq * B, H->d_n, (size_t)nseq * 4));
+  return DF_OK;
+}
+
+// Host bookkeeping after a cycle's results reached h_pin.
+df_status cycle_finish(df_handle* H, const int32_t* slots, int nseq, int32_t* acc_host, int32_t* n_host) {
+  const int B = H->B;
+  const int* acc = H->h_pin;
+  const int* n = H->h_pin + (size_t)nseq * B;
+  for (int i = 0; i < nseq; ++i) {
+    SeqHost& s = H->seqs[slots[i]];
+    const int k = n[i] - 1;
+    if (k < 0 || k > B - 1) return fail(H, DF_ECUDA, "accept kernel produced an invalid count");
+    s.len += k + 1;
+    s.bonus = acc[(size_t)i * B + k];
+    CKS(trim_pages(H, slots[i], s.len + B));
+    H->stats.cycles += 1;
+    H->stats.accepted_drafts += k;
+    H->stats.accept_hist[std::min(k, 64)] += 1;
+  }
+  float a = 0.f, b = 0.f;
+  if (cudaEventElapsedTime(&a, H->ev[0], H->ev[1]) == cudaSuccess) H->stats.draft_us += 1000.0 * a;
+  if (cudaEventElapsedTime(&b, H->ev[2], H->ev[3]) == cudaSuccess) H->stats.verify_us += 1000.0 * b;
+  if (acc_host) std::memcpy(acc_host, acc, (size_t)nseq * B * 4);
+  if (n_host) std::memcpy(n_host, n, (size_t)nseq * 4);
+  return DF_OK;
+}
+
+void drop_graph(df_handle* H) {
+  if (H->gexec) cudaGraphExecDestroy(H->gexec);
+  H->gexec = nullptr;
+  H->gkey.clear();
+}
+
+// One draft + verify cycle for df_generate.  After the first (eager) cycle of
+// a handle, the cycle's ~350 launches are captured once into a CUDA graph and
+// replayed; a new capture is made when the slots change or an attention
+// chunk boundary is crossed (the attention grids depend on the lengths).
+df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int32_t* acc_host, int32_t* n_host) {
+  CKS(check_slots(H, slots, nseq));
+  const int B = H->B;
+  int max_t = 0, max_d = 0;
+  for (int i = 0; i < nseq; ++i) {
+    SeqHost& s = H->seqs[slots[i]];
+    if (s.len + B > H->cfg.max_ctx) return fail(H, DF_EINVAL, "sequence would exceed max_ctx");
+    CKS(ensure_pages(H, slots[i], s.len + B));
+    max_t = std::max(max_t, s.len + B);
+    max_d = std::max(max_d, s.len);
+  }
+  const bool graphs = H->use_graphs && !H->profiling && H->graph_ready_cycles > 0;
+  if (!graphs) {
+    CK(h2d(H, H->d_slots, slots, nseq * 4));
+    CKS(cycle_work(H, H->d_slots, nseq, max_d, max_t, false));
+    CKS(sync(H));
+    H->graph_ready_cycles += 1;
+    return cycle_finish(H, slots, nseq, acc_host, n_host);
+  }
+  std::vector<int> key(slots, slots + nseq);
+  key.push_back((max_t + 63) / 64);
+  key.push_back((max_d + 63) / 64);
+  // the caller's stream may be the legacy default stream, which cannot be
+  // captured: graphs run on the engine's own stream, ordered after the
+  // caller's stream and joined back to it with events
+  const cudaStream_t user = H->st;
+  CK(cudaEventRecord(H->gjoin[0], user));
+  CK(cudaStreamWaitEvent(H->gstream, H->gjoin[0], 0));
+  if (!H->gexec || key != H->gkey) {
+    drop_graph(H);
+    CK(h2d(H, H->d_gslots, slots, nseq * 4));
+    CK(cudaStreamSynchronize(user));
+    const df_stats before = H->stats;
+    bool ok = cudaStreamBeginCapture(H->gstream, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+    df_status st = DF_OK;
+    cudaGraph_t g = nullptr;
+    if (ok) {
+      H->st = H->gstream;
+      st = cycle_work(H, H->d_gslots, nseq, max_d, max_t, true);
+      H->st = user;
+      ok = cudaStreamEndCapture(H->gstream, &g) == cudaSuccess && st == DF_OK;
+    }
+    H->st = user;
+    if (ok) ok = cudaGraphInstantiate(&H->gexec, g, 0) == cudaSuccess;
+    if (g) cudaGraphDestroy(g);
+    H->g_launches = H->stats.kernel_launches - before.kernel_launches;
+    H->g_h2d = H->stats.h2d_bytes - before.h2d_bytes;
+    H->g_d2h = H->stats.d2h_bytes - before.d2h_bytes;
+    H->stats = before;  // counted again at each replay
+    if (!ok) {
+      // capture is not available here: run this handle's cycles eagerly
+      (void)cudaGetLastError();
+      H->gexec = nullptr;
+      H->use_graphs = false;
+      CK(h2d(H, H->d_slots, slots, nseq * 4));
+      CKS(cycle_work(H, H->d_slots, nseq, max_d, max_t, false));
+      CKS(sync(H));
+      return cycle_finish(H, slots, nseq, acc_host, n_host);
+    }
+    H->gkey = key;
+  }
+  CK(cudaGraphLaunch(H->gexec, H->gstream));
+  CK(cudaEventRecord(H->gjoin[1], H->gstream));
+  CK(cudaStreamWaitEvent(H->st, H->gjoin[1], 0));
+  H->stats.kernel_launches += H->g_launches;
+  H->stats.h2d_bytes += H->g_h2d;
+  H->stats.d2h_bytes += H->g_d2h;
+  CKS(sync(H));
+  return cycle_finish(H, slots, nseq, acc_host, n_host);
+}
+
 df_status release(df_handle* H, int slot) {
   SeqHost& s = H->seqs[slot];
   for (int p : s.pages) H->free_pages.push_back(p);
@@ -812,6 +983,14 @@ df_status pack_weights(df_handle* H, const void* const* w, int nw) {
   H->inj = Linear{A + o_inj, (int)(H->Ld * 2 * kd), d, {}};
   CKS(gain(o_dfn, w[i++]));
   H->d_final_norm = reinterpret_cast<float*>(A + o_dfn);
+  // Fold each RMSNorm's gain into the columns of the weight that consumes the
+  // normalised rows (the norms themselves run in those GEMMs' epilogues).
+  for (auto* layers : {&H->tl, &H->dl})
+    for (Layer& Lw : *layers) {
+      CK(launch_scale_cols(Lw.qkv.ptr, H->bf16, Lw.qkv.N, d, Lw.attn_norm, st));
+      CK(launch_scale_cols(Lw.gu.ptr, H->bf16, Lw.gu.N, d, Lw.mlp_norm, st));
+    }
+  CK(launch_scale_cols(H->inj.ptr, H->bf16, H->inj.N, d, H->fc_norm, st));
   CK(cudaStreamSynchronize(st));
 
   if (H->bf16) {
@@ -849,6 +1028,7 @@ df_status alloc_state(df_handle* H) {
   CKS(dalloc_t(H, &H->d_inj_pos, M * 4));
   CKS(dalloc_t(H, &H->d_ids, M * 4));
   CKS(dalloc_t(H, &H->d_slots, c.max_batch * 4));
+  CKS(dalloc_t(H, &H->d_gslots, c.max_batch * 4));
   CKS(dalloc_t(H, &H->d_drafts, (size_t)c.max_batch * H->B * 4));
   CKS(dalloc_t(H, &H->d_acc, (size_t)c.max_batch * H->B * 4));
   CKS(dalloc_t(H, &H->d_n, c.max_batch * 4));
@@ -863,9 +1043,14 @@ df_status alloc_state(df_handle* H) {
   CKS(dalloc(H, &H->attn, (size_t)M * H->qdim * es));
   CKS(dalloc(H, &H->act, (size_t)M * H->F * es));
   CKS(dalloc(H, &H->taps, (size_t)M * 5 * d * es));
-  CKS(dalloc_t(H, &H->fcout, (size_t)M * d * 4));
   CKS(dalloc(H, &H->ctx, (size_t)M * d * es));
   CKS(dalloc(H, &H->blk, (size_t)2 * H->Hkv * M * H->hd * es));
+  CKS(dalloc(H, &H->xraw, (size_t)M * d * es));
+  CKS(dalloc_t(H, &H->ss, (size_t)M * (d / 128) * 4));
+  CKS(dalloc_t(H, &H->ss_ctx, (size_t)M * (d / 128) * 4));
+  CK(cudaMemset(H->xraw, 0, (size_t)M * d * es));
+  CK(cudaMemset(H->ss, 0, (size_t)M * (d / 128) * 4));
+  CK(cudaMemset(H->ss_ctx, 0, (size_t)M * (d / 128) * 4));
   // zero the activation buffers once so rows a pass does not write are finite
   CK(cudaMemset(H->xb, 0, (size_t)M * d * es));
   CK(cudaMemset(H->attn, 0, (size_t)M * H->qdim * es));
@@ -913,6 +1098,8 @@ df_status alloc_state(df_handle* H) {
   H->h_pin_ints = std::max<size_t>((size_t)c.max_batch * (H->B + 2) * 2, 64);
   CK(cudaMallocHost(&H->h_pin, H->h_pin_ints * 4));
   for (auto& e : H->ev) CK(cudaEventCreate(&e));
+  CK(cudaStreamCreateWithFlags(&H->gstream, cudaStreamNonBlocking));
+  for (auto& e : H->gjoin) CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
   return DF_OK;
 }
 
@@ -985,6 +1172,10 @@ df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_we
   H->kvdim = H->Hkv * H->hd;
   H->qkv_n = H->qdim + 2 * H->kvdim;
   H->Mmax = std::max(std::min(PREFILL_CHUNK, cfg->max_ctx), cfg->max_batch * cfg->block_size);
+  {
+    const char* g = getenv("DF_NO_GRAPH");
+    H->use_graphs = !(g && g[0] == '1');
+  }
   for (int l = 0; l < 1024; ++l) H->tap_of_layer[l] = -1;
   for (int i = 0; i < 5; ++i) H->tap_of_layer[cfg->feat_layers[i]] = i;
   int dev = 0;
@@ -1003,6 +1194,11 @@ df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_we
       delete H;
       return DF_ECUDA;
     }
+  }
+  if (tc_prepare() != cudaSuccess || attention_prepare() != cudaSuccess) {
+    delete H;
+    (void)cudaGetLastError();
+    return DF_ECUDA;
   }
   df_status s = pack_weights(H, weights, n_weights);
   if (s == DF_OK) s = alloc_state(H);
@@ -1068,9 +1264,7 @@ df_status df_generate(df_handle* H, const int32_t* prompts_host, const int32_t* 
     for (int i = 0; i < nseq; ++i)
       if (count[i] < n_new) active.push_back(i);
     if (active.empty()) break;
-    s = draft_impl(H, active.data(), (int)active.size(), nullptr);
-    if (s != DF_OK) break;
-    s = verify_impl(H, active.data(), (int)active.size(), nullptr, acc.data(), n.data(), true);
+    s = cycle_impl(H, active.data(), (int)active.size(), acc.data(), n.data());
     if (s != DF_OK) break;
     for (size_t j = 0; j < active.size(); ++j) {
       const int i = active[j];
@@ -1177,6 +1371,13 @@ void df_destroy(df_handle* H) {
   for (auto& e : H->ev)
     if (e) cudaEventDestroy(e);
   for (auto& e : H->evpool) cudaEventDestroy(e);
+  drop_graph(H);
+  if (H->gstream) {
+    cudaStreamSynchronize(H->gstream);
+    cudaStreamDestroy(H->gstream);
+  }
+  for (auto& e : H->gjoin)
+    if (e) cudaEventDestroy(e);
   delete H;
 }
 
@@ -1204,7 +1405,7 @@ df_status df_debug_read(df_handle* H, int32_t what, float* out_host, int64_t max
     case DF_DBG_LOGITS: src = H->dbg_logits; rows = H->rows_last_logits; cols = H->V; break;
     case DF_DBG_DRAFT_LOGITS: src = H->dbg_dlogits; rows = H->rows_last_draft; cols = H->V; break;
     case DF_DBG_DRAFT_HIDDEN: src = H->dbg_dh; rows = H->rows_last_draft; cols = H->d; break;
-    case DF_DBG_CTX: src = H->ctx; typed = true; rows = H->rows_last_ctx; cols = H->d; break;
+    case DF_DBG_CTX: src = H->ctx; typed = true; rows = H->rows_last_ctx; cols = H->d; break;  // normalised below
     case DF_DBG_HIDDEN: src = H->dbg_th; rows = H->rows_last_target; cols = H->d; break;
     default: return fail(H, DF_EINVAL, "unknown debug buffer");
   }
@@ -1220,6 +1421,20 @@ df_status df_debug_read(df_handle* H, int32_t what, float* out_host, int64_t max
     }
   } else {
     CK(cudaMemcpy(out_host, src, n * 4, cudaMemcpyDeviceToHost));
+  }
+  if (what == DF_DBG_CTX && rows > 0) {
+    // the fused context rows are stored before their RMSNorm (which runs folded
+    // into the injection GEMM): apply it here for inspection
+    const int tiles = H->d / 128;
+    std::vector<float> ss((size_t)rows * tiles), g(H->d);
+    CK(cudaMemcpy(ss.data(), H->ss_ctx, ss.size() * 4, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(g.data(), H->fc_norm, g.size() * 4, cudaMemcpyDeviceToHost));
+    for (int r = 0; r < rows; ++r) {
+      double t = 0.0;
+      for (int k = 0; k < tiles; ++k) t += ss[(size_t)r * tiles + k];
+      const double inv = 1.0 / std::sqrt(t / H->d + (double)H->cfg.rms_eps);
+      for (int i = 0; i < H->d; ++i) out_host[(size_t)r * H->d + i] = (float)(out_host[(size_t)r * H->d + i] * inv * g[i]);
+    }
   }
   if (rows_out) *rows_out = rows;
   return DF_OK;

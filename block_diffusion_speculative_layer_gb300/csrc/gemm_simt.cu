@@ -33,11 +33,12 @@ __global__ void __launch_bounds__(128) epilogue_f32_kernel(const float* __restri
   pdl_trigger();
   __shared__ float tile[EPI_ROWS * EPI_LD];
   __shared__ RowMeta meta[EPI_ROWS];
+  __shared__ float red[EPI_ROWS * 4];
   const int n0 = blockIdx.x * 128, m0 = blockIdx.y * EPI_ROWS;
   const int rows = min(EPI_ROWS, M - m0);
   for (int r = 0; r < rows; ++r) tile[r * EPI_LD + threadIdx.x] = y[(size_t)(m0 + r) * N + n0 + threadIdx.x];
   __syncthreads();
-  epilogue_tile<float>(ep, tile, EPI_LD, n0, m0, rows, M, meta);
+  epilogue_tile<float>(ep, tile, EPI_LD, n0, m0, rows, M, meta, red);
 }
 
 cudaError_t launch_gemm_f32(const float* x, const float* w, float* tmp, int M, int N, int K, const EpiParams& ep,

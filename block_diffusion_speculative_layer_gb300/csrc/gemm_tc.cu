@@ -146,7 +146,7 @@ struct TcCfg {
   static constexpr int TMEM_COLS = NT < 32 ? 32 : NT;
   static constexpr int TLD = BM + 4;  // epilogue tile row stride (floats)
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
-  static_assert(NT * TLD * 4 + NT * 8 <= STAGES * STAGE_BYTES, "epilogue tile and row facts must fit in the ring");
+  static_assert(NT * TLD * 4 + NT * (12 + 16) <= STAGES * STAGE_BYTES, "epilogue tile and row facts must fit in the ring");
 };
 
 template <int NT>
@@ -331,7 +331,8 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
     __syncthreads();
   }
   epilogue_tile<__nv_bfloat16>(ep, tile, C::TLD, n0, m0, rows, M,
-                               reinterpret_cast<RowMeta*>(smem + (size_t)NT * C::TLD * 4));
+                               reinterpret_cast<RowMeta*>(smem + (size_t)NT * C::TLD * 4),
+                               reinterpret_cast<float*>(smem + (size_t)NT * C::TLD * 4 + (size_t)NT * sizeof(RowMeta)));
 }
 
 // ----------------------------------------------------------------------------
@@ -395,6 +396,22 @@ size_t tc_workspace_floats(int M, int N, int splits, int nt) {
   return tiles * splits * nt * BM;
 }
 size_t tc_counter_ints(int M, int N, int nt) { return (size_t)(N / BM) * ((M + nt - 1) / nt); }
+
+template <int NT>
+static cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(gemm_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<NT>::SMEM);
+}
+
+// Set every token-tile variant's shared-memory limit up front (before any
+// stream capture).
+cudaError_t tc_prepare() {
+  cudaError_t e;
+  if ((e = set_smem_attr<16>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<32>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<64>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<128>()) != cudaSuccess) return e;
+  return set_smem_attr<256>();
+}
 
 template <int NT>
 static cudaError_t launch_nt(const void* tmW, const void* tmX, int M, int N, int K, int splits, float* ws,

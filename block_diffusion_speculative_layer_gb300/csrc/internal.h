@@ -34,6 +34,7 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 // ---- tcgen05 GEMM (gemm_tc.cu)
 bool make_tmap_bf16(void* map_out, const void* ptr, long long rows, long long cols, int box_rows);
 int tc_token_tile(int M);
+cudaError_t tc_prepare();         // kernel attributes, once, before any stream capture
 int tc_splits(int N, int K, int sm_count);
 size_t tc_workspace_floats(int M, int N, int splits, int nt);
 size_t tc_counter_ints(int M, int N, int nt);
@@ -69,12 +70,17 @@ struct AttnParams {
   int* err;
 };
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st);
+cudaError_t attention_prepare();  // kernel attributes, once, before any stream capture
 // bf16, head_dim 128: tensor-core partials (attention_mma.cu); merged by launch_attention.
 cudaError_t launch_attention_mma(const AttnParams& p, cudaStream_t st);
 
 // ---- small kernels (misc.cu)
-cudaError_t launch_embed(const void* embed, bool bf16, const int* tok, float* h, int M, int d, int vocab, int* err,
-                         cudaStream_t st);
+// h[m] = embed[tok[m]] (fp32), xraw[m] = the same row in the model dtype,
+// ss[m][tile] = its sum of squares per 128-feature tile.
+cudaError_t launch_embed(const void* embed, bool bf16, const int* tok, float* h, void* xraw, float* ss, int M, int d,
+                         int vocab, int* err, cudaStream_t st);
+// W[n][k] *= gain[k] (init only).
+cudaError_t launch_scale_cols(void* w, bool bf16, long long rows, int cols, const float* gain, cudaStream_t st);
 // out[m] = T(h[m] * rsqrt(mean(h[m]^2) + eps) * gain); optionally taps[m][tap][:] = T(h[m]).
 // rows with row_pos[m] < 0 (if row_pos given) are skipped.
 cudaError_t launch_rmsnorm(const float* h, int ldh, const float* gain, void* out, int ldo, bool bf16, int M, int d,

@@ -17,27 +17,62 @@ bool pdl_enabled() {
   return on != 0;
 }
 
+// Embedding gather for the rows of a pass: h[m] = embed[tok[m]] (fp32), the
+// same row in the model dtype for the first layer's GEMM, and its sum of
+// squares per 128-feature tile (the folded RMSNorm of that GEMM).  128 threads.
 template <typename T>
-__global__ void embed_kernel(const T* __restrict__ embed, const int* __restrict__ tok, float* __restrict__ h, int d,
-                             int vocab, int* err) {
+__global__ void __launch_bounds__(128) embed_kernel(const T* __restrict__ embed, const int* __restrict__ tok,
+                                                    float* __restrict__ h, T* __restrict__ xraw,
+                                                    float* __restrict__ ss, int d, int vocab, int* err) {
   pdl_wait();
   pdl_trigger();
+  __shared__ float red[4];
   const int m = blockIdx.x;
   const int t = tok[m];
-  if (t < 0 || t >= vocab) {
-    if (threadIdx.x == 0 && t >= vocab) flag_error(err, ERR_BOUNDS);
-    for (int i = threadIdx.x; i < d; i += blockDim.x) h[(size_t)m * d + i] = 0.f;
-    return;
+  const bool ok = t >= 0 && t < vocab;
+  if (!ok && threadIdx.x == 0 && t >= vocab) flag_error(err, ERR_BOUNDS);
+  const int tiles = d >> 7;
+  for (int tl = 0; tl < tiles; ++tl) {
+    const int i = tl * 128 + threadIdx.x;
+    const float v = ok ? Cvt<T>::to_f(embed[(size_t)t * d + i]) : 0.f;
+    h[(size_t)m * d + i] = v;
+    xraw[(size_t)m * d + i] = Cvt<T>::from_f(v);
+    float q = v * v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = q;
+    __syncthreads();
+    if (threadIdx.x == 0) ss[(size_t)m * tiles + tl] = ((red[0] + red[1]) + red[2]) + red[3];
+    __syncthreads();
   }
-  for (int i = threadIdx.x; i < d; i += blockDim.x) h[(size_t)m * d + i] = Cvt<T>::to_f(embed[(size_t)t * d + i]);
 }
 
-cudaError_t launch_embed(const void* embed, bool bf16, const int* tok, float* h, int M, int d, int vocab, int* err,
-                         cudaStream_t st) {
+cudaError_t launch_embed(const void* embed, bool bf16, const int* tok, float* h, void* xraw, float* ss, int M, int d,
+                         int vocab, int* err, cudaStream_t st) {
+  if (d % 128) return cudaErrorInvalidValue;
   if (bf16)
-    return launch_k(embed_kernel<__nv_bfloat16>, dim3(M), dim3(256), 0, st, reinterpret_cast<const __nv_bfloat16*>(embed), tok, h, d, vocab, err);
+    return launch_k(embed_kernel<__nv_bfloat16>, dim3(M), dim3(128), 0, st,
+                    reinterpret_cast<const __nv_bfloat16*>(embed), tok, h, reinterpret_cast<__nv_bfloat16*>(xraw), ss, d,
+                    vocab, err);
+  return launch_k(embed_kernel<float>, dim3(M), dim3(128), 0, st, reinterpret_cast<const float*>(embed), tok, h,
+                  reinterpret_cast<float*>(xraw), ss, d, vocab, err);
+}
+
+// W[n][k] *= gain[k] for a [rows][cols] matrix (a norm's gain folded into the
+// weight that consumes the normalised rows).
+template <typename T>
+__global__ void scale_cols_kernel(T* __restrict__ w, long long rows, int cols, const float* __restrict__ gain) {
+  const long long n = rows * cols;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    w[i] = Cvt<T>::from_f(Cvt<T>::to_f(w[i]) * gain[i % cols]);
+}
+
+cudaError_t launch_scale_cols(void* w, bool bf16, long long rows, int cols, const float* gain, cudaStream_t st) {
+  if (bf16)
+    scale_cols_kernel<__nv_bfloat16><<<1024, 256, 0, st>>>(reinterpret_cast<__nv_bfloat16*>(w), rows, cols, gain);
   else
-    return launch_k(embed_kernel<float>, dim3(M), dim3(256), 0, st, reinterpret_cast<const float*>(embed), tok, h, d, vocab, err);
+    scale_cols_kernel<float><<<1024, 256, 0, st>>>(reinterpret_cast<float*>(w), rows, cols, gain);
+  return cudaGetLastError();
 }
 
 // One block per row; the sum of squares is reduced in a fixed order

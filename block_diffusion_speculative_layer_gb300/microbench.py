@@ -33,6 +33,10 @@ def drafter(a):
     for B in blocks:
         # the target is not used by the drafter step: its minimum depth keeps memory low
         shape = syn.QWEN3_8B.replace(name=f"drafter-step-B{B}", n_layers=8, block_size=B)
+        if a.reduced:
+            # Qwen3-8B width and heads, one drafter layer, a 4096-token vocabulary:
+            # the same kernels on a few GB of device memory (profiling captures)
+            shape = shape.replace(draft_layers=1, vocab=4096)
         d, kvd = shape.d_model, shape.kv_dim
         max_b = max(batches)
         eng = dfl.Engine(shape, syn.iter_weights(shape), max_batch=max_b, max_ctx=max(ctxs) + 2 * B)
@@ -68,6 +72,7 @@ def main():
     ap.add_argument("--blocks", default="8,16")
     ap.add_argument("--ctx", default="1024,4096,16384,32768")
     ap.add_argument("--batch", default="1,4,16,32")
+    ap.add_argument("--reduced", action="store_true", help="drafter: 1 drafter layer, vocab 4096")
     ap.add_argument("--M", type=int, default=16)
     ap.add_argument("--N", type=int, default=24576)
     ap.add_argument("--K", type=int, default=4096)
@@ -78,7 +83,7 @@ def main():
     a = ap.parse_args()
     build.build()
     if a.op == "drafter":
-        a.iters = min(a.iters, 5)
+        a.iters = min(a.iters, 5) if a.iters != 20 else 5
         drafter(a)
         return
     g = torch.Generator(device="cuda").manual_seed(0)

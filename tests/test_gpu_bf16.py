@@ -158,3 +158,41 @@ def test_wide_lossless(wide):
     p = syn.make_prompt(WIDE, 64, stream=5)
     spec, _ = wide.eng.generate([p], 40)
     np.testing.assert_array_equal(spec, wide.eng.greedy_reference([p], 40))
+
+
+# ---------------------------------------------------------------- serving-shaped batch and the 27B-class width
+
+def test_serving_batch_lossless(dfl, small):
+    """16 sequences with prompt lengths uniform over 128..2048 in 16-token
+    pages, block 16: speculative == greedy per sequence, every sequence's own
+    accept lengths and rollback in one batch."""
+    eng = dfl.Engine(SMALL, small.w, max_batch=16, max_ctx=2048 + 64 + 64)
+    try:
+        lens = syn.make_prompt_lengths(16, 128, 2048)
+        prompts = [syn.make_prompt(SMALL, int(L), stream=100 + i) for i, L in enumerate(lens)]
+        spec, stats = eng.generate(prompts, 48)
+        greedy = eng.greedy_reference(prompts, 48)
+        np.testing.assert_array_equal(spec, greedy)
+        assert stats["cycles"] >= 16
+        # pages were returned: the same slots serve a second batch
+        spec2, _ = eng.generate(prompts[:3], 20)
+        np.testing.assert_array_equal(spec2, greedy[:3, :20])
+    finally:
+        eng.close()
+
+
+DENSE27 = syn.DENSE_27B.replace(name="27b-width-8-layers", n_layers=8, draft_layers=1)
+
+
+def test_27b_width_parity_and_lossless(dfl):
+    """d=5120, 40 query / 8 KV heads (5 per group), SwiGLU 17408, vocab 151936:
+    teacher-forced parity with the oracle at the full-width bound, and
+    speculative == greedy."""
+    s = Setup(dfl, DENSE27, 0.0, 1, 256, cache=False)
+    try:
+        _verify_parity(dfl, s, syn.make_prompt(DENSE27, 40, stream=6), tol=TOL_WIDE)
+        p = syn.make_prompt(DENSE27, 64, stream=7)
+        spec, _ = s.eng.generate([p], 24)
+        np.testing.assert_array_equal(spec, s.eng.greedy_reference([p], 24))
+    finally:
+        s.eng.close()
