@@ -127,22 +127,17 @@ __device__ __forceinline__ void row_sumsq(float v, int r, float* red) {
   if ((threadIdx.x & 31) == 0) red[r * 4 + (threadIdx.x >> 5)] = q;
 }
 
-constexpr int EPI_BATCH = 8;  // rows whose global loads are issued together
+constexpr int EPI_BATCH = 16;  // rows whose global loads are issued together
 
-// Apply the epilogue to one result tile held in shared memory.
-//   tile[r * ld + f] = acc for row m0 + r, feature n0 + f, f in [0, 128),
-//   r in [0, rows), rows <= M - m0.  Called by exactly 128 threads (one per
-//   feature column); meta has room for `rows` entries.  Contains
-//   __syncthreads(), so all 128 threads must call it.
-template <typename T>
-__device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, int n0, int m0, int rows, int M,
-                              RowMeta* meta, float* red) {
-  const int f = threadIdx.x & 127;
-  const int n = n0 + f;
+// Stage the per-row facts the epilogue needs (positions, KV pages, 1/rms of
+// folded norms) into meta.  Run by `nthr` threads (whole warps) with index
+// `tid`; the caller synchronises before epilogue_tile reads meta.
+__device__ __forceinline__ void epilogue_stage(const EpiParams& ep, int m0, int rows, int M, RowMeta* meta, int tid,
+                                               int nthr) {
   rows = min(rows, M - m0);
   const bool need_meta = ep.kind == EPI_QKV || (ep.kind == EPI_RESID && ep.row_pos);
   if (need_meta) {
-    for (int r = threadIdx.x; r < rows; r += 128) {
+    for (int r = tid; r < rows; r += nthr) {
       const int m = m0 + r;
       const int pos = ep.row_pos[m];
       meta[r].pos = pos;
@@ -154,8 +149,9 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
   if (ep.ss_in) {
     // 1/rms per row: 8 threads per row each add every 8th tile partial, then a
     // fixed xor tree joins them (the same order for every row and batch).
-    for (int rb = 0; rb < rows; rb += 16) {
-      const int r = rb + (threadIdx.x >> 3), j = threadIdx.x & 7;
+    const int per_pass = nthr >> 3;
+    for (int rb = 0; rb < rows; rb += per_pass) {
+      const int r = rb + (tid >> 3), j = tid & 7;
       float part = 0.f;
       if (r < rows) {
         const float* sp = ep.ss_in + (size_t)(m0 + r) * ep.ss_tiles;
@@ -167,7 +163,24 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
       if (r < rows && j == 0) meta[r].scale = rsqrtf(part * ep.inv_d + ep.eps);
     }
   }
-  if (need_meta || ep.ss_in) __syncthreads();
+}
+
+// Apply the epilogue to one result tile held in shared memory.
+//   tile[r * ld + f] = acc for row m0 + r, feature n0 + f, f in [0, 128),
+//   r in [0, rows), rows <= M - m0.  Called by exactly 128 threads (one per
+//   feature column).  meta has room for `rows` entries; if `staged`, the
+//   caller already ran epilogue_stage into it and synchronised.  red holds
+//   4 floats per row.  Contains __syncthreads(), so all 128 threads call it.
+template <typename T>
+__device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, int n0, int m0, int rows, int M,
+                              RowMeta* meta, float* red, bool staged = false) {
+  const int f = threadIdx.x & 127;
+  const int n = n0 + f;
+  rows = min(rows, M - m0);
+  if (!staged) {
+    epilogue_stage(ep, m0, rows, M, meta, threadIdx.x & 127, 128);
+    __syncthreads();
+  }
   const bool scaled = ep.ss_in != nullptr;
   switch (ep.kind) {
     case EPI_STORE: {

@@ -145,8 +145,9 @@ struct TcCfg {
   static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
   static constexpr int TMEM_COLS = NT < 32 ? 32 : NT;
   static constexpr int TLD = BM + 4;  // epilogue tile row stride (floats)
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
-  static_assert(NT * TLD * 4 + NT * (12 + 16) <= STAGES * STAGE_BYTES, "epilogue tile and row facts must fit in the ring");
+  static constexpr int META_OFF = STAGES * STAGE_BYTES + 256;   // row facts staged during the mainloop
+  static constexpr int SMEM = 1024 + META_OFF + NT * (int)sizeof(RowMeta);
+  static_assert(NT * TLD * 4 + NT * 16 <= STAGES * STAGE_BYTES, "epilogue tile and row sums must fit in the ring");
 };
 
 template <int NT>
@@ -252,6 +253,11 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
     flags[1] = i;
     mma_commit(accum_bar);  // arrives once every MMA issued above has completed
   }
+  // Warps 2 and 3 are idle during the mainloop: they stage the epilogue's
+  // row facts (positions, KV pages, folded-norm scales) now, so the tail after
+  // the last MMA does no dependent global loads of its own.
+  RowMeta* meta = reinterpret_cast<RowMeta*>(smem + C::META_OFF);
+  if (warp >= 2) epilogue_stage(ep, m0, NT, M, meta, threadIdx.x - 64, 64);
   __syncwarp();
 
   // ---- drain the accumulator: thread t holds weight row n0 + t for all NT tokens
@@ -330,9 +336,8 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
     if (threadIdx.x == 0) counters[tile_id] = 0;
     __syncthreads();
   }
-  epilogue_tile<__nv_bfloat16>(ep, tile, C::TLD, n0, m0, rows, M,
-                               reinterpret_cast<RowMeta*>(smem + (size_t)NT * C::TLD * 4),
-                               reinterpret_cast<float*>(smem + (size_t)NT * C::TLD * 4 + (size_t)NT * sizeof(RowMeta)));
+  epilogue_tile<__nv_bfloat16>(ep, tile, C::TLD, n0, m0, rows, M, meta,
+                               reinterpret_cast<float*>(smem + (size_t)NT * C::TLD * 4), /*staged=*/true);
 }
 
 // ----------------------------------------------------------------------------
