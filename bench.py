@@ -197,6 +197,18 @@ def oracle_cycle_sample(shape, prompt_len: int, tau: float, repeats: int = 1):
 
 # ---------------------------------------------------------------------------- arms
 
+def aggregate(secs: float, tokens: int, dist=None, device="cpu"):
+    """Whole-job numbers over replicas: every rank's tokens over the slowest rank's time."""
+    if dist is None:
+        return secs, tokens
+    import torch
+    t = torch.tensor([secs], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -285,12 +297,8 @@ def run_ours(args):
     clk = clocks.stop()
     barrier()
     st = eng.stats()
-    secs = e0.elapsed_time(e1) / 1000.0
-    if dist is not None:
-        t = torch.tensor([secs], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = float(t.item())
-    value = world * args.steps * n_new / secs
+    secs, total_tokens = aggregate(e0.elapsed_time(e1) / 1000.0, args.steps * n_new, dist, "cuda")
+    value = total_tokens / secs
     cycles = max(st["cycles"], 1)
     tau = (st["accepted_drafts"] + st["cycles"]) / cycles
 

@@ -320,11 +320,12 @@ class Engine:
     def bench_drafter_step(self, nseq: int, ctx_len: int, taps: np.ndarray, iters: int = 5) -> Dict[str, float]:
         """Device microseconds per drafter step: fusion, injection, block attention, LM-head argmax."""
         t = np.ascontiguousarray(taps, dtype=np.float32).reshape(-1, 5 * self.d)
-        out = (ctypes.c_double * 4)()
+        out = (ctypes.c_double * 6)()
         self._check(self.L.df_bench_drafter_step(self.h, nseq, ctx_len,
                                                  t.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), t.shape[0],
                                                  iters, out), "df_bench_drafter_step")
-        return {"fuse_us": out[0], "inject_us": out[1], "block_attention_us": out[2], "lm_head_us": out[3]}
+        return {"fuse_us": out[0], "inject_us": out[1], "block_attention_us": out[2], "lm_head_us": out[3],
+                "layer_gemms_us": out[4], "drafter_pass_us": out[5]}
 
     def weight_ptr(self, which: int) -> int:
         a = ctypes.c_uint64()

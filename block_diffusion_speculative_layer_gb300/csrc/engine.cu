@@ -1488,7 +1488,7 @@ df_status df_profile_read(df_handle* H, df_kernel_stat* out, int32_t max, int32_
 }
 
 df_status df_bench_drafter_step(df_handle* H, int32_t nseq, int32_t ctx_len, const float* taps_host,
-                                 int32_t taps_rows, int32_t iters, double us_out[4]) {
+                                 int32_t taps_rows, int32_t iters, double us_out[6]) {
   GUARD(H);
   const int B = H->B, d = H->d;
   if (nseq < 1 || nseq > H->cfg.max_batch || ctx_len < 1 || ctx_len + B > H->cfg.max_ctx || iters < 1 || !us_out ||
@@ -1552,11 +1552,24 @@ df_status df_bench_drafter_step(df_handle* H, int32_t nseq, int32_t ctx_len, con
     }
     df_kernel_stat st[PC_N];
     CKS(df_profile_read(H, st, PC_N, &nj));
-    if (!was) CKS(df_profile_enable(H, 0));
+    CKS(df_profile_enable(H, 0));
     us_out[0] = st[PC_FUSE].total_us / iters;
     us_out[1] = st[PC_INJECT].total_us / iters;
     us_out[2] = st[PC_ATTN].total_us / iters;
     us_out[3] = st[PC_LMHEAD].total_us / iters;
+    us_out[4] = st[PC_GEMM].total_us / iters;
+    // the whole drafter pass without per-launch events (launch overlap intact)
+    CK(cudaEventRecord(H->ev[0], H->st));
+    for (int it = 0; it < iters; ++it) {
+      { ProfScope ps_(H, PC_CTRL, 1); CK(launch_prep_block(H->d_slots, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 0, H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st)); }
+      CKS(drafter_pass(H, nseq, ctx_len));
+    }
+    CK(cudaEventRecord(H->ev[1], H->st));
+    CKS(sync(H));
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, H->ev[0], H->ev[1]));
+    us_out[5] = 1000.0 * ms / iters;
+    if (was) CKS(df_profile_enable(H, 1));
     return DF_OK;
   };
   df_status s = body();

@@ -4,6 +4,7 @@
   python -m block_diffusion_speculative_layer_gb300.microbench lmhead --M 16 --N 151936 --K 4096
   python -m block_diffusion_speculative_layer_gb300.microbench drafter [--blocks 8,16] [--ctx 1024,4096,16384,32768]
                                                                        [--batch 1,4,16,32]
+  python -m block_diffusion_speculative_layer_gb300.microbench ar_proxy
 
 Inputs are seeded synthetic bf16 (N(0,1) activations, N(0,0.02) weights)
 drawn on the GPU by torch.  For small shapes several weight copies are used
@@ -55,10 +56,35 @@ def drafter(a):
                       "lm_head": r["lm_head_us"]}
                 print(json.dumps({"op": "drafter_step", "block": B, "ctx": C, "batch": nb,
                                   "us": {k: round(v, 2) for k, v in us.items()},
+                                  "drafter_pass_us": round(r["drafter_pass_us"], 2),
                                   "total_us": round(sum(us.values()), 2),
                                   "GB/s": {k: round(byts[k] / (us[k] * 1e-6) / 1e9, 1) for k in us if us[k] > 0}}),
                       flush=True)
         eng.close()
+
+
+def ar_proxy(a):
+    """Draft latency of one 5-layer, 16-slot drafter pass against an
+    autoregressive 1-layer drafter making 8 drafts in 8 sequential passes
+    (each pass: one layer over a 2-row block and the LM head), both at the
+    Qwen3-8B width, batch 1, 1024 context positions."""
+    import block_diffusion_speculative_layer_gb300 as dfl
+    import synthetic as syn
+
+    C = 1024
+    taps = syn.make_hidden(512, 5 * 4096).reshape(512, 5, 4096)
+    res = {}
+    for name, layers, B in (("dflash_5layer_block16", 5, 16), ("ar_1layer_step", 1, 2)):
+        shape = syn.QWEN3_8B.replace(name=name, n_layers=8, draft_layers=layers, block_size=B)
+        eng = dfl.Engine(shape, syn.iter_weights(shape), max_batch=1, max_ctx=C + 2 * B)
+        res[name] = eng.bench_drafter_step(1, C, taps, iters=10)["drafter_pass_us"]
+        eng.close()
+    ar8 = 8 * res["ar_1layer_step"]
+    print(json.dumps({"op": "draft_latency_proxy", "ctx": C,
+                      "dflash_5layer_16slots_us": round(res["dflash_5layer_block16"], 2),
+                      "ar_1layer_8steps_us": round(ar8, 2),
+                      "ratio_ar_over_dflash": round(ar8 / res["dflash_5layer_block16"], 3),
+                      "note": "random weights: latency only; one drafter pass includes its LM head"}))
 
 
 def main():
@@ -68,7 +94,7 @@ def main():
     from block_diffusion_speculative_layer_gb300 import build
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["gemm", "lmhead", "drafter"])
+    ap.add_argument("op", choices=["gemm", "lmhead", "drafter", "ar_proxy"])
     ap.add_argument("--blocks", default="8,16")
     ap.add_argument("--ctx", default="1024,4096,16384,32768")
     ap.add_argument("--batch", default="1,4,16,32")
@@ -82,6 +108,9 @@ def main():
     ap.add_argument("--token-tile", type=int, default=0)
     a = ap.parse_args()
     build.build()
+    if a.op == "ar_proxy":
+        ar_proxy(a)
+        return
     if a.op == "drafter":
         a.iters = min(a.iters, 5) if a.iters != 20 else 5
         drafter(a)

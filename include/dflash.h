@@ -277,11 +277,13 @@ df_status df_op_gemm_bf16_noalloc(const void* x_dev, const void* w_dev, float* y
  * then runs `iters` times: fusion and injection of one block of feature rows
  * per sequence, and one drafter pass over [bonus, MASK x (B-1)] at position
  * ctx_len.  us_out receives the mean device microseconds per iteration of
- * [0] the fusion GEMM + its RMSNorm, [1] the injection GEMM, [2] block
- * attention summed over the drafter layers, [3] the LM-head argmax (CUDA
- * events around each launch; [ARCH] 第一层/第二层/第三层 and Shared LM Head). */
+ * [0] the fusion GEMM (its RMSNorm is folded into the injection), [1] the
+ * injection GEMM, [2] block attention summed over the drafter layers, [3] the
+ * LM-head argmax, [4] the drafter's layer GEMMs (CUDA events around each
+ * launch), and [5] one whole drafter pass timed without per-launch events
+ * ([ARCH] 第一层/第二层/第三层 and Shared LM Head). */
 df_status df_bench_drafter_step(df_handle* h, int32_t nseq, int32_t ctx_len, const float* taps_host,
-                                int32_t taps_rows, int32_t iters, double us_out[4]);
+                                int32_t taps_rows, int32_t iters, double us_out[6]);
 
 /* Device time of the tcgen05 GEMM alone: y = x . w^T launched `iters` times
  * back to back on `stream` (tensor maps and split-K workspace made once),
