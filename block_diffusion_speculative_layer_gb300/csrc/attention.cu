@@ -47,8 +47,8 @@ __device__ __forceinline__ int ctx_len_of(const AttnParams& p, int m) {
 
 template <typename T, int HD, int MAXQ>
 __global__ void __launch_bounds__(ATT_THREADS) attn_partial_kernel(AttnParams p) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   constexpr int DPL = HD / 32;  // head dims per lane
   // MAXQ: query vectors per warp (16 rows x group size / 8 warps, rounded up)
   extern __shared__ float sm[];
@@ -196,8 +196,8 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial_kernel(AttnParams p)
 // Loads are issued eight chunks at a time; the sums still run in chunk order.
 template <typename T, int HD>
 __global__ void attn_combine_kernel(AttnParams p) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   constexpr int CB = 8;
   const int m = blockIdx.x, head = blockIdx.y, d = threadIdx.x;
   if (p.row_pos[m] < 0) return;

@@ -59,8 +59,8 @@ __device__ __forceinline__ int ctx_len_rows(const AttnParams& p, int m) {
 }
 
 __global__ void __launch_bounds__(256) attn_mma_kernel(AttnParams p) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   __shared__ __align__(128) uint8_t sK[MC * ROWB];
   __shared__ __align__(128) uint8_t sV[MC * ROWB];
   const int G = p.Hq / p.Hkv;

@@ -7,6 +7,13 @@
 
 namespace dfk {
 
+// Kernel-side L2 look-ahead of a GEMM launch (see gemm_tc.cu).
+struct L2Ahead {
+  const void* next;
+  unsigned long long next_bytes;
+  int own_tiles;
+};
+
 // Bits of the sticky device error word.
 enum : int {
   ERR_TIMEOUT = 1,     // a bounded mbarrier wait ran out
@@ -22,6 +29,11 @@ __device__ __forceinline__ void flag_error(int* err, int bit) {
 // that it may start while the kernel before it drains: pdl_wait() blocks until
 // that kernel has finished and its writes are visible (a no-op when launched
 // normally); pdl_trigger() lets the next kernel start its own prologue.
+// Kernels trigger first and then wait: a kernel launched early does nothing
+// before its own wait but read constant weights, and a kernel can only be
+// launched once every CTA of the one before it is resident, so a chain of
+// early launches never holds back a kernel it depends on.  (The GEMM lets its
+// weight loads run ahead of the wait.)
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

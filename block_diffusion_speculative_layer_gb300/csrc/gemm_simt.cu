@@ -10,8 +10,8 @@ namespace dfk {
 
 __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                        float* __restrict__ y, int M, int N, int K) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + warp;
   const int m = blockIdx.y;
@@ -29,8 +29,8 @@ constexpr int EPI_ROWS = 16;
 constexpr int EPI_LD = 129;
 
 __global__ void __launch_bounds__(128) epilogue_f32_kernel(const float* __restrict__ y, int N, int M, EpiParams ep) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   __shared__ float tile[EPI_ROWS * EPI_LD];
   __shared__ RowMeta meta[EPI_ROWS];
   __shared__ float red[EPI_ROWS * 4];

@@ -16,14 +16,25 @@
 // tcgen05.ld (thread t holds weight row n0+t for every token) into a shared
 // tile on which the fused epilogue runs.
 //
-// Split-K partials go to a workspace; the CTA that finishes a tile last (an
-// atomic ticket, no waiting) adds the partials in split order 0,1,2,... and
-// runs the epilogue.  The split count depends only on (N, K), and the MMA
-// sequence of one output does not depend on M, so every output is bitwise
-// the same whatever the number of token rows.
+// Split-K: the `splits` CTAs of a tile form a thread-block cluster.  Each
+// leaves its fp32 partial tile in its own shared memory; after a cluster
+// barrier, CTA q sums rows [rows*q/splits, rows*(q+1)/splits) of all partials
+// through distributed shared memory, in split order 0,1,2,..., and runs the
+// epilogue on those rows; a second barrier keeps every CTA's shared memory
+// alive until the reads are done.  (Without clusters the partials go to a
+// workspace instead and the CTA that finishes a tile last, by an atomic
+// ticket, adds them in the same order.)  The split count depends only on
+// (N, K), and the MMA sequence of one output does not depend on M, so every
+// output is bitwise the same whatever the number of token rows.
 //
 // Launched with programmatic dependent launch: the producer streams the first
-// STAGES weight tiles before waiting for the previous kernel's outputs.
+// STAGES weight tiles before waiting for the previous kernel's outputs, and
+// asks L2 for a further stretch of its weight slice (a byte budget split over
+// the grid) so that DRAM stays busy while the previous kernel drains.  Once
+// its own loads are issued it can also start another matrix (the next GEMM's
+// weights, which do not depend on anything computed here) towards L2: decode
+// runs a chain of small kernels, and this keeps the weight stream going across
+// the gaps between them (attention in particular).
 //
 // Every mbarrier wait is bounded (about two seconds); on expiry the kernel
 // records ERR_TIMEOUT, waits (bounded) for the TMA loads it issued, frees its
@@ -83,6 +94,37 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
+}
+
+// L2 prefetch of one weight tile (no shared memory is written, nothing to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+// L2 prefetch of a byte range (16-byte aligned start, size a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes) : "memory");
+}
+
+// Thread-block cluster helpers (all threads of every CTA execute the barriers).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory offset in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float dsmem_ld(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -154,7 +196,7 @@ template <int NT>
 __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                       const __grid_constant__ CUtensorMap tmX, int M, int N, int K,
                                                       int splits, float* __restrict__ ws, int* __restrict__ counters,
-                                                      EpiParams ep) {
+                                                      int creduce, L2Ahead pf, EpiParams ep) {
   using C = TcCfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -210,6 +252,10 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
       mbar_expect_tx(full0 + 8 * i, C::STAGE_BYTES);
       tma_load_2d(smem_u32(sW + i * C::W_BYTES), &tmW, full0 + 8 * i, (kb0 + i) * BK, n0, pol_w);
     }
+    if (tile_m == 0) {
+      const int pf_end = min(nk, pre + pf.own_tiles);
+      for (int i = pre; i < pf_end; ++i) tma_prefetch_2d(&tmW, (kb0 + i) * BK, n0);
+    }
     pdl_wait();
     for (int i = 0; i < pre; ++i)
       tma_load_2d(smem_u32(sX + i * C::X_BYTES), &tmX, full0 + 8 * i, (kb0 + i) * BK, m0, pol_x);
@@ -227,6 +273,20 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
       tma_load_2d(smem_u32(sX + s * C::X_BYTES), &tmX, full0 + 8 * s, kc, m0, pol_x);
     }
     flags[3] = i;
+    if (pf.next_bytes) {
+      // This CTA's share of the next matrix, in 16 KB pieces dealt round-robin over the grid.
+      constexpr unsigned long long CH = 16384;
+      const unsigned long long nct = (unsigned long long)gridDim.x * gridDim.y * gridDim.z;
+      const unsigned long long cid = ((unsigned long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+      const unsigned long long nch = (pf.next_bytes + CH - 1) / CH;
+      const uint8_t* base = reinterpret_cast<const uint8_t*>(pf.next);
+      for (unsigned long long c = cid; c < nch; c += nct) {
+        const unsigned long long off = c * CH;
+        const unsigned long long left = pf.next_bytes - off;
+        const uint32_t sz = (uint32_t)((left < CH ? left : CH) & ~15ull);
+        if (sz) bulk_prefetch_l2(base + off, sz);
+      }
+    }
   } else {
     pdl_wait();
   }
@@ -283,7 +343,7 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
   }
   if (failed) {
-    // Wait (bounded) for loads that were issued but never consumed, then leave.
+    // Wait (bounded) for loads that were issued but never consumed.
     if (threadIdx.x == 0) {
       const int consumed = flags[1], issued = flags[3];
       for (int i = consumed; i < issued; ++i) {
@@ -291,10 +351,48 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
       }
     }
     __syncthreads();
-    return;
+    // A cluster member still takes part in both cluster barriers below (its
+    // partial is garbage then, and the error word is already set).
+    if (!(creduce && splits > 1)) return;
   }
 
   const int rows = min(NT, M - m0);
+  float* red = reinterpret_cast<float*>(smem + (size_t)NT * C::TLD * 4);
+  if (splits > 1 && creduce) {
+    // ---- split-K through distributed shared memory: every partial is in its CTA's `tile`
+    cluster_arrive();
+    cluster_wait();
+    const int q = (int)cluster_rank();
+    const int r0 = rows * q / splits, r1 = rows * (q + 1) / splits;
+    const uint32_t my_tile = smem_u32(tile);
+    for (int rb = r0; rb < r1; rb += 4) {
+      float v[4][8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = rb + i;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[i][j] = 0.f;
+          if (r < r1 && j < splits) v[i][j] = dsmem_ld(dsmem_map(my_tile + (uint32_t)(r * C::TLD + f) * 4u, (uint32_t)j));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float acc = v[i][0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j)
+          if (j < splits) acc += v[i][j];
+        if (rb + i < r1) tile[(rb + i) * C::TLD + f] = acc;
+      }
+    }
+    cluster_arrive();  // this CTA's reads of the other partials are done
+    __syncthreads();
+    if (!failed)
+      epilogue_tile<__nv_bfloat16>(ep, tile + (size_t)r0 * C::TLD, C::TLD, n0, m0 + r0, r1 - r0, M, meta + r0, red,
+                                   /*staged=*/true);
+    cluster_wait();    // nobody leaves while another CTA may still read its tile
+    return;
+  }
   if (splits > 1) {
     const int tile_id = tile_m * gridDim.x + tile_n;
     float* part = ws + (size_t)tile_id * splits * NT * BM;
@@ -336,8 +434,7 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
     if (threadIdx.x == 0) counters[tile_id] = 0;
     __syncthreads();
   }
-  epilogue_tile<__nv_bfloat16>(ep, tile, C::TLD, n0, m0, rows, M, meta,
-                               reinterpret_cast<float*>(smem + (size_t)NT * C::TLD * 4), /*staged=*/true);
+  epilogue_tile<__nv_bfloat16>(ep, tile, C::TLD, n0, m0, rows, M, meta, red, /*staged=*/true);
 }
 
 // ----------------------------------------------------------------------------
@@ -402,6 +499,8 @@ size_t tc_workspace_floats(int M, int N, int splits, int nt) {
 }
 size_t tc_counter_ints(int M, int N, int nt) { return (size_t)(N / BM) * ((M + nt - 1) / nt); }
 
+bool tc_cluster_reduce(int nt, int splits);
+
 template <int NT>
 static cudaError_t set_smem_attr() {
   return cudaFuncSetAttribute(gemm_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<NT>::SMEM);
@@ -410,6 +509,8 @@ static cudaError_t set_smem_attr() {
 // Set every token-tile variant's shared-memory limit up front (before any
 // stream capture).
 cudaError_t tc_prepare() {
+  for (int nt = 16; nt <= 256; nt *= 2)
+    for (int cz = 2; cz <= 8; ++cz) tc_cluster_reduce(nt, cz);
   cudaError_t e;
   if ((e = set_smem_attr<16>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<32>()) != cudaSuccess) return e;
@@ -418,10 +519,61 @@ cudaError_t tc_prepare() {
   return set_smem_attr<256>();
 }
 
+// Whether clusters of cz CTAs of this token-tile variant can be resident
+// (asked once per variant and size; DF_NO_CLUSTER=1 in the environment
+// turns cluster reduction off).
+template <int NT>
+static bool cluster_fits(int cz) {
+  static int known[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // 0 unknown, 1 yes, 2 no
+  if (cz < 2 || cz > 8) return false;
+  if (!known[cz]) {
+    const char* env = getenv("DF_NO_CLUSTER");
+    bool ok = !(env && env[0] == '1');
+    if (ok) {
+      ok = set_smem_attr<NT>() == cudaSuccess;
+      cudaLaunchConfig_t c = {};
+      c.gridDim = dim3(1, 1, cz);
+      c.blockDim = dim3(128);
+      c.dynamicSmemBytes = TcCfg<NT>::SMEM;
+      cudaLaunchAttribute a[1];
+      a[0].id = cudaLaunchAttributeClusterDimension;
+      a[0].val.clusterDim.x = 1;
+      a[0].val.clusterDim.y = 1;
+      a[0].val.clusterDim.z = (unsigned)cz;
+      c.attrs = a;
+      c.numAttrs = 1;
+      int n = 0;
+      ok = ok && cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<NT>, &c) == cudaSuccess && n > 0;
+      cudaGetLastError();
+    }
+    known[cz] = ok ? 1 : 2;
+  }
+  return known[cz] == 1;
+}
+
+bool tc_cluster_reduce(int nt, int splits) {
+  switch (nt) {
+    case 16: return cluster_fits<16>(splits);
+    case 32: return cluster_fits<32>(splits);
+    case 64: return cluster_fits<64>(splits);
+    case 128: return cluster_fits<128>(splits);
+    case 256: return cluster_fits<256>(splits);
+    default: return false;
+  }
+}
+
 template <int NT>
 static cudaError_t launch_nt(const void* tmW, const void* tmX, int M, int N, int K, int splits, float* ws,
-                             int* counters, const EpiParams& ep, cudaStream_t st) {
+                             int* counters, const EpiParams& ep, const L2AheadArgs& la, bool creduce, cudaStream_t st) {
   using C = TcCfg<NT>;
+  // Spread the L2 budget over the CTAs that stream distinct weight tiles.
+  L2Ahead pf{la.next, la.next ? la.next_bytes : 0ull, 0};
+  const long long ctas = (long long)(N / BM) * splits;
+  if (la.budget_bytes > 0 && ctas > 0) {
+    const long long per = la.budget_bytes / (ctas * (long long)C::W_BYTES) - C::STAGES;
+    const long long nkc = (long long)(K / BK + splits - 1) / splits;
+    pf.own_tiles = (int)(per < 0 ? 0 : per > nkc ? nkc : per);
+  }
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -429,19 +581,24 @@ static cudaError_t launch_nt(const void* tmW, const void* tmX, int M, int N, int
     attr_set = true;
   }
   dim3 grid(N / BM, (M + NT - 1) / NT, splits);
-  return launch_k(gemm_tc_kernel<NT>, grid, dim3(128), (size_t)C::SMEM, st, *reinterpret_cast<const CUtensorMap*>(tmW),
-                  *reinterpret_cast<const CUtensorMap*>(tmX), M, N, K, splits, ws, counters, ep);
+  const int cz = (creduce && splits > 1) ? splits : 1;
+  return launch_kc(gemm_tc_kernel<NT>, grid, dim3(128), (size_t)C::SMEM, st, cz,
+                   *reinterpret_cast<const CUtensorMap*>(tmW), *reinterpret_cast<const CUtensorMap*>(tmX), M, N, K,
+                   splits, ws, counters, cz > 1 ? 1 : 0, pf, ep);
 }
 
 cudaError_t launch_gemm_tc(const void* tmW, const void* tmX, int nt, int M, int N, int K, int splits, float* ws,
-                           int* counters, const EpiParams& ep, cudaStream_t st) {
+                           int* counters, const EpiParams& ep, cudaStream_t st, const L2AheadArgs& la,
+                           bool creduce) {
   if (N % BM || K % BK || M < 1 || splits < 1 || splits > K / BK) return cudaErrorInvalidValue;
+  if (creduce && splits > 8) return cudaErrorInvalidValue;  // a portable cluster holds at most 8 CTAs
+  if (la.next && (reinterpret_cast<uintptr_t>(la.next) & 15)) return cudaErrorInvalidValue;
   switch (nt) {
-    case 16: return launch_nt<16>(tmW, tmX, M, N, K, splits, ws, counters, ep, st);
-    case 32: return launch_nt<32>(tmW, tmX, M, N, K, splits, ws, counters, ep, st);
-    case 64: return launch_nt<64>(tmW, tmX, M, N, K, splits, ws, counters, ep, st);
-    case 128: return launch_nt<128>(tmW, tmX, M, N, K, splits, ws, counters, ep, st);
-    case 256: return launch_nt<256>(tmW, tmX, M, N, K, splits, ws, counters, ep, st);
+    case 16: return launch_nt<16>(tmW, tmX, M, N, K, splits, ws, counters, ep, la, creduce, st);
+    case 32: return launch_nt<32>(tmW, tmX, M, N, K, splits, ws, counters, ep, la, creduce, st);
+    case 64: return launch_nt<64>(tmW, tmX, M, N, K, splits, ws, counters, ep, la, creduce, st);
+    case 128: return launch_nt<128>(tmW, tmX, M, N, K, splits, ws, counters, ep, la, creduce, st);
+    case 256: return launch_nt<256>(tmW, tmX, M, N, K, splits, ws, counters, ep, la, creduce, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -15,20 +15,34 @@ constexpr int TMAP_BYTES = 128;  // sizeof(CUtensorMap)
 // (on by default; DF_NO_PDL=1 in the environment turns it off).
 bool pdl_enabled();
 
-// Launch a kernel with programmatic dependent launch allowed.
+// Launch a kernel with programmatic dependent launch allowed and, when
+// cluster_z > 1, thread-block clusters of 1 x 1 x cluster_z CTAs.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+cudaError_t launch_kc(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster_z,
+                      Args... args) {
   cudaLaunchConfig_t c = {};
   c.gridDim = grid;
   c.blockDim = block;
   c.dynamicSmemBytes = smem;
   c.stream = st;
-  cudaLaunchAttribute a[1];
+  cudaLaunchAttribute a[2];
   a[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   a[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  int n = 1;
+  if (cluster_z > 1) {
+    a[1].id = cudaLaunchAttributeClusterDimension;
+    a[1].val.clusterDim.x = 1;
+    a[1].val.clusterDim.y = 1;
+    a[1].val.clusterDim.z = (unsigned)cluster_z;
+    n = 2;
+  }
   c.attrs = a;
-  c.numAttrs = 1;
+  c.numAttrs = n;
   return cudaLaunchKernelEx(&c, kernel, static_cast<KArgs>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  return launch_kc(kernel, grid, block, smem, st, 1, args...);
 }
 
 // ---- tcgen05 GEMM (gemm_tc.cu)
@@ -37,9 +51,23 @@ int tc_token_tile(int M);
 cudaError_t tc_prepare();         // kernel attributes, once, before any stream capture
 int tc_splits(int N, int K, int sm_count);
 size_t tc_workspace_floats(int M, int N, int splits, int nt);
+bool tc_cluster_reduce(int nt, int splits);  // split-K by clusters for this variant and split count
 size_t tc_counter_ints(int M, int N, int nt);
+// L2 look-ahead of a GEMM launch: budget_bytes of the launch's own weight
+// slices (beyond the shared-memory stages) are requested before the wait on
+// the previous kernel; next_bytes of `next` (16-byte aligned) are requested
+// once this launch's loads are issued.  Zero budget and null next: none.
+struct L2AheadArgs {
+  long long budget_bytes = 0;
+  const void* next = nullptr;
+  unsigned long long next_bytes = 0;
+};
+// Split-K partials are reduced across a cluster of the tile's `splits` CTAs
+// through distributed shared memory (cluster_reduce) or, otherwise, through
+// the workspace `ws` and the tile tickets `counters` (splits > 1 only).
 cudaError_t launch_gemm_tc(const void* tmW, const void* tmX, int nt, int M, int N, int K, int splits, float* ws,
-                           int* counters, const EpiParams& ep, cudaStream_t st);
+                           int* counters, const EpiParams& ep, cudaStream_t st, const L2AheadArgs& la = L2AheadArgs(),
+                           bool cluster_reduce = false);
 
 // ---- fp32 SIMT GEMM + epilogue (gemm_simt.cu)
 cudaError_t launch_gemm_f32(const float* x, const float* w, float* tmp, int M, int N, int K, const EpiParams& ep,

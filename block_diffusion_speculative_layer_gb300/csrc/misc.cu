@@ -24,8 +24,8 @@ template <typename T>
 __global__ void __launch_bounds__(128) embed_kernel(const T* __restrict__ embed, const int* __restrict__ tok,
                                                     float* __restrict__ h, T* __restrict__ xraw,
                                                     float* __restrict__ ss, int d, int vocab, int* err) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   __shared__ float red[4];
   const int m = blockIdx.x;
   const int t = tok[m];
@@ -83,8 +83,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
                                                       const float* __restrict__ gain, T* __restrict__ out, int ldo,
                                                       int d, float eps, T* __restrict__ taps, int tap_index,
                                                       const int* __restrict__ row_pos) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.x;
   if (row_pos && row_pos[m] < 0) return;
   const float* x = h + (size_t)m * ldh;
@@ -117,8 +117,8 @@ cudaError_t launch_rmsnorm(const float* h, int ldh, const float* gain, void* out
 }
 
 __global__ void fill_u64_kernel(unsigned long long* p, unsigned long long v, int n) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) p[i] = v;
 }
@@ -128,8 +128,8 @@ cudaError_t launch_fill_u64(unsigned long long* p, unsigned long long v, int n, 
 }
 
 __global__ void argmax_finalize_kernel(const unsigned long long* amax, int* ids, int M) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < M) ids[i] = argmax_key_index(amax[i]);
 }
@@ -142,8 +142,8 @@ cudaError_t launch_argmax_finalize(const unsigned long long* amax, int* ids, int
 // the last verification produced.
 __global__ void prep_block_kernel(const int* slots, int B, const int* bonus, const int* bonus_pos, const int* drafts,
                                   int mask_id, int verify, int* row_tok, int* row_pos, int* row_seq) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x, i = threadIdx.x;
   if (i >= B) return;
   const int s = slots[b];
@@ -169,8 +169,8 @@ cudaError_t launch_prep_block(const int* batch_slots, int nseq, int B, const int
 // 0..k become context positions p..p+k for injection, the rest are inactive.
 __global__ void accept_kernel(const int* slots, int B, const int* row_tok, const int* ids, int* bonus, int* bonus_pos,
                               int* acc_out, int* n_out, int* inj_pos) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   const int lane = threadIdx.x;  // one warp; B <= 32
   const int s = slots[b];
@@ -201,8 +201,8 @@ cudaError_t launch_accept(const int* batch_slots, int nseq, int B, const int* ro
 }
 
 __global__ void collect_drafts_kernel(const int* ids, int B, const int* slots, int* drafts) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x, i = threadIdx.x;
   if (i < B - 1) drafts[slots[b] * (B - 1) + i] = ids[b * B + 1 + i];
 }
@@ -212,8 +212,8 @@ cudaError_t launch_collect_drafts(const int* ids, int nseq, int B, const int* ba
 }
 
 __global__ void greedy_step_kernel(const int* ids, int nseq, int t, int n_new, int* out, int* row_tok, int* row_pos) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= nseq) return;
   const int tok = ids[b];
@@ -227,8 +227,8 @@ cudaError_t launch_greedy_step(const int* ids, int nseq, int t, int n_new, int* 
 }
 
 __global__ void copy_rows_kernel(const float* src, int lds, float* dst, int ldd, int cols) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   for (int i = threadIdx.x; i < cols; i += blockDim.x) dst[(size_t)r * ldd + i] = src[(size_t)r * lds + i];
 }
