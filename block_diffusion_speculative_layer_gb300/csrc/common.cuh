@@ -7,13 +7,6 @@
 
 namespace dfk {
 
-// Kernel-side L2 look-ahead of a GEMM launch (see gemm_tc.cu).
-struct L2Ahead {
-  const void* next;
-  unsigned long long next_bytes;
-  int own_tiles;
-};
-
 // Bits of the sticky device error word.
 enum : int {
   ERR_TIMEOUT = 1,     // a bounded mbarrier wait ran out
@@ -177,6 +170,54 @@ __device__ __forceinline__ void epilogue_stage(const EpiParams& ep, int m0, int 
   }
 }
 
+// Global operands of the epilogue that do not depend on the accumulator (the
+// residual rows, the rotary factors), loaded before the accumulator is final
+// so that their latency overlaps the accumulator drain and the split-K
+// reduction.  Only for tiles of at most EPI_BATCH rows.
+struct EpiPre {
+  float a[EPI_BATCH];  // EPI_RESID: residual value; EPI_QKV: cosine
+  float b[EPI_BATCH];  // EPI_QKV: sine
+};
+
+// Fill `pre` for rows [0, rows) of the tile at (m0, n0); all 128 threads
+// call it, thread f for feature n0 + f.  Returns whether `pre` was filled.
+__device__ __forceinline__ bool epilogue_preload(const EpiParams& ep, int n0, int m0, int rows, int M,
+                                                 const RowMeta* meta, EpiPre& pre) {
+  rows = min(rows, M - m0);
+  if (rows > EPI_BATCH) return false;
+  const int f = threadIdx.x & 127;
+  const int n = n0 + f;
+  if (ep.kind == EPI_RESID) {
+#pragma unroll
+    for (int i = 0; i < EPI_BATCH; ++i) pre.a[i] = (i < rows) ? ep.resid[(size_t)(m0 + i) * ep.ldr + n] : 0.f;
+    return true;
+  }
+  if (ep.kind == EPI_QKV) {
+    const int hd = ep.head_dim, half = hd >> 1;
+    const int dim = n & (hd - 1);
+    bool rotated = true;  // queries and keys; values are not rotated
+    if (n >= ep.q_dim) {
+      const int r2 = (n - ep.q_dim) % (2 * ep.kv_dim);
+      rotated = r2 < ep.kv_dim;
+    }
+#pragma unroll
+    for (int i = 0; i < EPI_BATCH; ++i) {
+      pre.a[i] = 1.f;
+      pre.b[i] = 0.f;
+      if (i < rows && rotated) {
+        const int pos = meta[i].pos;
+        if (pos >= 0 && pos < ep.rope_rows) {
+          const float2 cs = __ldg(ep.rope + (size_t)pos * half + (dim & (half - 1)));
+          pre.a[i] = cs.x;
+          pre.b[i] = cs.y;
+        }
+      }
+    }
+    return true;
+  }
+  return false;
+}
+
 // Apply the epilogue to one result tile held in shared memory.
 //   tile[r * ld + f] = acc for row m0 + r, feature n0 + f, f in [0, 128),
 //   r in [0, rows), rows <= M - m0.  Called by exactly 128 threads (one per
@@ -185,7 +226,7 @@ __device__ __forceinline__ void epilogue_stage(const EpiParams& ep, int m0, int 
 //   4 floats per row.  Contains __syncthreads(), so all 128 threads call it.
 template <typename T>
 __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, int n0, int m0, int rows, int M,
-                              RowMeta* meta, float* red, bool staged = false) {
+                              RowMeta* meta, float* red, bool staged = false, const EpiPre* pre = nullptr) {
   const int f = threadIdx.x & 127;
   const int n = n0 + f;
   rows = min(rows, M - m0);
@@ -204,26 +245,35 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
       for (int r = 0; r < rows; ++r) out[(size_t)(m0 + r) * ep.ldo + n] = tile[r * ld + f];
     } break;
     case EPI_RESID: {
-      // Load EPI_BATCH residual values, then add and store them; also write the
-      // new rows for the next normalising GEMM (model dtype, tap, sum of squares).
-      for (int rb = 0; rb < rows; rb += EPI_BATCH) {
-        float old[EPI_BATCH];
+      // Add the residual and store it; also write the new rows for the next
+      // normalising GEMM (model dtype, tap, sum of squares).
+      auto row = [&](int r, float old) {
+        const int m = m0 + r;
+        const bool live = !(ep.row_pos && meta[r].pos < 0);
+        const float nv = live ? old + tile[r * ld + f] : old;
+        if (live) ep.resid[(size_t)m * ep.ldr + n] = nv;
+        if (ep.xraw) reinterpret_cast<T*>(ep.xraw)[(size_t)m * ep.ldx + n] = Cvt<T>::from_f(nv);
+        if (ep.tap) reinterpret_cast<T*>(ep.tap)[((size_t)m * 5 + ep.tap_index) * ep.ldr + n] = Cvt<T>::from_f(nv);
+        if (ep.ss_out) row_sumsq(nv, r, red);
+      };
+      if (pre) {
+        // residuals already in registers: a compact row loop
+#pragma unroll 1
+        for (int r = 0; r < rows; ++r) row(r, pre->a[r]);
+      } else {
+        // issue EPI_BATCH residual loads together, then the rows
+        for (int rb = 0; rb < rows; rb += EPI_BATCH) {
+          float old[EPI_BATCH];
 #pragma unroll
-        for (int i = 0; i < EPI_BATCH; ++i) {
-          const int r = rb + i;
-          old[i] = (r < rows) ? ep.resid[(size_t)(m0 + r) * ep.ldr + n] : 0.f;
-        }
+          for (int i = 0; i < EPI_BATCH; ++i) {
+            const int r = rb + i;
+            old[i] = (r < rows) ? ep.resid[(size_t)(m0 + r) * ep.ldr + n] : 0.f;
+          }
 #pragma unroll
-        for (int i = 0; i < EPI_BATCH; ++i) {
-          const int r = rb + i;
-          if (r >= rows) break;
-          const int m = m0 + r;
-          const bool live = !(ep.row_pos && meta[r].pos < 0);
-          const float nv = live ? old[i] + tile[r * ld + f] : old[i];
-          if (live) ep.resid[(size_t)m * ep.ldr + n] = nv;
-          if (ep.xraw) reinterpret_cast<T*>(ep.xraw)[(size_t)m * ep.ldx + n] = Cvt<T>::from_f(nv);
-          if (ep.tap) reinterpret_cast<T*>(ep.tap)[((size_t)m * 5 + ep.tap_index) * ep.ldr + n] = Cvt<T>::from_f(nv);
-          if (ep.ss_out) row_sumsq(nv, r, red);
+          for (int i = 0; i < EPI_BATCH; ++i) {
+            if (rb + i >= rows) break;
+            row(rb + i, old[i]);
+          }
         }
       }
       if (ep.ss_out) {
@@ -275,58 +325,76 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
         head = (r2 % ep.kv_dim) / hd;
       }
       const size_t page_elems = (size_t)2 * ep.n_kv_heads * ep.page_tokens * hd;
-      for (int rb = 0; rb < rows; rb += EPI_BATCH) {
-        float val[EPI_BATCH];
-        // rotary tables for the batch's rows (independent read-only loads)
-#pragma unroll
-        for (int i = 0; i < EPI_BATCH; ++i) {
-          const int r = rb + i;
-          val[i] = 0.f;
-          if (r >= rows) continue;
-          const int pos = meta[r].pos;
-          if (pos < 0) continue;
-          const float sc = scaled ? meta[r].scale : 1.f;
-          float v = tile[r * ld + f] * sc;
-          if (kind < 2 && pos < ep.rope_rows) {
-            const float p = tile[r * ld + partner] * sc;
-            const float2 cs = __ldg(ep.rope + (size_t)pos * half + (dim & (half - 1)));
-            v = (dim < half) ? (v * cs.x - p * cs.y) : (v * cs.x + p * cs.y);
-          }
-          val[i] = v;
+      // the (scaled, rotated) value of row r, given its rotary factors
+      auto value = [&](int r, float2 cs) {
+        const float sc = scaled ? meta[r].scale : 1.f;
+        float v = tile[r * ld + f] * sc;
+        if (kind < 2) {
+          const float p = tile[r * ld + partner] * sc;
+          v = (dim < half) ? (v * cs.x - p * cs.y) : (v * cs.x + p * cs.y);
         }
-#pragma unroll
-        for (int i = 0; i < EPI_BATCH; ++i) {
-          const int r = rb + i;
-          if (r >= rows) break;
-          const int m = m0 + r;
-          const int pos = meta[r].pos;
-          if (pos < 0) continue;
-          if (kind < 2 && pos >= ep.rope_rows) {
+        return v;
+      };
+      // store row r: queries to `out`, keys and values to the cache
+      auto store = [&](int r, float v) {
+        const int m = m0 + r;
+        const int pos = meta[r].pos;
+        if (kind == 0) {
+          reinterpret_cast<T*>(ep.out)[(size_t)m * ep.ldo + n] = Cvt<T>::from_f(v);
+          return;
+        }
+        T* base = reinterpret_cast<T*>(ep.kv_base);
+        const int kv = kind - 1;
+        size_t off;
+        if (ep.kv_dest == KV_PAGED) {
+          const int page = meta[r].page;
+          if (page < 0 || page >= ep.n_pages) {
             flag_error(ep.err, ERR_BOUNDS);
-            continue;
+            return;
           }
-          if (kind == 0) {
-            reinterpret_cast<T*>(ep.out)[(size_t)m * ep.ldo + n] = Cvt<T>::from_f(val[i]);
-          } else {
-            T* base = reinterpret_cast<T*>(ep.kv_base);
-            const int kv = kind - 1;
-            size_t off;
-            if (ep.kv_dest == KV_PAGED) {
-              const int page = meta[r].page;
-              if (page < 0 || page >= ep.n_pages) {
-                flag_error(ep.err, ERR_BOUNDS);
-                continue;
-              }
-              off = (size_t)(ep.layer0 + layer) * ep.layer_stride + (size_t)page * page_elems +
-                    ((size_t)(kv * ep.n_kv_heads + head) * ep.page_tokens + (pos % ep.page_tokens)) * hd + dim;
-            } else {
-              if (m >= ep.rows_cap) {
-                flag_error(ep.err, ERR_BOUNDS);
-                continue;
-              }
-              off = ((size_t)(kv * ep.n_kv_heads + head) * ep.rows_cap + m) * hd + dim;
-            }
-            base[off] = Cvt<T>::from_f(val[i]);
+          off = (size_t)(ep.layer0 + layer) * ep.layer_stride + (size_t)page * page_elems +
+                ((size_t)(kv * ep.n_kv_heads + head) * ep.page_tokens + (pos % ep.page_tokens)) * hd + dim;
+        } else {
+          if (m >= ep.rows_cap) {
+            flag_error(ep.err, ERR_BOUNDS);
+            return;
+          }
+          off = ((size_t)(kv * ep.n_kv_heads + head) * ep.rows_cap + m) * hd + dim;
+        }
+        base[off] = Cvt<T>::from_f(v);
+      };
+      // rows without a position are skipped; a rotated row past the table is an error
+      auto usable = [&](int r) {
+        const int pos = meta[r].pos;
+        if (pos < 0) return false;
+        if (kind < 2 && pos >= ep.rope_rows) {
+          flag_error(ep.err, ERR_BOUNDS);
+          return false;
+        }
+        return true;
+      };
+      if (pre) {
+        // rotary factors already in registers: a compact row loop
+#pragma unroll 1
+        for (int r = 0; r < rows; ++r)
+          if (usable(r)) store(r, value(r, make_float2(pre->a[r], pre->b[r])));
+      } else {
+        for (int rb = 0; rb < rows; rb += EPI_BATCH) {
+          // the batch's rotary factors first (independent read-only loads)
+          float2 cs[EPI_BATCH];
+#pragma unroll
+          for (int i = 0; i < EPI_BATCH; ++i) {
+            const int r = rb + i;
+            cs[i] = make_float2(1.f, 0.f);
+            if (r >= rows || kind == 2) continue;
+            const int pos = meta[r].pos;
+            if (pos >= 0 && pos < ep.rope_rows) cs[i] = __ldg(ep.rope + (size_t)pos * half + (dim & (half - 1)));
+          }
+#pragma unroll
+          for (int i = 0; i < EPI_BATCH; ++i) {
+            const int r = rb + i;
+            if (r >= rows) break;
+            if (usable(r)) store(r, value(r, cs[i]));
           }
         }
       }

@@ -60,7 +60,6 @@ struct df_handle {
   size_t esz = 4;
   int d = 0, hd = 0, Hq = 0, Hkv = 0, F = 0, V = 0, L = 0, Ld = 0, B = 0, qdim = 0, kvdim = 0, qkv_n = 0;
   int sm_count = 152;
-  long long l2_ahead = 0;  // bytes of a GEMM's own weight stream requested from L2 ahead of its wait (DF_L2_AHEAD_MB)
   int tap_of_layer[1024];  // zero-based layer index -> tap slot (or -1)
   int Mmax = 0;
 
@@ -345,10 +344,7 @@ double gemm_bytes(const df_handle* H, const Linear& W, int M, const EpiParams& e
   return (double)W.N * W.K * es + (double)M * W.K * es + out;
 }
 
-// `next` (optional): the weight matrix the launch after the next kernel(s)
-// streams; this launch starts it towards L2 once its own loads are issued.
-df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiParams& ep, int cls = PC_GEMM,
-               const Linear* next = nullptr) {
+df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiParams& ep, int cls = PC_GEMM) {
   if (M <= 0) return DF_OK;
   ProfScope ps(H, cls, H->bf16 ? 1 : 2, gemm_bytes(H, W, M, ep), 2.0 * M * W.N * W.K);
   if (H->bf16) {
@@ -356,13 +352,7 @@ df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiPar
     const void* tmX = nullptr;
     CKS(xmap(H, X, W.K, nt, &tmX));
     const int splits = tc_splits(W.N, W.K, H->sm_count);
-    L2AheadArgs la;
-    la.budget_bytes = H->l2_ahead;
-    if (next && H->l2_ahead > 0) {
-      la.next = next->ptr;
-      la.next_bytes = (unsigned long long)next->N * next->K * 2ull;
-    }
-    CK(launch_gemm_tc(W.tm.b, tmX, nt, M, W.N, W.K, splits, H->ws, H->counters, ep, H->st, la,
+    CK(launch_gemm_tc(W.tm.b, tmX, nt, M, W.N, W.K, splits, H->ws, H->counters, ep, H->st,
                       tc_cluster_reduce(nt, splits)));
   } else {
     CK(launch_gemm_f32(reinterpret_cast<const float*>(X), reinterpret_cast<const float*>(W.ptr), H->tmp, M, W.N, W.K,
@@ -468,7 +458,7 @@ df_status layer_pass(df_handle* H, const Layer& Lw, int M, int R, int nseq, bool
     e.kv_dest = KV_ROWS;
     e.kv_base = H->blk;
   }
-  CKS(gemm(H, Lw.qkv, H->xraw, M, e, PC_GEMM, &Lw.wo));   // o-projection weights warm L2 during attention
+  CKS(gemm(H, Lw.qkv, H->xraw, M, e));
   CKS(attention(H, M, R, nseq, causal, kv_layer(H, causal ? H->kv_t : H->kv_d, cache_layer), max_len));
   EpiParams r = epi(H, EPI_RESID);
   r.resid = H->h;
@@ -1186,8 +1176,6 @@ df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_we
   {
     const char* g = getenv("DF_NO_GRAPH");
     H->use_graphs = !(g && g[0] == '1');
-    const char* a = getenv("DF_L2_AHEAD_MB");  // L2 look-ahead budget of the GEMMs (0: off)
-    if (a && a[0]) H->l2_ahead = std::max(0ll, atoll(a)) << 20;
   }
   for (int l = 0; l < 1024; ++l) H->tap_of_layer[l] = -1;
   for (int i = 0; i < 5; ++i) H->tap_of_layer[cfg->feat_layers[i]] = i;
@@ -1618,7 +1606,7 @@ df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, in
   e.kind = EPI_STORE_F32;
   e.out = y_dev;
   e.ldo = N;
-  cudaError_t r = launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st, L2AheadArgs(), tc_cluster_reduce(nt, sp));
+  cudaError_t r = launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st, tc_cluster_reduce(nt, sp));
   cudaFreeAsync(ws, st);
   cudaFreeAsync(cnt, st);
   return r == cudaSuccess ? DF_OK : DF_ECUDA;
@@ -1651,7 +1639,7 @@ df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32
   EpiParams e{};
   e.kind = EPI_ARGMAX;
   e.amax = amax;
-  cudaError_t r = launch_gemm_tc(tw.b, tx.b, nt, M, V, K, sp, ws, cnt, e, st, L2AheadArgs(), tc_cluster_reduce(nt, sp));
+  cudaError_t r = launch_gemm_tc(tw.b, tx.b, nt, M, V, K, sp, ws, cnt, e, st, tc_cluster_reduce(nt, sp));
   if (r == cudaSuccess) r = launch_argmax_finalize(amax, ids_dev, M, st);
   cudaFreeAsync(ws, st);
   cudaFreeAsync(cnt, st);
@@ -1690,10 +1678,10 @@ df_status df_op_bench_gemm_bf16(const void* x_dev, const void* w_dev, float* y_d
   cudaEventCreate(&a);
   cudaEventCreate(&b);
   const bool cr = tc_cluster_reduce(nt, sp);
-  cudaError_t r = launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st, L2AheadArgs(), cr);  // warm-up
+  cudaError_t r = launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st, cr);  // warm-up
   cudaEventRecord(a, st);
   for (int i = 0; i < iters && r == cudaSuccess; ++i)
-    r = launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st, L2AheadArgs(), cr);
+    r = launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st, cr);
   cudaEventRecord(b, st);
   cudaStreamSynchronize(st);
   float ms = 0.f;

@@ -28,13 +28,7 @@
 // output is bitwise the same whatever the number of token rows.
 //
 // Launched with programmatic dependent launch: the producer streams the first
-// STAGES weight tiles before waiting for the previous kernel's outputs, and
-// asks L2 for a further stretch of its weight slice (a byte budget split over
-// the grid) so that DRAM stays busy while the previous kernel drains.  Once
-// its own loads are issued it can also start another matrix (the next GEMM's
-// weights, which do not depend on anything computed here) towards L2: decode
-// runs a chain of small kernels, and this keeps the weight stream going across
-// the gaps between them (attention in particular).
+// STAGES weight tiles before waiting for the previous kernel's outputs.
 //
 // Every mbarrier wait is bounded (about two seconds); on expiry the kernel
 // records ERR_TIMEOUT, waits (bounded) for the TMA loads it issued, frees its
@@ -96,17 +90,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// L2 prefetch of one weight tile (no shared memory is written, nothing to wait for).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-// L2 prefetch of a byte range (16-byte aligned start, size a multiple of 16).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes) : "memory");
-}
-
 // Thread-block cluster helpers (all threads of every CTA execute the barriers).
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
@@ -121,9 +104,9 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float dsmem_ld(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+__device__ __forceinline__ float4 dsmem_ld4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
 }
 
@@ -190,13 +173,14 @@ struct TcCfg {
   static constexpr int META_OFF = STAGES * STAGE_BYTES + 256;   // row facts staged during the mainloop
   static constexpr int SMEM = 1024 + META_OFF + NT * (int)sizeof(RowMeta);
   static_assert(NT * TLD * 4 + NT * 16 <= STAGES * STAGE_BYTES, "epilogue tile and row sums must fit in the ring");
+  static_assert((TLD * 4) % 16 == 0, "tile rows must stay 16-byte aligned for vector copies");
 };
 
 template <int NT>
-__global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
+__global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                       const __grid_constant__ CUtensorMap tmX, int M, int N, int K,
                                                       int splits, float* __restrict__ ws, int* __restrict__ counters,
-                                                      int creduce, L2Ahead pf, EpiParams ep) {
+                                                      int creduce, EpiParams ep) {
   using C = TcCfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -252,10 +236,6 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
       mbar_expect_tx(full0 + 8 * i, C::STAGE_BYTES);
       tma_load_2d(smem_u32(sW + i * C::W_BYTES), &tmW, full0 + 8 * i, (kb0 + i) * BK, n0, pol_w);
     }
-    if (tile_m == 0) {
-      const int pf_end = min(nk, pre + pf.own_tiles);
-      for (int i = pre; i < pf_end; ++i) tma_prefetch_2d(&tmW, (kb0 + i) * BK, n0);
-    }
     pdl_wait();
     for (int i = 0; i < pre; ++i)
       tma_load_2d(smem_u32(sX + i * C::X_BYTES), &tmX, full0 + 8 * i, (kb0 + i) * BK, m0, pol_x);
@@ -273,20 +253,6 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
       tma_load_2d(smem_u32(sX + s * C::X_BYTES), &tmX, full0 + 8 * s, kc, m0, pol_x);
     }
     flags[3] = i;
-    if (pf.next_bytes) {
-      // This CTA's share of the next matrix, in 16 KB pieces dealt round-robin over the grid.
-      constexpr unsigned long long CH = 16384;
-      const unsigned long long nct = (unsigned long long)gridDim.x * gridDim.y * gridDim.z;
-      const unsigned long long cid = ((unsigned long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-      const unsigned long long nch = (pf.next_bytes + CH - 1) / CH;
-      const uint8_t* base = reinterpret_cast<const uint8_t*>(pf.next);
-      for (unsigned long long c = cid; c < nch; c += nct) {
-        const unsigned long long off = c * CH;
-        const unsigned long long left = pf.next_bytes - off;
-        const uint32_t sz = (uint32_t)((left < CH ? left : CH) & ~15ull);
-        if (sz) bulk_prefetch_l2(base + off, sz);
-      }
-    }
   } else {
     pdl_wait();
   }
@@ -324,6 +290,14 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
   if (!mbar_wait(accum_bar, 0, ep.err)) flags[2] = 1;
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   __syncthreads();
+  // The rows whose epilogue this CTA runs; their global operands are loaded
+  // now, ahead of the drain and the split-K reduction.
+  const int rows = min(NT, M - m0);
+  const bool cl = creduce && splits > 1;
+  const int q = cl ? (int)cluster_rank() : 0;
+  const int r0 = cl ? rows * q / splits : 0, r1 = cl ? rows * (q + 1) / splits : rows;
+  EpiPre pre;
+  const bool have_pre = (cl || splits == 1) && epilogue_preload(ep, n0, m0 + r0, r1 - r0, M, meta + r0, pre);
   float* tile = reinterpret_cast<float*>(smem);
   const int f = threadIdx.x;
   const bool failed = flags[2] != 0;
@@ -353,43 +327,47 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
     __syncthreads();
     // A cluster member still takes part in both cluster barriers below (its
     // partial is garbage then, and the error word is already set).
-    if (!(creduce && splits > 1)) return;
+    if (!cl) return;
   }
 
-  const int rows = min(NT, M - m0);
   float* red = reinterpret_cast<float*>(smem + (size_t)NT * C::TLD * 4);
-  if (splits > 1 && creduce) {
+  if (cl) {
     // ---- split-K through distributed shared memory: every partial is in its CTA's `tile`
     cluster_arrive();
     cluster_wait();
-    const int q = (int)cluster_rank();
-    const int r0 = rows * q / splits, r1 = rows * (q + 1) / splits;
-    const uint32_t my_tile = smem_u32(tile);
-    for (int rb = r0; rb < r1; rb += 4) {
-      float v[4][8];
+    const uint32_t tile_s = smem_u32(tile);
+    const int c4 = threadIdx.x & 31, rl = threadIdx.x >> 5;  // 4 columns x 1 row per thread and pass
+    for (int rb = r0; rb < r1; rb += 8) {
+      // the loads of two 4-row passes first, then the sums in split order
+      float4 v[2][8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = rb + i;
+      for (int i = 0; i < 2; ++i) {
+        const int r = rb + 4 * i + rl;
+        const uint32_t off = (uint32_t)(r * C::TLD + 4 * c4) * 4u;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          v[i][j] = 0.f;
-          if (r < r1 && j < splits) v[i][j] = dsmem_ld(dsmem_map(my_tile + (uint32_t)(r * C::TLD + f) * 4u, (uint32_t)j));
-        }
+        for (int j = 0; j < 8; ++j)
+          v[i][j] = (r < r1 && j < splits) ? dsmem_ld4(dsmem_map(tile_s + off, (uint32_t)j)) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float acc = v[i][0];
+      for (int i = 0; i < 2; ++i) {
+        const int r = rb + 4 * i + rl;
+        float4 acc = v[i][0];
 #pragma unroll
         for (int j = 1; j < 8; ++j)
-          if (j < splits) acc += v[i][j];
-        if (rb + i < r1) tile[(rb + i) * C::TLD + f] = acc;
+          if (j < splits) {
+            acc.x += v[i][j].x;
+            acc.y += v[i][j].y;
+            acc.z += v[i][j].z;
+            acc.w += v[i][j].w;
+          }
+        if (r < r1) *reinterpret_cast<float4*>(tile + r * C::TLD + 4 * c4) = acc;
       }
     }
     cluster_arrive();  // this CTA's reads of the other partials are done
     __syncthreads();
     if (!failed)
       epilogue_tile<__nv_bfloat16>(ep, tile + (size_t)r0 * C::TLD, C::TLD, n0, m0 + r0, r1 - r0, M, meta + r0, red,
-                                   /*staged=*/true);
+                                   /*staged=*/true, have_pre ? &pre : nullptr);
     cluster_wait();    // nobody leaves while another CTA may still read its tile
     return;
   }
@@ -434,7 +412,8 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(const __grid_constant__ CU
     if (threadIdx.x == 0) counters[tile_id] = 0;
     __syncthreads();
   }
-  epilogue_tile<__nv_bfloat16>(ep, tile, C::TLD, n0, m0, rows, M, meta, red, /*staged=*/true);
+  epilogue_tile<__nv_bfloat16>(ep, tile, C::TLD, n0, m0, rows, M, meta, red, /*staged=*/true,
+                               (have_pre && splits == 1) ? &pre : nullptr);
 }
 
 // ----------------------------------------------------------------------------
@@ -564,16 +543,8 @@ bool tc_cluster_reduce(int nt, int splits) {
 
 template <int NT>
 static cudaError_t launch_nt(const void* tmW, const void* tmX, int M, int N, int K, int splits, float* ws,
-                             int* counters, const EpiParams& ep, const L2AheadArgs& la, bool creduce, cudaStream_t st) {
+                             int* counters, const EpiParams& ep, bool creduce, cudaStream_t st) {
   using C = TcCfg<NT>;
-  // Spread the L2 budget over the CTAs that stream distinct weight tiles.
-  L2Ahead pf{la.next, la.next ? la.next_bytes : 0ull, 0};
-  const long long ctas = (long long)(N / BM) * splits;
-  if (la.budget_bytes > 0 && ctas > 0) {
-    const long long per = la.budget_bytes / (ctas * (long long)C::W_BYTES) - C::STAGES;
-    const long long nkc = (long long)(K / BK + splits - 1) / splits;
-    pf.own_tiles = (int)(per < 0 ? 0 : per > nkc ? nkc : per);
-  }
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -584,21 +555,19 @@ static cudaError_t launch_nt(const void* tmW, const void* tmX, int M, int N, int
   const int cz = (creduce && splits > 1) ? splits : 1;
   return launch_kc(gemm_tc_kernel<NT>, grid, dim3(128), (size_t)C::SMEM, st, cz,
                    *reinterpret_cast<const CUtensorMap*>(tmW), *reinterpret_cast<const CUtensorMap*>(tmX), M, N, K,
-                   splits, ws, counters, cz > 1 ? 1 : 0, pf, ep);
+                   splits, ws, counters, cz > 1 ? 1 : 0, ep);
 }
 
 cudaError_t launch_gemm_tc(const void* tmW, const void* tmX, int nt, int M, int N, int K, int splits, float* ws,
-                           int* counters, const EpiParams& ep, cudaStream_t st, const L2AheadArgs& la,
-                           bool creduce) {
+                           int* counters, const EpiParams& ep, cudaStream_t st, bool creduce) {
   if (N % BM || K % BK || M < 1 || splits < 1 || splits > K / BK) return cudaErrorInvalidValue;
   if (creduce && splits > 8) return cudaErrorInvalidValue;  // a portable cluster holds at most 8 CTAs
-  if (la.next && (reinterpret_cast<uintptr_t>(la.next) & 15)) return cudaErrorInvalidValue;
   switch (nt) {
-    case 16: return launch_nt<16>(tmW, tmX, M, N, K, splits, ws, counters, ep, la, creduce, st);
-    case 32: return launch_nt<32>(tmW, tmX, M, N, K, splits, ws, counters, ep, la, creduce, st);
-    case 64: return launch_nt<64>(tmW, tmX, M, N, K, splits, ws, counters, ep, la, creduce, st);
-    case 128: return launch_nt<128>(tmW, tmX, M, N, K, splits, ws, counters, ep, la, creduce, st);
-    case 256: return launch_nt<256>(tmW, tmX, M, N, K, splits, ws, counters, ep, la, creduce, st);
+    case 16: return launch_nt<16>(tmW, tmX, M, N, K, splits, ws, counters, ep, creduce, st);
+    case 32: return launch_nt<32>(tmW, tmX, M, N, K, splits, ws, counters, ep, creduce, st);
+    case 64: return launch_nt<64>(tmW, tmX, M, N, K, splits, ws, counters, ep, creduce, st);
+    case 128: return launch_nt<128>(tmW, tmX, M, N, K, splits, ws, counters, ep, creduce, st);
+    case 256: return launch_nt<256>(tmW, tmX, M, N, K, splits, ws, counters, ep, creduce, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -53,21 +53,11 @@ int tc_splits(int N, int K, int sm_count);
 size_t tc_workspace_floats(int M, int N, int splits, int nt);
 bool tc_cluster_reduce(int nt, int splits);  // split-K by clusters for this variant and split count
 size_t tc_counter_ints(int M, int N, int nt);
-// L2 look-ahead of a GEMM launch: budget_bytes of the launch's own weight
-// slices (beyond the shared-memory stages) are requested before the wait on
-// the previous kernel; next_bytes of `next` (16-byte aligned) are requested
-// once this launch's loads are issued.  Zero budget and null next: none.
-struct L2AheadArgs {
-  long long budget_bytes = 0;
-  const void* next = nullptr;
-  unsigned long long next_bytes = 0;
-};
 // Split-K partials are reduced across a cluster of the tile's `splits` CTAs
 // through distributed shared memory (cluster_reduce) or, otherwise, through
 // the workspace `ws` and the tile tickets `counters` (splits > 1 only).
 cudaError_t launch_gemm_tc(const void* tmW, const void* tmX, int nt, int M, int N, int K, int splits, float* ws,
-                           int* counters, const EpiParams& ep, cudaStream_t st, const L2AheadArgs& la = L2AheadArgs(),
-                           bool cluster_reduce = false);
+                           int* counters, const EpiParams& ep, cudaStream_t st, bool cluster_reduce = false);
 
 // ---- fp32 SIMT GEMM + epilogue (gemm_simt.cu)
 cudaError_t launch_gemm_f32(const float* x, const float* w, float* tmp, int M, int N, int K, const EpiParams& ep,

@@ -20,36 +20,49 @@ bool pdl_enabled() {
 // Embedding gather for the rows of a pass: h[m] = embed[tok[m]] (fp32), the
 // same row in the model dtype for the first layer's GEMM, and its sum of
 // squares per 128-feature tile (the folded RMSNorm of that GEMM).  128 threads.
+constexpr int EMBED_MAX_TILES = 128;  // model width up to 16384
+
 template <typename T>
 __global__ void __launch_bounds__(128) embed_kernel(const T* __restrict__ embed, const int* __restrict__ tok,
                                                     float* __restrict__ h, T* __restrict__ xraw,
                                                     float* __restrict__ ss, int d, int vocab, int* err) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float red[4];
+  __shared__ float red[EMBED_MAX_TILES * 4];  // per 128-feature tile, one partial per warp
   const int m = blockIdx.x;
   const int t = tok[m];
   const bool ok = t >= 0 && t < vocab;
   if (!ok && threadIdx.x == 0 && t >= vocab) flag_error(err, ERR_BOUNDS);
   const int tiles = d >> 7;
-  for (int tl = 0; tl < tiles; ++tl) {
-    const int i = tl * 128 + threadIdx.x;
-    const float v = ok ? Cvt<T>::to_f(embed[(size_t)t * d + i]) : 0.f;
-    h[(size_t)m * d + i] = v;
-    xraw[(size_t)m * d + i] = Cvt<T>::from_f(v);
-    float q = v * v;
+  const int warp = threadIdx.x >> 5;
+  for (int tb = 0; tb < tiles; tb += 32) {
+    // 32 tiles' loads in flight together
+    float v[32];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = q;
-    __syncthreads();
-    if (threadIdx.x == 0) ss[(size_t)m * tiles + tl] = ((red[0] + red[1]) + red[2]) + red[3];
-    __syncthreads();
+    for (int j = 0; j < 32; ++j) {
+      const int i = (tb + j) * 128 + threadIdx.x;
+      v[j] = (ok && tb + j < tiles) ? Cvt<T>::to_f(embed[(size_t)t * d + i]) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (tb + j >= tiles) break;
+      const int i = (tb + j) * 128 + threadIdx.x;
+      h[(size_t)m * d + i] = v[j];
+      xraw[(size_t)m * d + i] = Cvt<T>::from_f(v[j]);
+      float q = v[j] * v[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+      if ((threadIdx.x & 31) == 0) red[(tb + j) * 4 + warp] = q;
+    }
   }
+  __syncthreads();
+  for (int tl = threadIdx.x; tl < tiles; tl += 128)
+    ss[(size_t)m * tiles + tl] = ((red[tl * 4 + 0] + red[tl * 4 + 1]) + red[tl * 4 + 2]) + red[tl * 4 + 3];
 }
 
 cudaError_t launch_embed(const void* embed, bool bf16, const int* tok, float* h, void* xraw, float* ss, int M, int d,
                          int vocab, int* err, cudaStream_t st) {
-  if (d % 128) return cudaErrorInvalidValue;
+  if (d % 128 || d / 128 > EMBED_MAX_TILES) return cudaErrorInvalidValue;
   if (bf16)
     return launch_k(embed_kernel<__nv_bfloat16>, dim3(M), dim3(128), 0, st,
                     reinterpret_cast<const __nv_bfloat16*>(embed), tok, h, reinterpret_cast<__nv_bfloat16*>(xraw), ss, d,
