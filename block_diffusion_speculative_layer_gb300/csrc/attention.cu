@@ -258,7 +258,8 @@ static cudaError_t set_attn_attr() {
 // Set the CUDA-core attention kernels' shared-memory limits up front (before
 // any stream capture).
 cudaError_t attention_prepare() {
-  cudaError_t e = cudaSuccess;
+  cudaError_t e = attention_cluster_prepare();
+  if (e != cudaSuccess) return e;
 #define DF_ATTR(T, HD, Q) \
   if ((e = set_attn_attr<T, HD, Q>()) != cudaSuccess) return e;
   DF_ATTR(float, 64, 2) DF_ATTR(float, 64, 4) DF_ATTR(float, 64, 8) DF_ATTR(float, 64, 16)
@@ -287,7 +288,13 @@ static cudaError_t launch_t(const AttnParams& p, cudaStream_t st) {
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st) {
   if (p.Hq % p.Hkv || p.Hq / p.Hkv > 8 || p.M != p.rows_per_seq * p.n_seqs) return cudaErrorInvalidValue;
   if (bf16 && p.hd == 128) {
-    // tensor-core partials (attention_mma.cu), then the same ordered merge
+    // tensor cores, chunk partials merged inside a cluster (attention_mma.cu);
+    // DF_ATTN_SPLIT=1: partials to global memory and the ordered merge kernel
+    static const bool split = [] {
+      const char* e = getenv("DF_ATTN_SPLIT");
+      return e && e[0] == '1';
+    }();
+    if (!split) return launch_attention_cluster(p, st);
     cudaError_t e = launch_attention_mma(p, st);
     if (e != cudaSuccess) return e;
     return launch_k(attn_combine_kernel<__nv_bfloat16, 128>, dim3(p.M, p.Hq), dim3(128), 0, st, p);

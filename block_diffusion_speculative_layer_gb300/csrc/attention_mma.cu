@@ -1,9 +1,10 @@
 // bf16 attention over the paged caches on the tensor cores (mma.sync m16n8k16).
 //
-// Same split and masks as the CUDA-core kernel in attention.cu (fixed 64-key
-// chunks counted from position 0, the drafter's block rows as one extra chunk,
-// partials merged in chunk order by attn_combine), so verification and greedy
-// decoding give bitwise the same rows.
+// attn_mma_kernel: same split and masks as the CUDA-core kernel in
+// attention.cu (fixed 64-key chunks counted from position 0, the drafter's
+// block rows as one extra chunk, partials merged in chunk order by
+// attn_combine), so verification and greedy decoding give bitwise the same
+// rows.  attn_cl_kernel (below) keeps the chunks but merges inside a cluster.
 //
 // One CTA = one (chunk, KV head, 16-token tile); one warp per grouped query
 // head, so a warp's 16 token rows form exactly one m16 tile.  The chunk's keys
@@ -269,4 +270,401 @@ cudaError_t launch_attention_mma(const AttnParams& p, cudaStream_t st) {
   return launch_k(attn_mma_kernel, grid, dim3(threads), 0, st, p);
 }
 
+// ---------------------------------------------------------------------------
+// Cluster variant: partials merged inside the kernel.
+//
+// A cluster of CLA CTAs (16 where the device can place such clusters, else 8)
+// covers one (KV head, 16-token tile).  CTA rank j takes the 64-key context
+// chunks c = j, j + CLA, j + 2*CLA, ... (the drafter's block rows, as one more
+// chunk, go to rank CLA-1 after its context chunks) and runs
+// an online softmax over them, double-buffering the next chunk's keys and
+// values while it computes.  The CLA partials (running max, sum, unnormalised
+// output per row and query head) are then left in shared memory and, after a
+// cluster barrier, each CTA merges a share of the (head, row) pairs by reading
+// all CLA partials through distributed shared memory in rank order.
+//
+// A row's arithmetic depends only on its own visible length: which CTA takes a
+// chunk depends on the chunk index alone, chunks that a row cannot see leave
+// its state bit-for-bit unchanged, and the merge order is fixed, so a row gets
+// the same bits whatever the other rows of its tile or batch.
+constexpr int MAXPG = 2048;                 // page ids a CTA stages for its chunks
+constexpr int CL_STAGE = 2 * MC * ROWB;     // one chunk's keys and values
+
+__host__ __device__ constexpr int cl_merge_bytes(int G) { return G * 16 * MHD * 4 + G * 16 * 8; }
+__host__ __device__ constexpr int cl_pg_off(int G) {
+  return ((cl_merge_bytes(G) > 2 * CL_STAGE ? cl_merge_bytes(G) : 2 * CL_STAGE) + 127) / 128 * 128;
+}
+__host__ __device__ constexpr int cl_smem_bytes(int G) { return cl_pg_off(G) + MAXPG * 4; }
+
+__device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float2 cl_ld2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float4 cl_ld4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+template <int CLA>
+__global__ void __launch_bounds__(256) attn_cl_kernel(AttnParams p) {
+  // The GEMM before this kernel triggers it only after its own wait (see
+  // gemm_tc.cu), so everything older than that GEMM is complete here: the row
+  // metadata, the page table and the cache entries of earlier positions are
+  // read before the wait; the queries, this pass's keys and values and the
+  // drafter's block rows after it.
+  pdl_trigger();
+  extern __shared__ __align__(128) uint8_t smc[];
+  const int G = p.Hq / p.Hkv;
+  const int j = (int)cl_rank();
+  const int h = blockIdx.y;
+  const int qtiles = (p.rows_per_seq + 15) / 16;
+  const int z = blockIdx.z / qtiles;
+  const int qt = blockIdx.z % qtiles;
+  const int r0 = z * p.rows_per_seq + qt * 16;
+  const int nrows = min(16, p.rows_per_seq - qt * 16);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const bool causal = p.causal != 0;
+
+  // ---- the tile's rows: visible context length (-1: no position), longest
+  __shared__ int s_len[16];
+  __shared__ int s_first_new;  // cache positions from here on are written by this pass
+  if (threadIdx.x < 16) {
+    int l = -1;
+    if ((int)threadIdx.x < nrows && p.row_pos[r0 + threadIdx.x] >= 0) l = ctx_len_rows(p, r0 + threadIdx.x);
+    s_len[threadIdx.x] = l;
+  }
+  if (threadIdx.x == 32) {
+    const int f = p.row_pos[z * p.rows_per_seq];
+    s_first_new = causal ? (f >= 0 ? f : 0) : 0x7fffffff;
+  }
+  const int ppc = MC / p.page_tokens;
+  // ---- page ids of this CTA's chunks (every chunk the longest row could need)
+  int* s_pg = reinterpret_cast<int*>(smc + cl_pg_off(G));
+  const int seq_slot = p.row_seq[r0];
+  const int cap_chunks = (p.grid_chunks > j) ? (p.grid_chunks - j + CLA - 1) / CLA : 0;
+  for (int t = threadIdx.x; t < cap_chunks * ppc && t < MAXPG; t += blockDim.x) {
+    const int pg = (j + CLA * (t / ppc)) * ppc + t % ppc;  // page of the sequence
+    s_pg[t] = pg < p.pt_stride ? p.page_table[(size_t)seq_slot * p.pt_stride + pg] : -1;
+  }
+  __syncthreads();
+  int max_len = 0;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) max_len = max(max_len, s_len[r]);
+  const int first_new = s_first_new;
+  const int nA = (max_len + MC - 1) / MC;                       // context chunks of the tile
+  const int nmine = nA > j ? (nA - j + CLA - 1) / CLA : 0;       // this CTA's context chunks
+  const bool has_blk = !causal && j == CLA - 1;
+  const int nsteps = nmine + (has_blk ? 1 : 0);
+
+  const __nv_bfloat16* cache = reinterpret_cast<const __nv_bfloat16*>(p.cache);
+  const __nv_bfloat16* blk = reinterpret_cast<const __nv_bfloat16*>(p.blk);
+  const size_t page_elems = (size_t)2 * p.Hkv * p.page_tokens * MHD;
+  // Stage step `st`'s keys and values into buffer `buf`: which = 1 the keys
+  // of earlier positions, 2 the rest, 3 all.  (The caller commits the group.)
+  auto stage = [&](int st, int buf, int which) {
+    uint8_t* sK = smc + buf * CL_STAGE;
+    uint8_t* sV = sK + MC * ROWB;
+    const bool is_blk = st >= nmine;
+    const int key0 = is_blk ? 0 : (j + CLA * st) * MC;
+    const int nkeys = is_blk ? p.rows_per_seq : min(MC, max_len - key0);
+    for (int idx = threadIdx.x; idx < MC * (MHD / 8); idx += blockDim.x) {
+      const int key = idx >> 4, b = idx & 15;
+      const bool old = !is_blk && key0 + key < first_new;
+      if (!((old ? 1 : 2) & which)) continue;
+      bool ok = key < nkeys;
+      const __nv_bfloat16 *srck = nullptr, *srcv = nullptr;
+      if (ok) {
+        if (is_blk) {
+          const int row = z * p.rows_per_seq + key;
+          srck = blk + ((size_t)(0 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8;
+          srcv = blk + ((size_t)(1 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8;
+        } else {
+          const int kabs = key0 + key;
+          const int pi = st * ppc + key / p.page_tokens;
+          const int page = pi < MAXPG ? s_pg[pi] : -1;
+          if (page >= 0 && page < p.n_pages) {
+            const size_t base = (size_t)page * page_elems + (size_t)(kabs % p.page_tokens) * MHD + b * 8;
+            srck = cache + base + (size_t)(0 * p.Hkv + h) * p.page_tokens * MHD;
+            srcv = cache + base + (size_t)(1 * p.Hkv + h) * p.page_tokens * MHD;
+          } else {
+            ok = false;
+            if (b == 0) flag_error(p.err, ERR_BOUNDS);
+          }
+        }
+      }
+      if (ok) {
+        cp_async16(smem_addr(sK) + swz(key, b), srck);
+        cp_async16(smem_addr(sV) + swz(key, b), srcv);
+      } else {
+        *reinterpret_cast<uint4*>(sK + swz(key, b)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sV + swz(key, b)) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  // the first two steps' earlier-position keys and values go out before the wait
+  for (int st = 0; st < 2 && st < nsteps; ++st) stage(st, st, 1);
+  cp_async_commit();
+
+  pdl_wait();
+  // ---- this warp's query head and its 16 rows (A fragments straight from global)
+  const bool active = warp < G;
+  const int head = h * G + warp;
+  uint32_t qa[8][4];
+  const int len_lo = s_len[gid], len_hi = s_len[gid + 8];
+  if (active) {
+    const size_t q_ld = (size_t)p.Hq * MHD;
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
+    const bool vlo = len_lo >= 0, vhi = len_hi >= 0;
+    const size_t base_lo = ((size_t)(r0 + gid) * q_ld + (size_t)head * MHD) / 2;
+    const size_t base_hi = ((size_t)(r0 + gid + 8) * q_ld + (size_t)head * MHD) / 2;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int d0 = ks * 16 + tig * 2;
+      qa[ks][0] = vlo ? q32[base_lo + d0 / 2] : 0u;
+      qa[ks][1] = vhi ? q32[base_hi + d0 / 2] : 0u;
+      qa[ks][2] = vlo ? q32[base_lo + (d0 + 8) / 2] : 0u;
+      qa[ks][3] = vhi ? q32[base_hi + (d0 + 8) / 2] : 0u;
+    }
+  }
+  // the rest of the first two steps
+  for (int st = 0; st < 2 && st < nsteps; ++st) stage(st, st, 2);
+  cp_async_commit();
+
+  // ---- online softmax over this CTA's chunks
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+  float o[16][4];
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  const int lq = lane >> 3, lr = lane & 7;
+  for (int st = 0; st < nsteps; ++st) {
+    // step st's group is complete once at most the group of step st + 1 (issued
+    // after it, at the end of step st - 1) is still in flight
+    if (st >= 1 && st + 1 < nsteps) cp_async_wait_1();
+    else cp_async_wait_0();
+    __syncthreads();
+    if (active) {
+      const bool is_blk = st >= nmine;
+      const int key0 = is_blk ? 0 : (j + CLA * st) * MC;
+      // visible keys of the two rows in this chunk's numbering
+      const int vis_lo = len_lo < 0 ? 0 : (is_blk ? p.rows_per_seq : len_lo - key0);
+      const int vis_hi = len_hi < 0 ? 0 : (is_blk ? p.rows_per_seq : len_hi - key0);
+      const uint32_t kbase = smem_addr(smc + (st & 1) * CL_STAGE);
+      const uint32_t vbase = kbase + MC * ROWB;
+      float s[8][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kbase + swz(nt * 8 + lr, kp * 4 + lq), b0, b1, b2, b3);
+          mma_16816(s[nt], qa[2 * kp], b0, b1);
+          mma_16816(s[nt], qa[2 * kp + 1], b2, b3);
+        }
+      }
+      float mc_lo = -INFINITY, mc_hi = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int kk = nt * 8 + tig * 2 + e;
+          s[nt][e] = (kk < vis_lo) ? s[nt][e] * p.scale_log2 : -INFINITY;
+          s[nt][2 + e] = (kk < vis_hi) ? s[nt][2 + e] * p.scale_log2 : -INFINITY;
+          mc_lo = fmaxf(mc_lo, s[nt][e]);
+          mc_hi = fmaxf(mc_hi, s[nt][2 + e]);
+        }
+      }
+      mc_lo = fmaxf(mc_lo, __shfl_xor_sync(0xffffffffu, mc_lo, 1));
+      mc_lo = fmaxf(mc_lo, __shfl_xor_sync(0xffffffffu, mc_lo, 2));
+      mc_hi = fmaxf(mc_hi, __shfl_xor_sync(0xffffffffu, mc_hi, 1));
+      mc_hi = fmaxf(mc_hi, __shfl_xor_sync(0xffffffffu, mc_hi, 2));
+      const float mn_lo = fmaxf(m_lo, mc_lo), mn_hi = fmaxf(m_hi, mc_hi);
+      // rescale of the running state (exactly 1 when this chunk shows the row nothing new)
+      const float a_lo = (mn_lo == -INFINITY) ? 1.f : exp2f(m_lo - mn_lo);
+      const float a_hi = (mn_hi == -INFINITY) ? 1.f : exp2f(m_hi - mn_hi);
+      float cs_lo = 0.f, cs_hi = 0.f;
+      uint32_t pa[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const float p0 = (s[nt][0] == -INFINITY) ? 0.f : exp2f(s[nt][0] - mn_lo);
+        const float p1 = (s[nt][1] == -INFINITY) ? 0.f : exp2f(s[nt][1] - mn_lo);
+        const float p2 = (s[nt][2] == -INFINITY) ? 0.f : exp2f(s[nt][2] - mn_hi);
+        const float p3 = (s[nt][3] == -INFINITY) ? 0.f : exp2f(s[nt][3] - mn_hi);
+        cs_lo += p0 + p1;
+        cs_hi += p2 + p3;
+        const int kk = nt >> 1;
+        if ((nt & 1) == 0) {
+          pa[kk][0] = pack_bf16(p0, p1);
+          pa[kk][1] = pack_bf16(p2, p3);
+        } else {
+          pa[kk][2] = pack_bf16(p0, p1);
+          pa[kk][3] = pack_bf16(p2, p3);
+        }
+      }
+      cs_lo += __shfl_xor_sync(0xffffffffu, cs_lo, 1);
+      cs_lo += __shfl_xor_sync(0xffffffffu, cs_lo, 2);
+      cs_hi += __shfl_xor_sync(0xffffffffu, cs_hi, 1);
+      cs_hi += __shfl_xor_sync(0xffffffffu, cs_hi, 2);
+      l_lo = l_lo * a_lo + cs_lo;
+      l_hi = l_hi * a_hi + cs_hi;
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        o[nt][0] *= a_lo;
+        o[nt][1] *= a_lo;
+        o[nt][2] *= a_hi;
+        o[nt][3] *= a_hi;
+      }
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vbase + swz(kk * 16 + (lq & 1) * 8 + lr, np * 2 + (lq >> 1)), b0, b1, b2, b3);
+          mma_16816(o[2 * np], pa[kk], b0, b1);
+          mma_16816(o[2 * np + 1], pa[kk], b2, b3);
+        }
+      }
+    }
+    __syncthreads();  // this buffer is refilled now, for two steps on
+    if (st + 2 < nsteps) {
+      stage(st + 2, st & 1, 3);
+      cp_async_commit();
+    }
+  }
+
+  // ---- leave the partial in shared memory (over the stage buffers)
+  float* sO = reinterpret_cast<float*>(smc);
+  float2* sML = reinterpret_cast<float2*>(smc + G * 16 * MHD * 4);
+  if (active) {
+#pragma unroll
+    for (int hl = 0; hl < 2; ++hl) {
+      const int rr = gid + hl * 8;
+      float* dst = sO + (size_t)(warp * 16 + rr) * MHD;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt)
+        *reinterpret_cast<float2*>(dst + nt * 8 + tig * 2) = make_float2(o[nt][2 * hl], o[nt][2 * hl + 1]);
+      if (tig == 0) sML[warp * 16 + rr] = make_float2(hl ? m_hi : m_lo, hl ? l_hi : l_lo);
+    }
+  }
+  cl_arrive();
+  cl_wait();
+
+  // ---- merge: this CTA's share of the (head, row) pairs, 32 threads x 4 dims per pair
+  const int pairs = G * 16;
+  const int p0 = j * pairs / CLA, p1 = (j + 1) * pairs / CLA;
+  const uint32_t sO_s = smem_addr(sO), sML_s = smem_addr(sML);
+  for (int pp = p0 + warp; pp < p1; pp += blockDim.x >> 5) {
+    const int g = pp >> 4, rr = pp & 15;
+    if (rr >= nrows || s_len[rr] < 0) continue;
+    float2 ml[CLA];
+    float4 av[CLA];
+#pragma unroll
+    for (int i = 0; i < CLA; ++i) {
+      ml[i] = cl_ld2(cl_map(sML_s + (uint32_t)(g * 16 + rr) * 8u, (uint32_t)i));
+      av[i] = cl_ld4(cl_map(sO_s + (uint32_t)((g * 16 + rr) * MHD + lane * 4) * 4u, (uint32_t)i));
+    }
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < CLA; ++i) Mx = fmaxf(Mx, ml[i].x);
+    float L = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < CLA; ++i) {
+      const float w = (ml[i].x == -INFINITY) ? 0.f : exp2f(ml[i].x - Mx);
+      L = fmaf(ml[i].y, w, L);
+      a.x = fmaf(av[i].x, w, a.x);
+      a.y = fmaf(av[i].y, w, a.y);
+      a.z = fmaf(av[i].z, w, a.z);
+      a.w = fmaf(av[i].w, w, a.w);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)(r0 + rr) * p.Hq * MHD +
+                         (size_t)(h * G + g) * MHD + lane * 4;
+    uint2 packed;
+    packed.x = pack_bf16(a.x * inv, a.y * inv);
+    packed.y = pack_bf16(a.z * inv, a.w * inv);
+    *reinterpret_cast<uint2*>(out) = packed;
+  }
+  cl_arrive();  // this CTA's reads of the other partials are done
+  cl_wait();    // and nobody leaves while another CTA may still read its partial
+}
+
+template <int CLA>
+static bool cluster_placeable() {
+  cudaLaunchConfig_t c = {};
+  c.gridDim = dim3(CLA, 1, 1);
+  c.blockDim = dim3(256);
+  c.dynamicSmemBytes = cl_smem_bytes(8);
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeClusterDimension;
+  a[0].val.clusterDim.x = CLA;
+  a[0].val.clusterDim.y = 1;
+  a[0].val.clusterDim.z = 1;
+  c.attrs = a;
+  c.numAttrs = 1;
+  int n = 0;
+  const bool ok = cudaOccupancyMaxActiveClusters(&n, attn_cl_kernel<CLA>, &c) == cudaSuccess && n > 0;
+  cudaGetLastError();
+  return ok;
+}
+
+static int g_cla = 0;  // cluster size in use (0: not chosen yet)
+
+// Kernel attributes and the cluster size, once, before any stream capture.
+cudaError_t attention_cluster_prepare() {
+  if (g_cla) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(attn_cl_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, cl_smem_bytes(8));
+  if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(attn_cl_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, cl_smem_bytes(8))) !=
+      cudaSuccess)
+    return e;
+  const bool big = cudaFuncSetAttribute(attn_cl_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                       cudaSuccess &&
+                   cluster_placeable<16>();
+  cudaGetLastError();
+  g_cla = big ? 16 : 8;
+  return cudaSuccess;
+}
+
+template <int CLA>
+static cudaError_t launch_cl(const AttnParams& p, cudaStream_t st) {
+  const int G = p.Hq / p.Hkv;
+  const int per_cta = (p.grid_chunks + CLA - 1) / CLA;
+  if (per_cta * (MC / p.page_tokens) > MAXPG) return cudaErrorInvalidValue;
+  const int qtiles = (p.rows_per_seq + 15) / 16;
+  dim3 grid(CLA, p.Hkv, p.n_seqs * qtiles);
+  const int threads = ((G * 32 + 127) / 128) * 128;
+  return launch_kcl(attn_cl_kernel<CLA>, grid, dim3(threads), (size_t)cl_smem_bytes(G), st, dim3(CLA, 1, 1), p);
+}
+
+cudaError_t launch_attention_cluster(const AttnParams& p, cudaStream_t st) {
+  const int G = p.Hq / p.Hkv;
+  if (p.hd != MHD || p.chunk != MC || G > 8 || p.page_tokens <= 0 || MC % p.page_tokens) return cudaErrorInvalidValue;
+  if (!p.causal && p.rows_per_seq > MC) return cudaErrorInvalidValue;
+  cudaError_t e = attention_cluster_prepare();
+  if (e != cudaSuccess) return e;
+  return g_cla == 16 ? launch_cl<16>(p, st) : launch_cl<8>(p, st);
+}
 }  // namespace dfk

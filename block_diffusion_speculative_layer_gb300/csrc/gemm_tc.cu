@@ -224,7 +224,13 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
-  pdl_trigger();
+  // A GEMM that writes keys and values triggers its dependent (the attention)
+  // only once its own wait has returned: every kernel before this one is then
+  // complete, so the attention may read the older cache entries and the row
+  // metadata before its own wait.  Every other GEMM lets its dependent start
+  // at once.
+  const bool late_trigger = ep.kind == EPI_QKV;
+  if (!late_trigger) pdl_trigger();
   if (warp == 0 && lane == 0) {
     // ---- TMA producer
     const uint64_t pol_w = policy_evict_first();  // weights are read once per launch
@@ -237,6 +243,7 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
       tma_load_2d(smem_u32(sW + i * C::W_BYTES), &tmW, full0 + 8 * i, (kb0 + i) * BK, n0, pol_w);
     }
     pdl_wait();
+    if (late_trigger) pdl_trigger();
     for (int i = 0; i < pre; ++i)
       tma_load_2d(smem_u32(sX + i * C::X_BYTES), &tmX, full0 + 8 * i, (kb0 + i) * BK, m0, pol_x);
     int i = pre;
@@ -255,6 +262,7 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
     flags[3] = i;
   } else {
     pdl_wait();
+    if (late_trigger) pdl_trigger();
   }
   if (warp == 1 && lane == 0) {
     // ---- MMA issuer

@@ -15,11 +15,11 @@ constexpr int TMAP_BYTES = 128;  // sizeof(CUtensorMap)
 // (on by default; DF_NO_PDL=1 in the environment turns it off).
 bool pdl_enabled();
 
-// Launch a kernel with programmatic dependent launch allowed and, when
-// cluster_z > 1, thread-block clusters of 1 x 1 x cluster_z CTAs.
+// Launch a kernel with programmatic dependent launch allowed and, when the
+// cluster shape has more than one CTA, thread-block clusters of that shape.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_kc(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster_z,
-                      Args... args) {
+cudaError_t launch_kcl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, dim3 cluster,
+                       Args... args) {
   cudaLaunchConfig_t c = {};
   c.gridDim = grid;
   c.blockDim = block;
@@ -29,16 +29,21 @@ cudaError_t launch_kc(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
   a[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   a[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   int n = 1;
-  if (cluster_z > 1) {
+  if (cluster.x * cluster.y * cluster.z > 1) {
     a[1].id = cudaLaunchAttributeClusterDimension;
-    a[1].val.clusterDim.x = 1;
-    a[1].val.clusterDim.y = 1;
-    a[1].val.clusterDim.z = (unsigned)cluster_z;
+    a[1].val.clusterDim.x = cluster.x;
+    a[1].val.clusterDim.y = cluster.y;
+    a[1].val.clusterDim.z = cluster.z;
     n = 2;
   }
   c.attrs = a;
   c.numAttrs = n;
   return cudaLaunchKernelEx(&c, kernel, static_cast<KArgs>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kc(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster_z,
+                      Args... args) {
+  return launch_kcl(kernel, grid, block, smem, st, dim3(1, 1, cluster_z > 1 ? cluster_z : 1), args...);
 }
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
@@ -89,8 +94,11 @@ struct AttnParams {
 };
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st);
 cudaError_t attention_prepare();  // kernel attributes, once, before any stream capture
-// bf16, head_dim 128: tensor-core partials (attention_mma.cu); merged by launch_attention.
+// bf16, head_dim 128 (attention_mma.cu): tensor-core chunk partials for
+// attn_combine, or (cluster) one kernel that also merges them in a cluster.
 cudaError_t launch_attention_mma(const AttnParams& p, cudaStream_t st);
+cudaError_t launch_attention_cluster(const AttnParams& p, cudaStream_t st);
+cudaError_t attention_cluster_prepare();  // kernel attributes, once, before any stream capture
 
 // ---- small kernels (misc.cu)
 // h[m] = embed[tok[m]] (fp32), xraw[m] = the same row in the model dtype,
