@@ -580,10 +580,14 @@ __global__ void __launch_bounds__(256) attn_cl_kernel(AttnParams p) {
     if (rr >= nrows || s_len[rr] < 0) continue;
     float2 ml[CLA];
     float4 av[CLA];
+    // ranks without a chunk of this tile hold (-inf, 0, 0): their terms are
+    // exactly zero, so they are not read
 #pragma unroll
     for (int i = 0; i < CLA; ++i) {
-      ml[i] = cl_ld2(cl_map(sML_s + (uint32_t)(g * 16 + rr) * 8u, (uint32_t)i));
-      av[i] = cl_ld4(cl_map(sO_s + (uint32_t)((g * 16 + rr) * MHD + lane * 4) * 4u, (uint32_t)i));
+      const bool held = i < nA || (!causal && i == CLA - 1);
+      ml[i] = held ? cl_ld2(cl_map(sML_s + (uint32_t)(g * 16 + rr) * 8u, (uint32_t)i)) : make_float2(-INFINITY, 0.f);
+      av[i] = held ? cl_ld4(cl_map(sO_s + (uint32_t)((g * 16 + rr) * MHD + lane * 4) * 4u, (uint32_t)i))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float Mx = -INFINITY;
 #pragma unroll

@@ -60,6 +60,7 @@ struct df_handle {
   size_t esz = 4;
   int d = 0, hd = 0, Hq = 0, Hkv = 0, F = 0, V = 0, L = 0, Ld = 0, B = 0, qdim = 0, kvdim = 0, qkv_n = 0;
   int sm_count = 152;
+  int split_target = 253;  // CTAs a split-K GEMM aims for (DF_SPLIT_CTAS overrides tc_split_target)
   int tap_of_layer[1024];  // zero-based layer index -> tap slot (or -1)
   int Mmax = 0;
 
@@ -351,7 +352,7 @@ df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiPar
     const int nt = tc_token_tile(M);
     const void* tmX = nullptr;
     CKS(xmap(H, X, W.K, nt, &tmX));
-    const int splits = tc_splits(W.N, W.K, H->sm_count);
+    const int splits = tc_splits(W.N, W.K, H->split_target);
     CK(launch_gemm_tc(W.tm.b, tmX, nt, M, W.N, W.K, splits, H->ws, H->counters, ep, H->st,
                       tc_cluster_reduce(nt, splits)));
   } else {
@@ -413,7 +414,8 @@ df_status attention(df_handle* H, int M, int R, int nseq, bool causal, const voi
   // algorithmic bytes: the visible keys/values of every sequence, queries and outputs
   const double kv_bytes = (double)nseq * (double)(max_len + (causal ? 0 : R)) * 2.0 * H->kvdim * H->esz;
   const double qo_bytes = 2.0 * M * H->qdim * H->esz;
-  ProfScope ps(H, PC_ATTN, 2, kv_bytes + qo_bytes, 4.0 * M * H->qdim * (double)max_len);
+  ProfScope ps(H, PC_ATTN, attention_launches(H->bf16, H->hd), kv_bytes + qo_bytes,
+               4.0 * M * H->qdim * (double)max_len);
   CK(launch_attention(p, H->bf16, H->st));
   return DF_OK;
 }
@@ -1065,7 +1067,7 @@ df_status alloc_state(df_handle* H) {
   size_t ws = 0, cnt = 0;
   if (H->bf16) {
     for (auto& s : shapes) {
-      const int splits = tc_splits(s.first, s.second, H->sm_count);
+      const int splits = tc_splits(s.first, s.second, H->split_target);
       for (int nt : {16, 32, 64, 128, 256}) {
         ws = std::max(ws, tc_workspace_floats(M, s.first, splits, nt));
         cnt = std::max(cnt, tc_counter_ints(M, s.first, nt));
@@ -1182,6 +1184,11 @@ df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_we
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&H->sm_count, cudaDevAttrMultiProcessorCount, dev);
+  H->split_target = tc_split_target(H->sm_count);
+  {
+    const char* sc = getenv("DF_SPLIT_CTAS");
+    if (sc && atoi(sc) > 0) H->split_target = atoi(sc);
+  }
   if (e != cudaSuccess) {
     delete H;
     (void)cudaGetLastError();
@@ -1589,7 +1596,7 @@ df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, in
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int nt = token_tile ? token_tile : tc_token_tile(M);
   if (nt != 16 && nt != 32 && nt != 64 && nt != 128 && nt != 256) return DF_EINVAL;
-  const int sp = splits ? splits : tc_splits(N, K, sms);
+  const int sp = splits ? splits : tc_splits(N, K, tc_split_target(sms));
   if (sp < 1 || sp > K / 64) return DF_EINVAL;
   Tmap tw, tx;
   if (!make_tmap_bf16(tw.b, w_dev, N, K, 128) || !make_tmap_bf16(tx.b, x_dev, M, K, nt)) return DF_EINVAL;
@@ -1620,7 +1627,7 @@ df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int nt = tc_token_tile(M);
-  const int sp = tc_splits(V, K, sms);
+  const int sp = tc_splits(V, K, tc_split_target(sms));
   Tmap tw, tx;
   if (!make_tmap_bf16(tw.b, wlm_dev, V, K, 128) || !make_tmap_bf16(tx.b, x_dev, M, K, nt)) return DF_EINVAL;
   float* ws = nullptr;
@@ -1657,7 +1664,7 @@ df_status df_op_bench_gemm_bf16(const void* x_dev, const void* w_dev, float* y_d
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int nt = token_tile ? token_tile : tc_token_tile(M);
   if (nt != 16 && nt != 32 && nt != 64 && nt != 128 && nt != 256) return DF_EINVAL;
-  const int sp = splits ? splits : tc_splits(N, K, sms);
+  const int sp = splits ? splits : tc_splits(N, K, tc_split_target(sms));
   if (sp < 1 || sp > K / 64) return DF_EINVAL;
   Tmap tw, tx;
   if (!make_tmap_bf16(tw.b, w_dev, N, K, 128) || !make_tmap_bf16(tx.b, x_dev, M, K, nt)) return DF_EINVAL;

@@ -54,7 +54,8 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 bool make_tmap_bf16(void* map_out, const void* ptr, long long rows, long long cols, int box_rows);
 int tc_token_tile(int M);
 cudaError_t tc_prepare();         // kernel attributes, once, before any stream capture
-int tc_splits(int N, int K, int sm_count);
+int tc_split_target(int sm_count);  // CTA count split-K aims for
+int tc_splits(int N, int K, int target_ctas);  // split count for a target CTA count
 size_t tc_workspace_floats(int M, int N, int splits, int nt);
 bool tc_cluster_reduce(int nt, int splits);  // split-K by clusters for this variant and split count
 size_t tc_counter_ints(int M, int N, int nt);
@@ -93,6 +94,7 @@ struct AttnParams {
   int* err;
 };
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st);
+int attention_launches(bool bf16, int hd);  // kernels one launch_attention call makes
 cudaError_t attention_prepare();  // kernel attributes, once, before any stream capture
 // bf16, head_dim 128 (attention_mma.cu): tensor-core chunk partials for
 // attn_combine, or (cluster) one kernel that also merges them in a cluster.

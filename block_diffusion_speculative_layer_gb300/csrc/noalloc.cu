@@ -72,7 +72,7 @@ extern "C" df_status df_op_gemm_bf16_noalloc(const void* x_dev, const void* w_de
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DF_ECUDA;
   const int nt = token_tile ? token_tile : tc_token_tile(M);
   if (nt != 16 && nt != 32 && nt != 64 && nt != 128 && nt != 256) return DF_EINVAL;
-  const int sp = splits ? splits : tc_splits(N, K, sms);
+  const int sp = splits ? splits : tc_splits(N, K, tc_split_target(sms));
   if (sp < 1 || sp > K / 64) return DF_EINVAL;
   // The shape must fit the fixed scratch: reject it before touching the GPU.
   const size_t ws_floats = tc_workspace_floats(M, N, sp, nt);

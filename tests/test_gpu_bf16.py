@@ -196,3 +196,18 @@ def test_27b_width_parity_and_lossless(dfl):
         np.testing.assert_array_equal(spec, s.eng.greedy_reference([p], 24))
     finally:
         s.eng.close()
+
+
+def test_long_context_parity_and_lossless(dfl):
+    """A 3300-token prompt: 52 context chunks of 64 keys, four per CTA of a
+    16-CTA attention cluster (so the kernel's look-ahead staging of later
+    chunks runs), teacher-forced parity with the oracle and speculative ==
+    greedy."""
+    s = Setup(dfl, SMALL, 0.1, 1, 3456)
+    try:
+        _verify_parity(dfl, s, syn.make_prompt(SMALL, 3300, stream=8))
+        p = syn.make_prompt(SMALL, 3200, stream=9)
+        spec, _ = s.eng.generate([p], 48)
+        np.testing.assert_array_equal(spec, s.eng.greedy_reference([p], 48))
+    finally:
+        s.eng.close()
