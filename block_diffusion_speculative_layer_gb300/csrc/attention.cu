@@ -293,14 +293,16 @@ static bool attn_split() {
   return split;
 }
 
-int attention_launches(bool bf16, int hd) { return (bf16 && hd == 128 && !attn_split()) ? 1 : 2; }
+int attention_launches(const AttnParams& p, bool bf16) {
+  return (bf16 && !attn_split() && attention_cluster_fits(p)) ? 1 : 2;
+}
 
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st) {
   if (p.Hq % p.Hkv || p.Hq / p.Hkv > 8 || p.M != p.rows_per_seq * p.n_seqs) return cudaErrorInvalidValue;
   if (bf16 && p.hd == 128) {
     // tensor cores, chunk partials merged inside a cluster (attention_mma.cu);
     // DF_ATTN_SPLIT=1: partials to global memory and the ordered merge kernel
-    if (!attn_split()) return launch_attention_cluster(p, st);
+    if (!attn_split() && attention_cluster_fits(p)) return launch_attention_cluster(p, st);
     cudaError_t e = launch_attention_mma(p, st);
     if (e != cudaSuccess) return e;
     return launch_k(attn_combine_kernel<__nv_bfloat16, 128>, dim3(p.M, p.Hq), dim3(128), 0, st, p);

@@ -13,6 +13,8 @@
 // ldmatrix).  S = Q K^T (64 MMAs per warp), masked softmax statistics per row
 // (quad shuffles), P kept in registers as the A operand of P V (64 MMAs), fp32
 // accumulators.  A row's arithmetic never depends on the other rows.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -288,13 +290,68 @@ cudaError_t launch_attention_mma(const AttnParams& p, cudaStream_t st) {
 // its state bit-for-bit unchanged, and the merge order is fixed, so a row gets
 // the same bits whatever the other rows of its tile or batch.
 constexpr int MAXPG = 2048;                 // page ids a CTA stages for its chunks
-constexpr int CL_STAGE = 2 * MC * ROWB;     // one chunk's keys and values
+constexpr int CL_NST = 3;                   // key/value stages in flight
+// One stage: keys then values, each [2 halves of the head dim][64 keys][128 B]
+// in the 128-byte swizzle (16-byte piece b of a row at b ^ (key & 7)).
+constexpr int CL_HALF = MC * 128;
+constexpr int CL_STAGE = 2 * 2 * CL_HALF;
+constexpr unsigned long long CL_WAIT_NS = 2000000000ull;
 
 __host__ __device__ constexpr int cl_merge_bytes(int G) { return G * 16 * MHD * 4 + G * 16 * 8; }
 __host__ __device__ constexpr int cl_pg_off(int G) {
-  return ((cl_merge_bytes(G) > 2 * CL_STAGE ? cl_merge_bytes(G) : 2 * CL_STAGE) + 127) / 128 * 128;
+  return ((cl_merge_bytes(G) > CL_NST * CL_STAGE ? cl_merge_bytes(G) : CL_NST * CL_STAGE) + 1023) / 1024 * 1024;
 }
-__host__ __device__ constexpr int cl_smem_bytes(int G) { return cl_pg_off(G) + MAXPG * 4; }
+__host__ __device__ constexpr int cl_smem_bytes(int G) { return cl_pg_off(G) + MAXPG * 4 + 1024; }
+
+// Byte offset of (key, 16-byte piece b of the 256-byte row) in a stage's key or value tile.
+__device__ __forceinline__ uint32_t swz2(int key, int b) {
+  return (uint32_t)((b >> 3) * CL_HALF + key * 128 + (((b & 7) ^ (key & 7)) << 4));
+}
+__device__ __forceinline__ void cl_mbar_init(uint32_t bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cl_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cl_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool cl_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a stage barrier; false (error word set) after about two seconds.
+__device__ __noinline__ bool cl_wait_bar(uint32_t bar, uint32_t parity, int* err) {
+  if (cl_try_wait(bar, parity)) return true;
+  unsigned long long t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (cl_try_wait(bar, parity)) return true;
+    if ((it & 1023u) == 0) {
+      unsigned long long t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > CL_WAIT_NS) break;
+    }
+  }
+  flag_error(err, ERR_TIMEOUT);
+  return false;
+}
+// One page-half (page_tokens keys x 64 head dims = page_tokens x 128 B) of
+// cache slab `slab` = (page * 2 + k|v) * Hkv + head into shared memory.
+__device__ __forceinline__ void tma_kv(uint32_t dst, const CUtensorMap* map, uint32_t bar, int half, int slab) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(half), "r"(0), "r"(slab)
+      : "memory");
+}
 
 __device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
@@ -324,14 +381,16 @@ __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_
 __device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 template <int CLA>
-__global__ void __launch_bounds__(256) attn_cl_kernel(AttnParams p) {
+__global__ void __launch_bounds__(256) attn_cl_kernel(AttnParams p, const __grid_constant__ CUtensorMap kvmap) {
   // The GEMM before this kernel triggers it only after its own wait (see
   // gemm_tc.cu), so everything older than that GEMM is complete here: the row
   // metadata, the page table and the cache entries of earlier positions are
   // read before the wait; the queries, this pass's keys and values and the
   // drafter's block rows after it.
   pdl_trigger();
-  extern __shared__ __align__(128) uint8_t smc[];
+  extern __shared__ __align__(128) uint8_t smc_raw[];
+  // 1024-byte aligned: the TMA's 128-byte swizzle repeats every 1024 bytes
+  uint8_t* smc = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smc_raw) + 1023) & ~uintptr_t(1023));
   const int G = p.Hq / p.Hkv;
   const int j = (int)cl_rank();
   const int h = blockIdx.y;
@@ -375,54 +434,91 @@ __global__ void __launch_bounds__(256) attn_cl_kernel(AttnParams p) {
   const bool has_blk = !causal && j == CLA - 1;
   const int nsteps = nmine + (has_blk ? 1 : 0);
 
-  const __nv_bfloat16* cache = reinterpret_cast<const __nv_bfloat16*>(p.cache);
   const __nv_bfloat16* blk = reinterpret_cast<const __nv_bfloat16*>(p.blk);
-  const size_t page_elems = (size_t)2 * p.Hkv * p.page_tokens * MHD;
-  // Stage step `st`'s keys and values into buffer `buf`: which = 1 the keys
-  // of earlier positions, 2 the rest, 3 all.  (The caller commits the group.)
-  auto stage = [&](int st, int buf, int which) {
+  const int PT = p.page_tokens;
+  __shared__ __align__(8) uint64_t s_full[CL_NST];
+  __shared__ int s_failed;
+  if (threadIdx.x == 0) {
+    for (int b2 = 0; b2 < CL_NST; ++b2) cl_mbar_init(smem_addr(&s_full[b2]));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kvmap)) : "memory");
+    s_failed = 0;
+  }
+  __syncthreads();
+  // Stage step st into buffer buf: part 1 = the pages wholly before first_new
+  // (written by earlier passes), 2 = the rest, 3 = all.  Context chunks come
+  // by TMA, one 2 KB box per (page, k|v, half row), issued by thread 0; the
+  // drafter's block rows by 16-byte cp.async from every thread.  Part 2 (or
+  // 3) makes the stage barrier's one arrival.
+  auto stage = [&](int st, int buf, int part) {
     uint8_t* sK = smc + buf * CL_STAGE;
-    uint8_t* sV = sK + MC * ROWB;
-    const bool is_blk = st >= nmine;
-    const int key0 = is_blk ? 0 : (j + CLA * st) * MC;
-    const int nkeys = is_blk ? p.rows_per_seq : min(MC, max_len - key0);
-    for (int idx = threadIdx.x; idx < MC * (MHD / 8); idx += blockDim.x) {
-      const int key = idx >> 4, b = idx & 15;
-      const bool old = !is_blk && key0 + key < first_new;
-      if (!((old ? 1 : 2) & which)) continue;
-      bool ok = key < nkeys;
-      const __nv_bfloat16 *srck = nullptr, *srcv = nullptr;
-      if (ok) {
-        if (is_blk) {
+    uint8_t* sV = sK + 2 * CL_HALF;
+    const uint32_t bar = smem_addr(&s_full[buf]);
+    if (st >= nmine) {  // block chunk
+      if (!(part & 2)) return;
+      for (int idx = threadIdx.x; idx < MC * (MHD / 8); idx += blockDim.x) {
+        const int key = idx >> 4, b = idx & 15;
+        if (key < p.rows_per_seq) {
           const int row = z * p.rows_per_seq + key;
-          srck = blk + ((size_t)(0 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8;
-          srcv = blk + ((size_t)(1 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8;
+          cp_async16(smem_addr(sK) + swz2(key, b), blk + ((size_t)(0 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8);
+          cp_async16(smem_addr(sV) + swz2(key, b), blk + ((size_t)(1 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8);
         } else {
-          const int kabs = key0 + key;
-          const int pi = st * ppc + key / p.page_tokens;
-          const int page = pi < MAXPG ? s_pg[pi] : -1;
-          if (page >= 0 && page < p.n_pages) {
-            const size_t base = (size_t)page * page_elems + (size_t)(kabs % p.page_tokens) * MHD + b * 8;
-            srck = cache + base + (size_t)(0 * p.Hkv + h) * p.page_tokens * MHD;
-            srcv = cache + base + (size_t)(1 * p.Hkv + h) * p.page_tokens * MHD;
-          } else {
-            ok = false;
-            if (b == 0) flag_error(p.err, ERR_BOUNDS);
-          }
+          *reinterpret_cast<uint4*>(sK + swz2(key, b)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sV + swz2(key, b)) = make_uint4(0, 0, 0, 0);
         }
       }
-      if (ok) {
-        cp_async16(smem_addr(sK) + swz(key, b), srck);
-        cp_async16(smem_addr(sV) + swz(key, b), srcv);
-      } else {
-        *reinterpret_cast<uint4*>(sK + swz(key, b)) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sV + swz(key, b)) = make_uint4(0, 0, 0, 0);
+      cp_async_commit();
+      if (threadIdx.x == 0) cl_arrive_expect_tx(bar, 0);
+      return;
+    }
+    if (threadIdx.x != 0) return;
+    const int key0 = (j + CLA * st) * MC;
+    const int npg = (min(MC, max_len - key0) + PT - 1) / PT;  // pages holding a key the tile can see
+    auto wanted = [&](int pg) {
+      const bool old = key0 + (pg + 1) * PT <= first_new;
+      const int page = s_pg[st * ppc + pg];
+      return ((old ? 1 : 2) & part) && page >= 0 && page < p.n_pages;
+    };
+    uint32_t bytes = 0;
+    for (int pg = 0; pg < npg; ++pg)
+      if (wanted(pg)) bytes += 4u * (uint32_t)PT * 128u;
+    if (part == 1) {
+      if (bytes) cl_expect_tx(bar, bytes);
+    } else {
+      cl_arrive_expect_tx(bar, bytes);
+    }
+    for (int pg = 0; pg < npg; ++pg) {
+      if (!wanted(pg)) continue;
+      const int page = s_pg[st * ppc + pg];
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+          tma_kv(smem_addr((kv ? sV : sK) + half * CL_HALF + pg * PT * 128), &kvmap, bar, half,
+                 (page * 2 + kv) * p.Hkv + h);
+    }
+  };
+  // Keys and values the staged pages do not cover (past the tile's longest
+  // row, or in a page the table does not hold) read as zeros.
+  auto fixup = [&](int st, int buf) {
+    if (st >= nmine) return;
+    uint8_t* sK = smc + buf * CL_STAGE;
+    uint8_t* sV = sK + 2 * CL_HALF;
+    const int key0 = (j + CLA * st) * MC;
+    const int nkeys = min(MC, max_len - key0);
+    for (int idx = threadIdx.x; idx < MC * (MHD / 8); idx += blockDim.x) {
+      const int key = idx >> 4, b = idx & 15;
+      const int page = s_pg[st * ppc + key / PT];
+      const bool have = key < nkeys && page >= 0 && page < p.n_pages;
+      if (!have) {
+        if (key < nkeys && b == 0 && (key % PT) == 0) flag_error(p.err, ERR_BOUNDS);
+        *reinterpret_cast<uint4*>(sK + swz2(key, b)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sV + swz2(key, b)) = make_uint4(0, 0, 0, 0);
       }
     }
   };
-  // the first two steps' earlier-position keys and values go out before the wait
-  for (int st = 0; st < 2 && st < nsteps; ++st) stage(st, st, 1);
-  cp_async_commit();
+  // the first stages' earlier-position pages go out before the wait
+  for (int st = 0; st < CL_NST && st < nsteps; ++st) stage(st, st, 1);
 
   pdl_wait();
   // ---- this warp's query head and its 16 rows (A fragments straight from global)
@@ -445,9 +541,8 @@ __global__ void __launch_bounds__(256) attn_cl_kernel(AttnParams p) {
       qa[ks][3] = vhi ? q32[base_hi + (d0 + 8) / 2] : 0u;
     }
   }
-  // the rest of the first two steps
-  for (int st = 0; st < 2 && st < nsteps; ++st) stage(st, st, 2);
-  cp_async_commit();
+  // the rest of the first stages
+  for (int st = 0; st < CL_NST && st < nsteps; ++st) stage(st, st, 2);
 
   // ---- online softmax over this CTA's chunks
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
@@ -455,20 +550,23 @@ __global__ void __launch_bounds__(256) attn_cl_kernel(AttnParams p) {
 #pragma unroll
   for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
   const int lq = lane >> 3, lr = lane & 7;
+  int done = 0;  // steps consumed
   for (int st = 0; st < nsteps; ++st) {
-    // step st's group is complete once at most the group of step st + 1 (issued
-    // after it, at the end of step st - 1) is still in flight
-    if (st >= 1 && st + 1 < nsteps) cp_async_wait_1();
-    else cp_async_wait_0();
+    const int buf = st % CL_NST;
+    if (st >= nmine) cp_async_wait_0();  // the block rows (this thread's copies)
+    if (!cl_wait_bar(smem_addr(&s_full[buf]), (uint32_t)(st / CL_NST) & 1u, p.err)) s_failed = 1;
+    fixup(st, buf);
     __syncthreads();
+    if (s_failed) break;
+    done = st + 1;
     if (active) {
       const bool is_blk = st >= nmine;
       const int key0 = is_blk ? 0 : (j + CLA * st) * MC;
       // visible keys of the two rows in this chunk's numbering
       const int vis_lo = len_lo < 0 ? 0 : (is_blk ? p.rows_per_seq : len_lo - key0);
       const int vis_hi = len_hi < 0 ? 0 : (is_blk ? p.rows_per_seq : len_hi - key0);
-      const uint32_t kbase = smem_addr(smc + (st & 1) * CL_STAGE);
-      const uint32_t vbase = kbase + MC * ROWB;
+      const uint32_t kbase = smem_addr(smc + buf * CL_STAGE);
+      const uint32_t vbase = kbase + 2 * CL_HALF;
       float s[8][4];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
@@ -477,7 +575,7 @@ __global__ void __launch_bounds__(256) attn_cl_kernel(AttnParams p) {
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(kbase + swz(nt * 8 + lr, kp * 4 + lq), b0, b1, b2, b3);
+          ldsm_x4(kbase + swz2(nt * 8 + lr, kp * 4 + lq), b0, b1, b2, b3);
           mma_16816(s[nt], qa[2 * kp], b0, b1);
           mma_16816(s[nt], qa[2 * kp + 1], b2, b3);
         }
@@ -541,18 +639,22 @@ __global__ void __launch_bounds__(256) attn_cl_kernel(AttnParams p) {
 #pragma unroll
         for (int np = 0; np < 8; ++np) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vbase + swz(kk * 16 + (lq & 1) * 8 + lr, np * 2 + (lq >> 1)), b0, b1, b2, b3);
+          ldsm_x4_t(vbase + swz2(kk * 16 + (lq & 1) * 8 + lr, np * 2 + (lq >> 1)), b0, b1, b2, b3);
           mma_16816(o[2 * np], pa[kk], b0, b1);
           mma_16816(o[2 * np + 1], pa[kk], b2, b3);
         }
       }
     }
-    __syncthreads();  // this buffer is refilled now, for two steps on
-    if (st + 2 < nsteps) {
-      stage(st + 2, st & 1, 3);
-      cp_async_commit();
-    }
+    __syncthreads();  // this buffer is refilled now, for CL_NST steps on
+    if (st + CL_NST < nsteps) stage(st + CL_NST, buf, 3);
   }
+  if (s_failed && threadIdx.x == 0) {
+    // leave no copy in flight: wait (bounded) for the stages issued but not consumed
+    for (int st = done; st < nsteps && st < done + CL_NST; ++st)
+      if (st < nmine) cl_wait_bar(smem_addr(&s_full[st % CL_NST]), (uint32_t)(st / CL_NST) & 1u, p.err);
+  }
+  cp_async_wait_0();
+  __syncthreads();
 
   // ---- leave the partial in shared memory (over the stage buffers)
   float* sO = reinterpret_cast<float*>(smc);
@@ -660,13 +762,18 @@ static cudaError_t launch_cl(const AttnParams& p, cudaStream_t st) {
   const int qtiles = (p.rows_per_seq + 15) / 16;
   dim3 grid(CLA, p.Hkv, p.n_seqs * qtiles);
   const int threads = ((G * 32 + 127) / 128) * 128;
-  return launch_kcl(attn_cl_kernel<CLA>, grid, dim3(threads), (size_t)cl_smem_bytes(G), st, dim3(CLA, 1, 1), p);
+  return launch_kcl(attn_cl_kernel<CLA>, grid, dim3(threads), (size_t)cl_smem_bytes(G), st, dim3(CLA, 1, 1), p,
+                    *reinterpret_cast<const CUtensorMap*>(p.kv_map));
+}
+
+bool attention_cluster_fits(const AttnParams& p) {
+  const int G = p.Hq / p.Hkv;
+  return p.hd == MHD && p.chunk == MC && G <= 8 && p.page_tokens > 0 && MC % p.page_tokens == 0 &&
+         p.page_tokens % 8 == 0 && p.kv_map != nullptr && (p.causal || p.rows_per_seq <= MC);
 }
 
 cudaError_t launch_attention_cluster(const AttnParams& p, cudaStream_t st) {
-  const int G = p.Hq / p.Hkv;
-  if (p.hd != MHD || p.chunk != MC || G > 8 || p.page_tokens <= 0 || MC % p.page_tokens) return cudaErrorInvalidValue;
-  if (!p.causal && p.rows_per_seq > MC) return cudaErrorInvalidValue;
+  if (!attention_cluster_fits(p)) return cudaErrorInvalidValue;
   cudaError_t e = attention_cluster_prepare();
   if (e != cudaSuccess) return e;
   return g_cla == 16 ? launch_cl<16>(p, st) : launch_cl<8>(p, st);

@@ -73,6 +73,7 @@ struct df_handle {
 
   int PT = 16, pages_per_seq = 0, n_pages = 0;
   void *kv_t = nullptr, *kv_d = nullptr;
+  std::vector<Tmap> kvmap_t, kvmap_d;  // bf16: TMA maps of each cache layer (attention)
   long long layer_stride = 0;
   int* d_pt = nullptr;
   std::vector<int> free_pages;
@@ -383,8 +384,10 @@ df_status lm_head_argmax(df_handle* H, int M, float* dbg) {
   return DF_OK;
 }
 
-df_status attention(df_handle* H, int M, int R, int nseq, bool causal, const void* cache_layer, int max_len) {
+df_status attention(df_handle* H, int M, int R, int nseq, bool causal, const void* cache_layer, const void* kv_map,
+                    int max_len) {
   AttnParams p{};
+  p.kv_map = kv_map;
   p.q = H->q;
   p.out = H->attn;
   p.M = M;
@@ -414,7 +417,7 @@ df_status attention(df_handle* H, int M, int R, int nseq, bool causal, const voi
   // algorithmic bytes: the visible keys/values of every sequence, queries and outputs
   const double kv_bytes = (double)nseq * (double)(max_len + (causal ? 0 : R)) * 2.0 * H->kvdim * H->esz;
   const double qo_bytes = 2.0 * M * H->qdim * H->esz;
-  ProfScope ps(H, PC_ATTN, attention_launches(H->bf16, H->hd), kv_bytes + qo_bytes,
+  ProfScope ps(H, PC_ATTN, attention_launches(p, H->bf16), kv_bytes + qo_bytes,
                4.0 * M * H->qdim * (double)max_len);
   CK(launch_attention(p, H->bf16, H->st));
   return DF_OK;
@@ -461,7 +464,9 @@ df_status layer_pass(df_handle* H, const Layer& Lw, int M, int R, int nseq, bool
     e.kv_base = H->blk;
   }
   CKS(gemm(H, Lw.qkv, H->xraw, M, e));
-  CKS(attention(H, M, R, nseq, causal, kv_layer(H, causal ? H->kv_t : H->kv_d, cache_layer), max_len));
+  const std::vector<Tmap>& maps = causal ? H->kvmap_t : H->kvmap_d;
+  const void* kvm = (size_t)cache_layer < maps.size() ? maps[cache_layer].b : nullptr;
+  CKS(attention(H, M, R, nseq, causal, kv_layer(H, causal ? H->kv_t : H->kv_d, cache_layer), kvm, max_len));
   EpiParams r = epi(H, EPI_RESID);
   r.resid = H->h;
   r.ldr = H->d;
@@ -1018,6 +1023,16 @@ df_status alloc_state(df_handle* H) {
   H->layer_stride = (long long)(page_elems * H->n_pages);
   CKS(dalloc(H, &H->kv_t, (size_t)H->layer_stride * H->L * es));
   CKS(dalloc(H, &H->kv_d, (size_t)H->layer_stride * H->Ld * es));
+  if (H->bf16 && H->hd == 128) {
+    H->kvmap_t.resize(H->L);
+    H->kvmap_d.resize(H->Ld);
+    for (int l = 0; l < H->L; ++l)
+      if (!make_tmap_kvcache(H->kvmap_t[l].b, kv_layer(H, H->kv_t, l), H->n_pages, H->Hkv, H->PT))
+        return fail(H, DF_ECUDA, "tensor map encode failed (target cache)");
+    for (int l = 0; l < H->Ld; ++l)
+      if (!make_tmap_kvcache(H->kvmap_d[l].b, kv_layer(H, H->kv_d, l), H->n_pages, H->Hkv, H->PT))
+        return fail(H, DF_ECUDA, "tensor map encode failed (drafter cache)");
+  }
   CKS(dalloc_t(H, &H->d_pt, (size_t)c.max_batch * H->pages_per_seq * 4));
   CK(cudaMemset(H->d_pt, 0xFF, (size_t)c.max_batch * H->pages_per_seq * 4));
   for (int p = H->n_pages - 1; p >= 0; --p) H->free_pages.push_back(p);

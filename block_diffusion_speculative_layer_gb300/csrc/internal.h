@@ -52,6 +52,10 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // ---- tcgen05 GEMM (gemm_tc.cu)
 bool make_tmap_bf16(void* map_out, const void* ptr, long long rows, long long cols, int box_rows);
+// TMA map of one layer of a paged bf16 cache [page][k|v][Hkv][page_tokens][128]:
+// 4-D (64 head dims, 2 halves, page_tokens, page x k|v x head), boxes of one
+// page-half (page_tokens x 128 B), 128-byte swizzle.
+bool make_tmap_kvcache(void* map_out, const void* base, int n_pages, int n_kv_heads, int page_tokens);
 int tc_token_tile(int M);
 cudaError_t tc_prepare();         // kernel attributes, once, before any stream capture
 int tc_split_target(int sm_count);  // CTA count split-K aims for
@@ -92,14 +96,16 @@ struct AttnParams {
   float2* part_ml;        // [M][Hq][n_chunk_slots]
   float scale_log2;       // log2(e) / sqrt(hd)
   int* err;
+  const void* kv_map;     // host copy of a TMA map of `cache` (make_tmap_kvcache), or null
 };
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st);
-int attention_launches(bool bf16, int hd);  // kernels one launch_attention call makes
+int attention_launches(const AttnParams& p, bool bf16);  // kernels one launch_attention call makes
 cudaError_t attention_prepare();  // kernel attributes, once, before any stream capture
 // bf16, head_dim 128 (attention_mma.cu): tensor-core chunk partials for
 // attn_combine, or (cluster) one kernel that also merges them in a cluster.
 cudaError_t launch_attention_mma(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_attention_cluster(const AttnParams& p, cudaStream_t st);
+bool attention_cluster_fits(const AttnParams& p);  // shapes the cluster kernel takes
 cudaError_t attention_cluster_prepare();  // kernel attributes, once, before any stream capture
 
 // ---- small kernels (misc.cu)
