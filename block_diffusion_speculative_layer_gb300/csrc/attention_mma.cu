@@ -290,7 +290,7 @@ cudaError_t launch_attention_mma(const AttnParams& p, cudaStream_t st) {
 // its state bit-for-bit unchanged, and the merge order is fixed, so a row gets
 // the same bits whatever the other rows of its tile or batch.
 constexpr int MAXPG = 2048;                 // page ids a CTA stages for its chunks
-constexpr int CL_NST = 3;                   // key/value stages in flight
+constexpr int CL_NST = 2;                   // key/value stages in flight (three CTAs fit on an SM)
 // One stage: keys then values, each [2 halves of the head dim][64 keys][128 B]
 // in the 128-byte swizzle (16-byte piece b of a row at b ^ (key & 7)).
 constexpr int CL_HALF = MC * 128;
@@ -380,8 +380,11 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-template <int CLA>
-__global__ void __launch_bounds__(256) attn_cl_kernel(AttnParams p, const __grid_constant__ CUtensorMap kvmap) {
+// NW warps (one per query head of a group, at least four): four-warp CTAs are
+// held to 168 registers so that three fit on an SM next to their shared memory.
+template <int CLA, int NW>
+__global__ void __launch_bounds__(NW * 32, NW == 4 ? 3 : 1)
+    attn_cl_kernel(AttnParams p, const __grid_constant__ CUtensorMap kvmap) {
   // The GEMM before this kernel triggers it only after its own wait (see
   // gemm_tc.cu), so everything older than that GEMM is complete here: the row
   // metadata, the page table and the cache entries of earlier positions are
@@ -717,6 +720,31 @@ __global__ void __launch_bounds__(256) attn_cl_kernel(AttnParams p, const __grid
   cl_wait();    // and nobody leaves while another CTA may still read its partial
 }
 
+// TMA map of one layer of the paged cache (declared in internal.h).
+typedef CUresult (*PFN_kvEncodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                        const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                        CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool make_tmap_kvcache(void* map_out, const void* base, int n_pages, int n_kv_heads, int page_tokens) {
+  static PFN_kvEncodeTiled_t enc = nullptr;
+  if (!enc) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      enc = reinterpret_cast<PFN_kvEncodeTiled_t>(fn);
+  }
+  if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) || page_tokens <= 0 || page_tokens > 256) return false;
+  cuuint64_t gdim[4] = {64, 2, (cuuint64_t)page_tokens, (cuuint64_t)n_pages * 2 * n_kv_heads};
+  cuuint64_t gstride[3] = {128, (cuuint64_t)MHD * 2, (cuuint64_t)page_tokens * MHD * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)page_tokens, 1};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = enc(reinterpret_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
+                   gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int CLA>
 static bool cluster_placeable() {
   cudaLaunchConfig_t c = {};
@@ -731,7 +759,7 @@ static bool cluster_placeable() {
   c.attrs = a;
   c.numAttrs = 1;
   int n = 0;
-  const bool ok = cudaOccupancyMaxActiveClusters(&n, attn_cl_kernel<CLA>, &c) == cudaSuccess && n > 0;
+  const bool ok = cudaOccupancyMaxActiveClusters(&n, attn_cl_kernel<CLA, 8>, &c) == cudaSuccess && n > 0;
   cudaGetLastError();
   return ok;
 }
@@ -739,16 +767,21 @@ static bool cluster_placeable() {
 static int g_cla = 0;  // cluster size in use (0: not chosen yet)
 
 // Kernel attributes and the cluster size, once, before any stream capture.
+template <int CLA, int NW>
+static cudaError_t cl_attrs() {
+  return cudaFuncSetAttribute(attn_cl_kernel<CLA, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, cl_smem_bytes(8));
+}
+
 cudaError_t attention_cluster_prepare() {
   if (g_cla) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_cl_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, cl_smem_bytes(8));
-  if (e != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(attn_cl_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, cl_smem_bytes(8))) !=
-      cudaSuccess)
+  cudaError_t e;
+  if ((e = cl_attrs<8, 4>()) != cudaSuccess || (e = cl_attrs<8, 8>()) != cudaSuccess ||
+      (e = cl_attrs<16, 4>()) != cudaSuccess || (e = cl_attrs<16, 8>()) != cudaSuccess)
     return e;
-  const bool big = cudaFuncSetAttribute(attn_cl_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-                       cudaSuccess &&
-                   cluster_placeable<16>();
+  const bool big =
+      cudaFuncSetAttribute(attn_cl_kernel<16, 4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+      cudaFuncSetAttribute(attn_cl_kernel<16, 8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+      cluster_placeable<16>();
   cudaGetLastError();
   g_cla = big ? 16 : 8;
   return cudaSuccess;
@@ -761,9 +794,10 @@ static cudaError_t launch_cl(const AttnParams& p, cudaStream_t st) {
   if (per_cta * (MC / p.page_tokens) > MAXPG) return cudaErrorInvalidValue;
   const int qtiles = (p.rows_per_seq + 15) / 16;
   dim3 grid(CLA, p.Hkv, p.n_seqs * qtiles);
-  const int threads = ((G * 32 + 127) / 128) * 128;
-  return launch_kcl(attn_cl_kernel<CLA>, grid, dim3(threads), (size_t)cl_smem_bytes(G), st, dim3(CLA, 1, 1), p,
-                    *reinterpret_cast<const CUtensorMap*>(p.kv_map));
+  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(p.kv_map);
+  if (G <= 4)
+    return launch_kcl(attn_cl_kernel<CLA, 4>, grid, dim3(128), (size_t)cl_smem_bytes(G), st, dim3(CLA, 1, 1), p, map);
+  return launch_kcl(attn_cl_kernel<CLA, 8>, grid, dim3(256), (size_t)cl_smem_bytes(G), st, dim3(CLA, 1, 1), p, map);
 }
 
 bool attention_cluster_fits(const AttnParams& p) {

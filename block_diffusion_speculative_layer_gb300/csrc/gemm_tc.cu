@@ -459,20 +459,6 @@ bool make_tmap_bf16(void* map_out, const void* ptr, long long rows, long long co
   return r == CUDA_SUCCESS;
 }
 
-bool make_tmap_kvcache(void* map_out, const void* base, int n_pages, int n_kv_heads, int page_tokens) {
-  PFN_encodeTiled_t enc = encode_fn();
-  if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) || page_tokens <= 0 || page_tokens > 256) return false;
-  const int hd = 128;
-  cuuint64_t gdim[4] = {64, 2, (cuuint64_t)page_tokens, (cuuint64_t)n_pages * 2 * n_kv_heads};
-  cuuint64_t gstride[3] = {128, (cuuint64_t)hd * 2, (cuuint64_t)page_tokens * hd * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)page_tokens, 1};
-  cuuint32_t estride[4] = {1, 1, 1, 1};
-  CUresult r = enc(reinterpret_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
-                   gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 static_assert(sizeof(CUtensorMap) == TMAP_BYTES, "tensor map size");
 
 int tc_token_tile(int M) {

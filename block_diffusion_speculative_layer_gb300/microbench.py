@@ -5,6 +5,8 @@
   python -m block_diffusion_speculative_layer_gb300.microbench drafter [--blocks 8,16] [--ctx 1024,4096,16384,32768]
                                                                        [--batch 1,4,16,32]
   python -m block_diffusion_speculative_layer_gb300.microbench ar_proxy
+  python -m block_diffusion_speculative_layer_gb300.microbench serving [--new 1024]
+  python -m block_diffusion_speculative_layer_gb300.microbench dense27b [--new 1024]
 
 Inputs are seeded synthetic bf16 (N(0,1) activations, N(0,0.02) weights)
 drawn on the GPU by torch.  For small shapes several weight copies are used
@@ -15,6 +17,7 @@ import argparse
 import json
 import os
 import sys
+import time
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
@@ -87,6 +90,68 @@ def ar_proxy(a):
                       "note": "random weights: latency only; one drafter pass includes its LM head"}))
 
 
+def _generation(shape, prompts, n_new, max_ctx, label, config):
+    """One timed df_generate over a batch (device weights drawn on the GPU),
+    after one untimed warm-up generation of 16 tokens."""
+    import numpy as np
+    import torch
+
+    import block_diffusion_speculative_layer_gb300 as dfl
+    import synthetic as syn
+
+    t0 = time.time()
+    eng = dfl.Engine(shape, syn.iter_weights_device(shape), max_batch=len(prompts), max_ctx=max_ctx)
+    torch.cuda.empty_cache()
+    setup_s = time.time() - t0
+    eng.generate(prompts, 16)
+    torch.cuda.synchronize()
+    eng.reset_stats()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(eng.stream)
+    out, st = eng.generate(prompts, n_new)
+    e1.record(eng.stream)
+    torch.cuda.synchronize()
+    secs = e0.elapsed_time(e1) / 1000.0
+    s2 = eng.stats()
+    hist = [int(x) for x in s2["accept_hist"]]
+    eng.close()
+    tokens = len(prompts) * n_new
+    print(json.dumps({"op": label, "config": config, "sequences": len(prompts), "new_tokens_each": n_new,
+                      "tokens_per_s": tokens / secs, "wall_s": secs, "cycles": s2["cycles"],
+                      "mean_accept_len": s2["emitted_tokens"] / max(1, s2["cycles"] * len(prompts)),
+                      "accept_hist_k": {str(k): v for k, v in enumerate(hist) if v},
+                      "draft_us_per_cycle": s2["draft_us"] / max(1, s2["cycles"]),
+                      "verify_us_per_cycle": s2["verify_us"] / max(1, s2["cycles"]),
+                      "prefill_us": s2["prefill_us"], "kernel_launches": s2["kernel_launches"],
+                      "setup_s": setup_s, "data": "synthetic, weights drawn on the GPU (seeded), random prompt ids"}),
+          flush=True)
+
+
+def serving(a):
+    """Serving-shaped batch on the Qwen3-8B shape: 16 sequences, prompt lengths
+    uniform over 128..2048, 16-token pages, block 16, greedy."""
+    import synthetic as syn
+
+    shape = syn.QWEN3_8B
+    lens = syn.make_prompt_lengths(16, 128, 2048)
+    prompts = [syn.make_prompt(shape, int(L), stream=200 + i) for i, L in enumerate(lens)]
+    max_ctx = ((int(max(lens)) + a.new + 16 + 2 * shape.block_size + 63) // 64) * 64
+    _generation(shape, prompts, a.new, max_ctx, "serving_batch16",
+                "qwen3-8b-shape bf16, 16 sequences, prompts U[128,2048], block 16, %d new each" % a.new)
+
+
+def dense27b(a):
+    """27B-class target (64 layers, d 5120, 40/8 heads, FFN 17408, vocabulary
+    151936) with a 5-layer drafter, batch 4, 8192-token prompts, block 16."""
+    import synthetic as syn
+
+    shape = syn.DENSE_27B
+    prompts = [syn.make_prompt(shape, 8192, stream=300 + i) for i in range(4)]
+    max_ctx = ((8192 + a.new + 16 + 2 * shape.block_size + 63) // 64) * 64
+    _generation(shape, prompts, a.new, max_ctx, "dense27b_batch4",
+                "27b-class bf16, batch 4, prompt 8192, block 16, %d new each" % a.new)
+
+
 def main():
     import torch
 
@@ -94,7 +159,8 @@ def main():
     from block_diffusion_speculative_layer_gb300 import build
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["gemm", "lmhead", "drafter", "ar_proxy"])
+    ap.add_argument("op", choices=["gemm", "lmhead", "drafter", "ar_proxy", "serving", "dense27b"])
+    ap.add_argument("--new", type=int, default=1024, help="serving/dense27b: new tokens per sequence")
     ap.add_argument("--blocks", default="8,16")
     ap.add_argument("--ctx", default="1024,4096,16384,32768")
     ap.add_argument("--batch", default="1,4,16,32")
@@ -108,6 +174,12 @@ def main():
     ap.add_argument("--token-tile", type=int, default=0)
     a = ap.parse_args()
     build.build()
+    if a.op == "serving":
+        serving(a)
+        return
+    if a.op == "dense27b":
+        dense27b(a)
+        return
     if a.op == "ar_proxy":
         ar_proxy(a)
         return

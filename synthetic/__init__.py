@@ -178,6 +178,26 @@ def iter_weights(s: ModelShape, seed: int = WEIGHT_SEED, gain_std: float = 0.0,
             yield name, draw_weight(s, i, name, shape, seed, gain_std, pool)
 
 
+def iter_weights_device(s: ModelShape, seed: int = WEIGHT_SEED):
+    """Yield (name, tensor) in canonical order, drawn on the current CUDA
+    device: N(0, 0.02) matrices and unit norm gains, all in the model dtype.  A
+    different stream from iter_weights (torch's device generator, seeded per
+    matrix); for throughput runs of large shapes, where drawing on the host
+    would take minutes.  Imports torch on first use."""
+    import torch
+
+    dt = torch.bfloat16 if s.dtype == "bf16" else torch.float32
+    for i, (name, shape) in enumerate(weight_specs(s)):
+        if _is_norm(name):
+            yield name, torch.ones(shape, dtype=dt, device="cuda")
+            continue
+        g = torch.Generator(device="cuda").manual_seed(seed * 1_000_003 + i)
+        w = torch.empty(shape, dtype=torch.float32, device="cuda")
+        w.normal_(0.0, 0.02, generator=g)
+        yield name, w.to(dt)
+        del w
+
+
 def make_weights(s: ModelShape, seed: int = WEIGHT_SEED, gain_std: float = 0.0) -> Dict[str, np.ndarray]:
     return dict(iter_weights(s, seed, gain_std))
 
