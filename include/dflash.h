@@ -35,6 +35,20 @@
  *     index outside its buffer) in a sticky error word; once set, later calls
  *     on the handle return DF_ECUDA or DF_ETIMEOUT.
  *   - The library never prints, never aborts and never falls back to the CPU.
+ *
+ * Environment switches (read once per process; each keeps the results
+ * correct and exists to compare an implementation choice):
+ *   DF_NO_PDL=1      launch kernels without programmatic dependent launch
+ *   DF_NO_GRAPH=1    df_generate launches each cycle's kernels directly
+ *                    instead of replaying a captured CUDA graph
+ *   DF_NO_CLUSTER=1  split-K partials through a workspace, not a cluster
+ *   DF_ATTN_SPLIT=1  attention partials through global memory and a merge
+ *                    kernel instead of the cluster kernel (other rounding)
+ *   DF_SPLIT_CTAS=n  the CTA count the engine's split-K choice aims for
+ *                    (other rounding: the split counts change)
+ * The switches marked "other rounding" change the fp32 summation order, so
+ * results may differ in the last bits; verification and greedy decoding
+ * under the same switches still agree bitwise.
  */
 #ifndef DFLASH_H
 #define DFLASH_H
@@ -237,7 +251,12 @@ df_status df_debug_weight_ptr(const df_handle* h, int32_t which, uint64_t* addr)
 /* y[M][N] = x[M][K] . w[N][K]^T, bf16 operands, fp32 accumulation and output
  * (the tcgen05 GEMM the engine uses; fixed K order, so each output does not
  * depend on M).  N % 128 == 0, K % 64 == 0, M >= 1, 16-byte aligned pointers.
- * splits: 0 = the engine's choice for (N, K), else the split-K count.
+ * splits: 0 = the engine's choice for (N, K) (about 5/3 of the SM count in
+ * CTAs), else the split-K count.  With 2..8 splits the split CTAs of a tile
+ * form a thread-block cluster and add their partials in split order through
+ * distributed shared memory; otherwise (or with DF_NO_CLUSTER=1 in the
+ * environment) the partials go through a workspace allocated on `stream`
+ * for the call.  Both give bitwise the same y.
  * token_tile: 0 = the engine's choice for M, else one of 16,32,64,128,256. */
 df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, int32_t M, int32_t N, int32_t K,
                           int32_t splits, int32_t token_tile, void* stream);
@@ -251,8 +270,9 @@ df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32
  * have no counterpart of this call: it serves callers that may not allocate
  * device memory while they run (a process whose memory is reserved up front
  * by its own pool, a latency-critical loop that cannot afford the
- * synchronisation of an allocation and its release).  Instead of a
- * cudaMallocAsync'd workspace it uses fixed scratch compiled into the library:
+ * synchronisation of an allocation and its release).  It always adds the
+ * split partials through a workspace (never through a cluster), and instead
+ * of a cudaMallocAsync'd one it uses fixed scratch compiled into the library:
  * DF_NOALLOC_WS_FLOATS floats of split-K partial sums and DF_NOALLOC_TICKETS
  * tile tickets, held by every GPU that loads the library until the process
  * exits.  Arguments and result as df_op_gemm_bf16; returns DF_EINVAL, before
@@ -286,7 +306,8 @@ df_status df_bench_drafter_step(df_handle* h, int32_t nseq, int32_t ctx_len, con
                                 int32_t taps_rows, int32_t iters, double us_out[6]);
 
 /* Device time of the tcgen05 GEMM alone: y = x . w^T launched `iters` times
- * back to back on `stream` (tensor maps and split-K workspace made once),
+ * back to back on `stream` (tensor maps, and a split-K workspace where one is
+ * used, made once),
  * timed with CUDA events around the whole run; *us_per_launch receives the
  * mean.  Same shape rules as df_op_gemm_bf16.  Synchronises `stream`. */
 df_status df_op_bench_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, int32_t M, int32_t N, int32_t K,
