@@ -27,6 +27,8 @@ namespace {
 constexpr int ATTN_CHUNK = 64;
 constexpr int PREFILL_CHUNK = 512;
 
+constexpr int KMAX_CYCLES = 8;  // most draft+verify cycles in one captured graph
+
 struct Tmap {
   alignas(64) uint8_t b[TMAP_BYTES];
 };
@@ -103,6 +105,8 @@ struct df_handle {
   std::map<std::tuple<uintptr_t, int, int>, Tmap> xmaps;
   df_stats stats{};
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaEvent_t cev[4 * KMAX_CYCLES] = {};  // draft/verify bracket events of each cycle of a graph
+  int graph_cycles = 4;  // cycles df_generate captures into one graph (DF_GRAPH_CYCLES, 1..KMAX_CYCLES)
   std::string err;
   bool debug = false;
   bool failed = false;
@@ -734,49 +738,63 @@ df_status verify_impl(df_handle* H, const int32_t* slots, int nseq, const int32_
 // (stream-ordered, nothing read back): draft pass, verification, acceptance,
 // fusion and injection, then the accepted tokens and counts copied to h_pin.
 // ext_events: record the timing events as graph-visible event nodes.
-df_status cycle_work(df_handle* H, const int* d_slots_dev, int nseq, int max_len_d, int max_len_t, bool ext_events) {
+// Cycle c of a run of cycles: its events are cev[4c..4c+3] and its accepted
+// tokens and counts go to h_pin at cycle_pin(c).
+size_t cycle_pin(const df_handle* H, int nseq, int c) { return (size_t)c * nseq * (H->B + 1); }
+
+df_status cycle_work(df_handle* H, const int* d_slots_dev, int nseq, int max_len_d, int max_len_t, bool ext_events,
+                     int c) {
   const int B = H->B;
+  cudaEvent_t* ev = H->cev + 4 * c;
   auto rec = [&](cudaEvent_t e) {
     return ext_events ? cudaEventRecordWithFlags(e, H->st, cudaEventRecordExternal) : cudaEventRecord(e, H->st);
   };
-  CK(rec(H->ev[0]));
+  CK(rec(ev[0]));
   { ProfScope ps_(H, PC_CTRL, 1); CK(launch_prep_block(d_slots_dev, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 0, H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st)); }
   CKS(drafter_pass(H, nseq, max_len_d));
   { ProfScope ps_(H, PC_CTRL, 1); CK(launch_collect_drafts(H->d_ids, nseq, B, d_slots_dev, H->d_drafts, H->st)); }
-  CK(rec(H->ev[1]));
-  CK(rec(H->ev[2]));
+  CK(rec(ev[1]));
+  CK(rec(ev[2]));
   { ProfScope ps_(H, PC_CTRL, 1); CK(launch_prep_block(d_slots_dev, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 1, H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st)); }
   const int M = nseq * B;
   CKS(target_pass(H, M, B, nseq, max_len_t, true, -1));
   { ProfScope ps_(H, PC_CTRL, 1); CK(launch_accept(d_slots_dev, nseq, B, H->d_row_tok, H->d_ids, H->d_bonus, H->d_bonus_pos, H->d_acc, H->d_n, H->d_inj_pos, H->st)); }
   CKS(fuse_inject(H, M, H->d_inj_pos));
-  CK(rec(H->ev[3]));
-  CK(d2h(H, H->h_pin, H->d_acc, (size_t)nseq * B * 4));
-  CK(d2h(H, H->h_pin + (size_t)nseq * B, H->d_n, (size_t)nseq * 4));
+  CK(rec(ev[3]));
+  int* pin = H->h_pin + cycle_pin(H, nseq, c);
+  CK(d2h(H, pin, H->d_acc, (size_t)nseq * B * 4));
+  CK(d2h(H, pin + (size_t)nseq * B, H->d_n, (size_t)nseq * 4));
   return DF_OK;
 }
 
-// Host bookkeeping after a cycle's results reached h_pin.
-df_status cycle_finish(df_handle* H, const int32_t* slots, int nseq, int32_t* acc_host, int32_t* n_host) {
+// Host bookkeeping after cycle c's results reached h_pin: lengths, bonus
+// tokens, stats; acc_host/n_host (optional) receive this cycle's rows.
+df_status cycle_finish(df_handle* H, const int32_t* slots, int nseq, int c, int32_t* acc_host, int32_t* n_host) {
   const int B = H->B;
-  const int* acc = H->h_pin;
-  const int* n = H->h_pin + (size_t)nseq * B;
+  const int* acc = H->h_pin + cycle_pin(H, nseq, c);
+  const int* n = acc + (size_t)nseq * B;
   for (int i = 0; i < nseq; ++i) {
     SeqHost& s = H->seqs[slots[i]];
     const int k = n[i] - 1;
     if (k < 0 || k > B - 1) return fail(H, DF_ECUDA, "accept kernel produced an invalid count");
     s.len += k + 1;
     s.bonus = acc[(size_t)i * B + k];
-    CKS(trim_pages(H, slots[i], s.len + B));
     H->stats.cycles += 1;
     H->stats.accepted_drafts += k;
     H->stats.accept_hist[std::min(k, 64)] += 1;
   }
+  const cudaEvent_t* ev = H->cev + 4 * c;
   float a = 0.f, b = 0.f;
-  if (cudaEventElapsedTime(&a, H->ev[0], H->ev[1]) == cudaSuccess) H->stats.draft_us += 1000.0 * a;
-  if (cudaEventElapsedTime(&b, H->ev[2], H->ev[3]) == cudaSuccess) H->stats.verify_us += 1000.0 * b;
+  if (cudaEventElapsedTime(&a, ev[0], ev[1]) == cudaSuccess) H->stats.draft_us += 1000.0 * a;
+  if (cudaEventElapsedTime(&b, ev[2], ev[3]) == cudaSuccess) H->stats.verify_us += 1000.0 * b;
   if (acc_host) std::memcpy(acc_host, acc, (size_t)nseq * B * 4);
   if (n_host) std::memcpy(n_host, n, (size_t)nseq * 4);
+  return DF_OK;
+}
+
+// Pages past each sequence's kept length (+ one block) go back to the pool.
+df_status trim_all(df_handle* H, const int32_t* slots, int nseq) {
+  for (int i = 0; i < nseq; ++i) CKS(trim_pages(H, slots[i], H->seqs[slots[i]].len + H->B));
   return DF_OK;
 }
 
@@ -786,32 +804,44 @@ void drop_graph(df_handle* H) {
   H->gkey.clear();
 }
 
-// One draft + verify cycle for df_generate.  After the first (eager) cycle of
-// a handle, the cycle's ~350 launches are captured once into a CUDA graph and
-// replayed; a new capture is made when the slots change or an attention
-// chunk boundary is crossed (the attention grids depend on the lengths).
-df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int32_t* acc_host, int32_t* n_host) {
+// K draft + verify cycles for df_generate (acc_host [K][nseq][B], n_host
+// [K][nseq]).  Pages for K blocks of growth are reserved first.  After the
+// first (eager) cycle of a handle, the K cycles' launches are captured once
+// into a CUDA graph and replayed: the cycles chain on the device (positions,
+// bonus tokens and rollback live in device memory) and the host reads all K
+// results after one synchronisation.  The graph's attention launches are
+// sized for max_ctx, so a new capture is made only when the slots or K change.
+df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int32_t* acc_host, int32_t* n_host) {
   CKS(check_slots(H, slots, nseq));
   const int B = H->B;
-  int max_t = 0, max_d = 0;
+  if (K < 1 || K > KMAX_CYCLES) return fail(H, DF_EINVAL, "bad cycle count");
   for (int i = 0; i < nseq; ++i) {
     SeqHost& s = H->seqs[slots[i]];
-    if (s.len + B > H->cfg.max_ctx) return fail(H, DF_EINVAL, "sequence would exceed max_ctx");
-    CKS(ensure_pages(H, slots[i], s.len + B));
-    max_t = std::max(max_t, s.len + B);
-    max_d = std::max(max_d, s.len);
+    if (s.len + K * B > H->cfg.max_ctx) return fail(H, DF_EINVAL, "sequence would exceed max_ctx");
+    CKS(ensure_pages(H, slots[i], s.len + K * B));
   }
+  auto out_acc = [&](int c) { return acc_host ? acc_host + (size_t)c * nseq * B : nullptr; };
+  auto out_n = [&](int c) { return n_host ? n_host + (size_t)c * nseq : nullptr; };
   const bool graphs = H->use_graphs && !H->profiling && H->graph_ready_cycles > 0;
   if (!graphs) {
-    CK(h2d(H, H->d_slots, slots, nseq * 4));
-    CKS(cycle_work(H, H->d_slots, nseq, max_d, max_t, false));
-    CKS(sync(H));
-    H->graph_ready_cycles += 1;
-    return cycle_finish(H, slots, nseq, acc_host, n_host);
+    for (int c = 0; c < K; ++c) {
+      int max_t = 0, max_d = 0;
+      for (int i = 0; i < nseq; ++i) {
+        const SeqHost& s = H->seqs[slots[i]];
+        max_t = std::max(max_t, s.len + B);
+        max_d = std::max(max_d, s.len);
+      }
+      CK(h2d(H, H->d_slots, slots, nseq * 4));
+      CKS(cycle_work(H, H->d_slots, nseq, max_d, max_t, false, 0));
+      CKS(sync(H));
+      H->graph_ready_cycles += 1;
+      CKS(cycle_finish(H, slots, nseq, 0, out_acc(c), out_n(c)));
+    }
+    return trim_all(H, slots, nseq);
   }
   std::vector<int> key(slots, slots + nseq);
-  key.push_back((max_t + 63) / 64);
-  key.push_back((max_d + 63) / 64);
+  key.push_back(K);
+  const int max_len = H->cfg.max_ctx;  // length-independent launches
   // the caller's stream may be the legacy default stream, which cannot be
   // captured: graphs run on the engine's own stream, ordered after the
   // caller's stream and joined back to it with events
@@ -828,7 +858,7 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int32_t* acc_
     cudaGraph_t g = nullptr;
     if (ok) {
       H->st = H->gstream;
-      st = cycle_work(H, H->d_gslots, nseq, max_d, max_t, true);
+      for (int c = 0; c < K && st == DF_OK; ++c) st = cycle_work(H, H->d_gslots, nseq, max_len, max_len, true, c);
       H->st = user;
       ok = cudaStreamEndCapture(H->gstream, &g) == cudaSuccess && st == DF_OK;
     }
@@ -844,10 +874,7 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int32_t* acc_
       (void)cudaGetLastError();
       H->gexec = nullptr;
       H->use_graphs = false;
-      CK(h2d(H, H->d_slots, slots, nseq * 4));
-      CKS(cycle_work(H, H->d_slots, nseq, max_d, max_t, false));
-      CKS(sync(H));
-      return cycle_finish(H, slots, nseq, acc_host, n_host);
+      return cycle_impl(H, slots, nseq, K, acc_host, n_host);
     }
     H->gkey = key;
   }
@@ -858,7 +885,8 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int32_t* acc_
   H->stats.h2d_bytes += H->g_h2d;
   H->stats.d2h_bytes += H->g_d2h;
   CKS(sync(H));
-  return cycle_finish(H, slots, nseq, acc_host, n_host);
+  for (int c = 0; c < K; ++c) CKS(cycle_finish(H, slots, nseq, c, out_acc(c), out_n(c)));
+  return trim_all(H, slots, nseq);
 }
 
 df_status release(df_handle* H, int slot) {
@@ -1113,9 +1141,10 @@ df_status alloc_state(df_handle* H) {
   CKS(dalloc_t(H, &H->rope, rope.size() * sizeof(float2)));
   CK(cudaMemcpy(H->rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice));
 
-  H->h_pin_ints = std::max<size_t>((size_t)c.max_batch * (H->B + 2) * 2, 64);
+  H->h_pin_ints = std::max<size_t>((size_t)KMAX_CYCLES * c.max_batch * (H->B + 1) + (size_t)c.max_batch * (H->B + 2) * 2, 64);
   CK(cudaMallocHost(&H->h_pin, H->h_pin_ints * 4));
   for (auto& e : H->ev) CK(cudaEventCreate(&e));
+  for (auto& e : H->cev) CK(cudaEventCreate(&e));
   CK(cudaStreamCreateWithFlags(&H->gstream, cudaStreamNonBlocking));
   for (auto& e : H->gjoin) CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
   return DF_OK;
@@ -1193,6 +1222,8 @@ df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_we
   {
     const char* g = getenv("DF_NO_GRAPH");
     H->use_graphs = !(g && g[0] == '1');
+    const char* gc = getenv("DF_GRAPH_CYCLES");  // cycles per captured graph in df_generate
+    if (gc && atoi(gc) > 0) H->graph_cycles = std::min(KMAX_CYCLES, atoi(gc));
   }
   for (int l = 0; l < 1024; ++l) H->tap_of_layer[l] = -1;
   for (int i = 0; i < 5; ++i) H->tap_of_layer[cfg->feat_layers[i]] = i;
@@ -1281,18 +1312,36 @@ df_status df_generate(df_handle* H, const int32_t* prompts_host, const int32_t* 
     off += lens_host[i];
     if (s == DF_OK) out_host[(size_t)i * n_new] = bonus, count[i] = 1;
   }
-  std::vector<int> active, acc((size_t)nseq * B), n(nseq);
+  std::vector<int> active, acc((size_t)KMAX_CYCLES * nseq * B), n((size_t)KMAX_CYCLES * nseq);
+  long long cyc = 0, emitted = 0;  // sequence-cycles run and tokens they emitted, for the choice of K
   while (s == DF_OK) {
     active.clear();
+    int remaining = n_new, room = KMAX_CYCLES;
     for (int i = 0; i < nseq; ++i)
-      if (count[i] < n_new) active.push_back(i);
+      if (count[i] < n_new) {
+        active.push_back(i);
+        remaining = std::min(remaining, n_new - count[i]);
+        room = std::min(room, (H->cfg.max_ctx - H->seqs[i].len) / B);
+      }
     if (active.empty()) break;
-    s = cycle_impl(H, active.data(), (int)active.size(), acc.data(), n.data());
+    // Cycles per graph: as many as the sequence nearest to its end still
+    // needs at the tokens per cycle seen so far (no wasted cycles at one token
+    // per cycle), at most graph_cycles, and within max_ctx.
+    const double per_cycle = cyc > 0 ? std::max(1.0, (double)emitted / (double)cyc) : 1.0;
+    int K = (int)((double)remaining / per_cycle);
+    K = std::max(1, std::min({K, H->graph_cycles, room}));
+    const int na = (int)active.size();
+    s = cycle_impl(H, active.data(), na, K, acc.data(), n.data());
     if (s != DF_OK) break;
-    for (size_t j = 0; j < active.size(); ++j) {
-      const int i = active[j];
-      for (int t = 0; t < n[j] && count[i] < n_new; ++t) out_host[(size_t)i * n_new + count[i]++] = acc[j * B + t];
-    }
+    for (int c = 0; c < K; ++c)
+      for (int j = 0; j < na; ++j) {
+        const int i = active[j];
+        const int nj = n[(size_t)c * na + j];
+        cyc += 1;
+        emitted += nj;
+        for (int t = 0; t < nj && count[i] < n_new; ++t)
+          out_host[(size_t)i * n_new + count[i]++] = acc[((size_t)c * na + j) * B + t];
+      }
   }
   for (int i = 0; i < nseq; ++i)
     if (H->seqs[i].active) release(H, i);
@@ -1400,6 +1449,8 @@ void df_destroy(df_handle* H) {
     cudaStreamDestroy(H->gstream);
   }
   for (auto& e : H->gjoin)
+    if (e) cudaEventDestroy(e);
+  for (auto& e : H->cev)
     if (e) cudaEventDestroy(e);
   delete H;
 }

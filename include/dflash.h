@@ -40,7 +40,8 @@
  * correct and exists to compare an implementation choice):
  *   DF_NO_PDL=1      launch kernels without programmatic dependent launch
  *   DF_NO_GRAPH=1    df_generate launches each cycle's kernels directly
- *                    instead of replaying a captured CUDA graph
+ *                    instead of replaying captured CUDA graphs
+ *   DF_GRAPH_CYCLES=k  draft+verify cycles per captured graph (1..8, default 4)
  *   DF_NO_CLUSTER=1  split-K partials through a workspace, not a cluster
  *   DF_ATTN_SPLIT=1  attention partials through global memory and a merge
  *                    kernel instead of the cluster kernel (other rounding)
@@ -180,9 +181,13 @@ df_status df_verify_accept(df_handle* h, const int32_t* seqs_host, int32_t nseq,
 
 /* Whole speculative generation for nseq prompts (packed back to back in
  * prompts_host, lengths lens_host): prefill each into slots 0..nseq-1, then
- * draft/verify cycles until n_new tokens per sequence; the last cycle is
- * truncated.  out_host: [nseq][n_new].  stats (may be NULL) receives this
- * call's counters.  Slots are released at the end. */
+ * draft/verify cycles until n_new tokens per sequence; tokens past n_new are
+ * dropped.  Cycles run in groups replayed from captured CUDA graphs and
+ * chained on the device, with one host synchronisation per group.  A
+ * sequence that reaches n_new inside a group still runs that group's
+ * remaining cycles, and they count in the stats.
+ * out_host: [nseq][n_new].  stats (may be NULL) receives this call's
+ * counters.  Slots are released at the end. */
 df_status df_generate(df_handle* h, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,
                       int32_t n_new, int32_t* out_host, df_stats* stats);
 
