@@ -37,7 +37,15 @@ are:
   token at slot i; slot 0's own output is unused;
 * argmax compares the logits as computed and keeps the lowest index on ties;
 * verification keeps the longest prefix of drafts that equal the target's
-  greedy tokens, then the target's token after it (the bonus).
+  greedy tokens, then the target's token after it (the bonus);
+* sampling (temperature T > 0, nucleus top_p): the pages state that a draft
+  is accepted or rejected by the target's distribution, that a rejected
+  position is sampled again, and that the output keeps the target's
+  distribution; with drafter and target at the same T and top_p.  The
+  plainest rule with that property is the standard speculative-sampling
+  test: keep d_i with probability min(1, p(d_i) / q(d_i)), replace the first
+  rejected draft by a draw from max(0, p - q) normalised, and draw the token
+  after a fully kept block from p.  The uniforms every draw uses are inputs.
 
 Parity is pinned by tests against library routines (torch CPU attention and
 RMSNorm), closed forms (feature layers, unit-RMS context rows, RoPE as a
@@ -465,6 +473,130 @@ def spec_generate(m: Model, prompt: Sequence[int], n_new: int,
         g = argmax_lowest(vp.logits)
         k, new_bonus = accept_prefix(drafts, g)
         cycles.append(Cycle(pos, bonus, np.asarray(drafts), g, k, vp.taps, vp.logits))
+        cache.truncate(pos + k + 1)
+        inject_kv(W, cfg, ctxc, fuse_features(W, cfg, vp.taps[: k + 1]))
+        out += [int(t) for t in drafts[:k]] + [new_bonus]
+        bonus = new_bonus
+        pos += k + 1
+    return SpecResult(tokens=np.asarray(out[:n_new], dtype=np.int64), cycles=cycles)
+
+
+# ----------------------------------------------------------------------------
+# Sampling: the lossless rejection test ([ABS] 实践 4 on temperature and top-p,
+# 核心思想 step 3 and the Q&A on losslessness)
+# ----------------------------------------------------------------------------
+
+def sampling_probs(logits: np.ndarray, temperature: float, top_p: float = 1.0) -> np.ndarray:
+    """Rows of next-token probabilities for sampling.
+
+    softmax(logits / T), then restricted to the nucleus (the fewest most
+    probable tokens whose mass reaches top_p, ties by lower index) and
+    renormalised.  T == 0 means greedy: one-hot at the argmax (lowest index
+    on ties)."""
+    logits = np.atleast_2d(np.asarray(logits, dtype=np.float64))
+    n, V = logits.shape
+    if temperature == 0.0:
+        out = np.zeros((n, V))
+        out[np.arange(n), argmax_lowest(logits)] = 1.0
+        return out
+    z = logits / float(temperature)
+    z = z - z.max(axis=1, keepdims=True)
+    e = np.exp(z)
+    probs = e / e.sum(axis=1, keepdims=True)
+    if top_p >= 1.0:
+        return probs
+    out = np.zeros_like(probs)
+    for r in range(n):
+        order = np.lexsort((np.arange(V), -probs[r]))      # descending mass, lower index first on ties
+        csum = np.cumsum(probs[r, order])
+        keep = order[: int(np.searchsorted(csum, top_p)) + 1]
+        out[r, keep] = probs[r, keep]
+        out[r] /= out[r].sum()
+    return out
+
+
+def draw(probs: np.ndarray, u: float) -> int:
+    """Inverse-CDF draw from one row of (possibly unnormalised) mass with a
+    uniform u in [0, 1): the lowest index whose cumulative mass exceeds
+    u x total."""
+    c = np.cumsum(np.asarray(probs, dtype=np.float64))
+    return int(min(np.searchsorted(c, u * c[-1], side="right"), len(c) - 1))
+
+
+def accept_sampled(drafts: Sequence[int], q_rows: np.ndarray, p_rows: np.ndarray,
+                   u_accept: Sequence[float], u_final: float) -> Tuple[int, int]:
+    """Speculative sampling over one block.
+
+    drafts = d_1..d_{B-1}, d_i drawn from q_rows[i-1] (the drafter's
+    distribution at slot i); p_rows[i] is the target's distribution for the
+    token after slot i (row i of the verify pass), i = 0..B-1.  d_i is kept
+    while u_accept[i-1] < p_{i-1}(d_i) / q_{i-1}(d_i); at the first rejection
+    the token is drawn from max(0, p - q) (normalised) with u_final, and if
+    every draft is kept the token after the block is drawn from p_{B-1} with
+    u_final.  Returns (k, token): k kept drafts, then that token."""
+    k = 0
+    while k < len(drafts):
+        d = int(drafts[k])
+        pk, qk = p_rows[k][d], q_rows[k][d]
+        if qk > 0.0 and u_accept[k] < pk / qk:
+            k += 1
+            continue
+        residual = np.maximum(p_rows[k] - q_rows[k], 0.0)
+        if residual.sum() <= 0.0:          # p == q: nothing to correct
+            residual = p_rows[k]
+        return k, draw(residual, u_final)
+    return k, draw(p_rows[k], u_final)
+
+
+Uniforms = Callable[[int], np.ndarray]
+
+
+def sample_generate(m: Model, prompt: Sequence[int], n_new: int, temperature: float, top_p: float,
+                    uniforms: Uniforms) -> np.ndarray:
+    """Token-by-token sampling from the target (the distribution speculative
+    sampling must keep); uniforms(n) gives the next n uniforms."""
+    cfg = m.cfg
+    cache = KVCache(cfg.n_layers, cfg.n_kv_heads, cfg.head_dim)
+    out: List[int] = []
+    tp = target_forward(m.W, cfg, prompt, cache)
+    while True:
+        tok = draw(sampling_probs(tp.logits[-1:], temperature, top_p)[0], float(uniforms(1)[0]))
+        out.append(tok)
+        if len(out) >= n_new:
+            return np.asarray(out, dtype=np.int64)
+        tp = target_forward(m.W, cfg, [tok], cache)
+
+
+def spec_generate_sampled(m: Model, prompt: Sequence[int], n_new: int, temperature: float, top_p: float,
+                          uniforms: Uniforms) -> SpecResult:
+    """DFlash speculative decoding with sampling, one sequence.
+
+    The cycle of ``spec_generate``, with each slot's draft drawn from the
+    drafter's distribution at that slot (same temperature and top_p as the
+    target) and ``accept_sampled`` in place of the greedy prefix test.  The
+    bonus token after the prompt is drawn from the target's distribution.
+    Uniforms per cycle: B-1 for the drafts, B-1 for the tests, 1 for the
+    final draw.  At temperature 0 this is exactly ``spec_generate``."""
+    cfg = m.cfg
+    W = m.W
+    B = cfg.block_size
+    cache = KVCache(cfg.n_layers, cfg.n_kv_heads, cfg.head_dim)
+    ctxc = ContextCache(cfg.draft_layers, cfg.n_kv_heads, cfg.head_dim)
+    tp = target_forward(W, cfg, prompt, cache)
+    bonus = draw(sampling_probs(tp.logits[-1:], temperature, top_p)[0], float(uniforms(1)[0]))
+    inject_kv(W, cfg, ctxc, fuse_features(W, cfg, tp.taps))
+    pos = len(prompt)
+    out = [bonus]
+    cycles: List[Cycle] = []
+    while len(out) < n_new:
+        dp = draft_blocks(W, cfg, ctxc, [(bonus, pos)])
+        q_rows = sampling_probs(dp.logits[1:B], temperature, top_p)     # slots 1..B-1
+        u = uniforms(2 * (B - 1) + 1)
+        drafts = np.asarray([draw(q_rows[i], float(u[i])) for i in range(B - 1)], dtype=np.int64)
+        vp = target_forward(W, cfg, [bonus] + [int(t) for t in drafts], cache)
+        p_rows = sampling_probs(vp.logits, temperature, top_p)
+        k, new_bonus = accept_sampled(drafts, q_rows, p_rows, u[B - 1: 2 * (B - 1)], float(u[-1]))
+        cycles.append(Cycle(pos, bonus, drafts, argmax_lowest(vp.logits), k, vp.taps, vp.logits))
         cache.truncate(pos + k + 1)
         inject_kv(W, cfg, ctxc, fuse_features(W, cfg, vp.taps[: k + 1]))
         out += [int(t) for t in drafts[:k]] + [new_bonus]

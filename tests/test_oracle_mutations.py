@@ -11,6 +11,7 @@ import pytest
 
 from oracle import dflash_oracle as O
 from tests import test_oracle_pins as P
+from tests import test_oracle_sampling as S
 
 
 def _wrong_rope(x, positions, theta):
@@ -107,6 +108,44 @@ def _layer_without_q_rope(W, prefix, cfg, h, positions, kv_source):
         O.rope = orig
 
 
+def _accept_residual_from_p(drafts, q_rows, p_rows, u_accept, u_final):
+    k = 0
+    while k < len(drafts):
+        d = int(drafts[k])
+        if q_rows[k][d] > 0 and u_accept[k] < p_rows[k][d] / q_rows[k][d]:
+            k += 1
+            continue
+        return k, O.draw(p_rows[k], u_final)                                   # resamples from p, not max(0, p - q)
+    return k, O.draw(p_rows[k], u_final)
+
+
+def _accept_inverted_ratio(drafts, q_rows, p_rows, u_accept, u_final):
+    k = 0
+    while k < len(drafts):
+        d = int(drafts[k])
+        if p_rows[k][d] > 0 and u_accept[k] < q_rows[k][d] / p_rows[k][d]:   # q / p instead of p / q
+            k += 1
+            continue
+        return k, O.draw(np.maximum(p_rows[k] - q_rows[k], 0.0), u_final)
+    return k, O.draw(p_rows[k], u_final)
+
+
+def _accept_wrong_row(drafts, q_rows, p_rows, u_accept, u_final):
+    k = 0
+    while k < len(drafts):
+        d = int(drafts[k])
+        pk = p_rows[k + 1][d]                                                  # the row after the draft
+        if q_rows[k][d] > 0 and u_accept[k] < pk / q_rows[k][d]:
+            k += 1
+            continue
+        return k, O.draw(np.maximum(p_rows[k + 1] - q_rows[k], 0.0), u_final)
+    return k, O.draw(p_rows[k], u_final)
+
+
+def _sampled_pin():
+    S.check_keeps_target_distribution(O.accept_sampled, n=40_000)
+
+
 MUTATIONS = [
     ("rope", _wrong_rope, [P.test_rope_is_complex_rotation]),
     ("attention", _wrong_gqa, [lambda: P.test_attention_matches_torch_sdpa(8, 2)]),
@@ -117,6 +156,9 @@ MUTATIONS = [
     ("rms_norm", _rms_no_eps, [P.test_rms_norm_matches_torch]),
     ("rms_norm", _rms_no_gain, [P.test_rms_norm_matches_torch]),
     ("decoder_layer", _layer_without_q_rope, [lambda: P.test_target_relative_positions()]),
+    ("accept_sampled", _accept_residual_from_p, [_sampled_pin]),
+    ("accept_sampled", _accept_inverted_ratio, [_sampled_pin]),
+    ("accept_sampled", _accept_wrong_row, [_sampled_pin]),
 ]
 
 
