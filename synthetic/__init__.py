@@ -27,7 +27,7 @@ from __future__ import annotations
 import dataclasses
 import os
 from concurrent.futures import ThreadPoolExecutor
-from typing import Dict, Iterator, List, Tuple
+from typing import Dict, Iterator, List, Sequence, Tuple
 
 import numpy as np
 
@@ -245,3 +245,41 @@ def make_normal(shape: Tuple[int, ...], std: float, seed: int, stream: int = 0,
     with ThreadPoolExecutor(threads) as pool:
         parts = list(pool.map(one, range(nblk)))
     return np.concatenate(parts).reshape(shape) if nblk > 1 else parts[0].reshape(shape)
+
+
+# ----------------------------------------------------------------------------
+# Counter-based uniforms: Philox4x32-10 (Salmon, Moraes, Dror and Shaw,
+# "Parallel random numbers: as easy as 1, 2, 3", SC'11), for draws that the
+# CPU and the GPU must reproduce bit for bit.  A kernel that draws implements
+# the same generator from the same definition.
+# ----------------------------------------------------------------------------
+
+_PHILOX_M = (0xD2511F53, 0xCD9E8D57)
+_PHILOX_W = (0x9E3779B9, 0xBB67AE85)
+_U32 = 0xFFFFFFFF
+
+
+def philox4x32(ctr: Sequence[int], key: Sequence[int], rounds: int = 10) -> List[int]:
+    """Philox4x32 block function: 4 x 32-bit counter, 2 x 32-bit key -> 4 x 32-bit."""
+    c = [int(x) & _U32 for x in ctr]
+    k = [int(x) & _U32 for x in key]
+    for _ in range(rounds):
+        p0 = _PHILOX_M[0] * c[0]
+        p1 = _PHILOX_M[1] * c[2]
+        c = [((p1 >> 32) ^ c[1] ^ k[0]) & _U32, p1 & _U32, ((p0 >> 32) ^ c[3] ^ k[1]) & _U32, p0 & _U32]
+        k = [(k[0] + _PHILOX_W[0]) & _U32, (k[1] + _PHILOX_W[1]) & _U32]
+    return c
+
+
+def philox_uniforms(seed: int, stream: int, offset: int, n: int) -> np.ndarray:
+    """Uniforms number offset .. offset + n - 1 of (seed, stream), in [0, 1)
+    with 24 random bits each (exact in float32).  Uniform j is word j % 4 of
+    philox4x32(counter = (b, b >> 32, stream, 0), key = (seed, seed >> 32)),
+    b = j // 4, mapped as u = (word >> 8) * 2^-24."""
+    out = np.empty(n, dtype=np.float64)
+    for i in range(n):
+        j = offset + i
+        blk = j // 4
+        w = philox4x32([blk & _U32, (blk >> 32) & _U32, stream & _U32, 0], [seed & _U32, (seed >> 32) & _U32])[j % 4]
+        out[i] = (w >> 8) * (1.0 / 16777216.0)
+    return out
