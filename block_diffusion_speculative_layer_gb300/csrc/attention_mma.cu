@@ -1,10 +1,12 @@
 // bf16 attention over the paged caches on the tensor cores (mma.sync m16n8k16).
 //
-// attn_mma_kernel: same split and masks as the CUDA-core kernel in
-// attention.cu (fixed 64-key chunks counted from position 0, the drafter's
-// block rows as one extra chunk, partials merged in chunk order by
-// attn_combine), so verification and greedy decoding give bitwise the same
-// rows.  attn_cl_kernel (below) keeps the chunks but merges inside a cluster.
+// attn_cl_kernel (the engine's kernel; below): fixed 64-key chunks counted
+// from position 0, the drafter's block rows as one extra chunk, chunk
+// partials merged inside a thread-block cluster.
+// attn_mma_kernel: the same chunks with partials to global memory, merged in
+// chunk order by attn_combine (DF_ATTN_SPLIT=1, and shapes the cluster kernel
+// does not take).  Either way a row's result does not depend on the other
+// rows, so verification and greedy decoding give bitwise the same rows.
 //
 // One CTA = one (chunk, KV head, 16-token tile); one warp per grouped query
 // head, so a warp's 16 token rows form exactly one m16 tile.  The chunk's keys
@@ -278,9 +280,9 @@ cudaError_t launch_attention_mma(const AttnParams& p, cudaStream_t st) {
 // A cluster of CLA CTAs (16 where the device can place such clusters, else 8)
 // covers one (KV head, 16-token tile).  CTA rank j takes the 64-key context
 // chunks c = j, j + CLA, j + 2*CLA, ... (the drafter's block rows, as one more
-// chunk, go to rank CLA-1 after its context chunks) and runs
-// an online softmax over them, double-buffering the next chunk's keys and
-// values while it computes.  The CLA partials (running max, sum, unnormalised
+// chunk, go to rank CLA-1 after its context chunks) and runs an online softmax
+// over them.  The chunks' pages come by TMA into CL_NST shared-memory stages,
+// so the next chunks' keys and values load while one is computed.  The CLA partials (running max, sum, unnormalised
 // output per row and query head) are then left in shared memory and, after a
 // cluster barrier, each CTA merges a share of the (head, row) pairs by reading
 // all CLA partials through distributed shared memory in rank order.

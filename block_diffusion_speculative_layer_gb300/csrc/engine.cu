@@ -3,10 +3,11 @@
 // One handle holds one model on one GPU: a weight arena (target, drafter,
 // one shared embedding and LM head), a paged target KV cache, a paged drafter
 // context cache filled by KV injection, pre-allocated activation buffers,
-// split-K and split-KV workspaces, and the per-sequence state (bonus token and
-// its position) on the device.  A cycle launches only this library's kernels
-// on the caller's stream and reads back one small result per cycle (accepted
-// tokens and their count).
+// the split-K and split-KV workspaces of the non-cluster paths, and the
+// per-sequence state (bonus token and its position) on the device.  A cycle
+// launches only this library's kernels and reads back one small result
+// (accepted tokens and their count); df_generate replays groups of cycles
+// from CUDA graphs and reads a group's results after one synchronisation.
 #include <algorithm>
 #include <cmath>
 #include <cstdio>

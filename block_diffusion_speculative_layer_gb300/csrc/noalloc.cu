@@ -1,8 +1,10 @@
 // df_op_gemm_bf16_noalloc: the tcgen05 GEMM of df_op_gemm_bf16 for callers
 // that must not allocate device memory.
 //
-// df_op_gemm_bf16 gets its split-K workspace and tile tickets from
-// cudaMallocAsync on every call.  Some callers cannot do that: a process whose
+// df_op_gemm_bf16 adds split-K partials through a thread-block cluster, or
+// else through a workspace and tile tickets from cudaMallocAsync on every
+// call.  This variant always takes the workspace form, with scratch that is
+// never allocated.  Some callers cannot allocate: a process whose
 // device memory is reserved up front by its own pool (every byte accounted by
 // that pool), or a latency-critical loop where an allocation and its release
 // would add synchronisation.  This variant keeps that scratch in two
