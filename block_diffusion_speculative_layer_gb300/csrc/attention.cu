@@ -294,7 +294,7 @@ static bool attn_split() {
 }
 
 int attention_launches(const AttnParams& p, bool bf16) {
-  return (bf16 && !attn_split() && attention_cluster_fits(p)) ? 1 : 2;
+  return (bf16 && !attn_split() && attention_cluster_fits(p)) ? 1 : 2;  // either cluster form: one kernel
 }
 
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st) {
@@ -302,6 +302,12 @@ cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st) {
   if (bf16 && p.hd == 128) {
     // tensor cores, chunk partials merged inside a cluster (attention_mma.cu);
     // DF_ATTN_SPLIT=1: partials to global memory and the ordered merge kernel
+    // DF_ATTN_TC=1: the tcgen05 form of the cluster kernel (other rounding)
+    static const bool use_tc = [] {
+      const char* e = getenv("DF_ATTN_TC");
+      return e && e[0] == '1';
+    }();
+    if (use_tc && !attn_split() && attention_cluster_fits(p) && p.Hq / p.Hkv <= 4) return launch_attention_tc(p, st);
     if (!attn_split() && attention_cluster_fits(p)) return launch_attention_cluster(p, st);
     cudaError_t e = launch_attention_mma(p, st);
     if (e != cudaSuccess) return e;

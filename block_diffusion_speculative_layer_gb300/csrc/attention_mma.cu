@@ -722,6 +722,439 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 3 : 1)
   cl_wait();    // and nobody leaves while another CTA may still read its partial
 }
 
+
+// ---------------------------------------------------------------------------
+// tcgen05 form of the cluster attention (DF_ATTN_TC=1, groups of at most four
+// query heads).  Same chunks, staging and cluster merge as attn_cl_kernel;
+// per chunk, S = Q K^T (M = 128 rows: query head g x token row r at row
+// g * 16 + r, rows past 16 G zero; N = 64 keys) and O += P V (V read as an
+// MN-major operand) run on tcgen05 with accumulators in tensor memory, and
+// thread t runs the softmax of row t.  In this form each chunk is serial
+// (S, softmax, O rescale, P V) with one CTA per SM, which measured 2.6-3x
+// slower than attn_cl_kernel, so it is not the default.
+constexpr int TC_QHALF = 128 * 128;          // one 64-dim half of the 128-row Q tile
+constexpr int TC_QOFF = 2 * CL_STAGE;         // after the two key/value stages
+constexpr int TC_POFF = TC_QOFF + 2 * TC_QHALF;
+constexpr int TC_PGOFF = TC_POFF + 128 * 128;
+constexpr int TC_SMEM = TC_PGOFF + MAXPG * 4 + 1024;
+constexpr int TC_OLD = 132;                   // row stride (floats) of the partials left for the merge
+constexpr uint32_t TC_IDESC_S = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t TC_IDESC_PV =
+    (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+static_assert(4 * 16 * TC_OLD * 4 + 4 * 16 * 8 <= 2 * CL_STAGE, "partials fit over the stages");
+
+// Shared-memory descriptor, 128-byte swizzle: 8-row groups 1024 bytes apart;
+// lbo: K-major 16 (unused), MN-major the byte stride between 64-element column blocks.
+__device__ __forceinline__ uint64_t tc_desc(uint32_t addr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];" : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]) : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]) : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const float* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31])) : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+template <int CLA>
+__global__ void __launch_bounds__(128, 1) attn_tc_kernel(AttnParams p, const __grid_constant__ CUtensorMap kvmap) {
+  // The GEMM before this kernel triggers it only after its own wait (see
+  // gemm_tc.cu), so everything older than that GEMM is complete here: the row
+  // metadata, the page table and the cache entries of earlier positions are
+  // read before the wait; the queries, this pass's keys and values and the
+  // drafter's block rows after it.
+  pdl_trigger();
+  extern __shared__ __align__(128) uint8_t smc_raw[];
+  // 1024-byte aligned: the TMA's 128-byte swizzle repeats every 1024 bytes
+  uint8_t* smc = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smc_raw) + 1023) & ~uintptr_t(1023));
+  const int G = p.Hq / p.Hkv;
+  const int j = (int)cl_rank();
+  const int h = blockIdx.y;
+  const int qtiles = (p.rows_per_seq + 15) / 16;
+  const int z = blockIdx.z / qtiles;
+  const int qt = blockIdx.z % qtiles;
+  const int r0 = z * p.rows_per_seq + qt * 16;
+  const int nrows = min(16, p.rows_per_seq - qt * 16);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const bool causal = p.causal != 0;
+
+  // ---- the tile's rows: visible context length (-1: no position), longest
+  __shared__ int s_len[16];
+  __shared__ int s_first_new;  // cache positions from here on are written by this pass
+  if (threadIdx.x < 16) {
+    int l = -1;
+    if ((int)threadIdx.x < nrows && p.row_pos[r0 + threadIdx.x] >= 0) l = ctx_len_rows(p, r0 + threadIdx.x);
+    s_len[threadIdx.x] = l;
+  }
+  if (threadIdx.x == 32) {
+    const int f = p.row_pos[z * p.rows_per_seq];
+    s_first_new = causal ? (f >= 0 ? f : 0) : 0x7fffffff;
+  }
+  const int ppc = MC / p.page_tokens;
+  // ---- page ids of this CTA's chunks (every chunk the longest row could need)
+  int* s_pg = reinterpret_cast<int*>(smc + TC_PGOFF);
+  const int seq_slot = p.row_seq[r0];
+  const int cap_chunks = (p.grid_chunks > j) ? (p.grid_chunks - j + CLA - 1) / CLA : 0;
+  for (int t = threadIdx.x; t < cap_chunks * ppc && t < MAXPG; t += blockDim.x) {
+    const int pg = (j + CLA * (t / ppc)) * ppc + t % ppc;  // page of the sequence
+    s_pg[t] = pg < p.pt_stride ? p.page_table[(size_t)seq_slot * p.pt_stride + pg] : -1;
+  }
+  __syncthreads();
+  int max_len = 0;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) max_len = max(max_len, s_len[r]);
+  const int first_new = s_first_new;
+  const int nA = (max_len + MC - 1) / MC;                       // context chunks of the tile
+  const int nmine = nA > j ? (nA - j + CLA - 1) / CLA : 0;       // this CTA's context chunks
+  const bool has_blk = !causal && j == CLA - 1;
+  const int nsteps = nmine + (has_blk ? 1 : 0);
+
+  const __nv_bfloat16* blk = reinterpret_cast<const __nv_bfloat16*>(p.blk);
+  const int PT = p.page_tokens;
+  __shared__ __align__(8) uint64_t s_full[CL_NST];
+  __shared__ int s_failed;
+  __shared__ __align__(8) uint64_t s_mma[2];  // 0: S complete, 1: P V complete
+  __shared__ uint32_t s_tmem;
+  if (threadIdx.x == 0) {
+    cl_mbar_init(smem_addr(&s_mma[0]));
+    cl_mbar_init(smem_addr(&s_mma[1]));
+    for (int b2 = 0; b2 < CL_NST; ++b2) cl_mbar_init(smem_addr(&s_full[b2]));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kvmap)) : "memory");
+    s_failed = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_addr(&s_tmem))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = s_tmem;                    // columns [0, 64): S; [64, 192): O
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t bar_s = smem_addr(&s_mma[0]), bar_o = smem_addr(&s_mma[1]);
+  // Stage step st into buffer buf: part 1 = the pages wholly before first_new
+  // (written by earlier passes), 2 = the rest, 3 = all.  Context chunks come
+  // by TMA, one 2 KB box per (page, k|v, half row), issued by thread 0; the
+  // drafter's block rows by 16-byte cp.async from every thread.  Part 2 (or
+  // 3) makes the stage barrier's one arrival.
+  auto stage = [&](int st, int buf, int part) {
+    uint8_t* sK = smc + buf * CL_STAGE;
+    uint8_t* sV = sK + 2 * CL_HALF;
+    const uint32_t bar = smem_addr(&s_full[buf]);
+    if (st >= nmine) {  // block chunk
+      if (!(part & 2)) return;
+      for (int idx = threadIdx.x; idx < MC * (MHD / 8); idx += blockDim.x) {
+        const int key = idx >> 4, b = idx & 15;
+        if (key < p.rows_per_seq) {
+          const int row = z * p.rows_per_seq + key;
+          cp_async16(smem_addr(sK) + swz2(key, b), blk + ((size_t)(0 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8);
+          cp_async16(smem_addr(sV) + swz2(key, b), blk + ((size_t)(1 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8);
+        } else {
+          *reinterpret_cast<uint4*>(sK + swz2(key, b)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sV + swz2(key, b)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      cp_async_commit();
+      if (threadIdx.x == 0) cl_arrive_expect_tx(bar, 0);
+      return;
+    }
+    if (threadIdx.x != 0) return;
+    const int key0 = (j + CLA * st) * MC;
+    const int npg = (min(MC, max_len - key0) + PT - 1) / PT;  // pages holding a key the tile can see
+    auto wanted = [&](int pg) {
+      const bool old = key0 + (pg + 1) * PT <= first_new;
+      const int page = s_pg[st * ppc + pg];
+      return ((old ? 1 : 2) & part) && page >= 0 && page < p.n_pages;
+    };
+    uint32_t bytes = 0;
+    for (int pg = 0; pg < npg; ++pg)
+      if (wanted(pg)) bytes += 4u * (uint32_t)PT * 128u;
+    if (part == 1) {
+      if (bytes) cl_expect_tx(bar, bytes);
+    } else {
+      cl_arrive_expect_tx(bar, bytes);
+    }
+    for (int pg = 0; pg < npg; ++pg) {
+      if (!wanted(pg)) continue;
+      const int page = s_pg[st * ppc + pg];
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+          tma_kv(smem_addr((kv ? sV : sK) + half * CL_HALF + pg * PT * 128), &kvmap, bar, half,
+                 (page * 2 + kv) * p.Hkv + h);
+    }
+  };
+  // Keys and values the staged pages do not cover (past the tile's longest
+  // row, or in a page the table does not hold) read as zeros.
+  auto fixup = [&](int st, int buf) {
+    if (st >= nmine) return;
+    uint8_t* sK = smc + buf * CL_STAGE;
+    uint8_t* sV = sK + 2 * CL_HALF;
+    const int key0 = (j + CLA * st) * MC;
+    const int nkeys = min(MC, max_len - key0);
+    for (int idx = threadIdx.x; idx < MC * (MHD / 8); idx += blockDim.x) {
+      const int key = idx >> 4, b = idx & 15;
+      const int page = s_pg[st * ppc + key / PT];
+      const bool have = key < nkeys && page >= 0 && page < p.n_pages;
+      if (!have) {
+        if (key < nkeys && b == 0 && (key % PT) == 0) flag_error(p.err, ERR_BOUNDS);
+        *reinterpret_cast<uint4*>(sK + swz2(key, b)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sV + swz2(key, b)) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  // the first stages' earlier-position pages go out before the wait
+  for (int st = 0; st < CL_NST && st < nsteps; ++st) stage(st, st, 1);
+
+  pdl_wait();
+  // ---- Q as the A operand of S = Q K^T: 128 rows (g * 16 + r = query head g,
+  // token row r; rows past 16 G read as zeros), two 64-dim halves, 128-byte swizzle
+  uint8_t* sQ = smc + TC_QOFF;
+  for (int idx = threadIdx.x; idx < 128 * 16; idx += blockDim.x) {
+    const int row = idx >> 4, c = idx & 15;
+    const int g = row >> 4, r = row & 15;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (g < G && r < nrows && s_len[r] >= 0)
+      v = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + (size_t)(r0 + r) * p.Hq * MHD +
+                                          (size_t)(h * G + g) * MHD + c * 8);
+    *reinterpret_cast<uint4*>(sQ + (c >> 3) * TC_QHALF + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = v;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  // the rest of the first stages
+  for (int st = 0; st < CL_NST && st < nsteps; ++st) stage(st, st, 2);
+
+  // ---- online softmax over this CTA's chunks: thread t owns row t
+  const int trow = threadIdx.x, tg = trow >> 4, tr = trow & 15;
+  const bool row_ok = tg < G && tr < nrows && s_len[tr] >= 0;
+  float m_run = -INFINITY, l_run = 0.f;
+  bool pv_issued = false;
+  uint32_t ph_s = 0, ph_o = 0;
+  const uint32_t qbase = smem_addr(sQ), pbase = smem_addr(smc + TC_POFF);
+  int done = 0;  // steps consumed
+  for (int st = 0; st < nsteps; ++st) {
+    const int buf = st % CL_NST;
+    if (st >= nmine) cp_async_wait_0();  // the block rows (this thread's copies)
+    if (!cl_wait_bar(smem_addr(&s_full[buf]), (uint32_t)(st / CL_NST) & 1u, p.err)) s_failed = 1;
+    fixup(st, buf);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // zero rows and block rows: generic writes
+    __syncthreads();
+    if (s_failed) break;
+    done = st + 1;
+    {
+      const bool is_blk = st >= nmine;
+      const int key0 = is_blk ? 0 : (j + CLA * st) * MC;
+      const uint32_t kbase = smem_addr(smc + buf * CL_STAGE);
+      const uint32_t vbase = kbase + 2 * CL_HALF;
+      // S = Q K^T: M 128 rows, N 64 keys, K 128 dims, into TMEM columns [0, 64)
+      if (threadIdx.x == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma(tmem, tc_desc(qbase + (kk >> 2) * TC_QHALF + (kk & 3) * 32, 16),
+                 tc_desc(kbase + (kk >> 2) * CL_HALF + (kk & 3) * 32, 16), TC_IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(bar_s);
+      }
+      if (!cl_wait_bar(bar_s, ph_s, p.err)) s_failed = 1;
+      ph_s ^= 1u;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      float sv[64];
+      tc_ld64(tmem + lane_base, sv);
+      const int vis = !row_ok ? 0 : (is_blk ? p.rows_per_seq : s_len[tr] - key0);
+      float mc = -INFINITY;
+#pragma unroll
+      for (int kk = 0; kk < 64; ++kk) {
+        sv[kk] = (kk < vis) ? sv[kk] * p.scale_log2 : -INFINITY;
+        mc = fmaxf(mc, sv[kk]);
+      }
+      const float mn = fmaxf(m_run, mc);
+      const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m_run - mn);
+      float cs = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int kk = 0; kk < 64; kk += 2) {
+        const float e0 = (sv[kk] == -INFINITY) ? 0.f : exp2f(sv[kk] - mn);
+        const float e1 = (sv[kk + 1] == -INFINITY) ? 0.f : exp2f(sv[kk + 1] - mn);
+        cs += e0 + e1;
+        pk[kk >> 1] = pack_bf16(e0, e1);
+      }
+      l_run = l_run * alpha + cs;
+      m_run = mn;
+      // O rows rescaled in tensor memory (the previous P V finished at the end of
+      // its step); the loads and stores are warp-wide, rows that keep their
+      // scale multiply by exactly 1
+      if (__any_sync(0xffffffffu, pv_issued && alpha != 1.f)) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float ov[32];
+          tc_ld32(tmem + lane_base + 64u + 32u * c, ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+          tc_st32(tmem + lane_base + 64u + 32u * c, ov);
+        }
+      }
+      // P row t (64 keys, 128 bytes) as the A operand of P V, 128-byte swizzle
+      uint8_t* sP = smc + TC_POFF;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(sP + trow * 128 + ((c ^ (trow & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncthreads();
+      // O += P V: M 128 rows, N 128 dims (V read MN-major), K 64 keys, into TMEM columns [64, 192)
+      if (threadIdx.x == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma(tmem + 64u, tc_desc(pbase + kk * 32, 16), tc_desc(vbase + kk * 2048, CL_HALF), TC_IDESC_PV,
+                 (pv_issued || kk > 0) ? 1u : 0u);
+        tc_commit(bar_o);
+      }
+      pv_issued = true;
+      if (!cl_wait_bar(bar_o, ph_o, p.err)) s_failed = 1;   // V's stage is refilled below
+      ph_o ^= 1u;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    }
+    __syncthreads();  // this buffer is refilled now, for CL_NST steps on
+    if (st + CL_NST < nsteps) stage(st + CL_NST, buf, 3);
+  }
+  if (s_failed && threadIdx.x == 0) {
+    // leave no copy in flight: wait (bounded) for the stages issued but not consumed
+    for (int st = done; st < nsteps && st < done + CL_NST; ++st)
+      if (st < nmine) cl_wait_bar(smem_addr(&s_full[st % CL_NST]), (uint32_t)(st / CL_NST) & 1u, p.err);
+  }
+  cp_async_wait_0();
+  __syncthreads();
+
+  // ---- leave the partial in shared memory (over the stage buffers)
+  float* sO = reinterpret_cast<float*>(smc);
+  float2* sML = reinterpret_cast<float2*>(smc + G * 16 * TC_OLD * 4);
+  // (pv_issued is uniform over the CTA, so every warp takes part in the
+  // warp-wide loads; only rows of real query heads are stored)
+  float* dst = sO + (size_t)(tg * 16 + tr) * TC_OLD;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float ov[32];
+    if (pv_issued) {
+      tc_ld32(tmem + lane_base + 64u + 32u * c, ov);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+    }
+    if (tg < G) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(dst + 32 * c + i) = make_float4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
+    }
+  }
+  if (tg < G) sML[tg * 16 + tr] = make_float2(m_run, l_run);
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem) : "memory");
+  }
+  cl_arrive();
+  cl_wait();
+
+  // ---- merge: this CTA's share of the (head, row) pairs, 32 threads x 4 dims per pair
+  const int pairs = G * 16;
+  const int p0 = j * pairs / CLA, p1 = (j + 1) * pairs / CLA;
+  const uint32_t sO_s = smem_addr(sO), sML_s = smem_addr(sML);
+  for (int pp = p0 + warp; pp < p1; pp += blockDim.x >> 5) {
+    const int g = pp >> 4, rr = pp & 15;
+    if (rr >= nrows || s_len[rr] < 0) continue;
+    float2 ml[CLA];
+    float4 av[CLA];
+    // ranks without a chunk of this tile hold (-inf, 0, 0): their terms are
+    // exactly zero, so they are not read
+#pragma unroll
+    for (int i = 0; i < CLA; ++i) {
+      const bool held = i < nA || (!causal && i == CLA - 1);
+      ml[i] = held ? cl_ld2(cl_map(sML_s + (uint32_t)(g * 16 + rr) * 8u, (uint32_t)i)) : make_float2(-INFINITY, 0.f);
+      av[i] = held ? cl_ld4(cl_map(sO_s + (uint32_t)((g * 16 + rr) * TC_OLD + lane * 4) * 4u, (uint32_t)i))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < CLA; ++i) Mx = fmaxf(Mx, ml[i].x);
+    float L = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < CLA; ++i) {
+      const float w = (ml[i].x == -INFINITY) ? 0.f : exp2f(ml[i].x - Mx);
+      L = fmaf(ml[i].y, w, L);
+      a.x = fmaf(av[i].x, w, a.x);
+      a.y = fmaf(av[i].y, w, a.y);
+      a.z = fmaf(av[i].z, w, a.z);
+      a.w = fmaf(av[i].w, w, a.w);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)(r0 + rr) * p.Hq * MHD +
+                         (size_t)(h * G + g) * MHD + lane * 4;
+    uint2 packed;
+    packed.x = pack_bf16(a.x * inv, a.y * inv);
+    packed.y = pack_bf16(a.z * inv, a.w * inv);
+    *reinterpret_cast<uint2*>(out) = packed;
+  }
+  cl_arrive();  // this CTA's reads of the other partials are done
+  cl_wait();    // and nobody leaves while another CTA may still read its partial
+}
+
+
+static int g_cla_tc = 0;
+
+cudaError_t launch_attention_tc(const AttnParams& p, cudaStream_t st) {
+  const int G = p.Hq / p.Hkv;
+  if (!attention_cluster_fits(p) || G > 4) return cudaErrorInvalidValue;
+  const int per_cta = (p.grid_chunks + 15) / 16;
+  if (per_cta * (MC / p.page_tokens) > MAXPG) return cudaErrorInvalidValue;
+  if (!g_cla_tc) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    if (e != cudaSuccess) return e;
+    const bool big = cudaFuncSetAttribute(attn_tc_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    cudaGetLastError();
+    g_cla_tc = big ? 16 : 8;
+  }
+  const int qtiles = (p.rows_per_seq + 15) / 16;
+  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(p.kv_map);
+  if (g_cla_tc == 16)
+    return launch_kcl(attn_tc_kernel<16>, dim3(16, p.Hkv, p.n_seqs * qtiles), dim3(128), (size_t)TC_SMEM, st, dim3(16, 1, 1), p, map);
+  return launch_kcl(attn_tc_kernel<8>, dim3(8, p.Hkv, p.n_seqs * qtiles), dim3(128), (size_t)TC_SMEM, st, dim3(8, 1, 1), p, map);
+}
+
 // TMA map of one layer of the paged cache (declared in internal.h).
 typedef CUresult (*PFN_kvEncodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                         const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

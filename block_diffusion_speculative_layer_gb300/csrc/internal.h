@@ -105,6 +105,7 @@ cudaError_t attention_prepare();  // kernel attributes, once, before any stream 
 // attn_combine, or (cluster) one kernel that also merges them in a cluster.
 cudaError_t launch_attention_mma(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_attention_cluster(const AttnParams& p, cudaStream_t st);
+cudaError_t launch_attention_tc(const AttnParams& p, cudaStream_t st);
 bool attention_cluster_fits(const AttnParams& p);  // shapes the cluster kernel takes
 cudaError_t attention_cluster_prepare();  // kernel attributes, once, before any stream capture
 

@@ -45,6 +45,8 @@
  *   DF_NO_CLUSTER=1  split-K partials through a workspace, not a cluster
  *   DF_ATTN_SPLIT=1  attention partials through global memory and a merge
  *                    kernel instead of the cluster kernel (other rounding)
+ *   DF_ATTN_TC=1     attention math on tcgen05 (groups of <= 4 query heads;
+ *                    other rounding; slower in its present serial form)
  *   DF_SPLIT_CTAS=n  the CTA count the engine's split-K choice aims for
  *                    (other rounding: the split counts change)
  * The switches marked "other rounding" change the fp32 summation order, so
