@@ -26,6 +26,8 @@ EXPORTED = [
     "df_seq_info", "df_destroy", "df_last_error", "df_debug_enable", "df_debug_read", "df_debug_weight_ptr",
     "df_op_gemm_bf16", "df_op_lmhead_argmax_bf16", "df_profile_enable", "df_profile_read",
     "df_op_bench_gemm_bf16", "df_op_gemm_bf16_noalloc", "df_bench_drafter_step",
+    "df_generate_sampled", "df_philox4x32_10", "df_op_philox_uniforms", "df_op_sampling_probs",
+    "df_op_sample_draw", "df_op_accept_sampled",
 ]
 
 
@@ -113,6 +115,14 @@ def lib() -> ctypes.CDLL:
     L.df_op_bench_gemm_bf16.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, ctypes.POINTER(ctypes.c_float)]
     L.df_profile_enable.argtypes = [_P, _I]
     L.df_profile_read.argtypes = [_P, ctypes.POINTER(DfKernelStat), _I, _IP]
+    _F = ctypes.c_float
+    L.df_generate_sampled.argtypes = [_P, _IP, _IP, _I, _I, _F, _F, ctypes.c_uint64, _IP, ctypes.POINTER(DfStats)]
+    _U32P = ctypes.POINTER(ctypes.c_uint32)
+    L.df_philox4x32_10.argtypes = [_U32P, _U32P, _U32P]
+    L.df_op_philox_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint64, _I, _P, _P]
+    L.df_op_sampling_probs.argtypes = [_P, _I, _I, _F, _F, _P, _P, _P]
+    L.df_op_sample_draw.argtypes = [_P, _I, _I, _F, _F, _P, _P, _P, _P]
+    L.df_op_accept_sampled.argtypes = [_P, _P, _P, _I, _I, _I, _F, _F, _P, _P, _P, _P, _P]
     for name in EXPORTED:
         fn = getattr(L, name)
         if fn.restype is ctypes.c_int:  # default restype: the df_status enum
@@ -268,6 +278,19 @@ class Engine:
                                        ctypes.byref(stats)), "df_generate")
         return out, stats.as_dict()
 
+    def generate_sampled(self, prompts: Sequence[Sequence[int]], n_new: int, temperature: float = 1.0,
+                         top_p: float = 1.0, seed: int = 0):
+        """Speculative sampling: drafts drawn from the drafter, the rejection
+        test against the target; sequence i uses Philox stream i of `seed`."""
+        lens = _i32([len(p) for p in prompts])
+        flat = _i32(np.concatenate([_i32(p) for p in prompts]))
+        out = np.zeros((len(prompts), n_new), np.int32)
+        stats = DfStats()
+        self._check(self.L.df_generate_sampled(self.h, _ip(flat), _ip(lens), len(prompts), n_new, float(temperature),
+                                               float(top_p), int(seed), _ip(out), ctypes.byref(stats)),
+                    "df_generate_sampled")
+        return out, stats.as_dict()
+
     def greedy_reference(self, prompts: Sequence[Sequence[int]], n_new: int) -> np.ndarray:
         lens = _i32([len(p) for p in prompts])
         flat = _i32(np.concatenate([_i32(p) for p in prompts]))
@@ -376,3 +399,96 @@ def lmhead_argmax_bf16(x, w, stream=None):
     if st != DF_OK:
         raise DfError(st, "df_op_lmhead_argmax_bf16")
     return ids
+
+
+# ------------------------------------------------------------------ sampling ops
+def philox4x32_10(ctr: Sequence[int], key: Sequence[int]) -> List[int]:
+    """The library's Philox4x32-10 block function, evaluated on the host."""
+    c = (ctypes.c_uint32 * 4)(*[int(x) & 0xFFFFFFFF for x in ctr])
+    k = (ctypes.c_uint32 * 2)(*[int(x) & 0xFFFFFFFF for x in key])
+    o = (ctypes.c_uint32 * 4)()
+    st = lib().df_philox4x32_10(c, k, o)
+    if st != DF_OK:
+        raise DfError(st, "df_philox4x32_10")
+    return list(o)
+
+
+def _stream(stream):
+    import torch
+    return _P((stream if stream is not None else torch.cuda.current_stream()).cuda_stream)
+
+
+def _err_word(device):
+    import torch
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def _check_err(err, what: str):
+    e = int(err.item())
+    if e:
+        raise DfError(DF_ECUDA, f"{what}: device error bits {e}")
+
+
+def philox_uniforms(seed: int, stream_id: int, offset: int, n: int, device="cuda", stream=None):
+    """Uniforms offset .. offset + n - 1 of (seed, stream_id), generated on the GPU (float32 tensor)."""
+    import torch
+    u = torch.empty(max(n, 1), dtype=torch.float32, device=device)
+    st = lib().df_op_philox_uniforms(int(seed), int(stream_id), int(offset), n, _P(u.data_ptr()), _stream(stream))
+    if st != DF_OK:
+        raise DfError(st, "df_op_philox_uniforms")
+    return u[:n]
+
+
+def sampling_probs(logits, temperature: float, top_p: float = 1.0, stream=None):
+    """Rows of sampling probabilities of fp32 logits [rows, V] (torch, cuda)."""
+    import torch
+    assert logits.dtype == torch.float32 and logits.is_cuda and logits.dim() == 2
+    x = logits.contiguous()
+    rows, V = x.shape
+    probs = torch.empty_like(x)
+    err = _err_word(x.device)
+    st = lib().df_op_sampling_probs(_P(x.data_ptr()), rows, V, float(temperature), float(top_p), _P(probs.data_ptr()),
+                                    _P(err.data_ptr()), _stream(stream))
+    if st != DF_OK:
+        raise DfError(st, "df_op_sampling_probs")
+    _check_err(err, "df_op_sampling_probs")
+    return probs
+
+
+def sample_draw(logits, temperature: float, top_p: float, u, stream=None):
+    """One inverse-CDF draw per row of fp32 logits [rows, V] with uniforms u [rows]."""
+    import torch
+    x = logits.contiguous()
+    uu = u.to(device=x.device, dtype=torch.float32).contiguous()
+    rows, V = x.shape
+    assert uu.numel() == rows
+    idx = torch.empty(rows, dtype=torch.int32, device=x.device)
+    err = _err_word(x.device)
+    st = lib().df_op_sample_draw(_P(x.data_ptr()), rows, V, float(temperature), float(top_p), _P(uu.data_ptr()),
+                                 _P(idx.data_ptr()), _P(err.data_ptr()), _stream(stream))
+    if st != DF_OK:
+        raise DfError(st, "df_op_sample_draw")
+    _check_err(err, "df_op_sample_draw")
+    return idx
+
+
+def accept_sampled(drafts, q_logits, p_logits, temperature: float, top_p: float, u, stream=None):
+    """Speculative-sampling test of nseq blocks: drafts [nseq, B-1], q_logits
+    [nseq, B-1, V], p_logits [nseq, B, V], u [nseq, B] -> (k [nseq], token [nseq])."""
+    import torch
+    p = p_logits.contiguous()
+    nseq, B, V = p.shape
+    q = q_logits.contiguous()
+    d = drafts.to(device=p.device, dtype=torch.int32).contiguous()
+    uu = u.to(device=p.device, dtype=torch.float32).contiguous()
+    assert q.shape == (nseq, B - 1, V) and d.shape == (nseq, B - 1) and uu.shape == (nseq, B)
+    k = torch.empty(nseq, dtype=torch.int32, device=p.device)
+    tok = torch.empty(nseq, dtype=torch.int32, device=p.device)
+    err = _err_word(p.device)
+    st = lib().df_op_accept_sampled(_P(d.data_ptr()), _P(q.data_ptr()), _P(p.data_ptr()), nseq, B, V,
+                                    float(temperature), float(top_p), _P(uu.data_ptr()), _P(k.data_ptr()),
+                                    _P(tok.data_ptr()), _P(err.data_ptr()), _stream(stream))
+    if st != DF_OK:
+        raise DfError(st, "df_op_accept_sampled")
+    _check_err(err, "df_op_accept_sampled")
+    return k, tok

@@ -131,6 +131,16 @@ struct df_handle {
   std::vector<Pending> pending;
   df_kernel_stat prof[8];
   int rows_last_target = 0, rows_last_draft = 0, rows_last_ctx = 0, rows_last_logits = 0;
+  // speculative sampling (df_generate_sampled): the LM heads keep fp32 logits
+  // and the cycle draws drafts, tests them and draws the final token
+  bool sampling = false;
+  float samp_inv_t = 0.f, samp_top_p = 1.f;
+  unsigned long long samp_seed = 0;
+  float *d_qlog = nullptr, *d_plog = nullptr;    // [max_batch * B][V] drafter / target logits
+  SampleRow *d_qst = nullptr, *d_pst = nullptr;  // [max_batch * B] their sampling rows
+  float* d_u = nullptr;                          // [max_batch][2B] uniforms of the current cycle
+  uint32_t* d_ustream = nullptr;                 // [max_batch] generator stream of each slot
+  unsigned long long* d_ucount = nullptr;        // [max_batch] uniforms each slot has used
 };
 
 namespace {
@@ -389,6 +399,22 @@ df_status lm_head_argmax(df_handle* H, int M, float* dbg) {
   return DF_OK;
 }
 
+// LM head over rows [0, M) of xb.  Greedy: fused argmax into d_ids.
+// Sampling: fp32 logits into the drafter's (draft) or the target's buffer,
+// then each row's sampling distribution.
+df_status lm_head(df_handle* H, int M, float* dbg, bool draft) {
+  if (!H->sampling) return lm_head_argmax(H, M, dbg);
+  float* logits = draft ? H->d_qlog : H->d_plog;
+  EpiParams e = epi(H, EPI_STORE_F32);
+  e.out = logits;
+  e.ldo = H->V;
+  CKS(gemm(H, H->lm_head, H->xb, M, e, PC_LMHEAD));
+  ProfScope ps(H, PC_CTRL, 1);
+  CK(launch_sample_state(logits, H->V, M, H->V, H->samp_inv_t, H->samp_top_p, draft ? H->d_qst : H->d_pst, H->d_err,
+                         H->st));
+  return DF_OK;
+}
+
 df_status attention(df_handle* H, int M, int R, int nseq, bool causal, const void* cache_layer, const void* kv_map,
                     int max_len) {
   AttnParams p{};
@@ -511,7 +537,7 @@ df_status target_pass(df_handle* H, int M, int R, int nseq, int max_len, bool wa
   H->rows_last_logits = rows;
   { ProfScope ps_(H, PC_NORM, 1); CK(launch_rmsnorm(H->h + (size_t)first * H->d, H->d, H->final_norm, H->xb, H->d, H->bf16, rows, H->d,
                     H->cfg.rms_eps, nullptr, 0, nullptr, H->st)); }
-  return lm_head_argmax(H, rows, H->debug ? H->dbg_logits : nullptr);
+  return lm_head(H, rows, H->debug ? H->dbg_logits : nullptr, false);
 }
 
 // Fuse the taps of rows [0, M) and inject K/V of every drafter layer at the
@@ -548,7 +574,7 @@ df_status drafter_pass(df_handle* H, int nseq, int max_ctx_len) {
   if (H->debug) CK(cudaMemcpyAsync(H->dbg_dh, H->h, (size_t)M * H->d * 4, cudaMemcpyDeviceToDevice, H->st));
   { ProfScope ps_(H, PC_NORM, 1); CK(launch_rmsnorm(H->h, H->d, H->d_final_norm, H->xb, H->d, H->bf16, M, H->d, H->cfg.rms_eps, nullptr, 0, nullptr,
                     H->st)); }
-  CKS(lm_head_argmax(H, M, H->debug ? H->dbg_dlogits : nullptr));
+  CKS(lm_head(H, M, H->debug ? H->dbg_dlogits : nullptr, true));
   H->rows_last_draft = M;
   return DF_OK;
 }
@@ -647,7 +673,15 @@ df_status prefill_impl(df_handle* H, int seq, const int32_t* prompt, int len, bo
     CKS(target_pass(H, rows, rows, 1, c0 + rows, inject, last ? 1 : 0));
     if (inject) CKS(fuse_inject(H, rows, H->d_row_pos));
   }
-  // bonus token = argmax at the last prompt position; it sits at position len
+  // bonus token = argmax at the last prompt position (sampling: a draw from
+  // the target's distribution there, the sequence's first uniform); it sits
+  // at position len
+  if (H->sampling) {
+    CK(h2d(H, H->d_slots, &seq, 4));
+    ProfScope ps_(H, PC_CTRL, 2);
+    CK(launch_cycle_uniforms(H->d_slots, 1, 1, H->samp_seed, H->d_ustream, H->d_ucount, H->d_u, 2 * H->B, H->st));
+    CK(launch_sample_draw(H->d_plog, H->V, 1, H->V, H->d_pst, H->d_u, 1, 2 * H->B, 0, H->d_ids, H->d_err, H->st));
+  }
   CK(cudaMemcpyAsync(H->d_bonus + seq, H->d_ids, 4, cudaMemcpyDeviceToDevice, H->st));
   CK(h2d(H, H->d_bonus_pos + seq, &len, 4));
   CK(d2h(H, H->h_pin, H->d_ids, 4));
@@ -752,14 +786,32 @@ df_status cycle_work(df_handle* H, const int* d_slots_dev, int nseq, int max_len
   };
   CK(rec(ev[0]));
   { ProfScope ps_(H, PC_CTRL, 1); CK(launch_prep_block(d_slots_dev, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 0, H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st)); }
+  if (H->sampling) {
+    // the cycle's 2B - 1 uniforms per sequence: B - 1 draft draws, B - 1 tests, the final draw
+    ProfScope ps_(H, PC_CTRL, 1);
+    CK(launch_cycle_uniforms(d_slots_dev, nseq, 2 * B - 1, H->samp_seed, H->d_ustream, H->d_ucount, H->d_u, 2 * B, H->st));
+  }
   CKS(drafter_pass(H, nseq, max_len_d));
+  if (H->sampling) {
+    // draft i (slot i = 1..B-1) drawn from the drafter's distribution at slot i
+    ProfScope ps_(H, PC_CTRL, 1);
+    CK(launch_sample_draw(H->d_qlog, H->V, nseq * B, H->V, H->d_qst, H->d_u, B, 2 * B, 1, H->d_ids, H->d_err, H->st));
+  }
   { ProfScope ps_(H, PC_CTRL, 1); CK(launch_collect_drafts(H->d_ids, nseq, B, d_slots_dev, H->d_drafts, H->st)); }
   CK(rec(ev[1]));
   CK(rec(ev[2]));
   { ProfScope ps_(H, PC_CTRL, 1); CK(launch_prep_block(d_slots_dev, nseq, B, H->d_bonus, H->d_bonus_pos, H->d_drafts, H->cfg.mask_token_id, 1, H->d_row_tok, H->d_row_pos, H->d_row_seq, H->st)); }
   const int M = nseq * B;
   CKS(target_pass(H, M, B, nseq, max_len_t, true, -1));
-  { ProfScope ps_(H, PC_CTRL, 1); CK(launch_accept(d_slots_dev, nseq, B, H->d_row_tok, H->d_ids, H->d_bonus, H->d_bonus_pos, H->d_acc, H->d_n, H->d_inj_pos, H->st)); }
+  if (H->sampling) {
+    ProfScope ps_(H, PC_CTRL, 1);
+    CK(launch_accept_sampled(d_slots_dev, nseq, B, H->d_row_tok + 1, B, H->d_qlog, H->V, H->d_qst, B, 1, H->d_plog, H->V,
+                             H->d_pst, H->V, H->d_u, 2 * B, B - 1, H->d_bonus, H->d_bonus_pos, H->d_acc, H->d_n,
+                             H->d_inj_pos, nullptr, nullptr, H->d_err, H->st));
+  } else {
+    ProfScope ps_(H, PC_CTRL, 1);
+    CK(launch_accept(d_slots_dev, nseq, B, H->d_row_tok, H->d_ids, H->d_bonus, H->d_bonus_pos, H->d_acc, H->d_n, H->d_inj_pos, H->st));
+  }
   CKS(fuse_inject(H, M, H->d_inj_pos));
   CK(rec(ev[3]));
   int* pin = H->h_pin + cycle_pin(H, nseq, c);
@@ -842,6 +894,13 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int32_
   }
   std::vector<int> key(slots, slots + nseq);
   key.push_back(K);
+  if (H->sampling) {
+    // the sampling parameters are launch arguments of the captured kernels
+    int tb = 0, pb = 0;
+    std::memcpy(&tb, &H->samp_inv_t, 4);
+    std::memcpy(&pb, &H->samp_top_p, 4);
+    key.insert(key.end(), {-1, tb, pb, (int)(uint32_t)H->samp_seed, (int)(uint32_t)(H->samp_seed >> 32)});
+  }
   const int max_len = H->cfg.max_ctx;  // length-independent launches
   // the caller's stream may be the legacy default stream, which cannot be
   // captured: graphs run on the engine's own stream, ordered after the
@@ -1161,6 +1220,21 @@ df_status ensure_debug_buffers(df_handle* H) {
   return DF_OK;
 }
 
+// Buffers of speculative sampling, allocated on first use.
+df_status ensure_sampling_buffers(df_handle* H) {
+  if (H->d_qlog) return DF_OK;
+  if (H->V > SAMPLE_MAX_VOCAB) return fail(H, DF_EINVAL, "vocabulary too large for sampling");
+  const size_t rows = (size_t)H->cfg.max_batch * H->B;
+  CKS(dalloc_t(H, &H->d_qlog, rows * H->V * 4));
+  CKS(dalloc_t(H, &H->d_plog, rows * H->V * 4));
+  CKS(dalloc_t(H, &H->d_qst, rows * sizeof(SampleRow)));
+  CKS(dalloc_t(H, &H->d_pst, rows * sizeof(SampleRow)));
+  CKS(dalloc_t(H, &H->d_u, (size_t)H->cfg.max_batch * 2 * H->B * 4));
+  CKS(dalloc_t(H, &H->d_ustream, (size_t)H->cfg.max_batch * 4));
+  CKS(dalloc_t(H, &H->d_ucount, (size_t)H->cfg.max_batch * 8));
+  return DF_OK;
+}
+
 }  // namespace
 
 // =============================================================================
@@ -1298,9 +1372,8 @@ df_status df_verify_accept(df_handle* H, const int32_t* seqs_host, int32_t nseq,
   return verify_impl(H, seqs_host, nseq, drafts_host, accepted_host, n_host, false);
 }
 
-df_status df_generate(df_handle* H, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,
-                      int32_t n_new, int32_t* out_host, df_stats* stats) {
-  GUARD(H);
+static df_status generate_impl(df_handle* H, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,
+                               int32_t n_new, int32_t* out_host, df_stats* stats) {
   CKS(check_batch_args(H, prompts_host, lens_host, nseq, n_new, out_host));
   const df_stats before = H->stats;
   const int B = H->B;
@@ -1363,6 +1436,35 @@ df_status df_generate(df_handle* H, const int32_t* prompts_host, const int32_t* 
     *stats = d;
   }
   return DF_OK;
+}
+
+df_status df_generate(df_handle* H, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,
+                      int32_t n_new, int32_t* out_host, df_stats* stats) {
+  GUARD(H);
+  return generate_impl(H, prompts_host, lens_host, nseq, n_new, out_host, stats);
+}
+
+df_status df_generate_sampled(df_handle* H, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,
+                              int32_t n_new, float temperature, float top_p, uint64_t seed, int32_t* out_host,
+                              df_stats* stats) {
+  GUARD(H);
+  if (!sampling_args_ok(temperature, top_p))
+    return fail(H, DF_EINVAL, "temperature must be 0 or in [1e-3, 1e3] and top_p in [0, 1]");
+  CKS(check_batch_args(H, prompts_host, lens_host, nseq, n_new, out_host));
+  CKS(ensure_sampling_buffers(H));
+  // sequence i of the call draws from generator stream i, from its first uniform
+  std::vector<uint32_t> streams(nseq);
+  for (int i = 0; i < nseq; ++i) streams[i] = (uint32_t)i;
+  std::vector<unsigned long long> used(nseq, 0ull);
+  CK(h2d(H, H->d_ustream, streams.data(), (size_t)nseq * 4));
+  CK(h2d(H, H->d_ucount, used.data(), (size_t)nseq * 8));
+  H->sampling = true;
+  H->samp_inv_t = sampling_inv_t(temperature);
+  H->samp_top_p = top_p;
+  H->samp_seed = seed;
+  const df_status s = generate_impl(H, prompts_host, lens_host, nseq, n_new, out_host, stats);
+  H->sampling = false;
+  return s;
 }
 
 df_status df_greedy_reference(df_handle* H, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,

@@ -138,4 +138,41 @@ cudaError_t launch_greedy_step(const int* ids, int nseq, int t, int n_new, int* 
                                cudaStream_t st);
 cudaError_t launch_copy_row_f32(const float* src, int lds, float* dst, int ldd, int rows, int cols, cudaStream_t st);
 
+// ---- speculative sampling (sampling.cu)
+// A row's sampling distribution over its fp32 logits: token i is kept when
+// its logit's order key is above cut_key, or equal to it with i <= cut_idx;
+// a kept token's mass is exp((l_i - m) * inv_t) in units of 2^-44 (inv_t = 0:
+// greedy, the one kept token has mass 2^44); w_kept is the kept total.
+struct SampleRow {
+  float m;
+  float inv_t;
+  uint32_t cut_key;
+  int cut_idx;
+  unsigned long long w_kept;
+};
+constexpr int SAMPLE_MAX_VOCAB = 1 << 19;  // keeps a row's total mass below 2^63
+constexpr float SAMPLE_MIN_TEMPERATURE = 1e-3f, SAMPLE_MAX_TEMPERATURE = 1e3f;
+bool sampling_args_ok(float temperature, float top_p);  // temperature 0 or in [1e-3, 1e3]; top_p in [0, 1]
+float sampling_inv_t(float temperature);                // 0 for temperature 0
+// st[r] for rows r of logits (row stride ld floats): largest logit, total
+// mass and the nucleus for top_p < 1.  One 1024-thread block per row.
+cudaError_t launch_sample_state(const float* logits, long long ld, int rows, int V, float inv_t, float top_p,
+                                SampleRow* st, int* err, cudaStream_t s);
+// out[r] = inverse-CDF draw from row r with u[b * u_ld + i - skip], where
+// r = b * rows_per_seq + i; rows with i < skip are left alone.
+cudaError_t launch_sample_draw(const float* logits, long long ld, int rows, int V, const SampleRow* st, const float* u,
+                               int rows_per_seq, int u_ld, int skip, int* out, int* err, cudaStream_t s);
+// probs[r][i] = probability of token i in row r (tests and the single-op entry point).
+cudaError_t launch_sample_probs(const float* logits, long long ld, int rows, int V, const SampleRow* st, float* probs,
+                                long long ldp, cudaStream_t s);
+// u[b][j] = Philox uniform counts[slots[b]] + j of (seed, streams[slots[b]]), j < n; counts advance by n.
+cudaError_t launch_cycle_uniforms(const int* slots, int nseq, int n, unsigned long long seed, const uint32_t* streams,
+                                  unsigned long long* counts, float* u, int u_ld, cudaStream_t s);
+// The speculative-sampling test of nseq drafted blocks (one block of threads each).
+cudaError_t launch_accept_sampled(const int* slots, int nseq, int B, const int* drafts, int d_ld, const float* qlog,
+                                  long long ldq, const SampleRow* qst, int q_seq_rows, int q_row0, const float* plog,
+                                  long long ldp, const SampleRow* pst, int V, const float* u, int u_ld, int u0,
+                                  int* bonus, int* bonus_pos, int* acc_out, int* n_out, int* inj_pos, int* k_out,
+                                  int* tok_out, int* err, cudaStream_t s);
+
 }  // namespace dfk

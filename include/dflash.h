@@ -16,7 +16,9 @@
  *           (single forward pass, feature conditioning, lossless);
  *           实践 2 (block verification, keep up to the last correct token);
  *           实践 3 (the drafter never modifies the target's KV cache);
- *           实践 5 (pre-allocated activation pool, verification fused on the GPU).
+ *           实践 4 (temperature and top-p sampling, drafter and target aligned);
+ *           实践 5 (pre-allocated activation pool, verification fused on the GPU);
+ *           核心思想 step 3 (verification keeps the target's output distribution).
  *   [PRESS] DFlash press repost (zaocj.com): a single forward pass with
  *           bidirectional attention fills the 8-16 slots after the verified token.
  *
@@ -193,6 +195,32 @@ df_status df_verify_accept(df_handle* h, const int32_t* seqs_host, int32_t nseq,
 df_status df_generate(df_handle* h, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,
                       int32_t n_new, int32_t* out_host, df_stats* stats);
 
+/* df_generate with sampling instead of greedy decoding ([ABS] 实践 4; 核心思想
+ * step 3).  A token's sampling distribution is softmax(logits / temperature)
+ * over the fp32 logits of the shared LM head, restricted to the nucleus (the
+ * fewest most probable tokens whose mass reaches top_p; tokens of equal logit
+ * in index order) and renormalised; temperature 0 is the greedy argmax, and
+ * then the output equals df_generate's.  The drafter and the target use the
+ * same temperature and top_p.  Each cycle draws draft i from the drafter's
+ * distribution at slot i, keeps d_i while u_i * q_i(d_i) < p_i(d_i) (q the
+ * drafter's, p the target's distribution before d_i), and draws the token
+ * after the kept drafts from max(0, p - q) renormalised at the first
+ * rejection (from p where that is zero), or from the target's distribution
+ * after a fully kept block: the standard speculative-sampling test, under
+ * which the output follows the target's own sampling distribution.
+ * Masses are fixed-point integers (units of 2^-44 of the row's largest
+ * exp((l - max) / T)), so every draw is exact integer arithmetic and does
+ * not depend on the batch; masses below 2^-45 of the largest are zero.
+ * Uniforms: sequence i of the call uses Philox4x32-10 stream i of `seed`
+ * (df_op_philox_uniforms), one uniform for the first token after its prompt,
+ * then 2B - 1 per cycle (B - 1 draft draws, B - 1 tests, the final draw).
+ * temperature: 0, or in [1e-3, 1e3]; top_p in [0, 1] (1: no nucleus);
+ * vocab <= 2^19.  DF_EINVAL otherwise.  The first call allocates two fp32
+ * logit buffers of max_batch * B rows.  Other arguments as df_generate. */
+df_status df_generate_sampled(df_handle* h, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,
+                              int32_t n_new, float temperature, float top_p, uint64_t seed, int32_t* out_host,
+                              df_stats* stats);
+
 /* Plain token-by-token greedy decoding of the target on the GPU, with the
  * same kernels as verification: the lossless reference the speculative
  * output must equal bit for bit.  Same arguments as df_generate. */
@@ -319,6 +347,48 @@ df_status df_bench_drafter_step(df_handle* h, int32_t nseq, int32_t ctx_len, con
  * mean.  Same shape rules as df_op_gemm_bf16.  Synchronises `stream`. */
 df_status df_op_bench_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, int32_t M, int32_t N, int32_t K,
                                 int32_t splits, int32_t token_tile, int32_t iters, void* stream, float* us_per_launch);
+
+/* ---- speculative sampling, one operation at a time ----------------------
+ * The pieces of df_generate_sampled on caller-owned device buffers, for
+ * tests and for callers with their own loop.  Logit rows are fp32 [rows][V]
+ * (row stride V), V in [1, 2^19]; temperature and top_p as in
+ * df_generate_sampled.  err_dev (may be NULL): a device int that receives
+ * the sticky error bits of the kernels (2: a draw or a nucleus search found
+ * no token, which only invalid input can cause).  Each call is stream-ordered
+ * on `stream`, allocates its scratch on that stream and does not synchronise. */
+
+/* The Philox4x32-10 block function on the host (Salmon, Moraes, Dror and
+ * Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011), from the same
+ * source as the device generator: out = philox(counter ctr, key). */
+df_status df_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+
+/* u_dev[j] = uniform offset + j of (seed, stream_id), j < n: word
+ * (offset + j) mod 4 of the Philox4x32-10 block for counter ((offset + j) / 4
+ * as two 32-bit words, stream_id, 0) and key (seed as two 32-bit words),
+ * taken as (word >> 8) * 2^-24. */
+df_status df_op_philox_uniforms(uint64_t seed, uint32_t stream_id, uint64_t offset, int32_t n, float* u_dev,
+                                void* stream);
+
+/* probs_dev[r][v] = probability of token v in row r's sampling distribution
+ * (the kept fixed-point mass over the row's kept total, rounded to fp32). */
+df_status df_op_sampling_probs(const float* logits_dev, int32_t rows, int32_t V, float temperature, float top_p,
+                               float* probs_dev, int32_t* err_dev, void* stream);
+
+/* idx_dev[r] = the lowest index j whose cumulative mass in row r exceeds
+ * u_dev[r] x (row r's total mass): an inverse-CDF draw; u in [0, 1). */
+df_status df_op_sample_draw(const float* logits_dev, int32_t rows, int32_t V, float temperature, float top_p,
+                            const float* u_dev, int32_t* idx_dev, int32_t* err_dev, void* stream);
+
+/* The speculative-sampling test of nseq drafted blocks of B slots (2 <= B
+ * <= 32).  drafts_dev [nseq][B-1]: d_1..d_{B-1}; q_logits_dev [nseq][B-1][V]:
+ * the drafter's logits at slots 1..B-1; p_logits_dev [nseq][B][V]: the
+ * target's logits at slots 0..B-1 (row j predicts the token after slot j);
+ * u_dev [nseq][B]: B-1 test uniforms then the final draw's.  k_dev[b] = kept
+ * drafts, tok_dev[b] = the token after them (see df_generate_sampled). */
+df_status df_op_accept_sampled(const int32_t* drafts_dev, const float* q_logits_dev, const float* p_logits_dev,
+                               int32_t nseq, int32_t B, int32_t V, float temperature, float top_p,
+                               const float* u_dev, int32_t* k_dev, int32_t* tok_dev, int32_t* err_dev,
+                               void* stream);
 
 #ifdef __cplusplus
 }

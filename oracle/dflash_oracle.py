@@ -548,6 +548,57 @@ def accept_sampled(drafts: Sequence[int], q_rows: np.ndarray, p_rows: np.ndarray
     return k, draw(p_rows[k], u_final)
 
 
+def draw_margin(probs: np.ndarray, u: float) -> float:
+    """How far u x total lies from the ends of the interval that decides
+    draw(probs, u), as a fraction of the total mass (0 on a boundary).  A
+    draw from masses that differ by less than this picks the same index."""
+    c = np.cumsum(np.asarray(probs, dtype=np.float64))
+    total = c[-1]
+    j = draw(probs, u)
+    lo = c[j - 1] if j > 0 else 0.0
+    t = u * total
+    return float(min(t - lo, c[j] - t) / total)
+
+
+def nucleus_margin(logits: np.ndarray, temperature: float, top_p: float) -> float:
+    """Smallest distance, over the rows, between top_p and the cumulative
+    masses on either side of the row's nucleus cut (inf without a cut)."""
+    if temperature == 0.0 or top_p >= 1.0:
+        return math.inf
+    probs = sampling_probs(logits, temperature, 1.0)
+    out = math.inf
+    for r in range(probs.shape[0]):
+        order = np.lexsort((np.arange(probs.shape[1]), -probs[r]))
+        csum = np.cumsum(probs[r, order])
+        j = min(int(np.searchsorted(csum, top_p)), len(csum) - 1)
+        out = min(out, abs(csum[j] - top_p))
+        if j > 0:
+            out = min(out, abs(top_p - csum[j - 1]))
+    return float(out)
+
+
+def accept_margin(drafts: Sequence[int], q_rows: np.ndarray, p_rows: np.ndarray,
+                  u_accept: Sequence[float], u_final: float) -> float:
+    """Smallest distance from a tie of the decisions accept_sampled takes on
+    these inputs: |u_i - p/q| of each test it makes, then its final draw's
+    draw_margin."""
+    m = math.inf
+    k = 0
+    while k < len(drafts):
+        d = int(drafts[k])
+        pk, qk = p_rows[k][d], q_rows[k][d]
+        if qk > 0.0:
+            m = min(m, abs(u_accept[k] - pk / qk))
+            if u_accept[k] < pk / qk:
+                k += 1
+                continue
+        residual = np.maximum(p_rows[k] - q_rows[k], 0.0)
+        if residual.sum() <= 0.0:
+            residual = p_rows[k]
+        return min(m, draw_margin(residual, u_final))
+    return min(m, draw_margin(p_rows[k], u_final))
+
+
 Uniforms = Callable[[int], np.ndarray]
 
 
@@ -568,7 +619,7 @@ def sample_generate(m: Model, prompt: Sequence[int], n_new: int, temperature: fl
 
 
 def spec_generate_sampled(m: Model, prompt: Sequence[int], n_new: int, temperature: float, top_p: float,
-                          uniforms: Uniforms) -> SpecResult:
+                          uniforms: Uniforms, margins: Optional[List[float]] = None) -> SpecResult:
     """DFlash speculative decoding with sampling, one sequence.
 
     The cycle of ``spec_generate``, with each slot's draft drawn from the
@@ -576,14 +627,20 @@ def spec_generate_sampled(m: Model, prompt: Sequence[int], n_new: int, temperatu
     target) and ``accept_sampled`` in place of the greedy prefix test.  The
     bonus token after the prompt is drawn from the target's distribution.
     Uniforms per cycle: B-1 for the drafts, B-1 for the tests, 1 for the
-    final draw.  At temperature 0 this is exactly ``spec_generate``."""
+    final draw.  At temperature 0 this is exactly ``spec_generate``.
+    margins (optional) receives, in order, each decision's distance from a
+    tie (nucleus cuts, draws, tests), for comparisons with other arithmetic."""
     cfg = m.cfg
     W = m.W
     B = cfg.block_size
     cache = KVCache(cfg.n_layers, cfg.n_kv_heads, cfg.head_dim)
     ctxc = ContextCache(cfg.draft_layers, cfg.n_kv_heads, cfg.head_dim)
     tp = target_forward(W, cfg, prompt, cache)
-    bonus = draw(sampling_probs(tp.logits[-1:], temperature, top_p)[0], float(uniforms(1)[0]))
+    p0 = sampling_probs(tp.logits[-1:], temperature, top_p)[0]
+    u0 = float(uniforms(1)[0])
+    bonus = draw(p0, u0)
+    if margins is not None:
+        margins += [nucleus_margin(tp.logits[-1:], temperature, top_p), draw_margin(p0, u0)]
     inject_kv(W, cfg, ctxc, fuse_features(W, cfg, tp.taps))
     pos = len(prompt)
     out = [bonus]
@@ -596,6 +653,11 @@ def spec_generate_sampled(m: Model, prompt: Sequence[int], n_new: int, temperatu
         vp = target_forward(W, cfg, [bonus] + [int(t) for t in drafts], cache)
         p_rows = sampling_probs(vp.logits, temperature, top_p)
         k, new_bonus = accept_sampled(drafts, q_rows, p_rows, u[B - 1: 2 * (B - 1)], float(u[-1]))
+        if margins is not None:
+            margins.append(nucleus_margin(dp.logits[1:B], temperature, top_p))
+            margins += [draw_margin(q_rows[i], float(u[i])) for i in range(B - 1)]
+            margins.append(nucleus_margin(vp.logits, temperature, top_p))
+            margins.append(accept_margin(drafts, q_rows, p_rows, u[B - 1: 2 * (B - 1)], float(u[-1])))
         cycles.append(Cycle(pos, bonus, drafts, argmax_lowest(vp.logits), k, vp.taps, vp.logits))
         cache.truncate(pos + k + 1)
         inject_kv(W, cfg, ctxc, fuse_features(W, cfg, vp.taps[: k + 1]))

@@ -88,3 +88,24 @@ def test_parameter_counts_match_pages_sizing():
     s = syn.DENSE_27B
     n = sum(int(np.prod(shp)) for name, shp in syn.weight_specs(s) if name.startswith("d") or name.startswith("fc"))
     assert 1.7e9 < n < 2.0e9
+
+
+def test_sampling_calls_reject_bad_arguments_without_gpu(L):
+    # every check below returns before anything is launched
+    import block_diffusion_speculative_layer_gb300 as dfl
+    n = None
+    assert L.df_op_sampling_probs(n, 1, 10, -1.0, 1.0, n, n, n) == dfl.DF_EINVAL           # negative temperature
+    assert L.df_op_sampling_probs(n, 1, 10, 1e-4, 1.0, n, n, n) == dfl.DF_EINVAL           # below 1e-3
+    assert L.df_op_sampling_probs(n, 1, 10, float("nan"), 1.0, n, n, n) == dfl.DF_EINVAL
+    assert L.df_op_sampling_probs(n, 1, 10, 1.0, 1.5, n, n, n) == dfl.DF_EINVAL            # top_p above 1
+    assert L.df_op_sampling_probs(n, 1, 10, 1.0, -0.1, n, n, n) == dfl.DF_EINVAL
+    assert L.df_op_sampling_probs(n, 1, (1 << 19) + 1, 1.0, 1.0, n, n, n) == dfl.DF_EINVAL  # vocabulary too large
+    assert L.df_op_sampling_probs(n, 1, 10, 1.0, 0.9, n, n, n) == dfl.DF_EINVAL            # missing buffers
+    assert L.df_op_sampling_probs(n, 0, 10, 1.0, 0.9, n, n, n) == dfl.DF_OK                # no rows: nothing to do
+    assert L.df_op_sample_draw(n, 1, 10, 0.0, 1.0, n, n, n, n) == dfl.DF_EINVAL
+    assert L.df_op_accept_sampled(n, n, n, 1, 1, 10, 1.0, 1.0, n, n, n, n, n) == dfl.DF_EINVAL   # B < 2
+    assert L.df_op_accept_sampled(n, n, n, 1, 33, 10, 1.0, 1.0, n, n, n, n, n) == dfl.DF_EINVAL  # B > 32
+    assert L.df_op_accept_sampled(n, n, n, 0, 4, 10, 1.0, 1.0, n, n, n, n, n) == dfl.DF_OK
+    assert L.df_op_philox_uniforms(0, 0, 0, -1, n, n) == dfl.DF_EINVAL
+    assert L.df_op_philox_uniforms(0, 0, 0, 0, n, n) == dfl.DF_OK
+    assert L.df_generate_sampled(n, n, n, 1, 1, 1.0, 1.0, 0, n, n) == dfl.DF_EINVAL        # null handle

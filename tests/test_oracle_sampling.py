@@ -145,3 +145,56 @@ def test_sampling_loop_at_temperature_zero_is_greedy_speculation():
     np.testing.assert_array_equal(got.tokens, ref.tokens)
     np.testing.assert_array_equal(got.tokens, O.greedy_generate(m, prompt, 20))
     assert got.accepted == ref.accepted
+
+
+def test_draw_margin_is_the_distance_to_the_deciding_interval():
+    assert O.draw_margin([0.2, 0.3, 0.5], 0.25) == pytest.approx(0.05)
+    assert O.draw_margin([0.2, 0.3, 0.5], 0.1) == pytest.approx(0.1)
+    assert O.draw_margin([0.2, 0.3, 0.5], 0.0) == 0.0          # on the lower end
+    assert O.draw_margin([0.2, 0.3, 0.5], 0.5) == 0.0          # on a boundary
+    assert O.draw_margin([2.0, 6.0], 0.5) == pytest.approx(0.25)   # unnormalised: fraction of the total
+
+
+def test_margins_bound_the_effect_of_perturbed_masses():
+    # a draw or a test whose margin exceeds the perturbation keeps its result
+    rng = np.random.default_rng(8)
+    kept = 0
+    for _ in range(400):
+        V, B = 6, 4
+        q = rng.dirichlet(np.ones(V), size=B - 1)
+        p = rng.dirichlet(np.ones(V), size=B)
+        drafts = [O.draw(q[i], rng.random()) for i in range(B - 1)]
+        ua, uf = rng.random(B - 1), float(rng.random())
+        m = O.accept_margin(drafts, q, p, ua, uf)
+        eps = 1e-3
+        if m <= 20 * eps:
+            continue
+        kept += 1
+        q2 = q * (1 + eps * rng.uniform(-1, 1, q.shape))
+        p2 = p * (1 + eps * rng.uniform(-1, 1, p.shape))
+        q2 /= q2.sum(axis=1, keepdims=True)
+        p2 /= p2.sum(axis=1, keepdims=True)
+        assert O.accept_sampled(drafts, q2, p2, ua, uf) == O.accept_sampled(drafts, q, p, ua, uf)
+        u = float(rng.random())
+        if O.draw_margin(p[0], u) > 20 * eps:
+            assert O.draw(p2[0], u) == O.draw(p[0], u)
+    assert kept > 200
+
+
+def test_accept_margin_examples():
+    q = np.array([[0.5, 0.5]])
+    p = np.array([[0.25, 0.75], [1.0, 0.0]])
+    # kept (0.4 < p/q = 0.5, margin 0.1), then the final draw from [1, 0] at 0.1 (margin 0.1)
+    assert O.accept_sampled([0], q, p, [0.4], 0.1) == (1, 0)
+    assert O.accept_margin([0], q, p, [0.4], 0.1) == pytest.approx(0.1)
+    # rejected (0.55 > 0.5, margin 0.05); residual [0, 0.25] drawn at 0.1 (margin 0.1)
+    assert O.accept_sampled([0], q, p, [0.55], 0.1) == (0, 1)
+    assert O.accept_margin([0], q, p, [0.55], 0.1) == pytest.approx(0.05)
+
+
+def test_nucleus_margin_examples():
+    lg = np.log([[0.5, 0.3, 0.15, 0.05]])
+    assert O.nucleus_margin(lg, 1.0, 0.7) == pytest.approx(0.1)     # cut after 0.8; 0.5 is 0.2 below
+    assert O.nucleus_margin(lg, 1.0, 0.79) == pytest.approx(0.01)
+    assert O.nucleus_margin(lg, 1.0, 1.0) == np.inf
+    assert O.nucleus_margin(lg, 0.0, 0.5) == np.inf

@@ -1,16 +1,27 @@
 """The counter-based generator of the synthetic inputs: Philox4x32-10 against
-the known-answer vectors published with it, and the uniforms built on it."""
+the known-answer vectors published with it, and the uniforms built on it;
+the library's own Philox (its device generator's source, run on the host)
+against the same vectors."""
+import os
+
 import numpy as np
 
 import synthetic as syn
 
-# (counter, key) -> output, the published known-answer tests of philox4x32 with 10 rounds
-KAT = [
-    ([0, 0, 0, 0], [0, 0], [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]),
-    ([0xFFFFFFFF] * 4, [0xFFFFFFFF] * 2, [0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD]),
-    ([0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344], [0xA4093822, 0x299F31D0],
-     [0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1]),
-]
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "philox4x32_10_kat.txt")
+
+
+def kat_vectors():
+    """(counter, key, output) triples of the published known-answer tests."""
+    out = []
+    for line in open(GOLDEN):
+        if line.strip() and not line.startswith("#"):
+            w = [int(x, 16) for x in line.split()]
+            out.append((w[0:4], w[4:6], w[6:10]))
+    return out
+
+
+KAT = kat_vectors()
 
 
 def test_philox_known_answers():
@@ -31,3 +42,19 @@ def test_uniforms_layout_and_range():
     # streams and seeds differ
     assert not np.array_equal(syn.philox_uniforms(7, 4, 0, 16), u[:16])
     assert not np.array_equal(syn.philox_uniforms(8, 3, 0, 16), u[:16])
+
+
+def test_library_philox_known_answers():
+    # the CUDA library implements the generator separately from the inputs
+    # module; its block function runs on the host through the C ABI
+    import __graft_entry__ as g
+    g.build()
+    import block_diffusion_speculative_layer_gb300 as dfl
+    assert len(KAT) == 3
+    for ctr, key, want in KAT:
+        assert dfl.philox4x32_10(ctr, key) == want
+    rng = np.random.default_rng(0)
+    for _ in range(50):
+        ctr = [int(x) for x in rng.integers(0, 2 ** 32, 4)]
+        key = [int(x) for x in rng.integers(0, 2 ** 32, 2)]
+        assert dfl.philox4x32_10(ctr, key) == syn.philox4x32(ctr, key)
