@@ -27,7 +27,7 @@ EXPORTED = [
     "df_op_gemm_bf16", "df_op_lmhead_argmax_bf16", "df_profile_enable", "df_profile_read",
     "df_op_bench_gemm_bf16", "df_op_gemm_bf16_noalloc", "df_bench_drafter_step",
     "df_generate_sampled", "df_philox4x32_10", "df_op_philox_uniforms", "df_op_sampling_probs",
-    "df_op_sample_draw", "df_op_accept_sampled",
+    "df_op_sample_draw", "df_op_accept_sampled", "df_set_block_range", "df_block_size_for",
 ]
 
 
@@ -53,7 +53,7 @@ class DfStats(ctypes.Structure):
         ("cycles", ctypes.c_int64), ("accepted_drafts", ctypes.c_int64), ("emitted_tokens", ctypes.c_int64),
         ("accept_hist", ctypes.c_int64 * 65), ("draft_us", ctypes.c_double), ("verify_us", ctypes.c_double),
         ("prefill_us", ctypes.c_double), ("kernel_launches", ctypes.c_int64),
-        ("h2d_bytes", ctypes.c_int64), ("d2h_bytes", ctypes.c_int64),
+        ("h2d_bytes", ctypes.c_int64), ("d2h_bytes", ctypes.c_int64), ("block_hist", ctypes.c_int64 * 33),
     ]
 
     def as_dict(self) -> dict:
@@ -61,7 +61,7 @@ class DfStats(ctypes.Structure):
             "cycles": self.cycles, "accepted_drafts": self.accepted_drafts, "emitted_tokens": self.emitted_tokens,
             "accept_hist": list(self.accept_hist), "draft_us": self.draft_us, "verify_us": self.verify_us,
             "prefill_us": self.prefill_us, "kernel_launches": self.kernel_launches,
-            "h2d_bytes": self.h2d_bytes, "d2h_bytes": self.d2h_bytes,
+            "h2d_bytes": self.h2d_bytes, "d2h_bytes": self.d2h_bytes, "block_hist": list(self.block_hist),
         }
 
 
@@ -123,6 +123,9 @@ def lib() -> ctypes.CDLL:
     L.df_op_sampling_probs.argtypes = [_P, _I, _I, _F, _F, _P, _P, _P]
     L.df_op_sample_draw.argtypes = [_P, _I, _I, _F, _F, _P, _P, _P, _P]
     L.df_op_accept_sampled.argtypes = [_P, _P, _P, _I, _I, _I, _F, _F, _P, _P, _P, _P, _P]
+    L.df_set_block_range.argtypes = [_P, _I, _I]
+    L.df_block_size_for.argtypes = [ctypes.c_double, _I, _I]
+    L.df_block_size_for.restype = _I
     for name in EXPORTED:
         fn = getattr(L, name)
         if fn.restype is ctypes.c_int:  # default restype: the df_status enum
@@ -290,6 +293,11 @@ class Engine:
                                                float(top_p), int(seed), _ip(out), ctypes.byref(stats)),
                     "df_generate_sampled")
         return out, stats.as_dict()
+
+    def set_block_range(self, b_min: int, b_max: int):
+        """Block sizes df_generate may use: fixed when equal, else chosen per
+        group of cycles from the tokens per cycle seen so far."""
+        self._check(self.L.df_set_block_range(self.h, int(b_min), int(b_max)), "df_set_block_range")
 
     def greedy_reference(self, prompts: Sequence[Sequence[int]], n_new: int) -> np.ndarray:
         lens = _i32([len(p) for p in prompts])
@@ -492,3 +500,11 @@ def accept_sampled(drafts, q_logits, p_logits, temperature: float, top_p: float,
         raise DfError(st, "df_op_accept_sampled")
     _check_err(err, "df_op_accept_sampled")
     return k, tok
+
+
+def block_size_for(tokens_per_cycle: float, b_min: int, b_max: int) -> int:
+    """The engine's block-size rule (df_block_size_for)."""
+    b = lib().df_block_size_for(float(tokens_per_cycle), int(b_min), int(b_max))
+    if b < 0:
+        raise DfError(DF_EINVAL, "df_block_size_for: bad arguments")
+    return b

@@ -29,6 +29,7 @@ constexpr int ATTN_CHUNK = 64;
 constexpr int PREFILL_CHUNK = 512;
 
 constexpr int KMAX_CYCLES = 8;  // most draft+verify cycles in one captured graph
+constexpr size_t MAX_GRAPHS = 8;  // captured cycle graphs kept per handle
 
 struct Tmap {
   alignas(64) uint8_t b[TMAP_BYTES];
@@ -114,9 +115,14 @@ struct df_handle {
   // graph replay of the decode cycle (df_generate)
   bool use_graphs = true;
   int graph_ready_cycles = 0;        // eager cycles run by this handle (the first sets kernel attributes)
-  cudaGraphExec_t gexec = nullptr;
-  std::vector<int> gkey;             // slots + chunk counts the graph was captured for
-  int64_t g_launches = 0, g_h2d = 0, g_d2h = 0;
+  struct GraphRec {
+    cudaGraphExec_t exec = nullptr;
+    int64_t launches = 0, h2d = 0, d2h = 0;  // counted again at each replay
+  };
+  std::map<std::vector<int>, GraphRec> graphs;  // by slots, cycle count, block size (and sampling arguments)
+  std::vector<int> glast;                       // key of the graph whose slots d_gslots holds
+  // block size per cycle group (df_set_block_range): fixed at B unless blk_min < blk_max
+  int blk_min = 0, blk_max = 0;
   int* d_gslots = nullptr;
   cudaStream_t gstream = nullptr;    // capture/replay stream, joined to the caller's stream by events
   cudaEvent_t gjoin[2] = {nullptr, nullptr};
@@ -567,8 +573,9 @@ df_status fuse_inject(df_handle* H, int M, const int* row_pos) {
   return DF_OK;
 }
 
-df_status drafter_pass(df_handle* H, int nseq, int max_ctx_len) {
-  const int B = H->B, M = nseq * B;
+// Drafter over blocks of b slots (b = 0: the configured block size B).
+df_status drafter_pass(df_handle* H, int nseq, int max_ctx_len, int b = 0) {
+  const int B = b > 0 ? b : H->B, M = nseq * B;
   { ProfScope ps_(H, PC_EMBED, 1); CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, H->xraw, H->ss, M, H->d, H->V, H->d_err, H->st)); }
   for (int l = 0; l < H->Ld; ++l) CKS(layer_pass(H, H->dl[l], M, B, nseq, false, l, max_ctx_len, -1));
   if (H->debug) CK(cudaMemcpyAsync(H->dbg_dh, H->h, (size_t)M * H->d * 4, cudaMemcpyDeviceToDevice, H->st));
@@ -758,6 +765,7 @@ df_status verify_impl(df_handle* H, const int32_t* slots, int nseq, const int32_
     H->stats.cycles += 1;
     H->stats.accepted_drafts += k;
     H->stats.accept_hist[std::min(k, 64)] += 1;
+    H->stats.block_hist[B] += 1;
   }
   if (timed) {
     float a = 0.f, b = 0.f;
@@ -774,12 +782,13 @@ df_status verify_impl(df_handle* H, const int32_t* slots, int nseq, const int32_
 // fusion and injection, then the accepted tokens and counts copied to h_pin.
 // ext_events: record the timing events as graph-visible event nodes.
 // Cycle c of a run of cycles: its events are cev[4c..4c+3] and its accepted
-// tokens and counts go to h_pin at cycle_pin(c).
+// tokens ([nseq][b]) and counts ([nseq], at nseq * B) go to h_pin at
+// cycle_pin(c).  b is the cycle's block size (<= B).
 size_t cycle_pin(const df_handle* H, int nseq, int c) { return (size_t)c * nseq * (H->B + 1); }
 
 df_status cycle_work(df_handle* H, const int* d_slots_dev, int nseq, int max_len_d, int max_len_t, bool ext_events,
-                     int c) {
-  const int B = H->B;
+                     int c, int b) {
+  const int B = b;
   cudaEvent_t* ev = H->cev + 4 * c;
   auto rec = [&](cudaEvent_t e) {
     return ext_events ? cudaEventRecordWithFlags(e, H->st, cudaEventRecordExternal) : cudaEventRecord(e, H->st);
@@ -791,7 +800,7 @@ df_status cycle_work(df_handle* H, const int* d_slots_dev, int nseq, int max_len
     ProfScope ps_(H, PC_CTRL, 1);
     CK(launch_cycle_uniforms(d_slots_dev, nseq, 2 * B - 1, H->samp_seed, H->d_ustream, H->d_ucount, H->d_u, 2 * B, H->st));
   }
-  CKS(drafter_pass(H, nseq, max_len_d));
+  CKS(drafter_pass(H, nseq, max_len_d, B));
   if (H->sampling) {
     // draft i (slot i = 1..B-1) drawn from the drafter's distribution at slot i
     ProfScope ps_(H, PC_CTRL, 1);
@@ -816,16 +825,18 @@ df_status cycle_work(df_handle* H, const int* d_slots_dev, int nseq, int max_len
   CK(rec(ev[3]));
   int* pin = H->h_pin + cycle_pin(H, nseq, c);
   CK(d2h(H, pin, H->d_acc, (size_t)nseq * B * 4));
-  CK(d2h(H, pin + (size_t)nseq * B, H->d_n, (size_t)nseq * 4));
+  CK(d2h(H, pin + (size_t)nseq * H->B, H->d_n, (size_t)nseq * 4));
   return DF_OK;
 }
 
-// Host bookkeeping after cycle c's results reached h_pin: lengths, bonus
-// tokens, stats; acc_host/n_host (optional) receive this cycle's rows.
-df_status cycle_finish(df_handle* H, const int32_t* slots, int nseq, int c, int32_t* acc_host, int32_t* n_host) {
-  const int B = H->B;
+// Host bookkeeping after cycle c (block size b) reached h_pin: lengths,
+// bonus tokens, stats; acc_host ([nseq][B], first b of each row written) and
+// n_host (optional) receive this cycle's rows.
+df_status cycle_finish(df_handle* H, const int32_t* slots, int nseq, int c, int b, int32_t* acc_host,
+                       int32_t* n_host) {
+  const int B = b;
   const int* acc = H->h_pin + cycle_pin(H, nseq, c);
-  const int* n = acc + (size_t)nseq * B;
+  const int* n = acc + (size_t)nseq * H->B;
   for (int i = 0; i < nseq; ++i) {
     SeqHost& s = H->seqs[slots[i]];
     const int k = n[i] - 1;
@@ -835,12 +846,14 @@ df_status cycle_finish(df_handle* H, const int32_t* slots, int nseq, int c, int3
     H->stats.cycles += 1;
     H->stats.accepted_drafts += k;
     H->stats.accept_hist[std::min(k, 64)] += 1;
+    H->stats.block_hist[B] += 1;
   }
   const cudaEvent_t* ev = H->cev + 4 * c;
-  float a = 0.f, b = 0.f;
-  if (cudaEventElapsedTime(&a, ev[0], ev[1]) == cudaSuccess) H->stats.draft_us += 1000.0 * a;
-  if (cudaEventElapsedTime(&b, ev[2], ev[3]) == cudaSuccess) H->stats.verify_us += 1000.0 * b;
-  if (acc_host) std::memcpy(acc_host, acc, (size_t)nseq * B * 4);
+  float ta = 0.f, tb = 0.f;
+  if (cudaEventElapsedTime(&ta, ev[0], ev[1]) == cudaSuccess) H->stats.draft_us += 1000.0 * ta;
+  if (cudaEventElapsedTime(&tb, ev[2], ev[3]) == cudaSuccess) H->stats.verify_us += 1000.0 * tb;
+  if (acc_host)
+    for (int i = 0; i < nseq; ++i) std::memcpy(acc_host + (size_t)i * H->B, acc + (size_t)i * B, (size_t)B * 4);
   if (n_host) std::memcpy(n_host, n, (size_t)nseq * 4);
   return DF_OK;
 }
@@ -851,10 +864,21 @@ df_status trim_all(df_handle* H, const int32_t* slots, int nseq) {
   return DF_OK;
 }
 
+// Block size for the next group of cycles: the smallest power of two that is
+// at least twice the recent tokens per cycle, within [b_min, b_max] (b_max
+// itself where the power of two would pass it).  A block twice the accepted
+// length leaves room to grow: a group that keeps every draft doubles it.
+int block_size_for(double tokens_per_cycle, int b_min, int b_max) {
+  int b = 2;
+  while (b < b_max && (double)b < 2.0 * tokens_per_cycle) b *= 2;
+  return std::max(b_min, std::min(b, b_max));
+}
+
 void drop_graph(df_handle* H) {
-  if (H->gexec) cudaGraphExecDestroy(H->gexec);
-  H->gexec = nullptr;
-  H->gkey.clear();
+  for (auto& g : H->graphs)
+    if (g.second.exec) cudaGraphExecDestroy(g.second.exec);
+  H->graphs.clear();
+  H->glast.clear();
 }
 
 // K draft + verify cycles for df_generate (acc_host [K][nseq][B], n_host
@@ -863,11 +887,13 @@ void drop_graph(df_handle* H) {
 // into a CUDA graph and replayed: the cycles chain on the device (positions,
 // bonus tokens and rollback live in device memory) and the host reads all K
 // results after one synchronisation.  The graph's attention launches are
-// sized for max_ctx, so a new capture is made only when the slots or K change.
-df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int32_t* acc_host, int32_t* n_host) {
+// sized for max_ctx, so a new capture is made only for new slots, K or block
+// size b; a few captured graphs are kept.
+df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int b, int32_t* acc_host, int32_t* n_host) {
   CKS(check_slots(H, slots, nseq));
   const int B = H->B;
   if (K < 1 || K > KMAX_CYCLES) return fail(H, DF_EINVAL, "bad cycle count");
+  if (b < 2 || b > B) return fail(H, DF_EINVAL, "bad block size");
   for (int i = 0; i < nseq; ++i) {
     SeqHost& s = H->seqs[slots[i]];
     if (s.len + K * B > H->cfg.max_ctx) return fail(H, DF_EINVAL, "sequence would exceed max_ctx");
@@ -881,19 +907,20 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int32_
       int max_t = 0, max_d = 0;
       for (int i = 0; i < nseq; ++i) {
         const SeqHost& s = H->seqs[slots[i]];
-        max_t = std::max(max_t, s.len + B);
+        max_t = std::max(max_t, s.len + b);
         max_d = std::max(max_d, s.len);
       }
       CK(h2d(H, H->d_slots, slots, nseq * 4));
-      CKS(cycle_work(H, H->d_slots, nseq, max_d, max_t, false, 0));
+      CKS(cycle_work(H, H->d_slots, nseq, max_d, max_t, false, 0, b));
       CKS(sync(H));
       H->graph_ready_cycles += 1;
-      CKS(cycle_finish(H, slots, nseq, 0, out_acc(c), out_n(c)));
+      CKS(cycle_finish(H, slots, nseq, 0, b, out_acc(c), out_n(c)));
     }
     return trim_all(H, slots, nseq);
   }
   std::vector<int> key(slots, slots + nseq);
   key.push_back(K);
+  key.push_back(b);
   if (H->sampling) {
     // the sampling parameters are launch arguments of the captured kernels
     int tb = 0, pb = 0;
@@ -908,9 +935,11 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int32_
   const cudaStream_t user = H->st;
   CK(cudaEventRecord(H->gjoin[0], user));
   CK(cudaStreamWaitEvent(H->gstream, H->gjoin[0], 0));
-  if (!H->gexec || key != H->gkey) {
-    drop_graph(H);
+  auto it = H->graphs.find(key);
+  if (it == H->graphs.end()) {
+    if (H->graphs.size() >= MAX_GRAPHS) drop_graph(H);
     CK(h2d(H, H->d_gslots, slots, nseq * 4));
+    H->glast = key;
     CK(cudaStreamSynchronize(user));
     const df_stats before = H->stats;
     bool ok = cudaStreamBeginCapture(H->gstream, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
@@ -918,34 +947,41 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int32_
     cudaGraph_t g = nullptr;
     if (ok) {
       H->st = H->gstream;
-      for (int c = 0; c < K && st == DF_OK; ++c) st = cycle_work(H, H->d_gslots, nseq, max_len, max_len, true, c);
+      for (int c = 0; c < K && st == DF_OK; ++c) st = cycle_work(H, H->d_gslots, nseq, max_len, max_len, true, c, b);
       H->st = user;
       ok = cudaStreamEndCapture(H->gstream, &g) == cudaSuccess && st == DF_OK;
     }
     H->st = user;
-    if (ok) ok = cudaGraphInstantiate(&H->gexec, g, 0) == cudaSuccess;
+    df_handle::GraphRec rec;
+    if (ok) ok = cudaGraphInstantiate(&rec.exec, g, 0) == cudaSuccess;
     if (g) cudaGraphDestroy(g);
-    H->g_launches = H->stats.kernel_launches - before.kernel_launches;
-    H->g_h2d = H->stats.h2d_bytes - before.h2d_bytes;
-    H->g_d2h = H->stats.d2h_bytes - before.d2h_bytes;
+    rec.launches = H->stats.kernel_launches - before.kernel_launches;
+    rec.h2d = H->stats.h2d_bytes - before.h2d_bytes;
+    rec.d2h = H->stats.d2h_bytes - before.d2h_bytes;
     H->stats = before;  // counted again at each replay
     if (!ok) {
       // capture is not available here: run this handle's cycles eagerly
       (void)cudaGetLastError();
-      H->gexec = nullptr;
+      drop_graph(H);
       H->use_graphs = false;
-      return cycle_impl(H, slots, nseq, K, acc_host, n_host);
+      return cycle_impl(H, slots, nseq, K, b, acc_host, n_host);
     }
-    H->gkey = key;
+    it = H->graphs.emplace(key, rec).first;
+  } else if (H->glast != key) {
+    // the graphs read their slots from d_gslots: put this graph's there
+    CK(h2d(H, H->d_gslots, slots, nseq * 4));
+    CK(cudaEventRecord(H->gjoin[0], user));
+    CK(cudaStreamWaitEvent(H->gstream, H->gjoin[0], 0));
+    H->glast = key;
   }
-  CK(cudaGraphLaunch(H->gexec, H->gstream));
+  CK(cudaGraphLaunch(it->second.exec, H->gstream));
   CK(cudaEventRecord(H->gjoin[1], H->gstream));
   CK(cudaStreamWaitEvent(H->st, H->gjoin[1], 0));
-  H->stats.kernel_launches += H->g_launches;
-  H->stats.h2d_bytes += H->g_h2d;
-  H->stats.d2h_bytes += H->g_d2h;
+  H->stats.kernel_launches += it->second.launches;
+  H->stats.h2d_bytes += it->second.h2d;
+  H->stats.d2h_bytes += it->second.d2h;
   CKS(sync(H));
-  for (int c = 0; c < K; ++c) CKS(cycle_finish(H, slots, nseq, c, out_acc(c), out_n(c)));
+  for (int c = 0; c < K; ++c) CKS(cycle_finish(H, slots, nseq, c, b, out_acc(c), out_n(c)));
   return trim_all(H, slots, nseq);
 }
 
@@ -1290,6 +1326,7 @@ df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_we
   H->L = cfg->n_layers;
   H->Ld = cfg->draft_layers;
   H->B = cfg->block_size;
+  H->blk_min = H->blk_max = H->B;
   H->qdim = H->Hq * H->hd;
   H->kvdim = H->Hkv * H->hd;
   H->qkv_n = H->qdim + 2 * H->kvdim;
@@ -1388,6 +1425,12 @@ static df_status generate_impl(df_handle* H, const int32_t* prompts_host, const 
   }
   std::vector<int> active, acc((size_t)KMAX_CYCLES * nseq * B), n((size_t)KMAX_CYCLES * nseq);
   long long cyc = 0, emitted = 0;  // sequence-cycles run and tokens they emitted, for the choice of K
+  // block size: fixed, or chosen per group from the recent tokens per cycle
+  // (an average over groups, each weighted half as much as the next)
+  const bool adaptive = H->blk_min < H->blk_max;
+  int b = H->blk_max;
+  double tau = 0.0;
+  bool have_tau = false;
   while (s == DF_OK) {
     active.clear();
     int remaining = n_new, room = KMAX_CYCLES;
@@ -1405,17 +1448,26 @@ static df_status generate_impl(df_handle* H, const int32_t* prompts_host, const 
     int K = (int)((double)remaining / per_cycle);
     K = std::max(1, std::min({K, H->graph_cycles, room}));
     const int na = (int)active.size();
-    s = cycle_impl(H, active.data(), na, K, acc.data(), n.data());
+    s = cycle_impl(H, active.data(), na, K, b, acc.data(), n.data());
     if (s != DF_OK) break;
+    long long g_cyc = 0, g_emit = 0;
     for (int c = 0; c < K; ++c)
       for (int j = 0; j < na; ++j) {
         const int i = active[j];
         const int nj = n[(size_t)c * na + j];
-        cyc += 1;
-        emitted += nj;
+        g_cyc += 1;
+        g_emit += nj;
         for (int t = 0; t < nj && count[i] < n_new; ++t)
           out_host[(size_t)i * n_new + count[i]++] = acc[((size_t)c * na + j) * B + t];
       }
+    cyc += g_cyc;
+    emitted += g_emit;
+    if (adaptive && g_cyc > 0) {
+      const double t = (double)g_emit / (double)g_cyc;
+      tau = have_tau ? 0.5 * tau + 0.5 * t : t;
+      have_tau = true;
+      b = block_size_for(tau, H->blk_min, H->blk_max);
+    }
   }
   for (int i = 0; i < nseq; ++i)
     if (H->seqs[i].active) release(H, i);
@@ -1427,6 +1479,7 @@ static df_status generate_impl(df_handle* H, const int32_t* prompts_host, const 
     d.accepted_drafts = H->stats.accepted_drafts - before.accepted_drafts;
     d.emitted_tokens = H->stats.emitted_tokens - before.emitted_tokens;
     for (int k = 0; k < 65; ++k) d.accept_hist[k] = H->stats.accept_hist[k] - before.accept_hist[k];
+    for (int k = 0; k < 33; ++k) d.block_hist[k] = H->stats.block_hist[k] - before.block_hist[k];
     d.draft_us = H->stats.draft_us - before.draft_us;
     d.verify_us = H->stats.verify_us - before.verify_us;
     d.prefill_us = H->stats.prefill_us - before.prefill_us;
@@ -1442,6 +1495,20 @@ df_status df_generate(df_handle* H, const int32_t* prompts_host, const int32_t* 
                       int32_t n_new, int32_t* out_host, df_stats* stats) {
   GUARD(H);
   return generate_impl(H, prompts_host, lens_host, nseq, n_new, out_host, stats);
+}
+
+df_status df_set_block_range(df_handle* H, int32_t b_min, int32_t b_max) {
+  GUARD(H);
+  if (b_min < 2 || b_min > b_max || b_max > H->B)
+    return fail(H, DF_EINVAL, "block range must satisfy 2 <= b_min <= b_max <= block_size");
+  H->blk_min = b_min;
+  H->blk_max = b_max;
+  return DF_OK;
+}
+
+int32_t df_block_size_for(double tokens_per_cycle, int32_t b_min, int32_t b_max) {
+  if (b_min < 2 || b_min > b_max || b_max > 32 || !(tokens_per_cycle >= 0.0)) return -1;
+  return block_size_for(tokens_per_cycle, b_min, b_max);
 }
 
 df_status df_generate_sampled(df_handle* H, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,

@@ -90,9 +90,10 @@ def ar_proxy(a):
                       "note": "random weights: latency only; one drafter pass includes its LM head"}))
 
 
-def _generation(shape, prompts, n_new, max_ctx, label, config):
+def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None):
     """One timed df_generate over a batch (device weights drawn on the GPU),
-    after one untimed warm-up generation of 16 tokens."""
+    after one untimed warm-up generation of 16 tokens.  block_range: (b_min,
+    b_max) for df_set_block_range, or None for the configured block size."""
     import numpy as np
     import torch
 
@@ -103,6 +104,8 @@ def _generation(shape, prompts, n_new, max_ctx, label, config):
     eng = dfl.Engine(shape, syn.iter_weights_device(shape), max_batch=len(prompts), max_ctx=max_ctx)
     torch.cuda.empty_cache()
     setup_s = time.time() - t0
+    if block_range:
+        eng.set_block_range(*block_range)
     eng.generate(prompts, 16)
     torch.cuda.synchronize()
     eng.reset_stats()
@@ -120,6 +123,8 @@ def _generation(shape, prompts, n_new, max_ctx, label, config):
                       "tokens_per_s": tokens / secs, "wall_s": secs, "cycles": s2["cycles"],
                       "mean_accept_len": s2["emitted_tokens"] / max(1, s2["cycles"] * len(prompts)),
                       "accept_hist_k": {str(k): v for k, v in enumerate(hist) if v},
+                      "block_range": list(block_range) if block_range else None,
+                      "block_hist": {str(b): v for b, v in enumerate(s2["block_hist"]) if v},
                       "draft_us_per_cycle": s2["draft_us"] / max(1, s2["cycles"]),
                       "verify_us_per_cycle": s2["verify_us"] / max(1, s2["cycles"]),
                       "prefill_us": s2["prefill_us"], "kernel_launches": s2["kernel_launches"],
@@ -137,7 +142,8 @@ def serving(a):
     prompts = [syn.make_prompt(shape, int(L), stream=200 + i) for i, L in enumerate(lens)]
     max_ctx = ((int(max(lens)) + a.new + 16 + 2 * shape.block_size + 63) // 64) * 64
     _generation(shape, prompts, a.new, max_ctx, "serving_batch16",
-                "qwen3-8b-shape bf16, 16 sequences, prompts U[128,2048], block 16, %d new each" % a.new)
+                "qwen3-8b-shape bf16, 16 sequences, prompts U[128,2048], block 16, %d new each" % a.new,
+                _block_range(a))
 
 
 def dense27b(a):
@@ -149,7 +155,14 @@ def dense27b(a):
     prompts = [syn.make_prompt(shape, 8192, stream=300 + i) for i in range(4)]
     max_ctx = ((8192 + a.new + 16 + 2 * shape.block_size + 63) // 64) * 64
     _generation(shape, prompts, a.new, max_ctx, "dense27b_batch4",
-                "27b-class bf16, batch 4, prompt 8192, block 16, %d new each" % a.new)
+                "27b-class bf16, batch 4, prompt 8192, block 16, %d new each" % a.new, _block_range(a))
+
+
+def _block_range(a):
+    if not a.block_range:
+        return None
+    lo, hi = (int(x) for x in a.block_range.split(","))
+    return lo, hi
 
 
 def main():
@@ -162,6 +175,7 @@ def main():
     ap.add_argument("op", choices=["gemm", "lmhead", "drafter", "ar_proxy", "serving", "dense27b"])
     ap.add_argument("--new", type=int, default=1024, help="serving/dense27b: new tokens per sequence")
     ap.add_argument("--blocks", default="8,16")
+    ap.add_argument("--block-range", default="", help="serving/dense27b: b_min,b_max for df_set_block_range")
     ap.add_argument("--ctx", default="1024,4096,16384,32768")
     ap.add_argument("--batch", default="1,4,16,32")
     ap.add_argument("--reduced", action="store_true", help="drafter: 1 drafter layer, vocab 4096")

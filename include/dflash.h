@@ -115,6 +115,7 @@ typedef struct {
   int64_t kernel_launches; /* this library's kernels launched */
   int64_t h2d_bytes;       /* host-to-device bytes copied by the engine */
   int64_t d2h_bytes;       /* device-to-host bytes copied by the engine */
+  int64_t block_hist[33];  /* cycles run at each block size (df_set_block_range) */
 } df_stats;
 
 /* Device time per kernel class, from CUDA events recorded on the engine's
@@ -194,6 +195,25 @@ df_status df_verify_accept(df_handle* h, const int32_t* seqs_host, int32_t nseq,
  * counters.  Slots are released at the end. */
 df_status df_generate(df_handle* h, const int32_t* prompts_host, const int32_t* lens_host, int32_t nseq,
                       int32_t n_new, int32_t* out_host, df_stats* stats);
+
+/* Block size of df_generate / df_generate_sampled's cycles ([ABS] 实践 2:
+ * a long block rolls back more often, so the block size may follow how
+ * predictable the text is).  With b_min == b_max every cycle drafts and
+ * verifies b_max slots (b_max - 1 drafts); with b_min < b_max the first
+ * group of cycles uses b_max and each later group df_block_size_for() of the
+ * tokens per cycle seen so far (an average over the groups, each weighted
+ * half as much as the one after it).  A cycle of b slots verifies b rows per
+ * sequence, so the target's GEMMs and attention shrink with it; the output
+ * is the target's greedy (or sampled) stream whatever the block sizes.
+ * 2 <= b_min <= b_max <= the configured block size; default: both equal to
+ * it.  Stays in force for the handle until changed. */
+df_status df_set_block_range(df_handle* h, int32_t b_min, int32_t b_max);
+
+/* The block-size rule on the host: the smallest power of two that is at
+ * least 2 x tokens_per_cycle, clamped to [b_min, b_max] (b_max itself where
+ * the power of two passes it).  -1 for arguments outside 2 <= b_min <= b_max
+ * <= 32 or a negative rate. */
+int32_t df_block_size_for(double tokens_per_cycle, int32_t b_min, int32_t b_max);
 
 /* df_generate with sampling instead of greedy decoding ([ABS] 实践 4; 核心思想
  * step 3).  A token's sampling distribution is softmax(logits / temperature)

@@ -109,3 +109,26 @@ def test_sampling_calls_reject_bad_arguments_without_gpu(L):
     assert L.df_op_philox_uniforms(0, 0, 0, -1, n, n) == dfl.DF_EINVAL
     assert L.df_op_philox_uniforms(0, 0, 0, 0, n, n) == dfl.DF_OK
     assert L.df_generate_sampled(n, n, n, 1, 1, 1.0, 1.0, 0, n, n) == dfl.DF_EINVAL        # null handle
+
+
+def test_block_size_rule():
+    # the smallest power of two >= 2 x tokens per cycle, clamped to [b_min, b_max]
+    import block_diffusion_speculative_layer_gb300 as dfl
+    f = dfl.block_size_for
+    assert [f(t, 2, 16) for t in (0.0, 1.0, 1.2, 2.0, 2.5, 4.0, 5.0, 8.0, 30.0)] == [2, 2, 4, 4, 8, 8, 16, 16, 16]
+    assert f(1.0, 4, 16) == 4 and f(7.0, 2, 12) == 12 and f(3.0, 6, 6) == 6
+    for b in (2, 4, 8):
+        assert f(float(b), 2, 16) == min(2 * b, 16)     # a group that keeps every draft doubles the block
+    prev = 0
+    for t in np.linspace(0.0, 20.0, 401):
+        b = f(float(t), 2, 16)
+        assert b >= prev and (b >= 2 * t or b == 16) and b in (2, 4, 8, 16)
+        prev = b
+    for bad in [(1.0, 1, 8), (1.0, 8, 4), (1.0, 2, 33), (-1.0, 2, 8)]:
+        with pytest.raises(dfl.DfError):
+            f(*bad)
+
+
+def test_block_range_needs_a_handle(L):
+    import block_diffusion_speculative_layer_gb300 as dfl
+    assert L.df_set_block_range(None, 2, 8) == dfl.DF_EINVAL
