@@ -804,7 +804,6 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(AttnParams p, const __g
   const int r0 = z * p.rows_per_seq + qt * 16;
   const int nrows = min(16, p.rows_per_seq - qt * 16);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
   const bool causal = p.causal != 0;
 
   // ---- the tile's rows: visible context length (-1: no position), longest

@@ -385,10 +385,6 @@ df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiPar
 }
 
 // ---------------------------------------------------------------- passes
-void* row_ptr(df_handle* H, void* base, int row, int ld) {
-  return reinterpret_cast<uint8_t*>(base) + (size_t)row * ld * H->esz;
-}
-
 // LM head with fused argmax over rows [row0, row0 + M) of xb -> d_ids[0..M).
 df_status lm_head_argmax(df_handle* H, int M, float* dbg) {
   {
