@@ -90,10 +90,11 @@ def ar_proxy(a):
                       "note": "random weights: latency only; one drafter pass includes its LM head"}))
 
 
-def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None):
+def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None, sampling=None):
     """One timed df_generate over a batch (device weights drawn on the GPU),
     after one untimed warm-up generation of 16 tokens.  block_range: (b_min,
-    b_max) for df_set_block_range, or None for the configured block size."""
+    b_max) for df_set_block_range, or None for the configured block size.
+    sampling: (temperature, top_p, seed) for df_generate_sampled, or None."""
     import numpy as np
     import torch
 
@@ -106,12 +107,18 @@ def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None)
     setup_s = time.time() - t0
     if block_range:
         eng.set_block_range(*block_range)
-    eng.generate(prompts, 16)
+
+    def run(n):
+        if sampling:
+            return eng.generate_sampled(prompts, n, temperature=sampling[0], top_p=sampling[1], seed=sampling[2])
+        return eng.generate(prompts, n)
+
+    run(16)
     torch.cuda.synchronize()
     eng.reset_stats()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(eng.stream)
-    out, st = eng.generate(prompts, n_new)
+    out, st = run(n_new)
     e1.record(eng.stream)
     torch.cuda.synchronize()
     secs = e0.elapsed_time(e1) / 1000.0
@@ -124,6 +131,8 @@ def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None)
                       "mean_accept_len": s2["emitted_tokens"] / max(1, s2["cycles"] * len(prompts)),
                       "accept_hist_k": {str(k): v for k, v in enumerate(hist) if v},
                       "block_range": list(block_range) if block_range else None,
+                      "sampling": {"temperature": sampling[0], "top_p": sampling[1], "seed": sampling[2]}
+                      if sampling else None,
                       "block_hist": {str(b): v for b, v in enumerate(s2["block_hist"]) if v},
                       "draft_us_per_cycle": s2["draft_us"] / max(1, s2["cycles"]),
                       "verify_us_per_cycle": s2["verify_us"] / max(1, s2["cycles"]),
@@ -144,6 +153,19 @@ def serving(a):
     _generation(shape, prompts, a.new, max_ctx, "serving_batch16",
                 "qwen3-8b-shape bf16, 16 sequences, prompts U[128,2048], block 16, %d new each" % a.new,
                 _block_range(a))
+
+
+def sampled(a):
+    """Speculative sampling on the Qwen3-8B shape at batch 1: prompt 512,
+    block 16, temperature and top_p from --sampling (default 0.8, 0.95)."""
+    import synthetic as syn
+
+    shape = syn.QWEN3_8B
+    T, top_p = (float(x) for x in a.sampling.split(","))
+    prompts = [syn.make_prompt(shape, 512)]
+    _generation(shape, prompts, a.new, 512 + a.new + 64, "sampled_bs1",
+                "qwen3-8b-shape bf16, batch 1, prompt 512, block 16, %d new, temperature %g, top_p %g"
+                % (a.new, T, top_p), _block_range(a), (T, top_p, 1))
 
 
 def dense27b(a):
@@ -172,7 +194,8 @@ def main():
     from block_diffusion_speculative_layer_gb300 import build
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["gemm", "lmhead", "drafter", "ar_proxy", "serving", "dense27b"])
+    ap.add_argument("op", choices=["gemm", "lmhead", "drafter", "ar_proxy", "serving", "dense27b", "sampled"])
+    ap.add_argument("--sampling", default="0.8,0.95", help="sampled: temperature,top_p")
     ap.add_argument("--new", type=int, default=1024, help="serving/dense27b: new tokens per sequence")
     ap.add_argument("--blocks", default="8,16")
     ap.add_argument("--block-range", default="", help="serving/dense27b: b_min,b_max for df_set_block_range")
@@ -193,6 +216,9 @@ def main():
         return
     if a.op == "dense27b":
         dense27b(a)
+        return
+    if a.op == "sampled":
+        sampled(a)
         return
     if a.op == "ar_proxy":
         ar_proxy(a)
