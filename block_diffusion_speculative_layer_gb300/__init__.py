@@ -28,6 +28,7 @@ EXPORTED = [
     "df_op_bench_gemm_bf16", "df_op_gemm_bf16_noalloc", "df_bench_drafter_step",
     "df_generate_sampled", "df_philox4x32_10", "df_op_philox_uniforms", "df_op_sampling_probs",
     "df_op_sample_draw", "df_op_accept_sampled", "df_set_block_range", "df_block_size_for",
+    "df_generate_accept_hist",
 ]
 
 
@@ -124,6 +125,7 @@ def lib() -> ctypes.CDLL:
     L.df_op_sample_draw.argtypes = [_P, _I, _I, _F, _F, _P, _P, _P, _P]
     L.df_op_accept_sampled.argtypes = [_P, _P, _P, _I, _I, _I, _F, _F, _P, _P, _P, _P, _P]
     L.df_set_block_range.argtypes = [_P, _I, _I]
+    L.df_generate_accept_hist.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_int64)]
     L.df_block_size_for.argtypes = [ctypes.c_double, _I, _I]
     L.df_block_size_for.restype = _I
     for name in EXPORTED:
@@ -293,6 +295,15 @@ class Engine:
                                                float(top_p), int(seed), _ip(out), ctypes.byref(stats)),
                     "df_generate_sampled")
         return out, stats.as_dict()
+
+    def accept_hist_per_seq(self, nseq: int) -> np.ndarray:
+        """[nseq][33]: for each sequence of the last generate call, cycles
+        that kept k drafts (k >= 32 at 32), over the cycles that emitted its tokens."""
+        out = np.zeros((nseq, 33), np.int64)
+        for i in range(nseq):
+            self._check(self.L.df_generate_accept_hist(self.h, i, out[i].ctypes.data_as(ctypes.POINTER(ctypes.c_int64))),
+                        "df_generate_accept_hist")
+        return out
 
     def set_block_range(self, b_min: int, b_max: int):
         """Block sizes df_generate may use: fixed when equal, else chosen per

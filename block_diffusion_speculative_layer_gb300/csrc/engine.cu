@@ -13,6 +13,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <array>
 #include <map>
 #include <string>
 #include <tuple>
@@ -123,6 +124,9 @@ struct df_handle {
   std::vector<int> glast;                       // key of the graph whose slots d_gslots holds
   // block size per cycle group (df_set_block_range): fixed at B unless blk_min < blk_max
   int blk_min = 0, blk_max = 0;
+  // per sequence of the last df_generate call: histogram of k over the cycles
+  // that emitted its tokens
+  std::vector<std::array<int64_t, 33>> gen_khist;
   int* d_gslots = nullptr;
   cudaStream_t gstream = nullptr;    // capture/replay stream, joined to the caller's stream by events
   cudaEvent_t gjoin[2] = {nullptr, nullptr};
@@ -1425,6 +1429,7 @@ static df_status generate_impl(df_handle* H, const int32_t* prompts_host, const 
   // (an average over groups, each weighted half as much as the next)
   const bool adaptive = H->blk_min < H->blk_max;
   int b = H->blk_max;
+  H->gen_khist.assign(nseq, std::array<int64_t, 33>{});
   double tau = 0.0;
   bool have_tau = false;
   while (s == DF_OK) {
@@ -1453,6 +1458,7 @@ static df_status generate_impl(df_handle* H, const int32_t* prompts_host, const 
         const int nj = n[(size_t)c * na + j];
         g_cyc += 1;
         g_emit += nj;
+        if (count[i] < n_new) H->gen_khist[i][std::min(std::max(nj - 1, 0), 32)] += 1;
         for (int t = 0; t < nj && count[i] < n_new; ++t)
           out_host[(size_t)i * n_new + count[i]++] = acc[((size_t)c * na + j) * B + t];
       }
@@ -1491,6 +1497,13 @@ df_status df_generate(df_handle* H, const int32_t* prompts_host, const int32_t* 
                       int32_t n_new, int32_t* out_host, df_stats* stats) {
   GUARD(H);
   return generate_impl(H, prompts_host, lens_host, nseq, n_new, out_host, stats);
+}
+
+df_status df_generate_accept_hist(const df_handle* H, int32_t seq, int64_t out[33]) {
+  if (!H || !out) return DF_EINVAL;
+  if (seq < 0 || seq >= (int32_t)H->gen_khist.size()) return DF_EINVAL;
+  for (int k = 0; k < 33; ++k) out[k] = H->gen_khist[seq][k];
+  return DF_OK;
 }
 
 df_status df_set_block_range(df_handle* H, int32_t b_min, int32_t b_max) {

@@ -124,12 +124,14 @@ def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None,
     secs = e0.elapsed_time(e1) / 1000.0
     s2 = eng.stats()
     hist = [int(x) for x in s2["accept_hist"]]
+    per_seq = eng.accept_hist_per_seq(len(prompts))
     eng.close()
     tokens = len(prompts) * n_new
     print(json.dumps({"op": label, "config": config, "sequences": len(prompts), "new_tokens_each": n_new,
                       "tokens_per_s": tokens / secs, "wall_s": secs, "cycles": s2["cycles"],
                       "mean_accept_len": s2["emitted_tokens"] / max(1, s2["cycles"] * len(prompts)),
                       "accept_hist_k": {str(k): v for k, v in enumerate(hist) if v},
+                      "accept_hist_k_per_sequence": [{str(k): int(v) for k, v in enumerate(h) if v} for h in per_seq],
                       "block_range": list(block_range) if block_range else None,
                       "sampling": {"temperature": sampling[0], "top_p": sampling[1], "seed": sampling[2]}
                       if sampling else None,

@@ -241,6 +241,13 @@ df_status df_generate_sampled(df_handle* h, const int32_t* prompts_host, const i
                               int32_t n_new, float temperature, float top_p, uint64_t seed, int32_t* out_host,
                               df_stats* stats);
 
+/* Per-sequence acceptance of the last df_generate / df_generate_sampled
+ * call: out[k] = cycles of sequence `seq` (its index in that call) that kept
+ * k drafts (k >= 32 counted at 32), over the cycles that emitted its tokens
+ * (a group's cycles after a sequence reached n_new are not counted here).
+ * DF_EINVAL if seq is outside the last call's sequences. */
+df_status df_generate_accept_hist(const df_handle* h, int32_t seq, int64_t out[33]);
+
 /* Plain token-by-token greedy decoding of the target on the GPU, with the
  * same kernels as verification: the lossless reference the speculative
  * output must equal bit for bit.  Same arguments as df_generate. */

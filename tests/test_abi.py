@@ -132,3 +132,5 @@ def test_block_size_rule():
 def test_block_range_needs_a_handle(L):
     import block_diffusion_speculative_layer_gb300 as dfl
     assert L.df_set_block_range(None, 2, 8) == dfl.DF_EINVAL
+    out = (ctypes.c_int64 * 33)()
+    assert L.df_generate_accept_hist(None, 0, out) == dfl.DF_EINVAL
