@@ -28,7 +28,7 @@ EXPORTED = [
     "df_op_bench_gemm_bf16", "df_op_gemm_bf16_noalloc", "df_bench_drafter_step",
     "df_generate_sampled", "df_philox4x32_10", "df_op_philox_uniforms", "df_op_sampling_probs",
     "df_op_sample_draw", "df_op_accept_sampled", "df_set_block_range", "df_block_size_for",
-    "df_generate_accept_hist",
+    "df_generate_accept_hist", "df_debug_wait_probe",
 ]
 
 
@@ -126,6 +126,7 @@ def lib() -> ctypes.CDLL:
     L.df_op_accept_sampled.argtypes = [_P, _P, _P, _I, _I, _I, _F, _F, _P, _P, _P, _P, _P]
     L.df_set_block_range.argtypes = [_P, _I, _I]
     L.df_generate_accept_hist.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_int64)]
+    L.df_debug_wait_probe.argtypes = [_P]
     L.df_block_size_for.argtypes = [ctypes.c_double, _I, _I]
     L.df_block_size_for.restype = _I
     for name in EXPORTED:
@@ -368,6 +369,11 @@ class Engine:
                                                  iters, out), "df_bench_drafter_step")
         return {"fuse_us": out[0], "inject_us": out[1], "block_attention_us": out[2], "lm_head_us": out[3],
                 "layer_gemms_us": out[4], "drafter_pass_us": out[5]}
+
+    def wait_probe(self):
+        """Run the failure-detection check (df_debug_wait_probe): raises
+        DfError with DF_ETIMEOUT, and the handle is failed afterwards."""
+        self._check(self.L.df_debug_wait_probe(self.h), "df_debug_wait_probe")
 
     def weight_ptr(self, which: int) -> int:
         a = ctypes.c_uint64()

@@ -1206,6 +1206,20 @@ static cudaError_t cl_attrs() {
   return cudaFuncSetAttribute(attn_cl_kernel<CLA, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, cl_smem_bytes(8));
 }
 
+// Failure-detection check: one bounded wait on a barrier that nothing
+// completes.  The wait the attention kernels use runs out after its limit,
+// records ERR_TIMEOUT in `err`, and the kernel returns normally.
+__global__ void wait_probe_kernel(int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) cl_mbar_init(smem_addr(&bar));
+  __syncthreads();
+  if (threadIdx.x == 0) (void)cl_wait_bar(smem_addr(&bar), 0u, err);
+}
+cudaError_t launch_wait_probe(int* err, cudaStream_t st) {
+  wait_probe_kernel<<<1, 32, 0, st>>>(err);
+  return cudaGetLastError();
+}
+
 cudaError_t attention_cluster_prepare() {
   if (g_cla) return cudaSuccess;
   cudaError_t e;

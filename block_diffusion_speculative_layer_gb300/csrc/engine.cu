@@ -1499,6 +1499,15 @@ df_status df_generate(df_handle* H, const int32_t* prompts_host, const int32_t* 
   return generate_impl(H, prompts_host, lens_host, nseq, n_new, out_host, stats);
 }
 
+df_status df_debug_wait_probe(df_handle* H) {
+  GUARD(H);
+  {
+    ProfScope ps_(H, PC_CTRL, 1);
+    CK(launch_wait_probe(H->d_err, H->st));
+  }
+  return sync(H);
+}
+
 df_status df_generate_accept_hist(const df_handle* H, int32_t seq, int64_t out[33]) {
   if (!H || !out) return DF_EINVAL;
   if (seq < 0 || seq >= (int32_t)H->gen_khist.size()) return DF_EINVAL;

@@ -108,6 +108,9 @@ cudaError_t launch_attention_cluster(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_attention_tc(const AttnParams& p, cudaStream_t st);
 bool attention_cluster_fits(const AttnParams& p);  // shapes the cluster kernel takes
 cudaError_t attention_cluster_prepare();  // kernel attributes, once, before any stream capture
+// One kernel whose bounded wait on a barrier nothing completes runs out and
+// sets ERR_TIMEOUT in err (about two seconds); it returns normally.
+cudaError_t launch_wait_probe(int* err, cudaStream_t st);
 
 // ---- small kernels (misc.cu)
 // h[m] = embed[tok[m]] (fp32), xraw[m] = the same row in the model dtype,

@@ -241,6 +241,14 @@ df_status df_generate_sampled(df_handle* h, const int32_t* prompts_host, const i
                               int32_t n_new, float temperature, float top_p, uint64_t seed, int32_t* out_host,
                               df_stats* stats);
 
+/* Failure-detection check.  Launches one kernel whose bounded wait on a
+ * barrier that nothing completes runs out after the limit every wait of the
+ * engine's kernels has (about two seconds), records the timeout in the
+ * handle's error word and returns.  The call returns DF_ETIMEOUT and leaves
+ * the handle failed (later calls return DF_ECUDA); the CUDA context stays
+ * usable, so a new handle works.  For tests of the error path only. */
+df_status df_debug_wait_probe(df_handle* h);
+
 /* Per-sequence acceptance of the last df_generate / df_generate_sampled
  * call: out[k] = cycles of sequence `seq` (its index in that call) that kept
  * k drafts (k >= 32 counted at 32), over the cycles that emitted its tokens

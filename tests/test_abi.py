@@ -134,3 +134,4 @@ def test_block_range_needs_a_handle(L):
     assert L.df_set_block_range(None, 2, 8) == dfl.DF_EINVAL
     out = (ctypes.c_int64 * 33)()
     assert L.df_generate_accept_hist(None, 0, out) == dfl.DF_EINVAL
+    assert L.df_debug_wait_probe(None) == dfl.DF_EINVAL
