@@ -142,6 +142,53 @@ def _accept_wrong_row(drafts, q_rows, p_rows, u_accept, u_final):
     return k, O.draw(p_rows[k], u_final)
 
 
+_orig_inject = O.inject_kv
+
+
+def _inject_without_rope(W, cfg, ctx_cache, ctx):
+    orig = O.rope
+    O.rope = lambda x, positions, theta: x                                   # keys injected unrotated
+    try:
+        return _orig_inject(W, cfg, ctx_cache, ctx)
+    finally:
+        O.rope = orig
+
+
+def _inject_positions_from_zero(W, cfg, ctx_cache, ctx):
+    # keys of appended rows rotated as if they started at position 0
+    n = ctx.shape[0]
+    tmp = O.ContextCache(cfg.draft_layers, cfg.n_kv_heads, cfg.head_dim)
+    _orig_inject(W, cfg, tmp, ctx)
+    for l in range(cfg.draft_layers):
+        ctx_cache.k[l] = np.concatenate([ctx_cache.k[l], tmp.k[l][:n]], axis=0)
+        ctx_cache.v[l] = np.concatenate([ctx_cache.v[l], tmp.v[l][:n]], axis=0)
+
+
+def _inject_value_from_key_matrix(W, cfg, ctx_cache, ctx):
+    class Swap:
+        def __getitem__(self, name):
+            return W[name.replace(".wv", ".wk")] if name.endswith(".wv") else W[name]
+    return _orig_inject(Swap(), cfg, ctx_cache, ctx)
+
+
+_orig_target = O.target_forward
+
+
+def _tap_layer_input(W, cfg, tokens, cache):
+    # taps the residual entering layer s instead of the output of layer s
+    tp = _orig_target(W, cfg, tokens, cache)
+    for i, l in enumerate(O.feature_layers(cfg.n_layers)):
+        tp.taps[:, i] = tp.hidden[l - 1]
+    return tp
+
+
+def _tap_next_layer(W, cfg, tokens, cache):
+    tp = _orig_target(W, cfg, tokens, cache)
+    for i, l in enumerate(O.feature_layers(cfg.n_layers)):
+        tp.taps[:, i] = tp.hidden[l + 1]
+    return tp
+
+
 def _sampled_pin():
     S.check_keeps_target_distribution(O.accept_sampled, n=40_000)
 
@@ -156,6 +203,11 @@ MUTATIONS = [
     ("rms_norm", _rms_no_eps, [P.test_rms_norm_matches_torch]),
     ("rms_norm", _rms_no_gain, [P.test_rms_norm_matches_torch]),
     ("decoder_layer", _layer_without_q_rope, [lambda: P.test_target_relative_positions()]),
+    ("inject_kv", _inject_without_rope, [P.test_injected_keys_match_block_keys_for_same_input]),
+    ("inject_kv", _inject_positions_from_zero, [P.test_injected_keys_match_block_keys_for_same_input]),
+    ("inject_kv", _inject_value_from_key_matrix, [P.test_injected_keys_match_block_keys_for_same_input]),
+    ("target_forward", _tap_layer_input, [P.test_tap_is_the_output_of_its_layer]),
+    ("target_forward", _tap_next_layer, [P.test_tap_is_the_output_of_its_layer]),
     ("accept_sampled", _accept_residual_from_p, [_sampled_pin]),
     ("accept_sampled", _accept_inverted_ratio, [_sampled_pin]),
     ("accept_sampled", _accept_wrong_row, [_sampled_pin]),

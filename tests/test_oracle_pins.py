@@ -201,6 +201,44 @@ def test_taps_are_layer_outputs():
         np.testing.assert_array_equal(tp.taps[:, i], tp.hidden[l])
 
 
+def _truncated(m, keep):
+    """The same model with only its first `keep` target layers."""
+    raw = {k: v for k, v in m.W.raw.items() if not (k[0] == "t" and int(k[1:k.index(".")]) >= keep)}
+    return O.Model(O.Weights(raw), m.cfg.replace(n_layers=keep))
+
+
+def _silenced(m, keep):
+    """The same model with target layers keep.. made the identity (their
+    attention output and down projections zeroed)."""
+    raw = dict(m.W.raw)
+    for l in range(keep, m.cfg.n_layers):
+        for name in (f"t{l}.wo", f"t{l}.w_down"):
+            raw[name] = np.zeros_like(raw[name])
+    return O.Model(O.Weights(raw), m.cfg)
+
+
+def test_tap_is_the_output_of_its_layer():
+    # Tap i of an L-layer model is the output of (1-based) layer s_i: the
+    # pre-norm final residual of the same model cut after s_i layers, either
+    # truncated (s_i >= 8, the oracle's smallest model) or with the layers
+    # after s_i made the identity.  Independent of the tap loop's indexing.
+    s = tiny(n_layers=20)
+    m = model(s, seed=23)
+    toks = syn.make_prompt(s, 6, seed=8)
+    full = O.teacher_forced(m, toks)
+    feats = O.feature_layers(s.n_layers)
+    assert feats == [2, 6, 10, 14, 18]
+    for i, layer in enumerate(feats):
+        cut = O.teacher_forced(_silenced(m, layer), toks).hidden[-1]
+        np.testing.assert_allclose(full.taps[:, i], cut, rtol=0, atol=1e-12)
+        if layer >= 8:
+            trunc = O.teacher_forced(_truncated(m, layer), toks).hidden[-1]
+            np.testing.assert_allclose(full.taps[:, i], trunc, rtol=0, atol=1e-12)
+        # not the input of that layer, nor the output of the next one
+        assert np.abs(full.taps[:, i] - O.teacher_forced(_silenced(m, layer - 1), toks).hidden[-1]).max() > 1e-6
+        assert np.abs(full.taps[:, i] - O.teacher_forced(_silenced(m, layer + 1), toks).hidden[-1]).max() > 1e-6
+
+
 # ---------------------------------------------------------------- fusion, injection, drafter
 
 def test_fused_context_has_unit_rms():
@@ -229,21 +267,33 @@ def test_fusion_concat_order_shallow_to_deep():
 
 def test_injected_keys_match_block_keys_for_same_input():
     # Injection uses the drafter layer's own W_k/W_v and RoPE at the context
-    # position: a context row equal to a block token's normalised input at the
-    # same position yields the same key/value that token produces in the block.
-    s = tiny(draft_layers=1)
-    m = model(s, seed=16)
+    # row's absolute position: injecting a context row equal to a block
+    # token's normalised layer input, at that token's position, gives the key
+    # and value the drafter layer itself makes for the token in a block pass
+    # (read from the layer's keys/values, not restated).
+    s = tiny(draft_layers=2)
+    m = model(s, seed=16, gain_std=0.1)
     W = m.W
-    rng = np.random.default_rng(10)
-    h = rng.standard_normal((1, s.d_model))
-    x = O.rms_norm(h, W["d0.attn_norm"], s.rms_eps)
-    cc = O.ContextCache(1, s.n_kv_heads, s.head_dim)
-    cc.k[0] = np.zeros((5, s.n_kv_heads, s.head_dim))
-    cc.v[0] = np.zeros((5, s.n_kv_heads, s.head_dim))
-    O.inject_kv(W, s, cc, x)
-    k = O.rope((x @ W["d0.wk"].T).reshape(1, s.n_kv_heads, s.head_dim), np.array([5]), s.rope_theta)
-    np.testing.assert_allclose(cc.k[0][5:], k, rtol=1e-12)
-    np.testing.assert_allclose(cc.v[0][5:], (x @ W["d0.wv"].T).reshape(1, s.n_kv_heads, s.head_dim), rtol=1e-12)
+    B = s.block_size
+    anchor = 7
+    toks = np.asarray([3] + [s.mask_token_id] * (B - 1))
+    pos = np.arange(anchor, anchor + B)
+    h = W["embed"][toks]
+    for l in range(s.draft_layers):
+        seen = {}
+
+        def kv(k_new, v_new):
+            seen["k"], seen["v"] = k_new, v_new
+            return k_new, v_new, np.ones((B, B), bool)
+
+        h_next = O.decoder_layer(W, f"d{l}", s, h, pos, kv)
+        x = O.rms_norm(h, W[f"d{l}.attn_norm"], s.rms_eps)
+        cc = O.ContextCache(s.draft_layers, s.n_kv_heads, s.head_dim)
+        O.inject_kv(W, s, cc, np.random.default_rng(10).standard_normal((anchor, s.d_model)))
+        O.inject_kv(W, s, cc, x)
+        np.testing.assert_allclose(cc.k[l][anchor:], seen["k"], rtol=1e-10, atol=1e-13)
+        np.testing.assert_allclose(cc.v[l][anchor:], seen["v"], rtol=1e-10, atol=1e-13)
+        h = h_next
 
 
 def _ctx_cache(m, n, seed):
