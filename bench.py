@@ -198,6 +198,50 @@ def oracle_cycle_sample(shape, prompt_len: int, tau: float, repeats: int = 1):
             "fuse_s": fu, "inject_layer_s": ij, "cores": os.cpu_count()}
 
 
+def oracle_tiny_full():
+    """The float64 oracle on the tiny fp32 configuration in full: 8-layer
+    target (d 256), 1-layer drafter, block 8, prompt 64, 128 new tokens,
+    speculative decoding (spec_generate)."""
+    import synthetic as syn
+    from oracle import dflash_oracle as O
+
+    shape = syn.TINY
+    m = O.Model(O.Weights(syn.make_weights(shape)), shape)
+    prompt = syn.make_prompt(shape, 64)
+    t0 = time.perf_counter()
+    res = O.spec_generate(m, prompt, 128)
+    secs = time.perf_counter() - t0
+    return {"value": 128 / secs, "unit": UNIT, "cores": os.cpu_count(), "wall_s": secs,
+            "cycles": len(res.cycles), "mean_accept_len": res.mean_accept_len,
+            "workload": "tiny fp32 (8 layers, d 256, block 8), prompt 64, 128 new tokens, speculative, whole run"}
+
+
+def draft_latency_proxy(eng, shape, ctx=1024):
+    """Latency of one drafter pass of the engine (5 layers over a 16-slot
+    block, with fusion, injection and the LM head) against an autoregressive
+    1-layer drafter of the same width making 8 drafts in 8 sequential passes
+    (each one layer over a 2-row block and the LM head), batch 1, `ctx`
+    context positions; the AR drafter's weights are drawn on the GPU."""
+    import torch
+
+    import block_diffusion_speculative_layer_gb300 as dfl
+    import synthetic as syn
+
+    d = shape.d_model
+    taps = syn.make_hidden(512, 5 * d).reshape(512, 5, d)
+    dflash = eng.bench_drafter_step(1, ctx, taps, iters=10)["drafter_pass_us"]
+    ar_shape = shape.replace(name="ar-1-layer", n_layers=8, draft_layers=1, block_size=2)
+    ar = dfl.Engine(ar_shape, syn.iter_weights_device(ar_shape), max_batch=1, max_ctx=ctx + 64)
+    torch.cuda.empty_cache()
+    step = ar.bench_drafter_step(1, ctx, taps, iters=10)["drafter_pass_us"]
+    ar.close()
+    torch.cuda.empty_cache()
+    return {"ctx": ctx, "dflash_5layer_16slots_us": dflash, "ar_1layer_8steps_us": 8 * step,
+            "ratio_ar_over_dflash": 8 * step / dflash,
+            "note": "random weights, latency only: one 5-layer pass over a 16-slot block vs eight 1-layer steps "
+                    "(each pass includes its LM head)"}
+
+
 # ---------------------------------------------------------------------------- arms
 
 def aggregate(secs: float, tokens: int, dist=None, device="cpu"):
@@ -317,30 +361,54 @@ def run_ours(args):
     e2e_s = time.perf_counter() - w0
     st_e2e = eng.stats()
 
-    # ---- kernel-class device times (events around every launch) for the roofline
+    # ---- kernel classes in situ: device-timer stamps inside the captured cycles
+    # (graphs and programmatic dependent launch as timed above); the classes
+    # partition the decode cycles' device time
+    eng.profile(True, in_situ=True)
+    eng.generate([prompt], n_new)
+    insitu = eng.profile_read()
+    eng.profile(False)
+    # ---- the same classes serialised (events around every launch, no graphs), for comparison
     eng.profile(True)
     eng.generate([prompt], n_new)
     prof = eng.profile_read()
     eng.profile(False)
     peaks = measured_peaks()
+
+    def class_rate(pr, keys):
+        ks = [pr[k] for k in keys if k in pr]
+        b, us, n = sum(x["bytes"] for x in ks), sum(x["us"] for x in ks), sum(x["launches"] for x in ks)
+        return b, us, n, (b / (us * 1e-6) / 1e9 if us > 0 else None)
+
     # every launch of the tcgen05 GEMM kernel: layer GEMMs, LM head, fusion, injection
-    gk = [prof[k] for k in ("gemm", "lm_head", "fuse", "inject") if k in prof]
-    g = {"bytes": sum(x["bytes"] for x in gk), "us": sum(x["us"] for x in gk),
-         "launches": sum(x["launches"] for x in gk)}
-    gemm_gbs = g["bytes"] / (g["us"] * 1e-6) / 1e9 if g["us"] > 0 else None
+    gemm_keys = ("gemm", "lm_head", "fuse", "inject")
+    g_bytes, g_us, g_n, gemm_gbs = class_rate(insitu, gemm_keys)
+    _, gs_us, _, gemm_gbs_serial = class_rate(prof, gemm_keys)
     traffic = None
     if NCU_TRAFFIC["source_sha"] == kernel_source_sha() and NCU_TRAFFIC["bytes_per_gemm_launch_avg"]:
         traffic = NCU_TRAFFIC["bytes_per_gemm_launch_avg"]
     roofline = {
-        "bound": "hbm", "kernel": "gemm_tc_kernel (tcgen05, weight-streaming; every GEMM launch of one generation)",
+        "bound": "hbm", "kernel": "gemm_tc_kernel (tcgen05, weight-streaming; every GEMM launch of the decode cycles)",
         "achieved": gemm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
         "frac": (gemm_gbs / peaks["hbm_gbs"]) if gemm_gbs else None, "traffic": traffic,
-        "peak_source": peaks["source"], "algorithmic_bytes_per_launch": g["bytes"] / max(g["launches"], 1),
-        "avg_launch_us": g["us"] / max(g["launches"], 1),
+        "peak_source": peaks["source"], "algorithmic_bytes_per_launch": g_bytes / max(g_n, 1),
+        "avg_launch_us": g_us / max(g_n, 1),
+        "timing": "in situ: the decode cycles of one generation as timed (CUDA graphs, programmatic dependent "
+                  "launch); each GEMM/attention launch stamps the device timer at its first CTA's entry and last "
+                  "CTA's exit and is charged the time since the previous stamped exit",
+        "serialised": {"achieved": gemm_gbs_serial,
+                       "frac": (gemm_gbs_serial / peaks["hbm_gbs"]) if gemm_gbs_serial else None,
+                       "avg_launch_us": gs_us / max(g_n, 1),
+                       "timing": "CUDA events around every launch, cycles launched without graphs"},
     }
-    breakdown = {k: {"launches": v["launches"], "ms": v["us"] / 1000.0,
-                     "GB/s": (v["bytes"] / (v["us"] * 1e-6) / 1e9) if v["us"] > 0 and v["bytes"] > 0 else None}
-                 for k, v in prof.items()}
+
+    def table(pr):
+        return {k: {"launches": v["launches"], "ms": v["us"] / 1000.0,
+                    "GB/s": (v["bytes"] / (v["us"] * 1e-6) / 1e9) if v["us"] > 0 and v["bytes"] > 0 else None}
+                for k, v in pr.items() if v["launches"]}
+
+    kernels = {"in_situ": table(insitu), "in_situ_sum_ms": sum(v["us"] for v in insitu.values()) / 1000.0,
+               "serialised": table(prof)}
 
     # ---- forced acceptance: drafts replaced by the target's greedy continuation (tau = B)
     forced = None
@@ -369,8 +437,19 @@ def run_ours(args):
     verify_us = st["verify_us"] / cycles
     d, F, V, L, Ld = shape.d_model, shape.d_ffn, shape.vocab, shape.n_layers, shape.draft_layers
     layer_w = 2 * (d * (shape.q_dim + 2 * shape.kv_dim) + shape.q_dim * d + 3 * d * F)
-    cycle_bytes = (L + Ld) * layer_w + 2 * 2 * V * d + 2 * (5 * d * d + Ld * 2 * shape.kv_dim * d)
-    floor_us = cycle_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+    # keys and values read per cycle at the mean context of the generation (2 bytes, K and V)
+    ctx_mean = P + n_new / 2.0
+    kv_row = 2 * 2 * shape.kv_dim
+    draft_bytes = Ld * layer_w + 2 * V * d + Ld * ctx_mean * kv_row
+    verify_bytes = L * layer_w + 2 * V * d + 2 * (5 * d * d + Ld * 2 * shape.kv_dim * d) + L * ctx_mean * kv_row
+    cycle_bytes = draft_bytes + verify_bytes
+    bw = peaks["hbm_gbs"] * 1e9
+    floor_us = cycle_bytes / bw * 1e6
+
+    # ---- draft-latency proxy: one 5-layer, 16-slot drafter pass against eight 1-layer autoregressive steps
+    proxy = None
+    if not args.no_proxy:
+        proxy = draft_latency_proxy(eng, shape)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -378,7 +457,8 @@ def run_ours(args):
         cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                "sample": "float64 numpy oracle, one decode cycle sampled (1 of 36 target layers, 1 of 5 drafter "
                          "layers, LM head over 31 rows, one fusion row, one injection layer), scaled to the full "
-                         f"cycle at the measured tau={tau:.3f}; cycle {r['cycle_s']:.2f} s"}
+                         f"cycle at the measured tau={tau:.3f}; cycle {r['cycle_s']:.2f} s",
+               "tiny_full": oracle_tiny_full()}
 
     if rank == 0:
         line = {
@@ -390,9 +470,15 @@ def run_ours(args):
             "cycle": {"draft_us": draft_us, "verify_us": verify_us, "cycle_us": draft_us + verify_us,
                       "mean_accept_len": tau, "cycles_per_step": st["cycles"] / args.steps,
                       "floor_us": floor_us, "floor_frac": floor_us / (draft_us + verify_us),
-                      "cycle_algorithmic_bytes": cycle_bytes},
+                      "cycle_algorithmic_bytes": cycle_bytes,
+                      "draft_algorithmic_bytes": draft_bytes, "verify_algorithmic_bytes": verify_bytes,
+                      "draft_frac": draft_bytes / bw * 1e6 / draft_us,
+                      "verify_frac": verify_bytes / bw * 1e6 / verify_us,
+                      "fracs": "algorithmic bytes / measured HBM bandwidth / measured time; verify includes "
+                               "acceptance, fusion and injection"},
             "roofline": roofline,
-            "kernels": breakdown,
+            "kernels": kernels,
+            "draft_latency_proxy": proxy,
             "forced_acceptance": forced,
             "cpu_baseline": cpu,
             "e2e": {"value": world * args.steps * n_new / e2e_s, "unit": UNIT,
@@ -419,6 +505,7 @@ def main():
     ap.add_argument("--new-tokens", type=int, default=512)
     ap.add_argument("--no-forced", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-proxy", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

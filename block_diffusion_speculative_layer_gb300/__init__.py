@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libdflash.so")
 DF_OK, DF_EINVAL, DF_ENOMEM, DF_ECUDA, DF_ETIMEOUT, DF_ESTATE = range(6)
 DF_FP32, DF_BF16 = 0, 1
 DF_DBG_TAPS, DF_DBG_LOGITS, DF_DBG_DRAFT_LOGITS, DF_DBG_DRAFT_HIDDEN, DF_DBG_CTX, DF_DBG_HIDDEN = 1, 2, 3, 4, 5, 6
+DF_DBG_TARGET_LAYERS, DF_DBG_DRAFT_LAYERS = 7, 8
 STATUS_NAMES = {0: "DF_OK", 1: "DF_EINVAL", 2: "DF_ENOMEM", 3: "DF_ECUDA", 4: "DF_ETIMEOUT", 5: "DF_ESTATE"}
 
 EXPORTED = [
@@ -341,16 +342,24 @@ class Engine:
 
     def debug_read(self, what: int) -> np.ndarray:
         cols = {DF_DBG_TAPS: 5 * self.d, DF_DBG_LOGITS: self.V, DF_DBG_DRAFT_LOGITS: self.V,
-                DF_DBG_DRAFT_HIDDEN: self.d, DF_DBG_CTX: self.d, DF_DBG_HIDDEN: self.d}[what]
-        cap = max(512, self.cfg.max_batch * self.B) * cols
+                DF_DBG_DRAFT_HIDDEN: self.d, DF_DBG_CTX: self.d, DF_DBG_HIDDEN: self.d,
+                DF_DBG_TARGET_LAYERS: self.d, DF_DBG_DRAFT_LAYERS: self.d}[what]
+        layers = {DF_DBG_TARGET_LAYERS: self.shape.n_layers + 1, DF_DBG_DRAFT_LAYERS: self.shape.draft_layers + 1}
+        cap = max(512, self.cfg.max_batch * self.B) * cols * layers.get(what, 1)
         buf = np.zeros(cap, np.float32)
         rows = ctypes.c_int32()
         self._check(self.L.df_debug_read(self.h, what, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), cap,
                                          ctypes.byref(rows)), "df_debug_read")
-        return buf[: rows.value * cols].reshape(rows.value, cols)
+        out = buf[: rows.value * cols].reshape(rows.value, cols)
+        if what in layers:
+            return out.reshape(layers[what], rows.value // layers[what], cols)
+        return out
 
-    def profile(self, on: bool = True):
-        self._check(self.L.df_profile_enable(self.h, 1 if on else 0), "df_profile_enable")
+    def profile(self, on: bool = True, in_situ: bool = False):
+        """Kernel-class timing: events around every launch (serialised), or
+        with in_situ=True device-timer stamps inside the captured cycles."""
+        mode = (2 if in_situ else 1) if on else 0
+        self._check(self.L.df_profile_enable(self.h, mode), "df_profile_enable")
 
     def profile_read(self) -> Dict[str, dict]:
         """Per kernel class: launches, device microseconds, algorithmic bytes and flops (then cleared)."""

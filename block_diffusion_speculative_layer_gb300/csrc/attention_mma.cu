@@ -385,8 +385,7 @@ __device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_
 // NW warps (one per query head of a group, at least four): four-warp CTAs are
 // held to 168 registers so that three fit on an SM next to their shared memory.
 template <int CLA, int NW>
-__global__ void __launch_bounds__(NW * 32, NW == 4 ? 3 : 1)
-    attn_cl_kernel(AttnParams p, const __grid_constant__ CUtensorMap kvmap) {
+__device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensorMap& kvmap) {
   // The GEMM before this kernel triggers it only after its own wait (see
   // gemm_tc.cu), so everything older than that GEMM is complete here: the row
   // metadata, the page table and the cache entries of earlier positions are
@@ -720,6 +719,14 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 3 : 1)
   }
   cl_arrive();  // this CTA's reads of the other partials are done
   cl_wait();    // and nobody leaves while another CTA may still read its partial
+}
+
+template <int CLA, int NW>
+__global__ void __launch_bounds__(NW * 32, NW == 4 ? 3 : 1)
+    attn_cl_kernel(AttnParams p, const __grid_constant__ CUtensorMap kvmap) {
+  trace_entry(p.trace);
+  attn_cl_body<CLA, NW>(p, kvmap);
+  trace_exit(p.trace);
 }
 
 

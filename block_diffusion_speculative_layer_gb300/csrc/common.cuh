@@ -30,6 +30,21 @@ __device__ __forceinline__ void flag_error(int* err, int bit) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// In-situ launch timing: each CTA's thread 0 folds its entry and exit times
+// (the %globaltimer, ns) into trace[0] = max ~entry (so ~trace[0] is the
+// first CTA's entry) and trace[1] = max exit.  trace null: off.
+__device__ __forceinline__ unsigned long long device_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void trace_entry(unsigned long long* trace) {
+  if (trace && threadIdx.x == 0) atomicMax(trace, ~device_ns());
+}
+__device__ __forceinline__ void trace_exit(unsigned long long* trace) {
+  if (trace && threadIdx.x == 0) atomicMax(trace + 1, device_ns());
+}
+
 template <typename T> struct Cvt;
 template <> struct Cvt<float> {
   static __device__ __forceinline__ float to_f(float v) { return v; }
@@ -111,6 +126,9 @@ struct EpiParams {
   void* tap;                 // [M][5][N] feature-layer tap of the new rows; null: none
   int tap_index;
   int* err;
+  // In-situ timing (null: off): trace[0] = max over CTAs of ~(entry time),
+  // trace[1] = max over CTAs of the exit time, in device-timer nanoseconds.
+  unsigned long long* trace;
 };
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }

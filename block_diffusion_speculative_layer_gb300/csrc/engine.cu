@@ -95,6 +95,7 @@ struct df_handle {
   float *ss = nullptr, *ss_ctx = nullptr;  // per-row, per-128-feature-tile sums of squares
   float* tmp = nullptr;
   float *dbg_logits = nullptr, *dbg_dlogits = nullptr, *dbg_dh = nullptr, *dbg_th = nullptr;
+  float *dbg_tl = nullptr, *dbg_dl = nullptr;  // [layers + 1][rows][d] residual rows entering each layer, then the output
   float* ws = nullptr;
   int* counters = nullptr;
   float* part_acc = nullptr;
@@ -116,9 +117,20 @@ struct df_handle {
   // graph replay of the decode cycle (df_generate)
   bool use_graphs = true;
   int graph_ready_cycles = 0;        // eager cycles run by this handle (the first sets kernel attributes)
+  // in-situ timing (df_profile_enable mode 2): per stamped launch of the
+  // cycles being recorded, its class, launch count and algorithmic bytes;
+  // d_trace[2i], d_trace[2i + 1] are its stamps (see trace_entry)
+  struct TraceSlot {
+    int cls, n;
+    double bytes, flops;
+  };
+  bool tracing = false;
+  unsigned long long* d_trace = nullptr;
+  std::vector<TraceSlot> trace_meta;
   struct GraphRec {
     cudaGraphExec_t exec = nullptr;
     int64_t launches = 0, h2d = 0, d2h = 0;  // counted again at each replay
+    std::vector<TraceSlot> trace_meta;      // stamped launches of the graph (in-situ timing)
   };
   std::map<std::vector<int>, GraphRec> graphs;  // by slots, cycle count, block size (and sampling arguments)
   std::vector<int> glast;                       // key of the graph whose slots d_gslots holds
@@ -210,17 +222,27 @@ int ev_take(df_handle* H) {
   return (int)H->ev_used++;
 }
 
-// Counts this library's launches; with profiling on, brackets them with events.
+constexpr size_t TRACE_MAX = 8192;  // stamped launches per recorded run of cycles
+
+// Counts this library's launches; with profiling on, brackets them with
+// events; with in-situ timing on, gives GEMM and attention launches a stamp
+// slot (tp, passed to the kernel).
 struct ProfScope {
   df_handle* H;
   int cls, n, e0 = -1;
   double bytes, flops;
+  unsigned long long* tp = nullptr;
   ProfScope(df_handle* h, int c, int nlaunch, double b = 0.0, double f = 0.0)
       : H(h), cls(c), n(nlaunch), bytes(b), flops(f) {
     H->stats.kernel_launches += n;
     if (H->profiling) {
       e0 = ev_take(H);
       if (e0 >= 0) cudaEventRecord(H->evpool[e0], H->st);
+    }
+    const bool stamped = c == PC_GEMM || c == PC_LMHEAD || c == PC_FUSE || c == PC_INJECT || c == PC_ATTN;
+    if (H->tracing && stamped && H->trace_meta.size() < TRACE_MAX) {
+      tp = H->d_trace + 2 * H->trace_meta.size();
+      H->trace_meta.push_back({c, n, b, f});
     }
   }
   ~ProfScope() {
@@ -231,6 +253,30 @@ struct ProfScope {
     H->pending.push_back({cls, e0, e1, n, bytes, flops});
   }
 };
+
+// In-situ timing: read the stamps of the launches in `meta` (the stream is
+// synchronised) and charge each launch the time from the previous stamped
+// exit (the first launch's entry for the first one) to its own exit.
+cudaError_t trace_collect(df_handle* H, const std::vector<df_handle::TraceSlot>& meta) {
+  if (meta.empty()) return cudaSuccess;
+  std::vector<unsigned long long> t(2 * meta.size());
+  cudaError_t e = cudaMemcpy(t.data(), H->d_trace, t.size() * 8, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return e;
+  unsigned long long prev = 0;
+  for (size_t i = 0; i < meta.size(); ++i) {
+    const unsigned long long entry = ~t[2 * i], exit = t[2 * i + 1];
+    if (t[2 * i] == 0 || exit == 0) continue;  // not stamped (a path without stamps)
+    if (prev == 0) prev = entry;
+    const unsigned long long dt = exit > prev ? exit - prev : 0ull;
+    prev = exit > prev ? exit : prev;
+    df_kernel_stat& k = H->prof[meta[i].cls];
+    k.launches += meta[i].n;
+    k.total_us += 1e-3 * (double)dt;
+    k.bytes += meta[i].bytes;
+    k.flops += meta[i].flops;
+  }
+  return cudaSuccess;
+}
 
 // Host<->device copies on the engine's stream, counted for the end-to-end byte totals.
 cudaError_t h2d(df_handle* H, void* dst, const void* src, size_t bytes) {
@@ -379,7 +425,9 @@ df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiPar
     const void* tmX = nullptr;
     CKS(xmap(H, X, W.K, nt, &tmX));
     const int splits = tc_splits(W.N, W.K, H->split_target);
-    CK(launch_gemm_tc(W.tm.b, tmX, nt, M, W.N, W.K, splits, H->ws, H->counters, ep, H->st,
+    EpiParams e = ep;
+    e.trace = ps.tp;
+    CK(launch_gemm_tc(W.tm.b, tmX, nt, M, W.N, W.K, splits, H->ws, H->counters, e, H->st,
                       tc_cluster_reduce(nt, splits)));
   } else {
     CK(launch_gemm_f32(reinterpret_cast<const float*>(X), reinterpret_cast<const float*>(W.ptr), H->tmp, M, W.N, W.K,
@@ -456,6 +504,7 @@ df_status attention(df_handle* H, int M, int R, int nseq, bool causal, const voi
   const double qo_bytes = 2.0 * M * H->qdim * H->esz;
   ProfScope ps(H, PC_ATTN, attention_launches(p, H->bf16), kv_bytes + qo_bytes,
                4.0 * M * H->qdim * (double)max_len);
+  p.trace = ps.tp;
   CK(launch_attention(p, H->bf16, H->st));
   return DF_OK;
 }
@@ -525,14 +574,23 @@ df_status layer_pass(df_handle* H, const Layer& Lw, int M, int R, int nseq, bool
   return DF_OK;
 }
 
+// Debug capture: the fp32 residual rows [0, M) as they stand before layer
+// `slot` (slot = layer count: after the last layer) into buf[slot][M][d].
+df_status debug_layer_rows(df_handle* H, float* buf, int slot, int M) {
+  CK(cudaMemcpyAsync(buf + (size_t)slot * M * H->d, H->h, (size_t)M * H->d * 4, cudaMemcpyDeviceToDevice, H->st));
+  return DF_OK;
+}
+
 // Target over M rows (row_tok / row_pos / row_seq already set).  head_rows:
 // 0 = no LM head; -1 = every row; else only the last row (prefill).
 df_status target_pass(df_handle* H, int M, int R, int nseq, int max_len, bool want_taps, int head_mode) {
   { ProfScope ps_(H, PC_EMBED, 1); CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, H->xraw, H->ss, M, H->d, H->V, H->d_err, H->st)); }
+  if (H->debug) CKS(debug_layer_rows(H, H->dbg_tl, 0, M));
   for (int l = 0; l < H->L; ++l) {
     // the output of layer l is the input of layer l+1: tap it if selected
     const int tap = (want_taps && l + 1 < H->L) ? H->tap_of_layer[l + 1] : -1;
     CKS(layer_pass(H, H->tl[l], M, R, nseq, true, l, max_len, tap));
+    if (H->debug) CKS(debug_layer_rows(H, H->dbg_tl, l + 1, M));
   }
   H->rows_last_target = M;
   if (H->debug) CK(cudaMemcpyAsync(H->dbg_th, H->h, (size_t)M * H->d * 4, cudaMemcpyDeviceToDevice, H->st));
@@ -577,7 +635,11 @@ df_status fuse_inject(df_handle* H, int M, const int* row_pos) {
 df_status drafter_pass(df_handle* H, int nseq, int max_ctx_len, int b = 0) {
   const int B = b > 0 ? b : H->B, M = nseq * B;
   { ProfScope ps_(H, PC_EMBED, 1); CK(launch_embed(H->embed, H->bf16, H->d_row_tok, H->h, H->xraw, H->ss, M, H->d, H->V, H->d_err, H->st)); }
-  for (int l = 0; l < H->Ld; ++l) CKS(layer_pass(H, H->dl[l], M, B, nseq, false, l, max_ctx_len, -1));
+  if (H->debug) CKS(debug_layer_rows(H, H->dbg_dl, 0, M));
+  for (int l = 0; l < H->Ld; ++l) {
+    CKS(layer_pass(H, H->dl[l], M, B, nseq, false, l, max_ctx_len, -1));
+    if (H->debug) CKS(debug_layer_rows(H, H->dbg_dl, l + 1, M));
+  }
   if (H->debug) CK(cudaMemcpyAsync(H->dbg_dh, H->h, (size_t)M * H->d * 4, cudaMemcpyDeviceToDevice, H->st));
   { ProfScope ps_(H, PC_NORM, 1); CK(launch_rmsnorm(H->h, H->d, H->d_final_norm, H->xb, H->d, H->bf16, M, H->d, H->cfg.rms_eps, nullptr, 0, nullptr,
                     H->st)); }
@@ -911,8 +973,11 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int b,
         max_d = std::max(max_d, s.len);
       }
       CK(h2d(H, H->d_slots, slots, nseq * 4));
+      H->trace_meta.clear();
+      if (H->tracing) CK(cudaMemsetAsync(H->d_trace, 0, TRACE_MAX * 16, H->st));
       CKS(cycle_work(H, H->d_slots, nseq, max_d, max_t, false, 0, b));
       CKS(sync(H));
+      if (H->tracing) CK(trace_collect(H, H->trace_meta));
       H->graph_ready_cycles += 1;
       CKS(cycle_finish(H, slots, nseq, 0, b, out_acc(c), out_n(c)));
     }
@@ -921,6 +986,7 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int b,
   std::vector<int> key(slots, slots + nseq);
   key.push_back(K);
   key.push_back(b);
+  key.push_back(H->tracing ? 1 : 0);  // stamp slots are launch arguments of the captured kernels
   if (H->sampling) {
     // the sampling parameters are launch arguments of the captured kernels
     int tb = 0, pb = 0;
@@ -942,6 +1008,7 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int b,
     H->glast = key;
     CK(cudaStreamSynchronize(user));
     const df_stats before = H->stats;
+    H->trace_meta.clear();
     bool ok = cudaStreamBeginCapture(H->gstream, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
     df_status st = DF_OK;
     cudaGraph_t g = nullptr;
@@ -958,6 +1025,7 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int b,
     rec.launches = H->stats.kernel_launches - before.kernel_launches;
     rec.h2d = H->stats.h2d_bytes - before.h2d_bytes;
     rec.d2h = H->stats.d2h_bytes - before.d2h_bytes;
+    rec.trace_meta = H->trace_meta;
     H->stats = before;  // counted again at each replay
     if (!ok) {
       // capture is not available here: run this handle's cycles eagerly
@@ -974,6 +1042,7 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int b,
     CK(cudaStreamWaitEvent(H->gstream, H->gjoin[0], 0));
     H->glast = key;
   }
+  if (!it->second.trace_meta.empty()) CK(cudaMemsetAsync(H->d_trace, 0, it->second.trace_meta.size() * 16, H->gstream));
   CK(cudaGraphLaunch(it->second.exec, H->gstream));
   CK(cudaEventRecord(H->gjoin[1], H->gstream));
   CK(cudaStreamWaitEvent(H->st, H->gjoin[1], 0));
@@ -981,6 +1050,7 @@ df_status cycle_impl(df_handle* H, const int32_t* slots, int nseq, int K, int b,
   H->stats.h2d_bytes += it->second.h2d;
   H->stats.d2h_bytes += it->second.d2h;
   CKS(sync(H));
+  if (!it->second.trace_meta.empty()) CK(trace_collect(H, it->second.trace_meta));
   for (int c = 0; c < K; ++c) CKS(cycle_finish(H, slots, nseq, c, b, out_acc(c), out_n(c)));
   return trim_all(H, slots, nseq);
 }
@@ -1253,6 +1323,8 @@ df_status ensure_debug_buffers(df_handle* H) {
   CKS(dalloc_t(H, &H->dbg_dlogits, M * H->V * 4));
   CKS(dalloc_t(H, &H->dbg_dh, M * H->d * 4));
   CKS(dalloc_t(H, &H->dbg_th, M * H->d * 4));
+  CKS(dalloc_t(H, &H->dbg_tl, (size_t)(H->L + 1) * M * H->d * 4));
+  CKS(dalloc_t(H, &H->dbg_dl, (size_t)(H->Ld + 1) * M * H->d * 4));
   return DF_OK;
 }
 
@@ -1669,6 +1741,8 @@ df_status df_debug_read(df_handle* H, int32_t what, float* out_host, int64_t max
     case DF_DBG_DRAFT_HIDDEN: src = H->dbg_dh; rows = H->rows_last_draft; cols = H->d; break;
     case DF_DBG_CTX: src = H->ctx; typed = true; rows = H->rows_last_ctx; cols = H->d; break;  // normalised below
     case DF_DBG_HIDDEN: src = H->dbg_th; rows = H->rows_last_target; cols = H->d; break;
+    case DF_DBG_TARGET_LAYERS: src = H->dbg_tl; rows = (H->L + 1) * H->rows_last_target; cols = H->d; break;
+    case DF_DBG_DRAFT_LAYERS: src = H->dbg_dl; rows = (H->Ld + 1) * H->rows_last_draft; cols = H->d; break;
     default: return fail(H, DF_EINVAL, "unknown debug buffer");
   }
   if (!src) return fail(H, DF_ESTATE, "debug buffers are off (df_debug_enable)");
@@ -1718,13 +1792,16 @@ df_status df_debug_weight_ptr(const df_handle* H, int32_t which, uint64_t* addr)
 }
 
 df_status df_profile_enable(df_handle* H, int32_t on) {
-  if (!H) return DF_EINVAL;
-  if (on && H->evpool.empty()) {
+  if (!H || on < 0 || on > 2) return DF_EINVAL;
+  if (on == 1 && H->evpool.empty()) {
     H->evpool.resize(EV_POOL, nullptr);
     for (auto& e : H->evpool) CK(cudaEventCreate(&e));
   }
-  if (!on) prof_resolve(H);
-  H->profiling = on != 0;
+  if (on == 2 && !H->d_trace) CKS(dalloc_t(H, &H->d_trace, TRACE_MAX * 16));
+  if (on != 1) prof_resolve(H);
+  H->profiling = on == 1;
+  H->tracing = on == 2;
+  H->trace_meta.clear();
   for (int c = 0; c < PC_N; ++c) {
     std::memset(H->prof[c].name, 0, 32);
     std::strncpy(H->prof[c].name, PC_NAMES[c], 31);

@@ -177,10 +177,9 @@ struct TcCfg {
 };
 
 template <int NT>
-__global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
-                                                      const __grid_constant__ CUtensorMap tmX, int M, int N, int K,
-                                                      int splits, float* __restrict__ ws, int* __restrict__ counters,
-                                                      int creduce, EpiParams ep) {
+__device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUtensorMap& tmX, int M, int N, int K,
+                                             int splits, float* __restrict__ ws, int* __restrict__ counters,
+                                             int creduce, const EpiParams& ep) {
   using C = TcCfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -422,6 +421,16 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
   }
   epilogue_tile<__nv_bfloat16>(ep, tile, C::TLD, n0, m0, rows, M, meta, red, /*staged=*/true,
                                (have_pre && splits == 1) ? &pre : nullptr);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                      const __grid_constant__ CUtensorMap tmX, int M, int N, int K,
+                                                      int splits, float* __restrict__ ws, int* __restrict__ counters,
+                                                      int creduce, EpiParams ep) {
+  trace_entry(ep.trace);
+  gemm_tc_body<NT>(tmW, tmX, M, N, K, splits, ws, counters, creduce, ep);
+  trace_exit(ep.trace);
 }
 
 // ----------------------------------------------------------------------------

@@ -97,6 +97,7 @@ struct AttnParams {
   float scale_log2;       // log2(e) / sqrt(hd)
   int* err;
   const void* kv_map;     // host copy of a TMA map of `cache` (make_tmap_kvcache), or null
+  unsigned long long* trace;  // in-situ timing of the launch (see trace_entry), or null
 };
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st);
 int attention_launches(const AttnParams& p, bool bf16);  // kernels one launch_attention call makes

@@ -118,8 +118,8 @@ typedef struct {
   int64_t block_hist[33];  /* cycles run at each block size (df_set_block_range) */
 } df_stats;
 
-/* Device time per kernel class, from CUDA events recorded on the engine's
- * stream around every launch while profiling is on (df_profile_enable).
+/* Device time per kernel class while profiling is on (df_profile_enable:
+ * CUDA events around every launch, or the in-situ device-timer stamps).
  * bytes / flops are ALGORITHMIC: weights + inputs + outputs each counted once
  * (for a GEMM: N*K weights, M*K inputs, M*N outputs; for attention: the
  * visible keys and values plus queries and outputs), not measured traffic. */
@@ -275,9 +275,21 @@ df_status df_seq_info(const df_handle* h, int32_t seq, int32_t* length, int32_t*
 void df_destroy(df_handle* h);
 const char* df_last_error(const df_handle* h);
 
-/* Kernel-class profiling (off by default).  While on, every launch is
- * bracketed by two CUDA events on the engine's stream; the events are read
- * at the next synchronising call.  df_profile_read fills up to max entries
+/* Kernel-class profiling (off by default), in one of two modes.
+ *   on = 1 (serialised): every launch is bracketed by two CUDA events on the
+ *     engine's stream (df_generate then launches its cycles directly, without
+ *     graphs); the events are read at the next synchronising call.  Launches
+ *     no longer overlap, so the times include each launch's ramp and tail.
+ *   on = 2 (in situ): df_generate's cycles run as usual (captured graphs,
+ *     programmatic dependent launch), and every GEMM and cluster-attention
+ *     launch of a cycle stamps the device timer at its first CTA's entry and
+ *     its last CTA's exit.  A cycle's timeline is cut at those exit stamps:
+ *     each launch is charged the time from the previous stamped exit (the
+ *     cycle's first entry for the first) to its own exit, so the classes add
+ *     up to the cycles' device time and kernels that are not stamped (norms,
+ *     embedding, control) are charged to the launch after them.  Only
+ *     draft + verify cycles are recorded (not prefill).
+ * on = 0 turns profiling off.  df_profile_read fills up to max entries
  * (classes: gemm (layer GEMMs), lm_head, fuse, inject, attention, rmsnorm,
  * embed, control) and clears them. */
 df_status df_profile_enable(df_handle* h, int32_t on);
@@ -292,7 +304,12 @@ df_status df_profile_read(df_handle* h, df_kernel_stat* out, int32_t max, int32_
  *   DF_DBG_DRAFT_HIDDEN  [rows][d]     drafter output before its final norm
  *   DF_DBG_CTX           [rows][d]     fused context features of the last injection
  *   DF_DBG_HIDDEN        [rows][d]     target output before the final norm
- * rows is the row count of that pass (*rows_out).  With debug on, the fused
+ *   DF_DBG_TARGET_LAYERS [L+1][M][d]   fp32 residual rows of the last target pass (M
+ *                                      rows) entering each of its L layers, then the
+ *                                      last layer's output (needs debug on)
+ *   DF_DBG_DRAFT_LAYERS  [Ld+1][M][d]  the same for the last drafter pass
+ * rows is the row count of that pass (*rows_out; (layers + 1) x M for the
+ * two per-layer buffers).  With debug on, the fused
  * LM-head argmax also stores the logits it reduces; off by default.
  * ------------------------------------------------------------------------ */
 enum {
@@ -301,7 +318,9 @@ enum {
   DF_DBG_DRAFT_LOGITS = 3,
   DF_DBG_DRAFT_HIDDEN = 4,
   DF_DBG_CTX = 5,
-  DF_DBG_HIDDEN = 6
+  DF_DBG_HIDDEN = 6,
+  DF_DBG_TARGET_LAYERS = 7,
+  DF_DBG_DRAFT_LAYERS = 8
 };
 df_status df_debug_enable(df_handle* h, int32_t on);
 df_status df_debug_read(df_handle* h, int32_t what, float* out_host, int64_t max_floats, int32_t* rows_out);
