@@ -19,6 +19,7 @@ DF_OK, DF_EINVAL, DF_ENOMEM, DF_ECUDA, DF_ETIMEOUT, DF_ESTATE = range(6)
 DF_FP32, DF_BF16 = 0, 1
 DF_DBG_TAPS, DF_DBG_LOGITS, DF_DBG_DRAFT_LOGITS, DF_DBG_DRAFT_HIDDEN, DF_DBG_CTX, DF_DBG_HIDDEN = 1, 2, 3, 4, 5, 6
 DF_DBG_TARGET_LAYERS, DF_DBG_DRAFT_LAYERS = 7, 8
+DF_ATTN_AUTO, DF_ATTN_MMA, DF_ATTN_PIPE = 0, 1, 2
 STATUS_NAMES = {0: "DF_OK", 1: "DF_EINVAL", 2: "DF_ENOMEM", 3: "DF_ECUDA", 4: "DF_ETIMEOUT", 5: "DF_ESTATE"}
 
 EXPORTED = [
@@ -29,7 +30,7 @@ EXPORTED = [
     "df_op_bench_gemm_bf16", "df_op_gemm_bf16_noalloc", "df_bench_drafter_step",
     "df_generate_sampled", "df_philox4x32_10", "df_op_philox_uniforms", "df_op_sampling_probs",
     "df_op_sample_draw", "df_op_accept_sampled", "df_set_block_range", "df_block_size_for",
-    "df_generate_accept_hist", "df_debug_wait_probe",
+    "df_generate_accept_hist", "df_debug_wait_probe", "df_op_attention_bf16",
 ]
 
 
@@ -46,7 +47,7 @@ class DfConfig(ctypes.Structure):
         ("vocab", ctypes.c_int32), ("draft_layers", ctypes.c_int32), ("block_size", ctypes.c_int32),
         ("feat_layers", ctypes.c_int32 * 5), ("max_batch", ctypes.c_int32), ("max_ctx", ctypes.c_int32),
         ("page_tokens", ctypes.c_int32), ("dtype", ctypes.c_int32), ("mask_token_id", ctypes.c_int32),
-        ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
+        ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("attn_kernel", ctypes.c_int32),
     ]
 
 
@@ -128,6 +129,7 @@ def lib() -> ctypes.CDLL:
     L.df_set_block_range.argtypes = [_P, _I, _I]
     L.df_generate_accept_hist.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_int64)]
     L.df_debug_wait_probe.argtypes = [_P]
+    L.df_op_attention_bf16.argtypes = [_P, _P, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]
     L.df_block_size_for.argtypes = [ctypes.c_double, _I, _I]
     L.df_block_size_for.restype = _I
     for name in EXPORTED:
@@ -155,7 +157,7 @@ def default_feat_layers(n_layers: int) -> List[int]:
 
 
 def make_config(shape, max_batch: int, max_ctx: int, page_tokens: int = 16,
-                feat_layers: Optional[Sequence[int]] = None) -> DfConfig:
+                feat_layers: Optional[Sequence[int]] = None, attn_kernel: int = DF_ATTN_AUTO) -> DfConfig:
     c = DfConfig()
     c.n_layers, c.d_model, c.n_q_heads = shape.n_layers, shape.d_model, shape.n_q_heads
     c.n_kv_heads, c.head_dim, c.d_ffn, c.vocab = shape.n_kv_heads, shape.head_dim, shape.d_ffn, shape.vocab
@@ -167,6 +169,7 @@ def make_config(shape, max_batch: int, max_ctx: int, page_tokens: int = 16,
     c.dtype = DF_BF16 if shape.dtype == "bf16" else DF_FP32
     c.mask_token_id = shape.vocab - 1
     c.rms_eps, c.rope_theta = shape.rms_eps, shape.rope_theta
+    c.attn_kernel = attn_kernel
     return c
 
 
@@ -199,11 +202,11 @@ class Engine:
 
     def __init__(self, shape, weights: Union[Dict[str, np.ndarray], Iterable[Tuple[str, np.ndarray]]],
                  max_batch: int = 1, max_ctx: int = 1024, page_tokens: int = 16,
-                 feat_layers: Optional[Sequence[int]] = None, stream=None):
+                 feat_layers: Optional[Sequence[int]] = None, stream=None, attn_kernel: int = DF_ATTN_AUTO):
         import torch
         self.L = lib()
         self.shape = shape
-        self.cfg = make_config(shape, max_batch, max_ctx, page_tokens, feat_layers)
+        self.cfg = make_config(shape, max_batch, max_ctx, page_tokens, feat_layers, attn_kernel)
         self.B = shape.block_size
         self.V = shape.vocab
         self.d = shape.d_model
@@ -419,6 +422,34 @@ def bench_gemm_bf16(x, w, iters: int = 20, splits: int = 0, token_tile: int = 0,
     if st != DF_OK:
         raise DfError(st, "df_op_bench_gemm_bf16")
     return us.value
+
+
+def attention_bf16(q, cache, page_table, row_pos, row_seq, nseq: int, rows_per_seq: int, n_kv_heads: int,
+                   causal: bool, max_len: int, blk=None, kernel: int = DF_ATTN_PIPE, out=None, err=None,
+                   stream=None):
+    """One attention launch on torch CUDA tensors (df_op_attention_bf16).
+    q: [rows, Hq*128] bf16; cache: [n_pages, 2, Hkv, 16, 128] bf16; page_table:
+    [slots, pt_stride] int32; row_pos, row_seq: [rows] int32; blk: [2, Hkv,
+    rows_cap, 128] bf16 for the drafter's block attention.  Returns (out, err)."""
+    import torch
+    assert q.dtype == torch.bfloat16 and cache.dtype == torch.bfloat16 and q.is_cuda and cache.is_cuda
+    rows = q.shape[0]
+    Hq = q.shape[1] // 128
+    assert rows == nseq * rows_per_seq and row_pos.numel() == rows and row_seq.numel() == rows
+    assert page_table.dtype == torch.int32 and row_pos.dtype == torch.int32 and row_seq.dtype == torch.int32
+    seq_cpu = row_seq.cpu()
+    assert int(seq_cpu.min()) >= 0 and int(seq_cpu.max()) < page_table.shape[0], "row_seq must index page_table"
+    out = torch.empty_like(q) if out is None else out
+    err = _err_word(q.device) if err is None else err
+    blk_p = _P(blk.data_ptr()) if blk is not None else None
+    rows_cap = blk.shape[2] if blk is not None else 0
+    st = lib().df_op_attention_bf16(_P(q.data_ptr()), _P(out.data_ptr()), _P(cache.data_ptr()), cache.shape[0],
+                                    _P(page_table.data_ptr()), page_table.shape[1], _P(row_pos.data_ptr()),
+                                    _P(row_seq.data_ptr()), blk_p, rows_cap, nseq, rows_per_seq, Hq, n_kv_heads,
+                                    1 if causal else 0, max_len, kernel, _P(err.data_ptr()), _stream(stream))
+    if st != DF_OK:
+        raise DfError(st, "df_op_attention_bf16")
+    return out, err
 
 
 def lmhead_argmax_bf16(x, w, stream=None):

@@ -260,6 +260,7 @@ static cudaError_t set_attn_attr() {
 cudaError_t attention_prepare() {
   cudaError_t e = attention_cluster_prepare();
   if (e != cudaSuccess) return e;
+  if ((e = attention_tp_prepare()) != cudaSuccess) return e;
 #define DF_ATTR(T, HD, Q) \
   if ((e = set_attn_attr<T, HD, Q>()) != cudaSuccess) return e;
   DF_ATTR(float, 64, 2) DF_ATTR(float, 64, 4) DF_ATTR(float, 64, 8) DF_ATTR(float, 64, 16)
@@ -307,6 +308,7 @@ cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st) {
       const char* e = getenv("DF_ATTN_TC");
       return e && e[0] == '1';
     }();
+    if (p.pipelined && !attn_split() && attention_cluster_fits(p)) return launch_attention_tp(p, st);
     if (use_tc && !attn_split() && attention_cluster_fits(p) && p.Hq / p.Hkv <= 4) return launch_attention_tc(p, st);
     if (!attn_split() && attention_cluster_fits(p)) return launch_attention_cluster(p, st);
     cudaError_t e = launch_attention_mma(p, st);

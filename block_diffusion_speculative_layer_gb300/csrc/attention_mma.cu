@@ -1139,13 +1139,504 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(AttnParams p, const __g
 }
 
 
+// ---------------------------------------------------------------------------
+// Pipelined tcgen05 attention (attn_tp_kernel): the chunks, staging and
+// cluster merge of attn_cl_kernel, with the per-chunk arithmetic on tcgen05
+// and the chunks in flight at once.  Warp roles in a CTA of six warps:
+//   warps 0-3  softmax: thread t owns tensor-memory lane t, i.e. MMA row t.
+//              Query head g, token row r sits at row (g & 3) * 32 + (g >> 2) * 16
+//              + r, so each warp holds the rows of one or two heads;
+//   warp 4     producer: the chunks' pages by TMA into TP_NST stages (the
+//              drafter's block rows by cp.async);
+//   warp 5     MMA issuer (one thread) and tensor-memory owner.
+// Per chunk i, the issuer computes S_i = Q K_i^T (M 128 rows, N 64 keys) into
+// one of two tensor-memory buffers, then O += P_i V_i once the softmax has
+// written P_i; S_{i+2} is issued right after P_i V_i, so the softmax of chunk
+// i+1 overlaps the tensor cores' work on chunks i and i+2.  The running maximum
+// is updated lazily: a chunk whose maximum exceeds it by at most 2^8 keeps it
+// (P values up to 256), otherwise O is rescaled in tensor memory once P_{i-1}
+// V_{i-1} has finished.  Every decision depends on the row's own scores only,
+// and rows that keep their scale multiply by exactly 1, so a row's bits do not
+// depend on the other rows of its tile or batch.
+constexpr int TP_NST = 4;                          // key/value stages
+constexpr int TP_QOFF = TP_NST * CL_STAGE;         // Q tile: two 64-dim halves x 128 rows x 128 B
+constexpr int TP_POFF = TP_QOFF + 2 * TC_QHALF;    // P tiles: two buffers x 128 rows x 128 B
+constexpr int TP_PGOFF = TP_POFF + 2 * 128 * 128;  // page ids of the CTA's chunks
+constexpr int TP_SMEM = TP_PGOFF + MAXPG * 4 + 1024;
+constexpr int TP_THREADS = 192;
+constexpr float TP_RESCALE = 8.f;                  // lazy rescale threshold (log2 units)
+static_assert(8 * 16 * TC_OLD * 4 + 8 * 16 * 8 <= TP_NST * CL_STAGE, "partials fit over the stages");
+static_assert(TP_SMEM <= 227 * 1024, "shared memory of one CTA");
+
+__device__ __forceinline__ void tp_mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void tp_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// A bounded wait whose outcome is the same for every lane of the warp (the
+// warp-collective tensor-memory loads after it need all 32 lanes).
+__device__ __forceinline__ bool tp_wait_warp(uint32_t bar, uint32_t parity, int* err) {
+  return __all_sync(0xffffffffu, cl_wait_bar(bar, parity, err)) != 0;
+}
+
+template <int CLA>
+__device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensorMap& kvmap) {
+  // Everything older than the key/value GEMM before this kernel is complete
+  // here (that GEMM triggers only after its own wait): the row metadata, the
+  // page table and older cache entries are read before the wait; the
+  // queries, this pass's keys and values and the block rows after it.
+  pdl_trigger();
+  extern __shared__ __align__(128) uint8_t smc_raw[];
+  uint8_t* smc = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smc_raw) + 1023) & ~uintptr_t(1023));
+  const int G = p.Hq / p.Hkv;
+  const int j = (int)cl_rank();
+  const int h = blockIdx.y;
+  const int qtiles = (p.rows_per_seq + 15) / 16;
+  const int z = blockIdx.z / qtiles;
+  const int qt = blockIdx.z % qtiles;
+  const int r0 = z * p.rows_per_seq + qt * 16;
+  const int nrows = min(16, p.rows_per_seq - qt * 16);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool causal = p.causal != 0;
+
+  // ---- the tile's rows: visible context length (-1: no position), longest
+  __shared__ int s_len[16];
+  __shared__ int s_first_new;  // cache positions from here on are written by this pass
+  if (threadIdx.x < 16) {
+    int l = -1;
+    if ((int)threadIdx.x < nrows && p.row_pos[r0 + threadIdx.x] >= 0) l = ctx_len_rows(p, r0 + threadIdx.x);
+    s_len[threadIdx.x] = l;
+  }
+  if (threadIdx.x == 32) {
+    const int f = p.row_pos[z * p.rows_per_seq];
+    s_first_new = causal ? (f >= 0 ? f : 0) : 0x7fffffff;
+  }
+  const int ppc = MC / p.page_tokens;
+  int* s_pg = reinterpret_cast<int*>(smc + TP_PGOFF);
+  const int seq_slot = p.row_seq[r0];
+  const int cap_chunks = (p.grid_chunks > j) ? (p.grid_chunks - j + CLA - 1) / CLA : 0;
+  for (int t = threadIdx.x; t < cap_chunks * ppc && t < MAXPG; t += blockDim.x) {
+    const int pg = (j + CLA * (t / ppc)) * ppc + t % ppc;  // page of the sequence
+    s_pg[t] = pg < p.pt_stride ? p.page_table[(size_t)seq_slot * p.pt_stride + pg] : -1;
+  }
+
+  __shared__ __align__(8) uint64_t s_full[TP_NST], s_empty[TP_NST], s_bs[2], s_bp[2], s_bpv[2], s_done;
+  __shared__ int s_failed;
+  __shared__ uint32_t s_tmem;
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < TP_NST; ++b) {
+      tp_mbar_init(smem_addr(&s_full[b]), 1);
+      tp_mbar_init(smem_addr(&s_empty[b]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tp_mbar_init(smem_addr(&s_bs[b]), 1);
+      tp_mbar_init(smem_addr(&s_bp[b]), 4);  // one arrival per softmax warp
+      tp_mbar_init(smem_addr(&s_bpv[b]), 1);
+    }
+    tp_mbar_init(smem_addr(&s_done), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kvmap)) : "memory");
+    s_failed = 0;
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_addr(&s_tmem))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = s_tmem;  // columns [0, 128): S buffers 0 and 1; [128, 256): O
+
+  int max_len = 0;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) max_len = max(max_len, s_len[r]);
+  const int first_new = s_first_new;
+  const int nA = (max_len + MC - 1) / MC;                       // context chunks of the tile
+  const int nmine = nA > j ? (nA - j + CLA - 1) / CLA : 0;       // this CTA's context chunks
+  const bool has_blk = !causal && j == CLA - 1;
+  const int nsteps = nmine + (has_blk ? 1 : 0);
+  const int PT = p.page_tokens;
+  const __nv_bfloat16* blk = reinterpret_cast<const __nv_bfloat16*>(p.blk);
+
+  if (warp == 4) {
+    // ================================================================ producer
+    // TMA of context chunk st into stage buf: part 1 = pages wholly before
+    // first_new (written by earlier passes), 2 = the rest, 3 = all; part 2 or
+    // 3 makes the stage barrier's one arrival.
+    auto stage_tma = [&](int st, int buf, int part) {
+      uint8_t* sK = smc + buf * CL_STAGE;
+      uint8_t* sV = sK + 2 * CL_HALF;
+      const uint32_t bar = smem_addr(&s_full[buf]);
+      const int key0 = (j + CLA * st) * MC;
+      const int npg = (min(MC, max_len - key0) + PT - 1) / PT;  // pages holding a key the tile can see
+      auto wanted = [&](int pg) {
+        const bool old = key0 + (pg + 1) * PT <= first_new;
+        const int page = s_pg[st * ppc + pg];
+        return ((old ? 1 : 2) & part) && page >= 0 && page < p.n_pages;
+      };
+      uint32_t bytes = 0;
+      for (int pg = 0; pg < npg; ++pg)
+        if (wanted(pg)) bytes += 4u * (uint32_t)PT * 128u;
+      if (part == 1) {
+        if (bytes) cl_expect_tx(bar, bytes);
+      } else {
+        cl_arrive_expect_tx(bar, bytes);
+      }
+      for (int pg = 0; pg < npg; ++pg) {
+        if (!wanted(pg)) continue;
+        const int page = s_pg[st * ppc + pg];
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+            tma_kv(smem_addr((kv ? sV : sK) + half * CL_HALF + pg * PT * 128), &kvmap, bar, half,
+                   (page * 2 + kv) * p.Hkv + h);
+      }
+    };
+    if (lane == 0)
+      for (int st = 0; st < TP_NST && st < nmine; ++st) stage_tma(st, st, 1);
+    pdl_wait();
+    int issued = 0;
+    for (int st = 0; st < nsteps; ++st) {
+      const int buf = st % TP_NST;
+      if (st >= TP_NST) {
+        // the stage is free once P V of chunk st - TP_NST has finished
+        bool ok = true;
+        if (lane == 0) ok = cl_wait_bar(smem_addr(&s_empty[buf]), (uint32_t)((st / TP_NST) - 1) & 1u, p.err);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok || *reinterpret_cast<volatile int*>(&s_failed)) {
+          s_failed = 1;
+          break;
+        }
+      }
+      if (st < nmine) {
+        if (lane == 0) stage_tma(st, buf, st < TP_NST ? 2 : 3);
+      } else {
+        // the drafter's block rows (keys past the block read as zeros)
+        uint8_t* sK = smc + buf * CL_STAGE;
+        uint8_t* sV = sK + 2 * CL_HALF;
+        for (int idx = lane; idx < MC * (MHD / 8); idx += 32) {
+          const int key = idx >> 4, b = idx & 15;
+          if (key < p.rows_per_seq) {
+            const int row = z * p.rows_per_seq + key;
+            cp_async16(smem_addr(sK) + swz2(key, b), blk + ((size_t)(0 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8);
+            cp_async16(smem_addr(sV) + swz2(key, b), blk + ((size_t)(1 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8);
+          } else {
+            *reinterpret_cast<uint4*>(sK + swz2(key, b)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sV + swz2(key, b)) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        cp_async_commit();
+        cp_async_wait_0();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) tp_arrive(smem_addr(&s_full[buf]));
+      }
+      issued = st + 1;
+    }
+    // leave no copy in flight: wait (bounded) for the last stages issued
+    if (lane == 0)
+      for (int st = max(0, issued - TP_NST); st < issued; ++st)
+        if (st < nmine) cl_wait_bar(smem_addr(&s_full[st % TP_NST]), (uint32_t)(st / TP_NST) & 1u, p.err);
+    __syncwarp();
+  } else if (warp == 5) {
+    // ================================================================ MMA issuer
+    asm volatile("bar.sync 1, 160;" ::: "memory");  // the Q tile is in shared memory
+    if (lane == 0 && nsteps > 0) {
+      const uint32_t qbase = smem_addr(smc + TP_QOFF);
+      auto issue_s = [&](int i) -> bool {
+        const int buf = i % TP_NST;
+        if (!cl_wait_bar(smem_addr(&s_full[buf]), (uint32_t)(i / TP_NST) & 1u, p.err)) return false;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t kbase = smem_addr(smc + buf * CL_STAGE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma(tmem + (uint32_t)(i & 1) * 64u, tc_desc(qbase + (kk >> 2) * TC_QHALF + (kk & 3) * 32, 16),
+                 tc_desc(kbase + (kk >> 2) * CL_HALF + (kk & 3) * 32, 16), TC_IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(smem_addr(&s_bs[i & 1]));
+        return true;
+      };
+      bool ok = issue_s(0);
+      if (ok && nsteps > 1) ok = issue_s(1);
+      for (int i = 0; ok && i < nsteps; ++i) {
+        if (!cl_wait_bar(smem_addr(&s_bp[i & 1]), (uint32_t)(i >> 1) & 1u, p.err)) {
+          ok = false;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t vbase = smem_addr(smc + (i % TP_NST) * CL_STAGE) + 2 * CL_HALF;
+        const uint32_t pbase = smem_addr(smc + TP_POFF + (i & 1) * 128 * 128);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma(tmem + 128u, tc_desc(pbase + kk * 32, 16), tc_desc(vbase + kk * 2048, CL_HALF), TC_IDESC_PV,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(smem_addr(&s_bpv[i & 1]));
+        tc_commit(smem_addr(&s_empty[i % TP_NST]));
+        if (i + 2 < nsteps) ok = issue_s(i + 2);
+      }
+      if (!ok) s_failed = 1;
+      // every MMA issued above has finished before tensor memory is freed
+      tc_commit(smem_addr(&s_done));
+      cl_wait_bar(smem_addr(&s_done), 0u, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ softmax
+    pdl_wait();
+    // Q as the A operand of S = Q K^T: 128 rows, two 64-dim halves, 128-byte swizzle;
+    // rows without a (head, token) read as zeros
+    uint8_t* sQ = smc + TP_QOFF;
+    for (int idx = threadIdx.x; idx < 128 * 16; idx += 128) {
+      const int row = idx >> 4, c = idx & 15;
+      const int g = (row >> 5) + 4 * ((row >> 4) & 1), r = row & 15;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (g < G && r < nrows && s_len[r] >= 0)
+        v = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + (size_t)(r0 + r) * p.Hq * MHD +
+                                            (size_t)(h * G + g) * MHD + c * 8);
+      *reinterpret_cast<uint4*>(sQ + (c >> 3) * TC_QHALF + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = v;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("bar.arrive 1, 160;" ::: "memory");
+
+    const int trow = threadIdx.x;  // tensor-memory lane = MMA row
+    const int g = warp + 4 * ((lane >> 4) & 1), r = lane & 15;
+    const bool row_ok = g < G && r < nrows && s_len[r] >= 0;
+    const int len = row_ok ? s_len[r] : 0;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool failed = false;
+    for (int i = 0; i < nsteps; ++i) {
+      const int sb = i & 1;
+      if (!tp_wait_warp(smem_addr(&s_bs[sb]), (uint32_t)(i >> 1) & 1u, p.err)) {
+        failed = true;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      float sv[64];
+      tc_ld64(tmem + lane_base + (uint32_t)sb * 64u, sv);
+      const bool is_blk = i >= nmine;
+      const int key0 = is_blk ? 0 : (j + CLA * i) * MC;
+      const int vis = !row_ok ? 0 : (is_blk ? p.rows_per_seq : len - key0);
+      float mc = -INFINITY;
+#pragma unroll
+      for (int kk = 0; kk < 64; ++kk) {
+        sv[kk] = (kk < vis) ? sv[kk] * p.scale_log2 : -INFINITY;
+        mc = fmaxf(mc, sv[kk]);
+      }
+      const bool resc = mc > m_run + TP_RESCALE;
+      const float m_new = resc ? mc : m_run;
+      const float alpha = resc ? exp2f(m_run - m_new) : 1.f;
+      float cs = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int kk = 0; kk < 64; kk += 2) {
+        const float e0 = (sv[kk] == -INFINITY) ? 0.f : exp2f(sv[kk] - m_new);
+        const float e1 = (sv[kk + 1] == -INFINITY) ? 0.f : exp2f(sv[kk + 1] - m_new);
+        cs += e0 + e1;
+        pk[kk >> 1] = pack_bf16(e0, e1);
+      }
+      l_run = l_run * alpha + cs;
+      m_run = m_new;
+      // values of keys the staged pages do not cover (past the tile's longest
+      // row, or a page the table does not hold) read as zeros in P V
+      if (!is_blk) {
+        const int nkeys = min(MC, max_len - key0);
+        bool partial = nkeys < MC;
+        for (int pg = 0; pg < (nkeys + PT - 1) / PT && !partial; ++pg) {
+          const int page = s_pg[i * ppc + pg];
+          partial = page < 0 || page >= p.n_pages;
+        }
+        if (partial) {
+          uint8_t* sV = smc + (i % TP_NST) * CL_STAGE + 2 * CL_HALF;
+          for (int idx = threadIdx.x; idx < MC * (MHD / 8); idx += 128) {
+            const int key = idx >> 4, b = idx & 15;
+            const int page = s_pg[i * ppc + key / PT];
+            const bool have = key < nkeys && page >= 0 && page < p.n_pages;
+            if (!have) {
+              if (key < nkeys && b == 0 && (key % PT) == 0) flag_error(p.err, ERR_BOUNDS);
+              *reinterpret_cast<uint4*>(sV + swz2(key, b)) = make_uint4(0, 0, 0, 0);
+            }
+          }
+        }
+      }
+      // the P buffer is free once P V of chunk i - 2 has finished
+      if (i >= 2 && !tp_wait_warp(smem_addr(&s_bpv[sb]), (uint32_t)((i - 2) >> 1) & 1u, p.err)) {
+        failed = true;
+        break;
+      }
+      // O rows rescaled in tensor memory (P V of chunk i - 1 finished first);
+      // warp-wide loads and stores, rows that keep their scale multiply by 1
+      if (i >= 1 && __any_sync(0xffffffffu, resc)) {
+        if (!tp_wait_warp(smem_addr(&s_bpv[(i - 1) & 1]), (uint32_t)((i - 1) >> 1) & 1u, p.err)) {
+          failed = true;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float ov[32];
+          tc_ld32(tmem + lane_base + 128u + 32u * c, ov);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+          tc_st32(tmem + lane_base + 128u + 32u * c, ov);
+        }
+      }
+      uint8_t* sP = smc + TP_POFF + sb * 128 * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(sP + trow * 128 + ((c ^ (trow & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) tp_arrive(smem_addr(&s_bp[sb]));
+    }
+    if (failed) s_failed = 1;
+    // the last P V
+    bool have_o = nsteps > 0 && !failed;
+    if (have_o && !tp_wait_warp(smem_addr(&s_bpv[(nsteps - 1) & 1]), (uint32_t)((nsteps - 1) >> 1) & 1u, p.err)) {
+      have_o = false;
+      s_failed = 1;
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    // the partial (running max, sum, unnormalised output) for the merge: wait
+    // until every warp's stages are consumed before writing over them
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+    float* sO = reinterpret_cast<float*>(smc);
+    float2* sML = reinterpret_cast<float2*>(smc + 8 * 16 * TC_OLD * 4);
+    float* dst = sO + (size_t)(g * 16 + r) * TC_OLD;
+    const bool any_o = __any_sync(0xffffffffu, have_o);
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      float ov[32];
+      if (any_o) {
+        tc_ld32(tmem + lane_base + 128u + 32u * c, ov);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ov[e] = 0.f;
+      }
+      if (row_ok) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(dst + 32 * c + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
+      }
+    }
+    if (row_ok) sML[g * 16 + r] = make_float2(m_run, l_run);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 5) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem) : "memory");
+  }
+  cl_arrive();
+  cl_wait();
+
+  // ---- merge: this CTA's share of the (head, row) pairs, 32 threads x 4 dims per pair
+  const float* sO = reinterpret_cast<const float*>(smc);
+  const float2* sML = reinterpret_cast<const float2*>(smc + 8 * 16 * TC_OLD * 4);
+  const int pairs = G * 16;
+  const int p0 = j * pairs / CLA, p1 = (j + 1) * pairs / CLA;
+  const uint32_t sO_s = smem_addr(sO), sML_s = smem_addr(sML);
+  for (int pp = p0 + warp; pp < p1; pp += TP_THREADS / 32) {
+    const int g = pp >> 4, rr = pp & 15;
+    if (rr >= nrows || s_len[rr] < 0) continue;
+    float2 ml[CLA];
+    float4 av[CLA];
+    // ranks without a chunk of this tile hold (-inf, 0, 0): their terms are
+    // exactly zero, so they are not read
+#pragma unroll
+    for (int i = 0; i < CLA; ++i) {
+      const bool held = i < nA || (!causal && i == CLA - 1);
+      ml[i] = held ? cl_ld2(cl_map(sML_s + (uint32_t)(g * 16 + rr) * 8u, (uint32_t)i)) : make_float2(-INFINITY, 0.f);
+      av[i] = held ? cl_ld4(cl_map(sO_s + (uint32_t)((g * 16 + rr) * TC_OLD + lane * 4) * 4u, (uint32_t)i))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < CLA; ++i) Mx = fmaxf(Mx, ml[i].x);
+    float L = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < CLA; ++i) {
+      const float w = (ml[i].x == -INFINITY) ? 0.f : exp2f(ml[i].x - Mx);
+      L = fmaf(ml[i].y, w, L);
+      a.x = fmaf(av[i].x, w, a.x);
+      a.y = fmaf(av[i].y, w, a.y);
+      a.z = fmaf(av[i].z, w, a.z);
+      a.w = fmaf(av[i].w, w, a.w);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)(r0 + rr) * p.Hq * MHD +
+                         (size_t)(h * G + g) * MHD + lane * 4;
+    uint2 packed;
+    packed.x = pack_bf16(a.x * inv, a.y * inv);
+    packed.y = pack_bf16(a.z * inv, a.w * inv);
+    *reinterpret_cast<uint2*>(out) = packed;
+  }
+  cl_arrive();  // this CTA's reads of the other partials are done
+  cl_wait();    // and nobody leaves while another CTA may still read its partial
+}
+
+template <int CLA>
+__global__ void __launch_bounds__(TP_THREADS, 1)
+    attn_tp_kernel(AttnParams p, const __grid_constant__ CUtensorMap kvmap) {
+  trace_entry(p.trace);
+  attn_tp_body<CLA>(p, kvmap);
+  trace_exit(p.trace);
+}
+
+static int g_cla_tp = 0;
+
+cudaError_t launch_attention_tp(const AttnParams& p, cudaStream_t st) {
+  if (!attention_cluster_fits(p)) return cudaErrorInvalidValue;
+  cudaError_t e = attention_tp_prepare();
+  if (e != cudaSuccess) return e;
+  // page ids a CTA stages for its chunks (the cluster's ranks take every g_cla_tp-th chunk)
+  const int per_cta = (p.grid_chunks + g_cla_tp - 1) / g_cla_tp;
+  if (per_cta * (MC / p.page_tokens) > MAXPG) return cudaErrorInvalidValue;
+  const int qtiles = (p.rows_per_seq + 15) / 16;
+  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(p.kv_map);
+  if (g_cla_tp == 16)
+    return launch_kcl(attn_tp_kernel<16>, dim3(16, p.Hkv, p.n_seqs * qtiles), dim3(TP_THREADS), (size_t)TP_SMEM, st,
+                      dim3(16, 1, 1), p, map);
+  return launch_kcl(attn_tp_kernel<8>, dim3(8, p.Hkv, p.n_seqs * qtiles), dim3(TP_THREADS), (size_t)TP_SMEM, st,
+                    dim3(8, 1, 1), p, map);
+}
+
+cudaError_t attention_tp_prepare() {
+  if (g_cla_tp) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(attn_tp_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tp_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
+  if (e != cudaSuccess) return e;
+  bool big = cudaFuncSetAttribute(attn_tp_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  if (big) {
+    cudaLaunchConfig_t c = {};
+    c.gridDim = dim3(16, 1, 1);
+    c.blockDim = dim3(TP_THREADS);
+    c.dynamicSmemBytes = TP_SMEM;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = 16;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    c.attrs = a;
+    c.numAttrs = 1;
+    int n = 0;
+    big = cudaOccupancyMaxActiveClusters(&n, attn_tp_kernel<16>, &c) == cudaSuccess && n > 0;
+  }
+  cudaGetLastError();
+  g_cla_tp = big ? 16 : 8;
+  return cudaSuccess;
+}
+
 static int g_cla_tc = 0;
 
 cudaError_t launch_attention_tc(const AttnParams& p, cudaStream_t st) {
   const int G = p.Hq / p.Hkv;
   if (!attention_cluster_fits(p) || G > 4) return cudaErrorInvalidValue;
-  const int per_cta = (p.grid_chunks + 15) / 16;
-  if (per_cta * (MC / p.page_tokens) > MAXPG) return cudaErrorInvalidValue;
   if (!g_cla_tc) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
@@ -1154,6 +1645,8 @@ cudaError_t launch_attention_tc(const AttnParams& p, cudaStream_t st) {
     cudaGetLastError();
     g_cla_tc = big ? 16 : 8;
   }
+  const int per_cta = (p.grid_chunks + g_cla_tc - 1) / g_cla_tc;  // page ids a CTA stages
+  if (per_cta * (MC / p.page_tokens) > MAXPG) return cudaErrorInvalidValue;
   const int qtiles = (p.rows_per_seq + 15) / 16;
   const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(p.kv_map);
   if (g_cla_tc == 16)

@@ -65,6 +65,7 @@ struct df_handle {
   size_t esz = 4;
   int d = 0, hd = 0, Hq = 0, Hkv = 0, F = 0, V = 0, L = 0, Ld = 0, B = 0, qdim = 0, kvdim = 0, qkv_n = 0;
   int sm_count = 152;
+  bool attn_pipe = false;  // bf16 attention on the pipelined tcgen05 kernel (df_config.attn_kernel)
   int split_target = 253;  // CTAs a split-K GEMM aims for (DF_SPLIT_CTAS overrides tc_split_target)
   int tap_of_layer[1024];  // zero-based layer index -> tap slot (or -1)
   int Mmax = 0;
@@ -369,6 +370,7 @@ df_status validate(const df_config* c, std::string& why) {
     if (i && c->feat_layers[i] <= c->feat_layers[i - 1]) return bad("feat_layers must increase");
   }
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.f)) return bad("bad rms_eps / rope_theta");
+  if (c->attn_kernel < DF_ATTN_AUTO || c->attn_kernel > DF_ATTN_PIPE) return bad("bad attn_kernel");
   return DF_OK;
 }
 
@@ -505,6 +507,7 @@ df_status attention(df_handle* H, int M, int R, int nseq, bool causal, const voi
   ProfScope ps(H, PC_ATTN, attention_launches(p, H->bf16), kv_bytes + qo_bytes,
                4.0 * M * H->qdim * (double)max_len);
   p.trace = ps.tp;
+  p.pipelined = H->attn_pipe ? 1 : 0;
   CK(launch_attention(p, H->bf16, H->st));
   return DF_OK;
 }
@@ -1403,6 +1406,7 @@ df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_we
   H->kvdim = H->Hkv * H->hd;
   H->qkv_n = H->qdim + 2 * H->kvdim;
   H->Mmax = std::max(std::min(PREFILL_CHUNK, cfg->max_ctx), cfg->max_batch * cfg->block_size);
+  H->attn_pipe = H->bf16 && cfg->attn_kernel == DF_ATTN_PIPE;
   {
     const char* g = getenv("DF_NO_GRAPH");
     H->use_graphs = !(g && g[0] == '1');
@@ -1948,6 +1952,54 @@ df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, in
   cudaFreeAsync(ws, st);
   cudaFreeAsync(cnt, st);
   return r == cudaSuccess ? DF_OK : DF_ECUDA;
+}
+
+df_status df_op_attention_bf16(const void* q_dev, void* out_dev, const void* cache_dev, int32_t n_pages,
+                               const int32_t* page_table_dev, int32_t pt_stride, const int32_t* row_pos_dev,
+                               const int32_t* row_seq_dev, const void* blk_dev, int32_t rows_cap, int32_t nseq,
+                               int32_t rows_per_seq, int32_t n_q_heads, int32_t n_kv_heads, int32_t causal,
+                               int32_t max_len, int32_t kernel, int32_t* err_dev, void* stream) {
+  if (!q_dev || !out_dev || !cache_dev || !page_table_dev || !row_pos_dev || !row_seq_dev || !err_dev) return DF_EINVAL;
+  if (n_pages < 1 || pt_stride < 1 || nseq < 1 || rows_per_seq < 1 || n_kv_heads < 1 || n_q_heads < n_kv_heads ||
+      n_q_heads % n_kv_heads || n_q_heads / n_kv_heads > 8 || max_len < 1 || (causal != 0 && causal != 1) ||
+      (kernel != DF_ATTN_MMA && kernel != DF_ATTN_PIPE))
+    return DF_EINVAL;
+  if ((long long)pt_stride * 16 < max_len) return DF_EINVAL;  // the page table cannot hold max_len positions
+  if (!causal && (!blk_dev || rows_per_seq > 64 || rows_cap < nseq * rows_per_seq)) return DF_EINVAL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Tmap map;
+  if (!make_tmap_kvcache(map.b, cache_dev, n_pages, n_kv_heads, 16)) return DF_EINVAL;
+  if (attention_prepare() != cudaSuccess) return DF_ECUDA;
+  AttnParams p{};
+  p.q = q_dev;
+  p.out = out_dev;
+  p.M = nseq * rows_per_seq;
+  p.rows_per_seq = rows_per_seq;
+  p.n_seqs = nseq;
+  p.Hq = n_q_heads;
+  p.Hkv = n_kv_heads;
+  p.hd = 128;
+  p.row_pos = row_pos_dev;
+  p.row_seq = row_seq_dev;
+  p.causal = causal;
+  p.cache = cache_dev;
+  p.page_table = page_table_dev;
+  p.pt_stride = pt_stride;
+  p.page_tokens = 16;
+  p.n_pages = n_pages;
+  p.blk = blk_dev;
+  p.rows_cap = rows_cap;
+  p.chunk = ATTN_CHUNK;
+  p.grid_chunks = (max_len + ATTN_CHUNK - 1) / ATTN_CHUNK;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
+  p.err = err_dev;
+  p.kv_map = map.b;
+  p.pipelined = kernel == DF_ATTN_PIPE ? 1 : 0;
+  if (!attention_cluster_fits(p)) return DF_EINVAL;
+  // one of the two cluster kernels, never the partial + merge path (which needs workspaces)
+  const cudaError_t e = p.pipelined ? launch_attention_tp(p, st) : launch_attention_cluster(p, st);
+  if (e == cudaErrorInvalidValue) return DF_EINVAL;
+  return e == cudaSuccess ? DF_OK : DF_ECUDA;
 }
 
 df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32_t* ids_dev, int32_t M, int32_t V,

@@ -98,6 +98,7 @@ struct AttnParams {
   int* err;
   const void* kv_map;     // host copy of a TMA map of `cache` (make_tmap_kvcache), or null
   unsigned long long* trace;  // in-situ timing of the launch (see trace_entry), or null
+  int pipelined;          // bf16: the pipelined tcgen05 kernel (attn_tp_kernel) instead of attn_cl_kernel
 };
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st);
 int attention_launches(const AttnParams& p, bool bf16);  // kernels one launch_attention call makes
@@ -107,6 +108,10 @@ cudaError_t attention_prepare();  // kernel attributes, once, before any stream 
 cudaError_t launch_attention_mma(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_attention_cluster(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_attention_tc(const AttnParams& p, cudaStream_t st);
+// The pipelined tcgen05 cluster kernel (warp-specialised: TMA producer, MMA
+// issuer, four softmax warps; S double-buffered in tensor memory).
+cudaError_t launch_attention_tp(const AttnParams& p, cudaStream_t st);
+cudaError_t attention_tp_prepare();  // kernel attributes, once, before any stream capture
 bool attention_cluster_fits(const AttnParams& p);  // shapes the cluster kernel takes
 cudaError_t attention_cluster_prepare();  // kernel attributes, once, before any stream capture
 // One kernel whose bounded wait on a barrier nothing completes runs out and

@@ -15,7 +15,12 @@
 // In host code the arrays' names are host-side stand-ins, not device
 // addresses, so the first call on each device looks their addresses up with
 // cudaGetSymbolAddress while that device is current, and every later call on
-// the device reuses them.
+// the device reuses them.  The addresses belong to the device's CUDA context:
+// after a reset of that context (cudaDeviceReset, or a new primary context)
+// the module is loaded again at other addresses, so the lookup is keyed on
+// the current context as well and repeated when it changes.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "dflash.h"
@@ -33,21 +38,46 @@ constexpr int kMaxDevices = 64;
 struct DeviceScratch {
   float* ws = nullptr;
   int* tickets = nullptr;
+  CUcontext ctx = nullptr;  // the context the addresses were looked up in
   bool ready = false;
 };
 
 std::mutex g_scratch_mu;
 DeviceScratch g_scratch[kMaxDevices];
 
-// Device addresses of the scratch arrays on the current device (looked up once per device).
+typedef CUresult (*PFN_ctxGetCurrent_t)(CUcontext*);
+
+// The current CUDA context (the runtime makes the device's primary context
+// current on first use), through the driver entry point the runtime exposes.
+cudaError_t current_context(CUcontext* ctx) {
+  static PFN_ctxGetCurrent_t fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return cudaErrorNotSupported;
+    fn = reinterpret_cast<PFN_ctxGetCurrent_t>(p);
+  }
+  *ctx = nullptr;
+  return fn(ctx) == CUDA_SUCCESS && *ctx ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device addresses of the scratch arrays in the current device's context
+// (looked up once per device and context).
 cudaError_t scratch_on_current_device(float** ws, int** tickets) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  e = cudaSetDevice(dev);  // makes the device's primary context current if it is not yet
+  if (e != cudaSuccess) return e;
+  CUcontext ctx = nullptr;
+  e = current_context(&ctx);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   DeviceScratch& s = g_scratch[dev];
-  if (!s.ready) {
+  if (!s.ready || s.ctx != ctx) {
     void* p = nullptr;
     void* q = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_ws);
@@ -56,6 +86,7 @@ cudaError_t scratch_on_current_device(float** ws, int** tickets) {
     if (e != cudaSuccess) return e;
     s.ws = static_cast<float*>(p);
     s.tickets = static_cast<int*>(q);
+    s.ctx = ctx;
     s.ready = true;
   }
   *ws = s.ws;

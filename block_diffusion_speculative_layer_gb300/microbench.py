@@ -7,6 +7,9 @@
   python -m block_diffusion_speculative_layer_gb300.microbench ar_proxy
   python -m block_diffusion_speculative_layer_gb300.microbench serving [--new 1024]
   python -m block_diffusion_speculative_layer_gb300.microbench dense27b [--new 1024]
+  python -m block_diffusion_speculative_layer_gb300.microbench profile_cycle [--ctx 1024] [--batch 1] [--vocab 4096]
+  python -m block_diffusion_speculative_layer_gb300.microbench attention [--ctx ...] [--batch ...] [--attn mma|pipe|auto]
+                                                                         [--causal] [--iters 5]
 
 Inputs are seeded synthetic bf16 (N(0,1) activations, N(0,0.02) weights)
 drawn on the GPU by torch.  For small shapes several weight copies are used
@@ -43,7 +46,8 @@ def drafter(a):
             shape = shape.replace(draft_layers=1, vocab=4096)
         d, kvd = shape.d_model, shape.kv_dim
         max_b = max(batches)
-        eng = dfl.Engine(shape, syn.iter_weights(shape), max_batch=max_b, max_ctx=max(ctxs) + 2 * B)
+        eng = dfl.Engine(shape, syn.iter_weights(shape), max_batch=max_b, max_ctx=max(ctxs) + 2 * B,
+                         attn_kernel=_attn(a))
         taps = syn.make_hidden(512, 5 * d).reshape(512, 5, d)   # N(0, 1) feature rows
         for C in ctxs:
             for nb in batches:
@@ -57,7 +61,7 @@ def drafter(a):
                 }
                 us = {"fuse": r["fuse_us"], "inject": r["inject_us"], "block_attention": r["block_attention_us"],
                       "lm_head": r["lm_head_us"]}
-                print(json.dumps({"op": "drafter_step", "block": B, "ctx": C, "batch": nb,
+                print(json.dumps({"op": "drafter_step", "block": B, "ctx": C, "batch": nb, "attn": a.attn,
                                   "us": {k: round(v, 2) for k, v in us.items()},
                                   "drafter_pass_us": round(r["drafter_pass_us"], 2),
                                   "total_us": round(sum(us.values()), 2),
@@ -90,7 +94,7 @@ def ar_proxy(a):
                       "note": "random weights: latency only; one drafter pass includes its LM head"}))
 
 
-def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None, sampling=None):
+def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None, sampling=None, attn=0):
     """One timed df_generate over a batch (device weights drawn on the GPU),
     after one untimed warm-up generation of 16 tokens.  block_range: (b_min,
     b_max) for df_set_block_range, or None for the configured block size.
@@ -102,7 +106,8 @@ def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None,
     import synthetic as syn
 
     t0 = time.time()
-    eng = dfl.Engine(shape, syn.iter_weights_device(shape), max_batch=len(prompts), max_ctx=max_ctx)
+    eng = dfl.Engine(shape, syn.iter_weights_device(shape), max_batch=len(prompts), max_ctx=max_ctx,
+                     attn_kernel=attn)
     torch.cuda.empty_cache()
     setup_s = time.time() - t0
     if block_range:
@@ -127,17 +132,20 @@ def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None,
     per_seq = eng.accept_hist_per_seq(len(prompts))
     eng.close()
     tokens = len(prompts) * n_new
-    print(json.dumps({"op": label, "config": config, "sequences": len(prompts), "new_tokens_each": n_new,
+    print(json.dumps({"op": label, "config": config, "attn_kernel": attn, "sequences": len(prompts),
+                      "new_tokens_each": n_new,
                       "tokens_per_s": tokens / secs, "wall_s": secs, "cycles": s2["cycles"],
-                      "mean_accept_len": s2["emitted_tokens"] / max(1, s2["cycles"] * len(prompts)),
+                      # the engine counts one cycle per sequence per draft + verify pass
+                      "mean_accept_len": s2["emitted_tokens"] / max(1, s2["cycles"]),
                       "accept_hist_k": {str(k): v for k, v in enumerate(hist) if v},
                       "accept_hist_k_per_sequence": [{str(k): int(v) for k, v in enumerate(h) if v} for h in per_seq],
                       "block_range": list(block_range) if block_range else None,
                       "sampling": {"temperature": sampling[0], "top_p": sampling[1], "seed": sampling[2]}
                       if sampling else None,
                       "block_hist": {str(b): v for b, v in enumerate(s2["block_hist"]) if v},
-                      "draft_us_per_cycle": s2["draft_us"] / max(1, s2["cycles"]),
-                      "verify_us_per_cycle": s2["verify_us"] / max(1, s2["cycles"]),
+                      # device time is summed once per cycle of the batch, cycles once per sequence
+                      "draft_us_per_cycle": s2["draft_us"] * len(prompts) / max(1, s2["cycles"]),
+                      "verify_us_per_cycle": s2["verify_us"] * len(prompts) / max(1, s2["cycles"]),
                       "prefill_us": s2["prefill_us"], "kernel_launches": s2["kernel_launches"],
                       "setup_s": setup_s, "data": "synthetic, weights drawn on the GPU (seeded), random prompt ids"}),
           flush=True)
@@ -154,7 +162,7 @@ def serving(a):
     max_ctx = ((int(max(lens)) + a.new + 16 + 2 * shape.block_size + 63) // 64) * 64
     _generation(shape, prompts, a.new, max_ctx, "serving_batch16",
                 "qwen3-8b-shape bf16, 16 sequences, prompts U[128,2048], block 16, %d new each" % a.new,
-                _block_range(a))
+                _block_range(a), attn=_attn(a))
 
 
 def sampled(a):
@@ -167,7 +175,7 @@ def sampled(a):
     prompts = [syn.make_prompt(shape, 512)]
     _generation(shape, prompts, a.new, 512 + a.new + 64, "sampled_bs1",
                 "qwen3-8b-shape bf16, batch 1, prompt 512, block 16, %d new, temperature %g, top_p %g"
-                % (a.new, T, top_p), _block_range(a), (T, top_p, 1))
+                % (a.new, T, top_p), _block_range(a), (T, top_p, 1), attn=_attn(a))
 
 
 def dense27b(a):
@@ -179,7 +187,131 @@ def dense27b(a):
     prompts = [syn.make_prompt(shape, 8192, stream=300 + i) for i in range(4)]
     max_ctx = ((8192 + a.new + 16 + 2 * shape.block_size + 63) // 64) * 64
     _generation(shape, prompts, a.new, max_ctx, "dense27b_batch4",
-                "27b-class bf16, batch 4, prompt 8192, block 16, %d new each" % a.new, _block_range(a))
+                "27b-class bf16, batch 4, prompt 8192, block 16, %d new each" % a.new, _block_range(a),
+                attn=_attn(a))
+
+
+def profile_cycle(a):
+    """Every kernel of one decode cycle, for profilers: the Qwen3-8B width and
+    heads with 8 target layers, 1 drafter layer and a vocabulary of --vocab
+    (weights drawn on the GPU), batch --batch with prompts of --ctx tokens, a
+    few cycles run one call at a time (df_draft_block, df_verify_accept),
+    cycle 2 inside the NVTX range "cycle".  Then the sampling operations on
+    fp32 logits of 16 rows x 151936 inside the NVTX range "sampling"."""
+    import numpy as np
+    import torch
+
+    import block_diffusion_speculative_layer_gb300 as dfl
+    import synthetic as syn
+
+    shape = syn.QWEN3_8B.replace(name="profile-cycle", n_layers=8, draft_layers=1, vocab=a.vocab)
+    nb, C = a.batch, a.ctx
+    eng = dfl.Engine(shape, syn.iter_weights_device(shape), max_batch=nb, max_ctx=C + 8 * shape.block_size,
+                     attn_kernel=_attn(a))
+    torch.cuda.empty_cache()
+    seqs = list(range(nb))
+    for i in seqs:
+        eng.prefill(i, syn.make_prompt(shape, C, stream=400 + i))
+    for c in range(4):
+        if c == 2:
+            torch.cuda.synchronize()
+            torch.cuda.nvtx.range_push("cycle")
+        eng.draft_block(seqs)
+        eng.verify_accept(seqs)
+        if c == 2:
+            torch.cuda.synchronize()
+            torch.cuda.nvtx.range_pop()
+    eng.close()
+    V, rows = 151936, 16
+    g = torch.Generator(device="cuda").manual_seed(5)
+    q = torch.randn(rows, V, device="cuda", generator=g) * 4.0
+    p = torch.randn(1, rows + 1, V, device="cuda", generator=g) * 4.0
+    u = dfl.philox_uniforms(1, 0, 0, rows)
+    for it in range(3):
+        if it == 2:
+            torch.cuda.synchronize()
+            torch.cuda.nvtx.range_push("sampling")
+        dfl.sampling_probs(q, 0.8, 0.95)
+        d = dfl.sample_draw(q, 0.8, 0.95, u)
+        dfl.accept_sampled(d.reshape(1, rows), q.reshape(1, rows, V), p, 0.8, 0.95,
+                           dfl.philox_uniforms(2, 0, 0, rows + 1).reshape(1, rows + 1))
+        if it == 2:
+            torch.cuda.synchronize()
+            torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    print(json.dumps({"op": "profile_cycle", "batch": nb, "ctx": C, "vocab": a.vocab, "ok": True}))
+
+
+def attention(a):
+    """One attention launch alone (df_op_attention_bf16) on the Qwen3-8B heads
+    (32 query / 8 KV x 128): the drafter's block attention over a context of
+    C positions plus its 16-row block (or, with --causal, the target's causal
+    attention of 16 verify rows), for each context and batch, on the
+    mma.sync and/or pipelined kernel.  Keys and values are random bf16 in a
+    paged cache with shuffled pages; L2 is flushed (a 256 MB write) before
+    every timed launch, and each launch is timed alone with CUDA events."""
+    import numpy as np
+    import torch
+
+    import block_diffusion_speculative_layer_gb300 as dfl
+
+    Hq, Hkv, R, PT = 32, 8, 16, 16
+    kernels = {"mma": [dfl.DF_ATTN_MMA], "pipe": [dfl.DF_ATTN_PIPE], "auto": [dfl.DF_ATTN_MMA, dfl.DF_ATTN_PIPE]}[a.attn]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(2)
+    peak = _hbm_peak()
+    for C in [int(x) for x in a.ctx.split(",")]:
+        for nb in [int(x) for x in a.batch.split(",")]:
+            need = C + (R if a.causal else 0)
+            ppseq = (need + PT - 1) // PT
+            n_pages = nb * ppseq
+            cache = torch.randn((n_pages, 2, Hkv, PT, 128), device="cuda", generator=g).to(torch.bfloat16)
+            perm = torch.randperm(n_pages, device="cuda", generator=g).to(torch.int32)
+            table = perm.reshape(nb, ppseq).contiguous()
+            q = torch.randn((nb * R, Hq * 128), device="cuda", generator=g).to(torch.bfloat16)
+            blk = torch.randn((2, Hkv, nb * R, 128), device="cuda", generator=g).to(torch.bfloat16)
+            pos = torch.tensor(np.concatenate([np.arange(C, C + R)] * nb), dtype=torch.int32, device="cuda")
+            seq = torch.tensor(np.repeat(np.arange(nb), R), dtype=torch.int32, device="cuda")
+            out = torch.empty_like(q)
+            torch.cuda.empty_cache()  # the fp32 draws' memory goes back before anything is timed or profiled
+            visible = C + R
+            byts = nb * visible * Hkv * 128 * 2 * 2 + 2 * nb * R * Hq * 128 * 2
+            for k in kernels:
+                def launch():
+                    dfl.attention_bf16(q, cache, table, pos, seq, nb, R, Hkv, a.causal, need,
+                                       blk=None if a.causal else blk, kernel=k, out=out)
+                for _ in range(a.warmup):
+                    launch()
+                ts = []
+                for _ in range(a.iters):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    launch()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1000.0)
+                us = float(np.median(ts))
+                print(json.dumps({"op": "attention", "kernel": "pipe" if k == dfl.DF_ATTN_PIPE else "mma",
+                                  "causal": bool(a.causal), "ctx": C, "batch": nb, "rows_per_seq": R,
+                                  "us": round(us, 2), "algorithmic_bytes": byts,
+                                  "GB/s": round(byts / (us * 1e-6) / 1e9, 1),
+                                  "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / peak, 3)}), flush=True)
+            del cache, perm, table, q, blk, out
+            torch.cuda.empty_cache()
+
+
+def _hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f)["hbm_gbs"]
+    return 6800.0
+
+
+def _attn(a):
+    """df_config.attn_kernel from --attn (auto, mma or pipe)."""
+    return {"auto": 0, "mma": 1, "pipe": 2}[a.attn]
 
 
 def _block_range(a):
@@ -196,7 +328,12 @@ def main():
     from block_diffusion_speculative_layer_gb300 import build
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["gemm", "lmhead", "drafter", "ar_proxy", "serving", "dense27b", "sampled"])
+    ap.add_argument("op", choices=["gemm", "lmhead", "drafter", "ar_proxy", "serving", "dense27b", "sampled",
+                                   "profile_cycle", "attention"])
+    ap.add_argument("--causal", action="store_true", help="attention: the target's causal verify rows")
+    ap.add_argument("--vocab", type=int, default=4096, help="profile_cycle: vocabulary")
+    ap.add_argument("--attn", default="auto", choices=["auto", "mma", "pipe"],
+                    help="attention kernel of the engine (df_config.attn_kernel)")
     ap.add_argument("--sampling", default="0.8,0.95", help="sampled: temperature,top_p")
     ap.add_argument("--new", type=int, default=1024, help="serving/dense27b: new tokens per sequence")
     ap.add_argument("--blocks", default="8,16")
@@ -221,6 +358,14 @@ def main():
         return
     if a.op == "sampled":
         sampled(a)
+        return
+    if a.op == "attention":
+        attention(a)
+        return
+    if a.op == "profile_cycle":
+        a.ctx = int(a.ctx.split(",")[0])
+        a.batch = int(a.batch.split(",")[0])
+        profile_cycle(a)
         return
     if a.op == "ar_proxy":
         ar_proxy(a)

@@ -91,6 +91,13 @@ typedef enum { DF_FP32 = 0, DF_BF16 = 1 } df_dtype;
  *                       weights and GEMM operands, fp32 accumulation,
  *                       fp32 residual stream).
  *   mask_token_id     : id embedded into the drafter's masked slots (vocab-1).
+ *   attn_kernel       : bf16 attention kernel for the whole handle (fixed, so
+ *                       that verification and greedy decoding stay bitwise
+ *                       equal): DF_ATTN_AUTO (0) = the measured faster one
+ *                       (today DF_ATTN_MMA everywhere), DF_ATTN_MMA (1) the
+ *                       mma.sync cluster kernel, DF_ATTN_PIPE (2) the
+ *                       warp-specialised tcgen05 cluster kernel.  The two
+ *                       round differently.
  */
 typedef struct {
   int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim, d_ffn, vocab;
@@ -100,7 +107,10 @@ typedef struct {
   int32_t dtype;
   int32_t mask_token_id;
   float rms_eps, rope_theta;
+  int32_t attn_kernel;
 } df_config;
+
+enum { DF_ATTN_AUTO = 0, DF_ATTN_MMA = 1, DF_ATTN_PIPE = 2 };
 
 /* Per-handle counters.  k = accepted drafts in a cycle; a cycle emits k+1
  * tokens, so the mean accepted length is (accepted_drafts + cycles) / cycles. */
@@ -350,6 +360,34 @@ df_status df_debug_weight_ptr(const df_handle* h, int32_t which, uint64_t* addr)
 df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, int32_t M, int32_t N, int32_t K,
                           int32_t splits, int32_t token_tile, void* stream);
 
+/* One attention launch of the engine on caller-owned device buffers: the
+ * causal attention of the target's verify pass or the drafter's block
+ * attention ([ARCH] 第三层 Block Diffusion and 稀疏注意力训练: the block sees
+ * the injected context before its anchor and, in both directions, its own
+ * block rows; nothing of another sequence).  bf16, head_dim 128, 16-token
+ * pages, scale 1/sqrt(128), fp32 softmax.
+ *   q_dev / out_dev  [nseq * rows_per_seq][n_q_heads * 128] (rows sequence-major)
+ *   cache_dev        one layer of the paged cache: [n_pages][k|v][n_kv_heads][16][128]
+ *   page_table_dev   [slots][pt_stride]: page ids of each slot's positions 0, 16, 32, ...
+ *   row_pos_dev      [rows]: each row's absolute position (< 0: row skipped)
+ *   row_seq_dev      [rows]: each row's slot in the page table
+ *   blk_dev          causal == 0: the block rows' keys and values
+ *                    [k|v][n_kv_heads][rows_cap][128] (rows_cap >= rows); else ignored
+ *   causal           1: row at position p sees cache positions 0..p;
+ *                    0: row j of a block anchored at a sees cache positions
+ *                    0..a-1 and every row of its own block (rows_per_seq <= 64)
+ *   max_len          bound on the cache positions any row sees (sets the grid)
+ *   kernel           DF_ATTN_MMA or DF_ATTN_PIPE (see df_config.attn_kernel)
+ *   err_dev          device int receiving the kernels' sticky error bits
+ *                    (1: a bounded wait ran out, 2: a page id outside the cache)
+ * Query heads per KV head <= 8.  Stream-ordered, no synchronisation, no
+ * allocation; DF_EINVAL for shapes the cluster kernels do not take. */
+df_status df_op_attention_bf16(const void* q_dev, void* out_dev, const void* cache_dev, int32_t n_pages,
+                               const int32_t* page_table_dev, int32_t pt_stride, const int32_t* row_pos_dev,
+                               const int32_t* row_seq_dev, const void* blk_dev, int32_t rows_cap, int32_t nseq,
+                               int32_t rows_per_seq, int32_t n_q_heads, int32_t n_kv_heads, int32_t causal,
+                               int32_t max_len, int32_t kernel, int32_t* err_dev, void* stream);
+
 /* ids[m] = argmax_v (x[m] . w_lm[v]) over V rows of w_lm (bf16 [V][K]),
  * fp32 logits, lowest index on ties; logits are never written.  V % 128 == 0. */
 df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32_t* ids_dev, int32_t M, int32_t V,
@@ -368,7 +406,10 @@ df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32
  * launching anything, when the shape's split-K scratch (tiles x splits x
  * token tile x 128 floats) or its ticket count exceeds those limits.
  * The first call on a device looks up the scratch's device address with that
- * device current; make that first call before any stream capture.  All calls
+ * device current; make that first call before any stream capture.  The
+ * address belongs to the device's CUDA context: after that context is reset
+ * (cudaDeviceReset) the next call looks it up again, so make that call
+ * before any capture too.  All calls
  * on a device share the one scratch, which keeps the last call's contents
  * (the tickets a call uses are cleared on its stream first): calls that can
  * overlap on the GPU (different streams without ordering) race and must not
