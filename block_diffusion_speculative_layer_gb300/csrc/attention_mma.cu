@@ -16,6 +16,7 @@
 // (quad shuffles), P kept in registers as the A operand of P V (64 MMAs), fp32
 // accumulators.  A row's arithmetic never depends on the other rows.
 #include <cuda.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -55,6 +56,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// 2^x on the special-function unit (ex2.approx, flush to zero): 2^-inf = +0,
+// so masked scores need no branch.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Lazy rescale threshold (log2 units): a chunk whose largest scaled score
+// exceeds the running maximum by at most this keeps the maximum (its
+// probabilities may reach 2^8), so the running output is rescaled only when
+// a much larger score appears.  The decision depends on the row alone.
+constexpr float ATT_RESCALE = 8.f;
+
 // Byte offset of (key, 16-byte column block) in a swizzled [MC][MHD] tile.
 __device__ __forceinline__ uint32_t swz(int key, int blk) { return (uint32_t)(key * ROWB + ((blk ^ (key & 7)) << 4)); }
 
@@ -584,36 +598,56 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
           mma_16816(s[nt], qa[2 * kp + 1], b2, b3);
         }
       }
-      float mc_lo = -INFINITY, mc_hi = -INFINITY;
+      if (vis_lo < MC || vis_hi < MC) {  // keys a row cannot see score -inf (full chunks skip this)
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+        for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int kk = nt * 8 + tig * 2 + e;
-          s[nt][e] = (kk < vis_lo) ? s[nt][e] * p.scale_log2 : -INFINITY;
-          s[nt][2 + e] = (kk < vis_hi) ? s[nt][2 + e] * p.scale_log2 : -INFINITY;
-          mc_lo = fmaxf(mc_lo, s[nt][e]);
-          mc_hi = fmaxf(mc_hi, s[nt][2 + e]);
+          for (int e = 0; e < 2; ++e) {
+            const int kk = nt * 8 + tig * 2 + e;
+            if (kk >= vis_lo) s[nt][e] = -INFINITY;
+            if (kk >= vis_hi) s[nt][2 + e] = -INFINITY;
+          }
         }
       }
+      // raw row maxima (two chains per row), then over the quad, scaled once (scale > 0)
+      float ma_lo = fmaxf(s[0][0], s[0][1]), mb_lo = fmaxf(s[1][0], s[1][1]);
+      float ma_hi = fmaxf(s[0][2], s[0][3]), mb_hi = fmaxf(s[1][2], s[1][3]);
+#pragma unroll
+      for (int nt = 2; nt < 8; nt += 2) {
+        ma_lo = fmaxf(ma_lo, fmaxf(s[nt][0], s[nt][1]));
+        mb_lo = fmaxf(mb_lo, fmaxf(s[nt + 1][0], s[nt + 1][1]));
+        ma_hi = fmaxf(ma_hi, fmaxf(s[nt][2], s[nt][3]));
+        mb_hi = fmaxf(mb_hi, fmaxf(s[nt + 1][2], s[nt + 1][3]));
+      }
+      float mc_lo = fmaxf(ma_lo, mb_lo), mc_hi = fmaxf(ma_hi, mb_hi);
       mc_lo = fmaxf(mc_lo, __shfl_xor_sync(0xffffffffu, mc_lo, 1));
       mc_lo = fmaxf(mc_lo, __shfl_xor_sync(0xffffffffu, mc_lo, 2));
       mc_hi = fmaxf(mc_hi, __shfl_xor_sync(0xffffffffu, mc_hi, 1));
       mc_hi = fmaxf(mc_hi, __shfl_xor_sync(0xffffffffu, mc_hi, 2));
-      const float mn_lo = fmaxf(m_lo, mc_lo), mn_hi = fmaxf(m_hi, mc_hi);
-      // rescale of the running state (exactly 1 when this chunk shows the row nothing new)
-      const float a_lo = (mn_lo == -INFINITY) ? 1.f : exp2f(m_lo - mn_lo);
-      const float a_hi = (mn_hi == -INFINITY) ? 1.f : exp2f(m_hi - mn_hi);
-      float cs_lo = 0.f, cs_hi = 0.f;
+      mc_lo *= p.scale_log2;
+      mc_hi *= p.scale_log2;
+      // lazy rescale: the running maximum moves only for a much larger score
+      const bool rs_lo = mc_lo > m_lo + ATT_RESCALE, rs_hi = mc_hi > m_hi + ATT_RESCALE;
+      const float mn_lo = rs_lo ? mc_lo : m_lo, mn_hi = rs_hi ? mc_hi : m_hi;
+      const float a_lo = rs_lo ? ex2_fast(m_lo - mn_lo) : 1.f;  // 0 for a row's first visible chunk
+      const float a_hi = rs_hi ? ex2_fast(m_hi - mn_hi) : 1.f;
+      const float ng_lo = (mn_lo == -INFINITY) ? 0.f : -mn_lo, ng_hi = (mn_hi == -INFINITY) ? 0.f : -mn_hi;
+      float cs_lo = 0.f, cs_hi = 0.f, cs2_lo = 0.f, cs2_hi = 0.f;
       uint32_t pa[4][4];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        const float p0 = (s[nt][0] == -INFINITY) ? 0.f : exp2f(s[nt][0] - mn_lo);
-        const float p1 = (s[nt][1] == -INFINITY) ? 0.f : exp2f(s[nt][1] - mn_lo);
-        const float p2 = (s[nt][2] == -INFINITY) ? 0.f : exp2f(s[nt][2] - mn_hi);
-        const float p3 = (s[nt][3] == -INFINITY) ? 0.f : exp2f(s[nt][3] - mn_hi);
-        cs_lo += p0 + p1;
-        cs_hi += p2 + p3;
+        // P = 2^(s * scale - m): one FFMA and one ex2 per score (2^-inf = 0)
+        const float p0 = ex2_fast(fmaf(s[nt][0], p.scale_log2, ng_lo));
+        const float p1 = ex2_fast(fmaf(s[nt][1], p.scale_log2, ng_lo));
+        const float p2 = ex2_fast(fmaf(s[nt][2], p.scale_log2, ng_hi));
+        const float p3 = ex2_fast(fmaf(s[nt][3], p.scale_log2, ng_hi));
+        if (nt & 1) {
+          cs2_lo += p0 + p1;
+          cs2_hi += p2 + p3;
+        } else {
+          cs_lo += p0 + p1;
+          cs_hi += p2 + p3;
+        }
         const int kk = nt >> 1;
         if ((nt & 1) == 0) {
           pa[kk][0] = pack_bf16(p0, p1);
@@ -623,6 +657,8 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
           pa[kk][3] = pack_bf16(p2, p3);
         }
       }
+      cs_lo += cs2_lo;
+      cs_hi += cs2_hi;
       cs_lo += __shfl_xor_sync(0xffffffffu, cs_lo, 1);
       cs_lo += __shfl_xor_sync(0xffffffffu, cs_lo, 2);
       cs_hi += __shfl_xor_sync(0xffffffffu, cs_hi, 1);
@@ -631,12 +667,14 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
       l_hi = l_hi * a_hi + cs_hi;
       m_lo = mn_lo;
       m_hi = mn_hi;
+      if (__any_sync(0xffffffffu, rs_lo || rs_hi)) {  // rows that keep their scale multiply by exactly 1
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        o[nt][0] *= a_lo;
-        o[nt][1] *= a_lo;
-        o[nt][2] *= a_hi;
-        o[nt][3] *= a_hi;
+        for (int nt = 0; nt < 16; ++nt) {
+          o[nt][0] *= a_lo;
+          o[nt][1] *= a_lo;
+          o[nt][2] *= a_hi;
+          o[nt][3] *= a_hi;
+        }
       }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -1146,13 +1184,16 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(AttnParams p, const __g
 //   warps 0-3  softmax: thread t owns tensor-memory lane t, i.e. MMA row t.
 //              Query head g, token row r sits at row (g & 3) * 32 + (g >> 2) * 16
 //              + r, so each warp holds the rows of one or two heads;
-//   warp 4     producer: the chunks' pages by TMA into TP_NST stages (the
-//              drafter's block rows by cp.async);
+//   warps 4, 6 producers: the chunks' key pages (warp 4) and value pages
+//              (warp 6) by TMA into TP_NST stages, each with its own
+//              barriers (the drafter's block rows by cp.async);
 //   warp 5     MMA issuer (one thread) and tensor-memory owner.
 // Per chunk i, the issuer computes S_i = Q K_i^T (M 128 rows, N 64 keys) into
 // one of two tensor-memory buffers, then O += P_i V_i once the softmax has
 // written P_i; S_{i+2} is issued right after P_i V_i, so the softmax of chunk
-// i+1 overlaps the tensor cores' work on chunks i and i+2.  The running maximum
+// i+1 overlaps the tensor cores' work on chunks i and i+2.  A key tile is
+// released when S_i has read it and a value tile when P_i V_i has, so each
+// load has about TP_NST chunks' time to land.  The running maximum
 // is updated lazily: a chunk whose maximum exceeds it by at most 2^8 keeps it
 // (P values up to 256), otherwise O is rescaled in tensor memory once P_{i-1}
 // V_{i-1} has finished.  Every decision depends on the row's own scores only,
@@ -1163,8 +1204,8 @@ constexpr int TP_QOFF = TP_NST * CL_STAGE;         // Q tile: two 64-dim halves 
 constexpr int TP_POFF = TP_QOFF + 2 * TC_QHALF;    // P tiles: two buffers x 128 rows x 128 B
 constexpr int TP_PGOFF = TP_POFF + 2 * 128 * 128;  // page ids of the CTA's chunks
 constexpr int TP_SMEM = TP_PGOFF + MAXPG * 4 + 1024;
-constexpr int TP_THREADS = 192;
-constexpr float TP_RESCALE = 8.f;                  // lazy rescale threshold (log2 units)
+constexpr int TP_THREADS = 224;
+constexpr float TP_RESCALE = ATT_RESCALE;          // lazy rescale threshold (log2 units)
 static_assert(8 * 16 * TC_OLD * 4 + 8 * 16 * 8 <= TP_NST * CL_STAGE, "partials fit over the stages");
 static_assert(TP_SMEM <= 227 * 1024, "shared memory of one CTA");
 
@@ -1221,13 +1262,17 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
     s_pg[t] = pg < p.pt_stride ? p.page_table[(size_t)seq_slot * p.pt_stride + pg] : -1;
   }
 
-  __shared__ __align__(8) uint64_t s_full[TP_NST], s_empty[TP_NST], s_bs[2], s_bp[2], s_bpv[2], s_done;
+  // full / empty barriers of the key (k) and value (v) tiles of each stage
+  __shared__ __align__(8) uint64_t s_fk[TP_NST], s_fv[TP_NST], s_ek[TP_NST], s_ev[TP_NST];
+  __shared__ __align__(8) uint64_t s_bs[2], s_bp[2], s_bpv[2], s_done;
   __shared__ int s_failed;
   __shared__ uint32_t s_tmem;
   if (threadIdx.x == 0) {
     for (int b = 0; b < TP_NST; ++b) {
-      tp_mbar_init(smem_addr(&s_full[b]), 1);
-      tp_mbar_init(smem_addr(&s_empty[b]), 1);
+      tp_mbar_init(smem_addr(&s_fk[b]), 1);
+      tp_mbar_init(smem_addr(&s_fv[b]), 1);
+      tp_mbar_init(smem_addr(&s_ek[b]), 1);
+      tp_mbar_init(smem_addr(&s_ev[b]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       tp_mbar_init(smem_addr(&s_bs[b]), 1);
@@ -1260,15 +1305,18 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
   const int PT = p.page_tokens;
   const __nv_bfloat16* blk = reinterpret_cast<const __nv_bfloat16*>(p.blk);
 
-  if (warp == 4) {
-    // ================================================================ producer
-    // TMA of context chunk st into stage buf: part 1 = pages wholly before
-    // first_new (written by earlier passes), 2 = the rest, 3 = all; part 2 or
-    // 3 makes the stage barrier's one arrival.
+  if (warp == 4 || warp == 6) {
+    // ================================================================ producers
+    // warp 4 stages the key tiles, warp 6 the value tiles.  TMA of context
+    // chunk st into stage buf: part 1 = pages wholly before first_new (written
+    // by earlier passes), 2 = the rest, 3 = all; part 2 or 3 makes the tile
+    // barrier's one arrival.
+    const int kv = warp == 4 ? 0 : 1;
+    uint64_t* fullb = kv ? s_fv : s_fk;
+    uint64_t* emptyb = kv ? s_ev : s_ek;
     auto stage_tma = [&](int st, int buf, int part) {
-      uint8_t* sK = smc + buf * CL_STAGE;
-      uint8_t* sV = sK + 2 * CL_HALF;
-      const uint32_t bar = smem_addr(&s_full[buf]);
+      uint8_t* sT = smc + buf * CL_STAGE + kv * 2 * CL_HALF;
+      const uint32_t bar = smem_addr(&fullb[buf]);
       const int key0 = (j + CLA * st) * MC;
       const int npg = (min(MC, max_len - key0) + PT - 1) / PT;  // pages holding a key the tile can see
       auto wanted = [&](int pg) {
@@ -1278,7 +1326,7 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
       };
       uint32_t bytes = 0;
       for (int pg = 0; pg < npg; ++pg)
-        if (wanted(pg)) bytes += 4u * (uint32_t)PT * 128u;
+        if (wanted(pg)) bytes += 2u * (uint32_t)PT * 128u;
       if (part == 1) {
         if (bytes) cl_expect_tx(bar, bytes);
       } else {
@@ -1288,11 +1336,8 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
         if (!wanted(pg)) continue;
         const int page = s_pg[st * ppc + pg];
 #pragma unroll
-        for (int kv = 0; kv < 2; ++kv)
-#pragma unroll
-          for (int half = 0; half < 2; ++half)
-            tma_kv(smem_addr((kv ? sV : sK) + half * CL_HALF + pg * PT * 128), &kvmap, bar, half,
-                   (page * 2 + kv) * p.Hkv + h);
+        for (int half = 0; half < 2; ++half)
+          tma_kv(smem_addr(sT + half * CL_HALF + pg * PT * 128), &kvmap, bar, half, (page * 2 + kv) * p.Hkv + h);
       }
     };
     if (lane == 0)
@@ -1302,9 +1347,9 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
     for (int st = 0; st < nsteps; ++st) {
       const int buf = st % TP_NST;
       if (st >= TP_NST) {
-        // the stage is free once P V of chunk st - TP_NST has finished
+        // the tile is free once chunk st - TP_NST's S (keys) or P V (values) has finished
         bool ok = true;
-        if (lane == 0) ok = cl_wait_bar(smem_addr(&s_empty[buf]), (uint32_t)((st / TP_NST) - 1) & 1u, p.err);
+        if (lane == 0) ok = cl_wait_bar(smem_addr(&emptyb[buf]), (uint32_t)((st / TP_NST) - 1) & 1u, p.err);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok || *reinterpret_cast<volatile int*>(&s_failed)) {
           s_failed = 1;
@@ -1315,31 +1360,28 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
         if (lane == 0) stage_tma(st, buf, st < TP_NST ? 2 : 3);
       } else {
         // the drafter's block rows (keys past the block read as zeros)
-        uint8_t* sK = smc + buf * CL_STAGE;
-        uint8_t* sV = sK + 2 * CL_HALF;
+        uint8_t* sT = smc + buf * CL_STAGE + kv * 2 * CL_HALF;
         for (int idx = lane; idx < MC * (MHD / 8); idx += 32) {
           const int key = idx >> 4, b = idx & 15;
           if (key < p.rows_per_seq) {
             const int row = z * p.rows_per_seq + key;
-            cp_async16(smem_addr(sK) + swz2(key, b), blk + ((size_t)(0 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8);
-            cp_async16(smem_addr(sV) + swz2(key, b), blk + ((size_t)(1 * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8);
+            cp_async16(smem_addr(sT) + swz2(key, b), blk + ((size_t)(kv * p.Hkv + h) * p.rows_cap + row) * MHD + b * 8);
           } else {
-            *reinterpret_cast<uint4*>(sK + swz2(key, b)) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(sV + swz2(key, b)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sT + swz2(key, b)) = make_uint4(0, 0, 0, 0);
           }
         }
         cp_async_commit();
         cp_async_wait_0();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) tp_arrive(smem_addr(&s_full[buf]));
+        if (lane == 0) tp_arrive(smem_addr(&fullb[buf]));
       }
       issued = st + 1;
     }
-    // leave no copy in flight: wait (bounded) for the last stages issued
+    // leave no copy in flight: wait (bounded) for the last tiles issued
     if (lane == 0)
       for (int st = max(0, issued - TP_NST); st < issued; ++st)
-        if (st < nmine) cl_wait_bar(smem_addr(&s_full[st % TP_NST]), (uint32_t)(st / TP_NST) & 1u, p.err);
+        if (st < nmine) cl_wait_bar(smem_addr(&fullb[st % TP_NST]), (uint32_t)(st / TP_NST) & 1u, p.err);
     __syncwarp();
   } else if (warp == 5) {
     // ================================================================ MMA issuer
@@ -1348,7 +1390,7 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
       const uint32_t qbase = smem_addr(smc + TP_QOFF);
       auto issue_s = [&](int i) -> bool {
         const int buf = i % TP_NST;
-        if (!cl_wait_bar(smem_addr(&s_full[buf]), (uint32_t)(i / TP_NST) & 1u, p.err)) return false;
+        if (!cl_wait_bar(smem_addr(&s_fk[buf]), (uint32_t)(i / TP_NST) & 1u, p.err)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t kbase = smem_addr(smc + buf * CL_STAGE);
 #pragma unroll
@@ -1356,12 +1398,14 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
           tc_mma(tmem + (uint32_t)(i & 1) * 64u, tc_desc(qbase + (kk >> 2) * TC_QHALF + (kk & 3) * 32, 16),
                  tc_desc(kbase + (kk >> 2) * CL_HALF + (kk & 3) * 32, 16), TC_IDESC_S, kk > 0 ? 1u : 0u);
         tc_commit(smem_addr(&s_bs[i & 1]));
+        tc_commit(smem_addr(&s_ek[buf]));  // the key tile is free once S_i has read it
         return true;
       };
       bool ok = issue_s(0);
       if (ok && nsteps > 1) ok = issue_s(1);
       for (int i = 0; ok && i < nsteps; ++i) {
-        if (!cl_wait_bar(smem_addr(&s_bp[i & 1]), (uint32_t)(i >> 1) & 1u, p.err)) {
+        if (!cl_wait_bar(smem_addr(&s_bp[i & 1]), (uint32_t)(i >> 1) & 1u, p.err) ||
+            !cl_wait_bar(smem_addr(&s_fv[i % TP_NST]), (uint32_t)(i / TP_NST) & 1u, p.err)) {
           ok = false;
           break;
         }
@@ -1373,7 +1417,7 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
           tc_mma(tmem + 128u, tc_desc(pbase + kk * 32, 16), tc_desc(vbase + kk * 2048, CL_HALF), TC_IDESC_PV,
                  (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(smem_addr(&s_bpv[i & 1]));
-        tc_commit(smem_addr(&s_empty[i % TP_NST]));
+        tc_commit(smem_addr(&s_ev[i % TP_NST]));  // the value tile is free once P_i V_i has read it
         if (i + 2 < nsteps) ok = issue_s(i + 2);
       }
       if (!ok) s_failed = 1;
@@ -1419,24 +1463,41 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
       const bool is_blk = i >= nmine;
       const int key0 = is_blk ? 0 : (j + CLA * i) * MC;
       const int vis = !row_ok ? 0 : (is_blk ? p.rows_per_seq : len - key0);
-      float mc = -INFINITY;
+      if (vis < 64) {  // keys the row cannot see score -inf (full chunks skip this)
 #pragma unroll
-      for (int kk = 0; kk < 64; ++kk) {
-        sv[kk] = (kk < vis) ? sv[kk] * p.scale_log2 : -INFINITY;
-        mc = fmaxf(mc, sv[kk]);
+        for (int kk = 0; kk < 64; ++kk) sv[kk] = (kk < vis) ? sv[kk] : -INFINITY;
       }
+      // the raw maximum in four independent chains, scaled once (scale > 0)
+      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+#pragma unroll
+      for (int kk = 4; kk < 64; kk += 4) {
+        mx0 = fmaxf(mx0, sv[kk]);
+        mx1 = fmaxf(mx1, sv[kk + 1]);
+        mx2 = fmaxf(mx2, sv[kk + 2]);
+        mx3 = fmaxf(mx3, sv[kk + 3]);
+      }
+      const float mc = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
       const bool resc = mc > m_run + TP_RESCALE;
       const float m_new = resc ? mc : m_run;
-      const float alpha = resc ? exp2f(m_run - m_new) : 1.f;
-      float cs = 0.f;
+      const float alpha = resc ? ex2_fast(m_run - m_new) : 1.f;  // 0 for a row's first visible chunk
+      const float mneg = (m_new == -INFINITY) ? 0.f : -m_new;
+      // P = 2^(s * scale - m): one FFMA and one ex2 per score, sums in four chains
+      float cs0 = 0.f, cs1 = 0.f, cs2 = 0.f, cs3 = 0.f;
       uint32_t pk[32];
 #pragma unroll
-      for (int kk = 0; kk < 64; kk += 2) {
-        const float e0 = (sv[kk] == -INFINITY) ? 0.f : exp2f(sv[kk] - m_new);
-        const float e1 = (sv[kk + 1] == -INFINITY) ? 0.f : exp2f(sv[kk + 1] - m_new);
-        cs += e0 + e1;
+      for (int kk = 0; kk < 64; kk += 4) {
+        const float e0 = ex2_fast(fmaf(sv[kk], p.scale_log2, mneg));
+        const float e1 = ex2_fast(fmaf(sv[kk + 1], p.scale_log2, mneg));
+        const float e2 = ex2_fast(fmaf(sv[kk + 2], p.scale_log2, mneg));
+        const float e3 = ex2_fast(fmaf(sv[kk + 3], p.scale_log2, mneg));
+        cs0 += e0;
+        cs1 += e1;
+        cs2 += e2;
+        cs3 += e3;
         pk[kk >> 1] = pack_bf16(e0, e1);
+        pk[(kk >> 1) + 1] = pack_bf16(e2, e3);
       }
+      const float cs = (cs0 + cs1) + (cs2 + cs3);
       l_run = l_run * alpha + cs;
       m_run = m_new;
       // values of keys the staged pages do not cover (past the tile's longest
@@ -1449,6 +1510,11 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
           partial = page < 0 || page >= p.n_pages;
         }
         if (partial) {
+          // the value tile has landed (its barrier cannot run ahead: the tile is refilled only after P_i V_i)
+          if (!tp_wait_warp(smem_addr(&s_fv[i % TP_NST]), (uint32_t)(i / TP_NST) & 1u, p.err)) {
+            failed = true;
+            break;
+          }
           uint8_t* sV = smc + (i % TP_NST) * CL_STAGE + 2 * CL_HALF;
           for (int idx = threadIdx.x; idx < MC * (MHD / 8); idx += 128) {
             const int key = idx >> 4, b = idx & 15;
@@ -1611,7 +1677,10 @@ cudaError_t attention_tp_prepare() {
   cudaError_t e = cudaFuncSetAttribute(attn_tp_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tp_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
   if (e != cudaSuccess) return e;
-  bool big = cudaFuncSetAttribute(attn_tp_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  // DF_ATTN_PIPE_CLA=8: clusters of 8 (easier to place at one CTA per SM); default 16 where placeable
+  const char* env = getenv("DF_ATTN_PIPE_CLA");
+  bool big = !(env && atoi(env) == 8) &&
+             cudaFuncSetAttribute(attn_tp_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
   if (big) {
     cudaLaunchConfig_t c = {};
     c.gridDim = dim3(16, 1, 1);

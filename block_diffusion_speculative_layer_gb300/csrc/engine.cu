@@ -1437,7 +1437,7 @@ df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_we
       return DF_ECUDA;
     }
   }
-  if (tc_prepare() != cudaSuccess || attention_prepare() != cudaSuccess) {
+  if (tc_prepare() != cudaSuccess || attention_prepare() != cudaSuccess || sampling_prepare() != cudaSuccess) {
     delete H;
     (void)cudaGetLastError();
     return DF_ECUDA;

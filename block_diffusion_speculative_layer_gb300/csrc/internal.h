@@ -161,6 +161,7 @@ struct SampleRow {
 };
 constexpr int SAMPLE_MAX_VOCAB = 1 << 19;  // keeps a row's total mass below 2^63
 constexpr float SAMPLE_MIN_TEMPERATURE = 1e-3f, SAMPLE_MAX_TEMPERATURE = 1e3f;
+cudaError_t sampling_prepare();  // kernel attributes (staged shared memory), once, before any stream capture
 bool sampling_args_ok(float temperature, float top_p);  // temperature 0 or in [1e-3, 1e3]; top_p in [0, 1]
 float sampling_inv_t(float temperature);                // 0 for temperature 0
 // st[r] for rows r of logits (row stride ld floats): largest logit, total

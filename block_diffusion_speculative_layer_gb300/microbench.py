@@ -94,7 +94,8 @@ def ar_proxy(a):
                       "note": "random weights: latency only; one drafter pass includes its LM head"}))
 
 
-def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None, sampling=None, attn=0):
+def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None, sampling=None, attn=0,
+                profile=False):
     """One timed df_generate over a batch (device weights drawn on the GPU),
     after one untimed warm-up generation of 16 tokens.  block_range: (b_min,
     b_max) for df_set_block_range, or None for the configured block size.
@@ -130,6 +131,17 @@ def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None,
     s2 = eng.stats()
     hist = [int(x) for x in s2["accept_hist"]]
     per_seq = eng.accept_hist_per_seq(len(prompts))
+    insitu = None
+    if profile:
+        # one more generation with in-situ stamps: device time per kernel class inside the cycles
+        eng.profile(True, in_situ=True)
+        run(n_new)
+        pr = eng.profile_read()
+        eng.profile(False)
+        insitu = {k: {"launches": v["launches"], "ms": round(v["us"] / 1000.0, 3),
+                      "GB/s": round(v["bytes"] / (v["us"] * 1e-6) / 1e9, 1) if v["us"] > 0 and v["bytes"] > 0 else None,
+                      "TFLOP/s": round(v["flops"] / (v["us"] * 1e-6) / 1e12, 1) if v["us"] > 0 and v["flops"] > 0 else None}
+                  for k, v in pr.items() if v["launches"]}
     eng.close()
     tokens = len(prompts) * n_new
     print(json.dumps({"op": label, "config": config, "attn_kernel": attn, "sequences": len(prompts),
@@ -147,7 +159,8 @@ def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None,
                       "draft_us_per_cycle": s2["draft_us"] * len(prompts) / max(1, s2["cycles"]),
                       "verify_us_per_cycle": s2["verify_us"] * len(prompts) / max(1, s2["cycles"]),
                       "prefill_us": s2["prefill_us"], "kernel_launches": s2["kernel_launches"],
-                      "setup_s": setup_s, "data": "synthetic, weights drawn on the GPU (seeded), random prompt ids"}),
+                      "setup_s": setup_s, "in_situ": insitu,
+                      "data": "synthetic, weights drawn on the GPU (seeded), random prompt ids"}),
           flush=True)
 
 
@@ -162,7 +175,7 @@ def serving(a):
     max_ctx = ((int(max(lens)) + a.new + 16 + 2 * shape.block_size + 63) // 64) * 64
     _generation(shape, prompts, a.new, max_ctx, "serving_batch16",
                 "qwen3-8b-shape bf16, 16 sequences, prompts U[128,2048], block 16, %d new each" % a.new,
-                _block_range(a), attn=_attn(a))
+                _block_range(a), attn=_attn(a), profile=a.profile)
 
 
 def sampled(a):
@@ -175,7 +188,7 @@ def sampled(a):
     prompts = [syn.make_prompt(shape, 512)]
     _generation(shape, prompts, a.new, 512 + a.new + 64, "sampled_bs1",
                 "qwen3-8b-shape bf16, batch 1, prompt 512, block 16, %d new, temperature %g, top_p %g"
-                % (a.new, T, top_p), _block_range(a), (T, top_p, 1), attn=_attn(a))
+                % (a.new, T, top_p), _block_range(a), (T, top_p, 1), attn=_attn(a), profile=a.profile)
 
 
 def dense27b(a):
@@ -188,7 +201,7 @@ def dense27b(a):
     max_ctx = ((8192 + a.new + 16 + 2 * shape.block_size + 63) // 64) * 64
     _generation(shape, prompts, a.new, max_ctx, "dense27b_batch4",
                 "27b-class bf16, batch 4, prompt 8192, block 16, %d new each" % a.new, _block_range(a),
-                attn=_attn(a))
+                attn=_attn(a), profile=a.profile)
 
 
 def profile_cycle(a):
@@ -331,6 +344,8 @@ def main():
     ap.add_argument("op", choices=["gemm", "lmhead", "drafter", "ar_proxy", "serving", "dense27b", "sampled",
                                    "profile_cycle", "attention"])
     ap.add_argument("--causal", action="store_true", help="attention: the target's causal verify rows")
+    ap.add_argument("--profile", action="store_true",
+                    help="serving/dense27b/sampled: also report in-situ device time per kernel class")
     ap.add_argument("--vocab", type=int, default=4096, help="profile_cycle: vocabulary")
     ap.add_argument("--attn", default="auto", choices=["auto", "mma", "pipe"],
                     help="attention kernel of the engine (df_config.attn_kernel)")

@@ -135,3 +135,29 @@ def test_block_range_needs_a_handle(L):
     out = (ctypes.c_int64 * 33)()
     assert L.df_generate_accept_hist(None, 0, out) == dfl.DF_EINVAL
     assert L.df_debug_wait_probe(None) == dfl.DF_EINVAL
+
+
+def test_attention_op_rejects_bad_arguments(L):
+    # every case is refused before any CUDA call (fake device addresses are never touched)
+    import block_diffusion_speculative_layer_gb300 as dfl
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    base = dict(q=fake, out=fake, cache=fake, n_pages=4, pt=fake, pt_stride=8, pos=fake, seq=fake, blk=fake,
+                rows_cap=16, nseq=1, rows=16, hq=32, hkv=8, causal=0, max_len=100, kernel=dfl.DF_ATTN_MMA, err=fake)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return L.df_op_attention_bf16(a["q"], a["out"], a["cache"], a["n_pages"], a["pt"], a["pt_stride"], a["pos"],
+                                      a["seq"], a["blk"], a["rows_cap"], a["nseq"], a["rows"], a["hq"], a["hkv"],
+                                      a["causal"], a["max_len"], a["kernel"], a["err"], None)
+
+    assert call(q=None) == dfl.DF_EINVAL
+    assert call(kernel=0) == dfl.DF_EINVAL            # AUTO is an engine setting, not a kernel
+    assert call(kernel=3) == dfl.DF_EINVAL
+    assert call(hq=36) == dfl.DF_EINVAL               # not a multiple of the KV heads
+    assert call(hq=72) == dfl.DF_EINVAL               # more than 8 query heads per KV head
+    assert call(causal=2) == dfl.DF_EINVAL
+    assert call(max_len=8 * 16 + 1) == dfl.DF_EINVAL  # more positions than the page table holds
+    assert call(blk=None) == dfl.DF_EINVAL            # the block form needs the block rows
+    assert call(rows=65) == dfl.DF_EINVAL             # a block holds at most 64 rows
+    assert call(rows_cap=8) == dfl.DF_EINVAL          # fewer block rows than query rows
