@@ -40,12 +40,14 @@ METRIC = "decoded tokens/s (Qwen3-8B shape, bs1) & draft+verify cycle us vs roof
 UNIT = "tokens/s"
 WORKLOAD = "qwen3-8b-shape bf16, drafter 5 layers, block 16, bs1, prompt 512, 512 new tokens, greedy"
 
-# DRAM bytes per launch of the decode GEMM class, from an ncu capture of one
-# launch (M=16, N=4096, K=4096, split-K 8: 33.76 MB read, 0 written, for 33.95
-# MB of algorithmic bytes, ratio 0.9945) scaled to this class's average
-# algorithmic bytes per launch (111.11 MB); reported only while the GEMM's
-# source hash still matches the captured kernel.
-NCU_TRAFFIC = {"source_sha": "e325c289d5ab173c", "bytes_per_gemm_launch_avg": 110496039}
+# DRAM bytes per launch of the decode GEMM class, from the ncu capture of one
+# decode cycle (profiles/kernels_decode_cycle_qwen3_8b_width_bs1.md: per GEMM
+# role, DRAM read + write over algorithmic bytes, 0.995-1.026; the LM head from
+# profiles/gemm_lmhead_argmax_v151936_m16.md, 1.002), weighted by each role's
+# share of the algorithmic bytes of a 36 + 5-layer cycle (ratio 1.011) and
+# applied to this class's average algorithmic bytes per launch (111.09 MB);
+# reported only while the GEMM's source hash still matches the captured kernel.
+NCU_TRAFFIC = {"source_sha": "4a059a2de383bef6", "bytes_per_gemm_launch_avg": 112295011}
 
 
 def kernel_source_sha() -> str:

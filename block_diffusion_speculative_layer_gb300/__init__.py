@@ -129,7 +129,7 @@ def lib() -> ctypes.CDLL:
     L.df_set_block_range.argtypes = [_P, _I, _I]
     L.df_generate_accept_hist.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_int64)]
     L.df_debug_wait_probe.argtypes = [_P]
-    L.df_op_attention_bf16.argtypes = [_P, _P, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]
+    L.df_op_attention_bf16.argtypes = [_P, _P, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]
     L.df_block_size_for.argtypes = [ctypes.c_double, _I, _I]
     L.df_block_size_for.restype = _I
     for name in EXPORTED:
@@ -426,7 +426,7 @@ def bench_gemm_bf16(x, w, iters: int = 20, splits: int = 0, token_tile: int = 0,
 
 def attention_bf16(q, cache, page_table, row_pos, row_seq, nseq: int, rows_per_seq: int, n_kv_heads: int,
                    causal: bool, max_len: int, blk=None, kernel: int = DF_ATTN_PIPE, out=None, err=None,
-                   stream=None):
+                   stream=None, cluster_ctas: int = 0):
     """One attention launch on torch CUDA tensors (df_op_attention_bf16).
     q: [rows, Hq*128] bf16; cache: [n_pages, 2, Hkv, 16, 128] bf16; page_table:
     [slots, pt_stride] int32; row_pos, row_seq: [rows] int32; blk: [2, Hkv,
@@ -446,7 +446,8 @@ def attention_bf16(q, cache, page_table, row_pos, row_seq, nseq: int, rows_per_s
     st = lib().df_op_attention_bf16(_P(q.data_ptr()), _P(out.data_ptr()), _P(cache.data_ptr()), cache.shape[0],
                                     _P(page_table.data_ptr()), page_table.shape[1], _P(row_pos.data_ptr()),
                                     _P(row_seq.data_ptr()), blk_p, rows_cap, nseq, rows_per_seq, Hq, n_kv_heads,
-                                    1 if causal else 0, max_len, kernel, _P(err.data_ptr()), _stream(stream))
+                                    1 if causal else 0, max_len, kernel, cluster_ctas, _P(err.data_ptr()),
+                                    _stream(stream))
     if st != DF_OK:
         raise DfError(st, "df_op_attention_bf16")
     return out, err

@@ -1654,33 +1654,45 @@ __global__ void __launch_bounds__(TP_THREADS, 1)
   trace_exit(p.trace);
 }
 
-static int g_cla_tp = 0;
+static int g_cla_tp = 0;         // default CTAs per cluster of the pipelined kernel (0: not prepared)
+static bool g_tp16_ok = false;  // clusters of 16 can be placed
 
 cudaError_t launch_attention_tp(const AttnParams& p, cudaStream_t st) {
   if (!attention_cluster_fits(p)) return cudaErrorInvalidValue;
   cudaError_t e = attention_tp_prepare();
   if (e != cudaSuccess) return e;
-  // page ids a CTA stages for its chunks (the cluster's ranks take every g_cla_tp-th chunk)
-  const int per_cta = (p.grid_chunks + g_cla_tp - 1) / g_cla_tp;
+  // CTAs per cluster: the launch's choice (2, 4, 8 or 16), else the process default
+  const int cla = (p.cla == 2 || p.cla == 4 || p.cla == 8 || (p.cla == 16 && g_tp16_ok)) ? p.cla : g_cla_tp;
+  // page ids a CTA stages for its chunks (the cluster's ranks take every cla-th chunk)
+  const int per_cta = (p.grid_chunks + cla - 1) / cla;
   if (per_cta * (MC / p.page_tokens) > MAXPG) return cudaErrorInvalidValue;
   const int qtiles = (p.rows_per_seq + 15) / 16;
   const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(p.kv_map);
-  if (g_cla_tp == 16)
-    return launch_kcl(attn_tp_kernel<16>, dim3(16, p.Hkv, p.n_seqs * qtiles), dim3(TP_THREADS), (size_t)TP_SMEM, st,
-                      dim3(16, 1, 1), p, map);
-  return launch_kcl(attn_tp_kernel<8>, dim3(8, p.Hkv, p.n_seqs * qtiles), dim3(TP_THREADS), (size_t)TP_SMEM, st,
-                    dim3(8, 1, 1), p, map);
+  switch (cla) {
+    case 16:
+      return launch_kcl(attn_tp_kernel<16>, dim3(16, p.Hkv, p.n_seqs * qtiles), dim3(TP_THREADS), (size_t)TP_SMEM,
+                        st, dim3(16, 1, 1), p, map);
+    case 8:
+      return launch_kcl(attn_tp_kernel<8>, dim3(8, p.Hkv, p.n_seqs * qtiles), dim3(TP_THREADS), (size_t)TP_SMEM, st,
+                        dim3(8, 1, 1), p, map);
+    case 4:
+      return launch_kcl(attn_tp_kernel<4>, dim3(4, p.Hkv, p.n_seqs * qtiles), dim3(TP_THREADS), (size_t)TP_SMEM, st,
+                        dim3(4, 1, 1), p, map);
+    default:
+      return launch_kcl(attn_tp_kernel<2>, dim3(2, p.Hkv, p.n_seqs * qtiles), dim3(TP_THREADS), (size_t)TP_SMEM, st,
+                        dim3(2, 1, 1), p, map);
+  }
 }
 
 cudaError_t attention_tp_prepare() {
   if (g_cla_tp) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(attn_tp_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tp_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tp_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tp_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
   if (e != cudaSuccess) return e;
-  // DF_ATTN_PIPE_CLA=8: clusters of 8 (easier to place at one CTA per SM); default 16 where placeable
-  const char* env = getenv("DF_ATTN_PIPE_CLA");
-  bool big = !(env && atoi(env) == 8) &&
-             cudaFuncSetAttribute(attn_tp_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  // clusters of 16 need the non-portable size and a device that can place them
+  bool big = cudaFuncSetAttribute(attn_tp_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
   if (big) {
     cudaLaunchConfig_t c = {};
     c.gridDim = dim3(16, 1, 1);
@@ -1697,7 +1709,12 @@ cudaError_t attention_tp_prepare() {
     big = cudaOccupancyMaxActiveClusters(&n, attn_tp_kernel<16>, &c) == cudaSuccess && n > 0;
   }
   cudaGetLastError();
-  g_cla_tp = big ? 16 : 8;
+  g_tp16_ok = big;
+  // the process default when a launch names no cluster size: DF_ATTN_PIPE_CLA (2, 4, 8 or 16), else 4
+  // (one CTA per SM: small clusters place on every SM and give each CTA a long chunk pipeline)
+  const char* env = getenv("DF_ATTN_PIPE_CLA");
+  const int want = env ? atoi(env) : 4;
+  g_cla_tp = (want == 2 || want == 4 || want == 8 || (want == 16 && big)) ? want : 4;
   return cudaSuccess;
 }
 

@@ -508,6 +508,7 @@ df_status attention(df_handle* H, int M, int R, int nseq, bool causal, const voi
                4.0 * M * H->qdim * (double)max_len);
   p.trace = ps.tp;
   p.pipelined = H->attn_pipe ? 1 : 0;
+  p.cla = DF_ATTN_PIPE_CLUSTER;
   CK(launch_attention(p, H->bf16, H->st));
   return DF_OK;
 }
@@ -1406,7 +1407,10 @@ df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_we
   H->kvdim = H->Hkv * H->hd;
   H->qkv_n = H->qdim + 2 * H->kvdim;
   H->Mmax = std::max(std::min(PREFILL_CHUNK, cfg->max_ctx), cfg->max_batch * cfg->block_size);
-  H->attn_pipe = H->bf16 && cfg->attn_kernel == DF_ATTN_PIPE;
+  // attention kernel of the handle: the pipelined tcgen05 kernel (clusters of 4) for batches of 4 or
+  // more sequences, where it streams the cache fastest; the mma.sync kernel (lowest latency) otherwise
+  H->attn_pipe = H->bf16 && (cfg->attn_kernel == DF_ATTN_PIPE ||
+                             (cfg->attn_kernel == DF_ATTN_AUTO && cfg->max_batch >= DF_ATTN_PIPE_MIN_BATCH));
   {
     const char* g = getenv("DF_NO_GRAPH");
     H->use_graphs = !(g && g[0] == '1');
@@ -1958,8 +1962,11 @@ df_status df_op_attention_bf16(const void* q_dev, void* out_dev, const void* cac
                                const int32_t* page_table_dev, int32_t pt_stride, const int32_t* row_pos_dev,
                                const int32_t* row_seq_dev, const void* blk_dev, int32_t rows_cap, int32_t nseq,
                                int32_t rows_per_seq, int32_t n_q_heads, int32_t n_kv_heads, int32_t causal,
-                               int32_t max_len, int32_t kernel, int32_t* err_dev, void* stream) {
+                               int32_t max_len, int32_t kernel, int32_t cluster_ctas, int32_t* err_dev,
+                               void* stream) {
   if (!q_dev || !out_dev || !cache_dev || !page_table_dev || !row_pos_dev || !row_seq_dev || !err_dev) return DF_EINVAL;
+  if (cluster_ctas != 0 && cluster_ctas != 2 && cluster_ctas != 4 && cluster_ctas != 8 && cluster_ctas != 16)
+    return DF_EINVAL;
   if (n_pages < 1 || pt_stride < 1 || nseq < 1 || rows_per_seq < 1 || n_kv_heads < 1 || n_q_heads < n_kv_heads ||
       n_q_heads % n_kv_heads || n_q_heads / n_kv_heads > 8 || max_len < 1 || (causal != 0 && causal != 1) ||
       (kernel != DF_ATTN_MMA && kernel != DF_ATTN_PIPE))
@@ -1995,6 +2002,7 @@ df_status df_op_attention_bf16(const void* q_dev, void* out_dev, const void* cac
   p.err = err_dev;
   p.kv_map = map.b;
   p.pipelined = kernel == DF_ATTN_PIPE ? 1 : 0;
+  p.cla = cluster_ctas;
   if (!attention_cluster_fits(p)) return DF_EINVAL;
   // one of the two cluster kernels, never the partial + merge path (which needs workspaces)
   const cudaError_t e = p.pipelined ? launch_attention_tp(p, st) : launch_attention_cluster(p, st);

@@ -99,6 +99,7 @@ struct AttnParams {
   const void* kv_map;     // host copy of a TMA map of `cache` (make_tmap_kvcache), or null
   unsigned long long* trace;  // in-situ timing of the launch (see trace_entry), or null
   int pipelined;          // bf16: the pipelined tcgen05 kernel (attn_tp_kernel) instead of attn_cl_kernel
+  int cla;                // pipelined kernel: CTAs per cluster (2, 4, 8, 16; 0: the process default)
 };
 cudaError_t launch_attention(const AttnParams& p, bool bf16, cudaStream_t st);
 int attention_launches(const AttnParams& p, bool bf16);  // kernels one launch_attention call makes

@@ -262,7 +262,9 @@ def attention(a):
     attention of 16 verify rows), for each context and batch, on the
     mma.sync and/or pipelined kernel.  Keys and values are random bf16 in a
     paged cache with shuffled pages; L2 is flushed (a 256 MB write) before
-    every timed launch, and each launch is timed alone with CUDA events."""
+    every timed launch, and each launch is timed alone with CUDA events
+    (after a device-side sleep that covers the host's preparation of the
+    launch, so the events bracket the kernel only)."""
     import numpy as np
     import torch
 
@@ -292,12 +294,16 @@ def attention(a):
             for k in kernels:
                 def launch():
                     dfl.attention_bf16(q, cache, table, pos, seq, nb, R, Hkv, a.causal, need,
-                                       blk=None if a.causal else blk, kernel=k, out=out)
+                                       blk=None if a.causal else blk, kernel=k, out=out,
+                                       cluster_ctas=a.cla if k == dfl.DF_ATTN_PIPE else 0)
                 for _ in range(a.warmup):
                     launch()
                 ts = []
                 for _ in range(a.iters):
                     flush.zero_()
+                    # the GPU sleeps while the host prepares the launch (tensor map, arguments), so the
+                    # events bracket the kernel alone and not the host's preparation
+                    torch.cuda._sleep(1_000_000)
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record()
                     launch()
@@ -306,6 +312,7 @@ def attention(a):
                     ts.append(e0.elapsed_time(e1) * 1000.0)
                 us = float(np.median(ts))
                 print(json.dumps({"op": "attention", "kernel": "pipe" if k == dfl.DF_ATTN_PIPE else "mma",
+                                  "cluster_ctas": a.cla if k == dfl.DF_ATTN_PIPE else 16,
                                   "causal": bool(a.causal), "ctx": C, "batch": nb, "rows_per_seq": R,
                                   "us": round(us, 2), "algorithmic_bytes": byts,
                                   "GB/s": round(byts / (us * 1e-6) / 1e9, 1),
@@ -344,6 +351,7 @@ def main():
     ap.add_argument("op", choices=["gemm", "lmhead", "drafter", "ar_proxy", "serving", "dense27b", "sampled",
                                    "profile_cycle", "attention"])
     ap.add_argument("--causal", action="store_true", help="attention: the target's causal verify rows")
+    ap.add_argument("--cla", type=int, default=4, help="attention: CTAs per cluster of the pipelined kernel")
     ap.add_argument("--profile", action="store_true",
                     help="serving/dense27b/sampled: also report in-situ device time per kernel class")
     ap.add_argument("--vocab", type=int, default=4096, help="profile_cycle: vocabulary")

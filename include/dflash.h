@@ -93,11 +93,13 @@ typedef enum { DF_FP32 = 0, DF_BF16 = 1 } df_dtype;
  *   mask_token_id     : id embedded into the drafter's masked slots (vocab-1).
  *   attn_kernel       : bf16 attention kernel for the whole handle (fixed, so
  *                       that verification and greedy decoding stay bitwise
- *                       equal): DF_ATTN_AUTO (0) = the measured faster one
- *                       (today DF_ATTN_MMA everywhere), DF_ATTN_MMA (1) the
- *                       mma.sync cluster kernel, DF_ATTN_PIPE (2) the
- *                       warp-specialised tcgen05 cluster kernel.  The two
- *                       round differently.
+ *                       equal): DF_ATTN_MMA (1) the mma.sync cluster kernel
+ *                       (lowest latency at batch 1-3), DF_ATTN_PIPE (2) the
+ *                       warp-specialised tcgen05 kernel in clusters of
+ *                       DF_ATTN_PIPE_CLUSTER CTAs (streams long contexts and
+ *                       batches fastest), DF_ATTN_AUTO (0) the pipelined
+ *                       kernel when max_batch >= DF_ATTN_PIPE_MIN_BATCH, else
+ *                       the mma.sync kernel.  The two round differently.
  */
 typedef struct {
   int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim, d_ffn, vocab;
@@ -111,6 +113,8 @@ typedef struct {
 } df_config;
 
 enum { DF_ATTN_AUTO = 0, DF_ATTN_MMA = 1, DF_ATTN_PIPE = 2 };
+#define DF_ATTN_PIPE_MIN_BATCH 4 /* DF_ATTN_AUTO: the pipelined kernel from this max_batch on */
+#define DF_ATTN_PIPE_CLUSTER 4   /* the engine's pipelined-kernel cluster size (CTAs) */
 
 /* Per-handle counters.  k = accepted drafts in a cycle; a cycle emits k+1
  * tokens, so the mean accepted length is (accepted_drafts + cycles) / cycles. */
@@ -378,6 +382,10 @@ df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, in
  *                    0..a-1 and every row of its own block (rows_per_seq <= 64)
  *   max_len          bound on the cache positions any row sees (sets the grid)
  *   kernel           DF_ATTN_MMA or DF_ATTN_PIPE (see df_config.attn_kernel)
+ *   cluster_ctas     DF_ATTN_PIPE: CTAs per cluster, 2, 4, 8 or 16 (0: 4,
+ *                    or DF_ATTN_PIPE_CLA from the environment); the chunks
+ *                    are split over a cluster's CTAs, so the size changes
+ *                    the rounding; DF_ATTN_MMA: 0 (16 where placeable)
  *   err_dev          device int receiving the kernels' sticky error bits
  *                    (1: a bounded wait ran out, 2: a page id outside the cache)
  * Query heads per KV head <= 8.  Stream-ordered, no synchronisation, no
@@ -386,7 +394,8 @@ df_status df_op_attention_bf16(const void* q_dev, void* out_dev, const void* cac
                                const int32_t* page_table_dev, int32_t pt_stride, const int32_t* row_pos_dev,
                                const int32_t* row_seq_dev, const void* blk_dev, int32_t rows_cap, int32_t nseq,
                                int32_t rows_per_seq, int32_t n_q_heads, int32_t n_kv_heads, int32_t causal,
-                               int32_t max_len, int32_t kernel, int32_t* err_dev, void* stream);
+                               int32_t max_len, int32_t kernel, int32_t cluster_ctas, int32_t* err_dev,
+                               void* stream);
 
 /* ids[m] = argmax_v (x[m] . w_lm[v]) over V rows of w_lm (bf16 [V][K]),
  * fp32 logits, lowest index on ties; logits are never written.  V % 128 == 0. */

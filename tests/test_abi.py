@@ -143,13 +143,14 @@ def test_attention_op_rejects_bad_arguments(L):
     P = ctypes.c_void_p
     fake = P(0x1000)
     base = dict(q=fake, out=fake, cache=fake, n_pages=4, pt=fake, pt_stride=8, pos=fake, seq=fake, blk=fake,
-                rows_cap=16, nseq=1, rows=16, hq=32, hkv=8, causal=0, max_len=100, kernel=dfl.DF_ATTN_MMA, err=fake)
+                rows_cap=16, nseq=1, rows=16, hq=32, hkv=8, causal=0, max_len=100, kernel=dfl.DF_ATTN_MMA, cla=0,
+                err=fake)
 
     def call(**kw):
         a = dict(base, **kw)
         return L.df_op_attention_bf16(a["q"], a["out"], a["cache"], a["n_pages"], a["pt"], a["pt_stride"], a["pos"],
                                       a["seq"], a["blk"], a["rows_cap"], a["nseq"], a["rows"], a["hq"], a["hkv"],
-                                      a["causal"], a["max_len"], a["kernel"], a["err"], None)
+                                      a["causal"], a["max_len"], a["kernel"], a["cla"], a["err"], None)
 
     assert call(q=None) == dfl.DF_EINVAL
     assert call(kernel=0) == dfl.DF_EINVAL            # AUTO is an engine setting, not a kernel
@@ -161,3 +162,4 @@ def test_attention_op_rejects_bad_arguments(L):
     assert call(blk=None) == dfl.DF_EINVAL            # the block form needs the block rows
     assert call(rows=65) == dfl.DF_EINVAL             # a block holds at most 64 rows
     assert call(rows_cap=8) == dfl.DF_EINVAL          # fewer block rows than query rows
+    assert call(cla=3) == dfl.DF_EINVAL               # clusters of 2, 4, 8 or 16 CTAs

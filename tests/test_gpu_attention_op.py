@@ -10,7 +10,9 @@ ragged context lengths; the reference is the oracle's attention (float64) on
 the same bf16 values, gathered and masked by the rule above.  Both kernels
 (mma.sync cluster and pipelined tcgen05), query-head groups of 4, 5 and 8.
 A row computed alone must equal the same row computed inside its block, bit
-for bit (what keeps verification and greedy decoding identical).
+for bit (what keeps verification and greedy decoding identical).  The
+pipelined kernel runs in clusters of 2, 4 and 16 CTAs (the chunk split, and
+so the rounding, follows the cluster size).
 """
 import math
 
@@ -91,11 +93,16 @@ def reference(c, lens, R, Hq, Hkv, causal):
     return np.concatenate(out)
 
 
+KERNELS = {"mma": (1, 0), "pipe2": (2, 2), "pipe4": (2, 4), "pipe16": (2, 16)}  # (df kernel, CTAs per cluster)
+
+
 def run(dfl, c, lens, R, Hkv, causal, kernel):
+    k, cla = KERNELS[kernel]
     max_len = max(L + (R if causal else 0) for L in lens)
     out, err = dfl.attention_bf16(bf(c["q"]), bf(c["cache"]), torch.from_numpy(c["table"]).cuda(),
                                   torch.from_numpy(c["pos"]).cuda(), torch.from_numpy(c["seq"]).cuda(), len(lens), R,
-                                  Hkv, causal, max_len, blk=None if causal else bf(c["blk"]), kernel=kernel)
+                                  Hkv, causal, max_len, blk=None if causal else bf(c["blk"]), kernel=k,
+                                  cluster_ctas=cla)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     return out.float().cpu().numpy()
@@ -104,14 +111,13 @@ def run(dfl, c, lens, R, Hkv, causal, kernel):
 CASES = [(4, 8, [1000, 37, 2048 + 5], 16), (5, 8, [300, 1500], 16), (8, 2, [700, 64], 8), (4, 8, [32768 - 16], 16)]
 
 
-@pytest.mark.parametrize("kernel", ["mma", "pipe"])
+@pytest.mark.parametrize("kernel", list(KERNELS))
 @pytest.mark.parametrize("causal", [True, False], ids=["causal", "block"])
 @pytest.mark.parametrize("G,Hkv,lens,R", CASES, ids=["g4-ragged", "g5", "g8", "g4-32k"])
 def test_attention_against_the_oracle(dfl, kernel, causal, G, Hkv, lens, R):
-    k = dfl.DF_ATTN_MMA if kernel == "mma" else dfl.DF_ATTN_PIPE
     Hq = G * Hkv
     c = make_case(7 + G + len(lens), lens, R, Hq, Hkv, causal)
-    got = run(dfl, c, lens, R, Hkv, causal, k)
+    got = run(dfl, c, lens, R, Hkv, causal, kernel)
     ref = reference(c, lens, R, Hq, Hkv, causal)
     assert T.rel_err(got, ref) <= 2e-2
     # each row against its own reference (rows differ in length and scale)
@@ -119,11 +125,11 @@ def test_attention_against_the_oracle(dfl, kernel, causal, G, Hkv, lens, R):
         assert T.rel_err(got[r], ref[r]) <= 2e-2, r
 
 
-@pytest.mark.parametrize("kernel", ["mma", "pipe"])
+@pytest.mark.parametrize("kernel", list(KERNELS))
 def test_a_row_alone_equals_the_row_in_its_block(dfl, kernel):
     # causal rows: row j of a 16-row verify block and the same position decoded
     # alone (a 1-row block) give bitwise the same output
-    k = dfl.DF_ATTN_MMA if kernel == "mma" else dfl.DF_ATTN_PIPE
+    k = kernel
     G, Hkv, R = 4, 8, 16
     lens = [900, 333]
     c = make_case(3, lens, R, G * Hkv, Hkv, True)
