@@ -426,19 +426,22 @@ def bench_gemm_bf16(x, w, iters: int = 20, splits: int = 0, token_tile: int = 0,
 
 def attention_bf16(q, cache, page_table, row_pos, row_seq, nseq: int, rows_per_seq: int, n_kv_heads: int,
                    causal: bool, max_len: int, blk=None, kernel: int = DF_ATTN_PIPE, out=None, err=None,
-                   stream=None, cluster_ctas: int = 0):
+                   stream=None, cluster_ctas: int = 0, check_rows: bool = True):
     """One attention launch on torch CUDA tensors (df_op_attention_bf16).
     q: [rows, Hq*128] bf16; cache: [n_pages, 2, Hkv, 16, 128] bf16; page_table:
     [slots, pt_stride] int32; row_pos, row_seq: [rows] int32; blk: [2, Hkv,
-    rows_cap, 128] bf16 for the drafter's block attention.  Returns (out, err)."""
+    rows_cap, 128] bf16 for the drafter's block attention.  Returns (out, err).
+    check_rows=False skips the host check that row_seq indexes page_table
+    (that check copies row_seq to the host and so waits for the stream)."""
     import torch
     assert q.dtype == torch.bfloat16 and cache.dtype == torch.bfloat16 and q.is_cuda and cache.is_cuda
     rows = q.shape[0]
     Hq = q.shape[1] // 128
     assert rows == nseq * rows_per_seq and row_pos.numel() == rows and row_seq.numel() == rows
     assert page_table.dtype == torch.int32 and row_pos.dtype == torch.int32 and row_seq.dtype == torch.int32
-    seq_cpu = row_seq.cpu()
-    assert int(seq_cpu.min()) >= 0 and int(seq_cpu.max()) < page_table.shape[0], "row_seq must index page_table"
+    if check_rows:
+        seq_cpu = row_seq.cpu()
+        assert int(seq_cpu.min()) >= 0 and int(seq_cpu.max()) < page_table.shape[0], "row_seq must index page_table"
     out = torch.empty_like(q) if out is None else out
     err = _err_word(q.device) if err is None else err
     blk_p = _P(blk.data_ptr()) if blk is not None else None

@@ -1221,7 +1221,13 @@ __device__ __forceinline__ bool tp_wait_warp(uint32_t bar, uint32_t parity, int*
   return __all_sync(0xffffffffu, cl_wait_bar(bar, parity, err)) != 0;
 }
 
-template <int CLA>
+// DUP (groups of at most four query heads): the 64 real rows of the 128-row
+// tile are each held twice, in tensor-memory lanes w*32 + r and w*32 + 16 + r
+// of softmax warp w (head w, token row r); the two threads of a row take its
+// keys 0..31 and 32..63 and meet through one shuffle for the maximum and the
+// sum, so every lane of a softmax warp does useful work.  Otherwise rows
+// (g & 3) * 32 + (g >> 2) * 16 + r hold head g, one thread per row.
+template <int CLA, bool DUP>
 __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensorMap& kvmap) {
   // Everything older than the key/value GEMM before this kernel is complete
   // here (that GEMM triggers only after its own wait): the row metadata, the
@@ -1434,7 +1440,7 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
     uint8_t* sQ = smc + TP_QOFF;
     for (int idx = threadIdx.x; idx < 128 * 16; idx += 128) {
       const int row = idx >> 4, c = idx & 15;
-      const int g = (row >> 5) + 4 * ((row >> 4) & 1), r = row & 15;
+      const int g = DUP ? (row >> 5) : (row >> 5) + 4 * ((row >> 4) & 1), r = row & 15;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (g < G && r < nrows && s_len[r] >= 0)
         v = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + (size_t)(r0 + r) * p.Hq * MHD +
@@ -1445,7 +1451,8 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
     asm volatile("bar.arrive 1, 160;" ::: "memory");
 
     const int trow = threadIdx.x;  // tensor-memory lane = MMA row
-    const int g = warp + 4 * ((lane >> 4) & 1), r = lane & 15;
+    const int half = lane >> 4;    // DUP: this thread's keys of a chunk are half * 32 + [0, 32)
+    const int g = DUP ? warp : warp + 4 * half, r = lane & 15;
     const bool row_ok = g < G && r < nrows && s_len[r] >= 0;
     const int len = row_ok ? s_len[r] : 0;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
@@ -1458,34 +1465,45 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      float sv[64];
-      tc_ld64(tmem + lane_base + (uint32_t)sb * 64u, sv);
+      constexpr int NK = DUP ? 32 : 64;  // scores of this thread per chunk
+      float sv[NK];
+      if constexpr (DUP) {
+        float s2[64];
+        tc_ld64(tmem + lane_base + (uint32_t)sb * 64u, s2);
+#pragma unroll
+        for (int kk = 0; kk < 32; ++kk) sv[kk] = half ? s2[32 + kk] : s2[kk];
+      } else {
+        tc_ld64(tmem + lane_base + (uint32_t)sb * 64u, sv);
+      }
+      const int koff = DUP ? half * 32 : 0;
       const bool is_blk = i >= nmine;
       const int key0 = is_blk ? 0 : (j + CLA * i) * MC;
-      const int vis = !row_ok ? 0 : (is_blk ? p.rows_per_seq : len - key0);
-      if (vis < 64) {  // keys the row cannot see score -inf (full chunks skip this)
+      const int vis = (!row_ok ? 0 : (is_blk ? p.rows_per_seq : len - key0)) - koff;
+      if (vis < NK) {  // keys the row cannot see score -inf (full chunks skip this)
 #pragma unroll
-        for (int kk = 0; kk < 64; ++kk) sv[kk] = (kk < vis) ? sv[kk] : -INFINITY;
+        for (int kk = 0; kk < NK; ++kk) sv[kk] = (kk < vis) ? sv[kk] : -INFINITY;
       }
       // the raw maximum in four independent chains, scaled once (scale > 0)
       float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
-      for (int kk = 4; kk < 64; kk += 4) {
+      for (int kk = 4; kk < NK; kk += 4) {
         mx0 = fmaxf(mx0, sv[kk]);
         mx1 = fmaxf(mx1, sv[kk + 1]);
         mx2 = fmaxf(mx2, sv[kk + 2]);
         mx3 = fmaxf(mx3, sv[kk + 3]);
       }
-      const float mc = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+      float mraw = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      if constexpr (DUP) mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 16));
+      const float mc = mraw * p.scale_log2;
       const bool resc = mc > m_run + TP_RESCALE;
       const float m_new = resc ? mc : m_run;
       const float alpha = resc ? ex2_fast(m_run - m_new) : 1.f;  // 0 for a row's first visible chunk
       const float mneg = (m_new == -INFINITY) ? 0.f : -m_new;
       // P = 2^(s * scale - m): one FFMA and one ex2 per score, sums in four chains
       float cs0 = 0.f, cs1 = 0.f, cs2 = 0.f, cs3 = 0.f;
-      uint32_t pk[32];
+      uint32_t pk[NK / 2];
 #pragma unroll
-      for (int kk = 0; kk < 64; kk += 4) {
+      for (int kk = 0; kk < NK; kk += 4) {
         const float e0 = ex2_fast(fmaf(sv[kk], p.scale_log2, mneg));
         const float e1 = ex2_fast(fmaf(sv[kk + 1], p.scale_log2, mneg));
         const float e2 = ex2_fast(fmaf(sv[kk + 2], p.scale_log2, mneg));
@@ -1497,7 +1515,8 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
         pk[kk >> 1] = pack_bf16(e0, e1);
         pk[(kk >> 1) + 1] = pack_bf16(e2, e3);
       }
-      const float cs = (cs0 + cs1) + (cs2 + cs3);
+      float cs = (cs0 + cs1) + (cs2 + cs3);
+      if constexpr (DUP) cs += __shfl_xor_sync(0xffffffffu, cs, 16);
       l_run = l_run * alpha + cs;
       m_run = m_new;
       // values of keys the staged pages do not cover (past the tile's longest
@@ -1550,10 +1569,21 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
         }
       }
       uint8_t* sP = smc + TP_POFF + sb * 128 * 128;
+      if constexpr (DUP) {
+        // this thread's 32 keys into both copies of its row (lanes r and 16 + r of the warp)
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(sP + trow * 128 + ((c ^ (trow & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          const int cc = half * 4 + c;
+          *reinterpret_cast<uint4*>(sP + (trow & ~16) * 128 + ((cc ^ (trow & 7)) << 4)) = v;
+          *reinterpret_cast<uint4*>(sP + (trow | 16) * 128 + ((cc ^ (trow & 7)) << 4)) = v;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(sP + trow * 128 + ((c ^ (trow & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
@@ -1583,13 +1613,14 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
 #pragma unroll
         for (int e = 0; e < 32; ++e) ov[e] = 0.f;
       }
-      if (row_ok) {
+      // DUP: the two copies of a row write the output's dims 0..63 and 64..127
+      if (row_ok && (!DUP || (c >> 1) == half)) {
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
           *reinterpret_cast<float4*>(dst + 32 * c + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
       }
     }
-    if (row_ok) sML[g * 16 + r] = make_float2(m_run, l_run);
+    if (row_ok && (!DUP || half == 0)) sML[g * 16 + r] = make_float2(m_run, l_run);
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
@@ -1646,16 +1677,40 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
   cl_wait();    // and nobody leaves while another CTA may still read its partial
 }
 
-template <int CLA>
+template <int CLA, bool DUP>
 __global__ void __launch_bounds__(TP_THREADS, 1)
     attn_tp_kernel(AttnParams p, const __grid_constant__ CUtensorMap kvmap) {
   trace_entry(p.trace);
-  attn_tp_body<CLA>(p, kvmap);
+  attn_tp_body<CLA, DUP>(p, kvmap);
   trace_exit(p.trace);
 }
 
 static int g_cla_tp = 0;         // default CTAs per cluster of the pipelined kernel (0: not prepared)
 static bool g_tp16_ok = false;  // clusters of 16 can be placed
+
+template <bool DUP>
+static cudaError_t launch_tp(const AttnParams& p, int cla, int qtiles, const CUtensorMap& map, cudaStream_t st) {
+  const dim3 grid(cla, p.Hkv, p.n_seqs * qtiles);
+  switch (cla) {
+    case 16:
+      return launch_kcl(attn_tp_kernel<16, DUP>, grid, dim3(TP_THREADS), (size_t)TP_SMEM, st, dim3(16, 1, 1), p, map);
+    case 8:
+      return launch_kcl(attn_tp_kernel<8, DUP>, grid, dim3(TP_THREADS), (size_t)TP_SMEM, st, dim3(8, 1, 1), p, map);
+    case 4:
+      return launch_kcl(attn_tp_kernel<4, DUP>, grid, dim3(TP_THREADS), (size_t)TP_SMEM, st, dim3(4, 1, 1), p, map);
+    default:
+      return launch_kcl(attn_tp_kernel<2, DUP>, grid, dim3(TP_THREADS), (size_t)TP_SMEM, st, dim3(2, 1, 1), p, map);
+  }
+}
+
+template <bool DUP>
+static cudaError_t tp_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(attn_tp_kernel<8, DUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tp_kernel<16, DUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tp_kernel<4, DUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tp_kernel<2, DUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
+  return e;
+}
 
 cudaError_t launch_attention_tp(const AttnParams& p, cudaStream_t st) {
   if (!attention_cluster_fits(p)) return cudaErrorInvalidValue;
@@ -1668,31 +1723,19 @@ cudaError_t launch_attention_tp(const AttnParams& p, cudaStream_t st) {
   if (per_cta * (MC / p.page_tokens) > MAXPG) return cudaErrorInvalidValue;
   const int qtiles = (p.rows_per_seq + 15) / 16;
   const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(p.kv_map);
-  switch (cla) {
-    case 16:
-      return launch_kcl(attn_tp_kernel<16>, dim3(16, p.Hkv, p.n_seqs * qtiles), dim3(TP_THREADS), (size_t)TP_SMEM,
-                        st, dim3(16, 1, 1), p, map);
-    case 8:
-      return launch_kcl(attn_tp_kernel<8>, dim3(8, p.Hkv, p.n_seqs * qtiles), dim3(TP_THREADS), (size_t)TP_SMEM, st,
-                        dim3(8, 1, 1), p, map);
-    case 4:
-      return launch_kcl(attn_tp_kernel<4>, dim3(4, p.Hkv, p.n_seqs * qtiles), dim3(TP_THREADS), (size_t)TP_SMEM, st,
-                        dim3(4, 1, 1), p, map);
-    default:
-      return launch_kcl(attn_tp_kernel<2>, dim3(2, p.Hkv, p.n_seqs * qtiles), dim3(TP_THREADS), (size_t)TP_SMEM, st,
-                        dim3(2, 1, 1), p, map);
-  }
+  return p.Hq / p.Hkv <= 4 ? launch_tp<true>(p, cla, qtiles, map, st) : launch_tp<false>(p, cla, qtiles, map, st);
 }
 
 cudaError_t attention_tp_prepare() {
   if (g_cla_tp) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_tp_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tp_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tp_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tp_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, TP_SMEM);
+  cudaError_t e = tp_attrs<true>();
+  if (e == cudaSuccess) e = tp_attrs<false>();
   if (e != cudaSuccess) return e;
   // clusters of 16 need the non-portable size and a device that can place them
-  bool big = cudaFuncSetAttribute(attn_tp_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  bool big = cudaFuncSetAttribute(attn_tp_kernel<16, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                 cudaSuccess &&
+             cudaFuncSetAttribute(attn_tp_kernel<16, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                 cudaSuccess;
   if (big) {
     cudaLaunchConfig_t c = {};
     c.gridDim = dim3(16, 1, 1);
@@ -1706,7 +1749,7 @@ cudaError_t attention_tp_prepare() {
     c.attrs = a;
     c.numAttrs = 1;
     int n = 0;
-    big = cudaOccupancyMaxActiveClusters(&n, attn_tp_kernel<16>, &c) == cudaSuccess && n > 0;
+    big = cudaOccupancyMaxActiveClusters(&n, attn_tp_kernel<16, true>, &c) == cudaSuccess && n > 0;
   }
   cudaGetLastError();
   g_tp16_ok = big;
@@ -1809,7 +1852,8 @@ cudaError_t launch_wait_probe(int* err, cudaStream_t st) {
 cudaError_t attention_cluster_prepare() {
   if (g_cla) return cudaSuccess;
   cudaError_t e;
-  if ((e = cl_attrs<8, 4>()) != cudaSuccess || (e = cl_attrs<8, 8>()) != cudaSuccess ||
+  if ((e = cl_attrs<4, 4>()) != cudaSuccess || (e = cl_attrs<4, 8>()) != cudaSuccess ||
+      (e = cl_attrs<8, 4>()) != cudaSuccess || (e = cl_attrs<8, 8>()) != cudaSuccess ||
       (e = cl_attrs<16, 4>()) != cudaSuccess || (e = cl_attrs<16, 8>()) != cudaSuccess)
     return e;
   const bool big =
@@ -1817,7 +1861,10 @@ cudaError_t attention_cluster_prepare() {
       cudaFuncSetAttribute(attn_cl_kernel<16, 8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
       cluster_placeable<16>();
   cudaGetLastError();
-  g_cla = big ? 16 : 8;
+  // DF_ATTN_CLA=4|8|16 in the environment picks the cluster size; otherwise 16 where it can be placed
+  const char* env = getenv("DF_ATTN_CLA");
+  const int want = env ? atoi(env) : 16;
+  g_cla = (want == 4 || want == 8) ? want : (big ? 16 : 8);
   return cudaSuccess;
 }
 
@@ -1844,6 +1891,6 @@ cudaError_t launch_attention_cluster(const AttnParams& p, cudaStream_t st) {
   if (!attention_cluster_fits(p)) return cudaErrorInvalidValue;
   cudaError_t e = attention_cluster_prepare();
   if (e != cudaSuccess) return e;
-  return g_cla == 16 ? launch_cl<16>(p, st) : launch_cl<8>(p, st);
+  return g_cla == 16 ? launch_cl<16>(p, st) : g_cla == 8 ? launch_cl<8>(p, st) : launch_cl<4>(p, st);
 }
 }  // namespace dfk

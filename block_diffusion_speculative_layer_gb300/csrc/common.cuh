@@ -152,6 +152,11 @@ __device__ __forceinline__ void row_sumsq(float v, int r, float* red) {
 
 constexpr int EPI_BATCH = 16;  // rows whose global loads are issued together
 
+// The epilogue's barrier: named barrier 1 over its 128 threads (the first four
+// warps), so that a kernel with further warps (producer, MMA issuer) can run
+// the epilogue on its first four warps alone.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 // Stage the per-row facts the epilogue needs (positions, KV pages, 1/rms of
 // folded norms) into meta.  Run by `nthr` threads (whole warps) with index
 // `tid`; the caller synchronises before epilogue_tile reads meta.
@@ -238,10 +243,11 @@ __device__ __forceinline__ bool epilogue_preload(const EpiParams& ep, int n0, in
 
 // Apply the epilogue to one result tile held in shared memory.
 //   tile[r * ld + f] = acc for row m0 + r, feature n0 + f, f in [0, 128),
-//   r in [0, rows), rows <= M - m0.  Called by exactly 128 threads (one per
-//   feature column).  meta has room for `rows` entries; if `staged`, the
-//   caller already ran epilogue_stage into it and synchronised.  red holds
-//   4 floats per row.  Contains __syncthreads(), so all 128 threads call it.
+//   r in [0, rows), rows <= M - m0.  Called by exactly the 128 threads of
+//   warps 0-3 (one per feature column).  meta has room for `rows` entries;
+//   if `staged`, the caller already ran epilogue_stage into it and
+//   synchronised.  red holds 4 floats per row.  Synchronises those 128
+//   threads (epi_sync), so all of them call it.
 template <typename T>
 __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, int n0, int m0, int rows, int M,
                               RowMeta* meta, float* red, bool staged = false, const EpiPre* pre = nullptr) {
@@ -250,7 +256,7 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
   rows = min(rows, M - m0);
   if (!staged) {
     epilogue_stage(ep, m0, rows, M, meta, threadIdx.x & 127, 128);
-    __syncthreads();
+    epi_sync();
   }
   const bool scaled = ep.ss_in != nullptr;
   switch (ep.kind) {
@@ -295,7 +301,7 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
         }
       }
       if (ep.ss_out) {
-        __syncthreads();
+        epi_sync();
         for (int r = threadIdx.x; r < rows; r += 128)
           ep.ss_out[(size_t)(m0 + r) * ep.ss_tiles + (n0 >> 7)] =
               ((red[r * 4 + 0] + red[r * 4 + 1]) + red[r * 4 + 2]) + red[r * 4 + 3];
@@ -308,7 +314,7 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
         out[(size_t)(m0 + r) * ep.ldo + n] = Cvt<T>::from_f(v);
         row_sumsq(v, r, red);
       }
-      __syncthreads();
+      epi_sync();
       for (int r = threadIdx.x; r < rows; r += 128)
         ep.ss_out[(size_t)(m0 + r) * ep.ss_tiles + (n0 >> 7)] =
             ((red[r * 4 + 0] + red[r * 4 + 1]) + red[r * 4 + 2]) + red[r * 4 + 3];

@@ -263,10 +263,14 @@ cudaError_t trace_collect(df_handle* H, const std::vector<df_handle::TraceSlot>&
   std::vector<unsigned long long> t(2 * meta.size());
   cudaError_t e = cudaMemcpy(t.data(), H->d_trace, t.size() * 8, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return e;
+  // DF_TRACE_FILE=<path>: also append every stamped launch (class, entry ns, exit ns) to that file
+  static const char* dump_path = getenv("DF_TRACE_FILE");
+  FILE* dump = dump_path ? fopen(dump_path, "a") : nullptr;
   unsigned long long prev = 0;
   for (size_t i = 0; i < meta.size(); ++i) {
     const unsigned long long entry = ~t[2 * i], exit = t[2 * i + 1];
     if (t[2 * i] == 0 || exit == 0) continue;  // not stamped (a path without stamps)
+    if (dump) fprintf(dump, "%s %llu %llu\n", PC_NAMES[meta[i].cls], entry, exit);
     if (prev == 0) prev = entry;
     const unsigned long long dt = exit > prev ? exit - prev : 0ull;
     prev = exit > prev ? exit : prev;
@@ -276,6 +280,7 @@ cudaError_t trace_collect(df_handle* H, const std::vector<df_handle::TraceSlot>&
     k.bytes += meta[i].bytes;
     k.flops += meta[i].flops;
   }
+  if (dump) fclose(dump);
   return cudaSuccess;
 }
 
@@ -423,14 +428,19 @@ df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiPar
   if (M <= 0) return DF_OK;
   ProfScope ps(H, cls, H->bf16 ? 1 : 2, gemm_bytes(H, W, M, ep), 2.0 * M * W.N * W.K);
   if (H->bf16) {
-    const int nt = tc_token_tile(M);
+    const int splits = tc_splits(W.N, W.K, H->split_target);
+    const int wide = tc_wide_tile(M, W.N);
+    const int nt = wide ? wide : tc_token_tile(M);
     const void* tmX = nullptr;
     CKS(xmap(H, X, W.K, nt, &tmX));
-    const int splits = tc_splits(W.N, W.K, H->split_target);
     EpiParams e = ep;
     e.trace = ps.tp;
-    CK(launch_gemm_tc(W.tm.b, tmX, nt, M, W.N, W.K, splits, H->ws, H->counters, e, H->st,
-                      tc_cluster_reduce(nt, splits)));
+    if (wide) {
+      CK(launch_gemm_tcw(W.tm.b, tmX, nt, M, W.N, W.K, splits, e, H->st));
+    } else {
+      CK(launch_gemm_tc(W.tm.b, tmX, nt, M, W.N, W.K, splits, H->ws, H->counters, e, H->st,
+                        tc_cluster_reduce(nt, splits)));
+    }
   } else {
     CK(launch_gemm_f32(reinterpret_cast<const float*>(X), reinterpret_cast<const float*>(W.ptr), H->tmp, M, W.N, W.K,
                        ep, H->st));
@@ -1933,12 +1943,18 @@ df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, in
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int nt = token_tile ? token_tile : tc_token_tile(M);
-  if (nt != 16 && nt != 32 && nt != 64 && nt != 128 && nt != 256) return DF_EINVAL;
   const int sp = splits ? splits : tc_splits(N, K, tc_split_target(sms));
   if (sp < 1 || sp > K / 64) return DF_EINVAL;
+  const int wide = token_tile < 0 ? -token_tile : (token_tile == 0 ? tc_wide_tile(M, N) : 0);
+  const int nt = wide ? wide : (token_tile ? token_tile : tc_token_tile(M));
+  if (wide ? (nt != 64 && nt != 128) : (nt != 16 && nt != 32 && nt != 64 && nt != 128 && nt != 256)) return DF_EINVAL;
   Tmap tw, tx;
   if (!make_tmap_bf16(tw.b, w_dev, N, K, 128) || !make_tmap_bf16(tx.b, x_dev, M, K, nt)) return DF_EINVAL;
+  EpiParams e{};
+  e.kind = EPI_STORE_F32;
+  e.out = y_dev;
+  e.ldo = N;
+  if (wide) return launch_gemm_tcw(tw.b, tx.b, nt, M, N, K, sp, e, st) == cudaSuccess ? DF_OK : DF_ECUDA;
   float* ws = nullptr;
   int* cnt = nullptr;
   const size_t wsf = tc_workspace_floats(M, N, sp, nt), cn = tc_counter_ints(M, N, nt);
@@ -1948,10 +1964,6 @@ df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, in
     return DF_ENOMEM;
   }
   cudaMemsetAsync(cnt, 0, cn * 4, st);
-  EpiParams e{};
-  e.kind = EPI_STORE_F32;
-  e.out = y_dev;
-  e.ldo = N;
   cudaError_t r = launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st, tc_cluster_reduce(nt, sp));
   cudaFreeAsync(ws, st);
   cudaFreeAsync(cnt, st);
@@ -2017,8 +2029,9 @@ df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int nt = tc_token_tile(M);
   const int sp = tc_splits(V, K, tc_split_target(sms));
+  const int wide = tc_wide_tile(M, V);  // the engine's choice of form
+  const int nt = wide ? wide : tc_token_tile(M);
   Tmap tw, tx;
   if (!make_tmap_bf16(tw.b, wlm_dev, V, K, 128) || !make_tmap_bf16(tx.b, x_dev, M, K, nt)) return DF_EINVAL;
   float* ws = nullptr;
@@ -2037,7 +2050,8 @@ df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32
   EpiParams e{};
   e.kind = EPI_ARGMAX;
   e.amax = amax;
-  cudaError_t r = launch_gemm_tc(tw.b, tx.b, nt, M, V, K, sp, ws, cnt, e, st, tc_cluster_reduce(nt, sp));
+  cudaError_t r = wide ? launch_gemm_tcw(tw.b, tx.b, nt, M, V, K, sp, e, st)
+                       : launch_gemm_tc(tw.b, tx.b, nt, M, V, K, sp, ws, cnt, e, st, tc_cluster_reduce(nt, sp));
   if (r == cudaSuccess) r = launch_argmax_finalize(amax, ids_dev, M, st);
   cudaFreeAsync(ws, st);
   cudaFreeAsync(cnt, st);
@@ -2053,10 +2067,11 @@ df_status df_op_bench_gemm_bf16(const void* x_dev, const void* w_dev, float* y_d
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int nt = token_tile ? token_tile : tc_token_tile(M);
-  if (nt != 16 && nt != 32 && nt != 64 && nt != 128 && nt != 256) return DF_EINVAL;
   const int sp = splits ? splits : tc_splits(N, K, tc_split_target(sms));
   if (sp < 1 || sp > K / 64) return DF_EINVAL;
+  const int wide = token_tile < 0 ? -token_tile : (token_tile == 0 ? tc_wide_tile(M, N) : 0);
+  const int nt = wide ? wide : (token_tile ? token_tile : tc_token_tile(M));
+  if (wide ? (nt != 64 && nt != 128) : (nt != 16 && nt != 32 && nt != 64 && nt != 128 && nt != 256)) return DF_EINVAL;
   Tmap tw, tx;
   if (!make_tmap_bf16(tw.b, w_dev, N, K, 128) || !make_tmap_bf16(tx.b, x_dev, M, K, nt)) return DF_EINVAL;
   float* ws = nullptr;
@@ -2076,10 +2091,13 @@ df_status df_op_bench_gemm_bf16(const void* x_dev, const void* w_dev, float* y_d
   cudaEventCreate(&a);
   cudaEventCreate(&b);
   const bool cr = tc_cluster_reduce(nt, sp);
-  cudaError_t r = launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st, cr);  // warm-up
+  auto one = [&]() {
+    return wide ? launch_gemm_tcw(tw.b, tx.b, nt, M, N, K, sp, e, st)
+                : launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st, cr);
+  };
+  cudaError_t r = one();  // warm-up
   cudaEventRecord(a, st);
-  for (int i = 0; i < iters && r == cudaSuccess; ++i)
-    r = launch_gemm_tc(tw.b, tx.b, nt, M, N, K, sp, ws, cnt, e, st, cr);
+  for (int i = 0; i < iters && r == cudaSuccess; ++i) r = one();
   cudaEventRecord(b, st);
   cudaStreamSynchronize(st);
   float ms = 0.f;

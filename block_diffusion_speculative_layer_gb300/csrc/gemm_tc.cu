@@ -434,6 +434,281 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
 }
 
 // ----------------------------------------------------------------------------
+// Serial-split form for many token rows.  With hundreds of token rows a
+// split-K tile is large (up to 128 x 256 fp32), one CTA fills an SM, and the
+// splits' clusters cannot all be resident at once: the launch runs in waves
+// with idle SMs.  Here one CTA per (weight tile, token tile) runs every K
+// range of its tile in order, each range into its own tensor-memory
+// accumulator (two, alternating, so the next range's MMAs overlap the fold of
+// the last), and four fold warps add the finished partials in split order
+// 0, 1, 2, ... in registers.  The split count, each partial's MMA sequence and
+// the fp32 additions and their order are those of the split-K form, so every
+// output is bitwise the same as there; no cluster and no workspace.
+//
+// Roles (192 threads): warps 0-3 fold (warp w reads tensor-memory lanes
+// 32w..32w+31, thread f holds weight row n0 + f for every token) and then run
+// the fused epilogue; warp 4 lane 0 issues the TMA loads; warp 5 lane 0 issues
+// the MMAs.  The token tile is the fastest grid index, so the CTAs that share
+// a weight tile run together and read it from DRAM once.
+constexpr int TW_THREADS = 192;
+
+// Stages and where the running sums live.  64-token tiles: 4 stages of 24 KB,
+// two CTAs per SM, sums in registers.  128-token tiles: 6 stages of 32 KB, one
+// CTA per SM, sums in a third tensor-memory accumulator (128 floats a thread
+// would spill).  (Measured at 256 and 512 token rows on the Qwen3-8B shapes:
+// 64-token tiles at two CTAs per SM are the fastest or equal in every case;
+// 8 stages at one CTA per SM gained nothing where the grid fits one wave and
+// lost up to 2x where it does not.)
+template <int NT>
+struct TwCfg {
+  using C = TcCfg<NT>;
+  static constexpr int STAGES = NT == 64 ? 4 : 6;
+  static constexpr bool RTMEM = NT > 64;
+  static constexpr int TCOLS = RTMEM ? 512 : 2 * NT;  // accumulators 0 and 1 (and the sums at 2 NT)
+  static constexpr int META_OFF = STAGES * C::STAGE_BYTES + 256;
+  static constexpr int SMEM = 1024 + META_OFF + NT * (int)sizeof(RowMeta);
+  static_assert(NT * C::TLD * 4 + NT * 16 <= STAGES * C::STAGE_BYTES, "epilogue tile and row sums fit in the ring");
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+};
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+template <int NT>
+__device__ __forceinline__ void gemm_tcw_body(const CUtensorMap& tmW, const CUtensorMap& tmX, int M, int N, int K,
+                                              int splits, const EpiParams& ep) {
+  using C = TcCfg<NT>;
+  using W = TwCfg<NT>;
+  constexpr int STAGES = W::STAGES;
+  constexpr int TCOLS = W::TCOLS;
+  static_assert(TCOLS >= 32 && TCOLS <= 512 && (TCOLS & (TCOLS - 1)) == 0, "tensor-memory allocation");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sW = smem;
+  uint8_t* sX = smem + STAGES * C::W_BYTES;
+  // barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], done
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // 0 failed, 1 consumed, 2 issued
+  RowMeta* meta = reinterpret_cast<RowMeta*>(smem + W::META_OFF);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * NT, n0 = blockIdx.y * BM;
+  const int nkb = K / BK;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+  const uint32_t afull0 = smem_u32(bars + 2 * STAGES), aempty0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t done_bar = smem_u32(bars + 2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(afull0 + 8 * b, 1);
+      mbar_init(aempty0 + 8 * b, 4);  // one arrival per fold warp
+    }
+    mbar_init(done_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    flags[0] = 0; flags[1] = 0; flags[2] = 0;
+  }
+  if (threadIdx.x == 32) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TCOLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  // as in the split-K form: a GEMM that writes keys and values lets its
+  // dependent start only after its own wait
+  const bool late_trigger = ep.kind == EPI_QKV;
+  if (!late_trigger) pdl_trigger();
+  // fold warps: the running sum of weight row n0 + threadIdx.x over the tile's tokens, in
+  // registers (R) or in tensor-memory columns [2 NT, 3 NT) of the thread's lane
+  constexpr bool RTMEM = W::RTMEM;
+  float R[RTMEM ? 1 : NT];
+  if (warp == 4) {
+    if (lane == 0) {
+      // ---- TMA producer: the tile's whole K, weight tiles of the first stages before the wait
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const int pre = nkb < STAGES ? nkb : STAGES;
+      for (int i = 0; i < pre; ++i) {
+        mbar_expect_tx(full0 + 8 * i, C::STAGE_BYTES);
+        tma_load_2d(smem_u32(sW + i * C::W_BYTES), &tmW, full0 + 8 * i, i * BK, n0, pol_w);
+      }
+      pdl_wait();
+      if (late_trigger) pdl_trigger();
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d(smem_u32(sX + i * C::X_BYTES), &tmX, full0 + 8 * i, i * BK, m0, pol_x);
+      int i = pre;
+      for (; i < nkb; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, ep.err)) {
+          flags[0] = 1;
+          break;
+        }
+        if (flags[0]) break;
+        mbar_expect_tx(full0 + 8 * s, C::STAGE_BYTES);
+        tma_load_2d(smem_u32(sW + s * C::W_BYTES), &tmW, full0 + 8 * s, i * BK, n0, pol_w);
+        tma_load_2d(smem_u32(sX + s * C::X_BYTES), &tmX, full0 + 8 * s, i * BK, m0, pol_x);
+      }
+      flags[2] = i;
+    } else {
+      pdl_wait();
+      if (late_trigger) pdl_trigger();
+    }
+  } else if (warp == 5) {
+    pdl_wait();
+    if (late_trigger) pdl_trigger();
+    if (lane == 0) {
+      // ---- MMA issuer: split q into accumulator q & 1, reused once the fold of split q - 2 is done
+      constexpr uint32_t idesc = idesc_bf16(BM, NT);
+      int i = 0;
+      bool ok = true;
+      for (int q = 0; q < splits && ok; ++q) {
+        const int kb0 = (int)((long long)nkb * q / splits), kb1 = (int)((long long)nkb * (q + 1) / splits);
+        const int b = q & 1;
+        if (q >= 2 && !mbar_wait(aempty0 + 8 * b, (uint32_t)((q - 2) >> 1) & 1u, ep.err)) {
+          ok = false;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        for (int kb = kb0; kb < kb1; ++kb, ++i) {
+          const int s = i % STAGES;
+          const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+          if (!mbar_wait(full0 + 8 * s, ph, ep.err)) {
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t aw = smem_u32(sW + s * C::W_BYTES);
+          const uint32_t ax = smem_u32(sX + s * C::X_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16(tmem + (uint32_t)(b * NT), desc_sw128(aw + kk * 32), desc_sw128(ax + kk * 32), idesc,
+                     (kb > kb0 || kk > 0) ? 1u : 0u);
+          mma_commit(empty0 + 8 * s);
+        }
+        if (ok) mma_commit(afull0 + 8 * b);
+      }
+      if (!ok) flags[0] = 1;
+      flags[1] = i;
+      mma_commit(done_bar);  // arrives once every MMA issued above has completed
+    }
+  } else {
+    // ---- fold warps: stage the epilogue's row facts, then add the partials in split order
+    pdl_wait();
+    if (late_trigger) pdl_trigger();
+    epilogue_stage(ep, m0, NT, M, meta, threadIdx.x, 128);
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    for (int q = 0; q < splits; ++q) {
+      const int b = q & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(afull0 + 8 * b, (uint32_t)(q >> 1) & 1u, ep.err))) {
+        flags[0] = 1;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+      for (int c = 0; c < NT; c += 16) {
+        float v[16];
+        tmem_ld16(tmem + lane_base + (uint32_t)(b * NT + c), v);
+        if constexpr (RTMEM) {
+          const uint32_t ra = tmem + lane_base + (uint32_t)(2 * NT + c);
+          if (q > 0) {
+            float r[16];
+            tmem_ld16(ra, r);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = r[j] + v[j];
+          }
+          tmem_st16(ra, v);
+        } else if (q == 0) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) R[c + j] = v[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) R[c + j] += v[j];
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(aempty0 + 8 * b);
+      if (flags[0]) break;
+    }
+    if (threadIdx.x == 0) mbar_wait(done_bar, 0, ep.err);  // every MMA has finished
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  const bool failed = flags[0] != 0;
+  auto free_tmem = [&]() {
+    if (warp == 0) {
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TCOLS) : "memory");
+    }
+  };
+  if (failed) {
+    free_tmem();
+    // wait (bounded) for loads that were issued but never consumed, then leave
+    if (threadIdx.x == 0) {
+      const int consumed = flags[1], issued = flags[2];
+      for (int i = consumed; i < issued; ++i)
+        if (!mbar_wait(full0 + 8 * (i % STAGES), (uint32_t)(i / STAGES) & 1u, ep.err)) break;
+    }
+    return;
+  }
+  if (warp >= 4) return;
+  // ---- the sums into a shared tile over the (now idle) stages, then the epilogue
+  float* tile = reinterpret_cast<float*>(smem);
+  if constexpr (RTMEM) {
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+#pragma unroll 1
+    for (int c = 0; c < NT; c += 16) {
+      float v[16];
+      tmem_ld16(tmem + lane_base + (uint32_t)(2 * NT + c), v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) tile[(c + j) * C::TLD + threadIdx.x] = v[j];
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  } else {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) tile[t * C::TLD + threadIdx.x] = R[t];
+  }
+  epi_sync();
+  free_tmem();  // every fold warp's last tensor-memory read is done
+  float* red = tile + (size_t)NT * C::TLD;
+  epilogue_tile<__nv_bfloat16>(ep, tile, C::TLD, n0, m0, min(NT, M - m0), M, meta, red, /*staged=*/true, nullptr);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(TW_THREADS, 1) gemm_tcw_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                              const __grid_constant__ CUtensorMap tmX, int M, int N,
+                                                              int K, int splits, EpiParams ep) {
+  trace_entry(ep.trace);
+  gemm_tcw_body<NT>(tmW, tmX, M, N, K, splits, ep);
+  trace_exit(ep.trace);
+}
+
+// ----------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------
 
@@ -519,7 +794,11 @@ cudaError_t tc_prepare() {
   if ((e = set_smem_attr<32>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<64>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<128>()) != cudaSuccess) return e;
-  return set_smem_attr<256>();
+  if ((e = set_smem_attr<256>()) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tcw_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, TwCfg<64>::SMEM)) !=
+      cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(gemm_tcw_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TwCfg<128>::SMEM);
 }
 
 // Whether clusters of cz CTAs of this token-tile variant can be resident
@@ -580,6 +859,50 @@ static cudaError_t launch_nt(const void* tmW, const void* tmX, int M, int N, int
   return launch_kc(gemm_tc_kernel<NT>, grid, dim3(128), (size_t)C::SMEM, st, cz,
                    *reinterpret_cast<const CUtensorMap*>(tmW), *reinterpret_cast<const CUtensorMap*>(tmX), M, N, K,
                    splits, ws, counters, cz > 1 ? 1 : 0, ep);
+}
+
+// Token tile of the serial-split form for an M-row GEMM with N outputs (0:
+// the split-K form).  Beyond 128 token rows the split-K form's tiles fill an
+// SM each and its clusters run in waves; the serial-split form takes over
+// with 64-token tiles.  (At 128 rows the split-K form is as fast or faster:
+// 45 against 69 us for the 4096 x 12288 down projection.)  DF_GEMM_WIDE=0 in
+// the environment turns it off; DF_GEMM_WIDE_MIN=m moves the threshold.
+int tc_wide_tile(int M, int N) {
+  static int min_m = -1;
+  if (min_m < 0) {
+    const char* off = getenv("DF_GEMM_WIDE");
+    const char* mm = getenv("DF_GEMM_WIDE_MIN");
+    min_m = (off && off[0] == '0') ? (1 << 30) : (mm ? atoi(mm) : 129);
+    if (min_m < 1) min_m = 1;
+  }
+  (void)N;
+  return M < min_m ? 0 : 64;
+}
+
+template <int NT>
+static cudaError_t launch_nt_wide(const void* tmW, const void* tmX, int M, int N, int K, int splits,
+                                  const EpiParams& ep, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tcw_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, TwCfg<NT>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid((M + NT - 1) / NT, N / BM);
+  return launch_k(gemm_tcw_kernel<NT>, grid, dim3(TW_THREADS), (size_t)TwCfg<NT>::SMEM, st,
+                  *reinterpret_cast<const CUtensorMap*>(tmW), *reinterpret_cast<const CUtensorMap*>(tmX), M, N, K,
+                  splits, ep);
+}
+
+cudaError_t launch_gemm_tcw(const void* tmW, const void* tmX, int nt, int M, int N, int K, int splits,
+                            const EpiParams& ep, cudaStream_t st) {
+  if (N % BM || K % BK || M < 1 || splits < 1 || splits > K / BK) return cudaErrorInvalidValue;
+  switch (nt) {
+    case 64: return launch_nt_wide<64>(tmW, tmX, M, N, K, splits, ep, st);
+    case 128: return launch_nt_wide<128>(tmW, tmX, M, N, K, splits, ep, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_gemm_tc(const void* tmW, const void* tmX, int nt, int M, int N, int K, int splits, float* ws,

@@ -68,6 +68,13 @@ size_t tc_counter_ints(int M, int N, int nt);
 // the workspace `ws` and the tile tickets `counters` (splits > 1 only).
 cudaError_t launch_gemm_tc(const void* tmW, const void* tmX, int nt, int M, int N, int K, int splits, float* ws,
                            int* counters, const EpiParams& ep, cudaStream_t st, bool cluster_reduce = false);
+// Serial-split form (one CTA per weight tile and token tile runs all `splits`
+// K ranges and adds them in split order: bitwise the split-K form's result).
+// nt is 64 or 128; the X map's box has nt rows.  tc_wide_tile(M, N) is the
+// engine's choice of nt for M token rows, 0 for the split-K form.
+int tc_wide_tile(int M, int N);
+cudaError_t launch_gemm_tcw(const void* tmW, const void* tmX, int nt, int M, int N, int K, int splits,
+                            const EpiParams& ep, cudaStream_t st);
 
 // ---- fp32 SIMT GEMM + epilogue (gemm_simt.cu)
 cudaError_t launch_gemm_f32(const float* x, const float* w, float* tmp, int M, int N, int K, const EpiParams& ep,

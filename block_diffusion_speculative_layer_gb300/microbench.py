@@ -288,21 +288,22 @@ def attention(a):
             pos = torch.tensor(np.concatenate([np.arange(C, C + R)] * nb), dtype=torch.int32, device="cuda")
             seq = torch.tensor(np.repeat(np.arange(nb), R), dtype=torch.int32, device="cuda")
             out = torch.empty_like(q)
+            err = torch.zeros(1, dtype=torch.int32, device="cuda")
             torch.cuda.empty_cache()  # the fp32 draws' memory goes back before anything is timed or profiled
             visible = C + R
             byts = nb * visible * Hkv * 128 * 2 * 2 + 2 * nb * R * Hq * 128 * 2
             for k in kernels:
-                def launch():
+                def launch(check=False):
                     dfl.attention_bf16(q, cache, table, pos, seq, nb, R, Hkv, a.causal, need,
-                                       blk=None if a.causal else blk, kernel=k, out=out,
-                                       cluster_ctas=a.cla if k == dfl.DF_ATTN_PIPE else 0)
-                for _ in range(a.warmup):
-                    launch()
+                                       blk=None if a.causal else blk, kernel=k, out=out, err=err,
+                                       cluster_ctas=a.cla if k == dfl.DF_ATTN_PIPE else 0, check_rows=check)
+                for w in range(a.warmup):
+                    launch(check=w == 0)
                 ts = []
                 for _ in range(a.iters):
                     flush.zero_()
-                    # the GPU sleeps while the host prepares the launch (tensor map, arguments), so the
-                    # events bracket the kernel alone and not the host's preparation
+                    # the GPU sleeps while the host prepares the launch (tensor map, arguments; nothing
+                    # that waits for the stream), so the events bracket the kernel alone
                     torch.cuda._sleep(1_000_000)
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record()
@@ -311,6 +312,7 @@ def attention(a):
                     torch.cuda.synchronize()
                     ts.append(e0.elapsed_time(e1) * 1000.0)
                 us = float(np.median(ts))
+                assert int(err.item()) == 0, f"attention error word {int(err.item())}"
                 print(json.dumps({"op": "attention", "kernel": "pipe" if k == dfl.DF_ATTN_PIPE else "mma",
                                   "cluster_ctas": a.cla if k == dfl.DF_ATTN_PIPE else 16,
                                   "causal": bool(a.causal), "ctx": C, "batch": nb, "rows_per_seq": R,

@@ -360,7 +360,13 @@ df_status df_debug_weight_ptr(const df_handle* h, int32_t which, uint64_t* addr)
  * distributed shared memory; otherwise (or with DF_NO_CLUSTER=1 in the
  * environment) the partials go through a workspace allocated on `stream`
  * for the call.  Both give bitwise the same y.
- * token_tile: 0 = the engine's choice for M, else one of 16,32,64,128,256. */
+ * token_tile: 0 = the engine's choice for M; 16, 32, 64, 128 or 256 = the
+ * split-K form with that many token rows per tile; -64 or -128 = the
+ * serial-split form with 64 or 128 token rows per tile, which the engine
+ * uses beyond 128 token rows: one CTA per (weight tile, token tile) runs
+ * every K range of its tile in order, each into its own tensor-memory
+ * accumulator, and adds the partials in split order (bitwise the split-K
+ * form's y, no cluster, no workspace). */
 df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, int32_t M, int32_t N, int32_t K,
                           int32_t splits, int32_t token_tile, void* stream);
 

@@ -118,6 +118,43 @@ def test_gemm_rows_independent_of_token_tile(dfl, nt):
     np.testing.assert_array_equal(a, b)
 
 
+# The serial-split form (token_tile -64 / -128; the engine's choice beyond 128
+# token rows): one CTA runs every K range of its tile and adds the partials in
+# split order, so it must equal the split-K form bit for bit.
+WIDE = [
+    # (M, N, K, splits, token_tile)
+    (129, 256, 512, 1, -64),
+    (200, 384, 1024, 3, -64),
+    (256, 512, 4096, 8, -128),
+    (300, 256, 640, 5, -128),
+    (512, 1024, 2048, 4, -64),
+    (77, 128, 256, 2, -128),
+]
+
+
+@pytest.mark.parametrize("M,N,K,splits,nt", WIDE)
+def test_gemm_wide_matches_float64_and_split_k(dfl, M, N, K, splits, nt):
+    x, w = inputs(M, N, K, seed=300 + M)
+    xd, wd = dev_bf16(x), dev_bf16(w)
+    y = dfl.gemm_bf16(xd, wd, splits=splits, token_tile=nt).cpu().numpy()
+    check_close(y, x, w)
+    ref = dfl.gemm_bf16(xd, wd, splits=splits, token_tile=16).cpu().numpy()
+    np.testing.assert_array_equal(y, ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 6144, 4096), (256, 4096, 12288), (144, 24576, 4096)])
+def test_gemm_wide_engine_shapes_bitwise(dfl, M, N, K):
+    # the engine's own choice (token_tile 0 picks the serial-split form here) against
+    # the split-K form with 16-token tiles, on the verify pass shapes of a 16-sequence batch
+    x, w = inputs(M, N, K, seed=17)
+    xd, wd = dev_bf16(x), dev_bf16(w)
+    a = dfl.gemm_bf16(xd, wd).cpu().numpy()
+    b = dfl.gemm_bf16(xd, wd, token_tile=16).cpu().numpy()
+    np.testing.assert_array_equal(a, b)
+    cols = np.random.default_rng(1).choice(N, size=256, replace=False)
+    check_close(a, x, w, cols)
+
+
 def check_argmax(ids, x, w):
     x64, w64 = x.astype(np.float64), w.astype(np.float64)
     logits = x64 @ w64.T
@@ -132,7 +169,8 @@ def check_argmax(ids, x, w):
             assert logits[m, ids[m]] >= srt[m, -1] - 2 * bound[m]
 
 
-@pytest.mark.parametrize("M,V,K", [(1, 1024, 256), (15, 2048, 512), (16, 151936, 4096), (33, 4096, 1024)])
+@pytest.mark.parametrize("M,V,K", [(1, 1024, 256), (15, 2048, 512), (16, 151936, 4096), (33, 4096, 1024),
+                                   (160, 8192, 1024), (256, 16384, 4096)])
 def test_lmhead_argmax(dfl, M, V, K):
     x, w = inputs(M, V, K, seed=21 + M)
     ids = dfl.lmhead_argmax_bf16(dev_bf16(x), dev_bf16(w)).cpu().numpy()
