@@ -296,28 +296,31 @@ cudaError_t launch_attention_mma(const AttnParams& p, cudaStream_t st) {
 // chunks c = j, j + CLA, j + 2*CLA, ... (the drafter's block rows, as one more
 // chunk, go to rank CLA-1 after its context chunks) and runs an online softmax
 // over them.  The chunks' pages come by TMA into CL_NST shared-memory stages,
-// so the next chunks' keys and values load while one is computed.  The CLA partials (running max, sum, unnormalised
-// output per row and query head) are then left in shared memory and, after a
-// cluster barrier, each CTA merges a share of the (head, row) pairs by reading
-// all CLA partials through distributed shared memory in rank order.
+// so the next chunks' keys and values load while one is computed.  Each CTA
+// owns a share of the (head, row) pairs: every CTA writes its partial of a pair
+// (running max, sum, unnormalised output) into the owner's receive region
+// through distributed shared memory and arrives on the owner's barrier, and
+// the owner merges the CLA partials in rank order from its own shared memory.
 //
 // A row's arithmetic depends only on its own visible length: which CTA takes a
 // chunk depends on the chunk index alone, chunks that a row cannot see leave
 // its state bit-for-bit unchanged, and the merge order is fixed, so a row gets
 // the same bits whatever the other rows of its tile or batch.
 constexpr int MAXPG = 2048;                 // page ids a CTA stages for its chunks
-constexpr int CL_NST = 2;                   // key/value stages in flight (three CTAs fit on an SM)
+constexpr int CL_NST = 2;                   // key/value stages in flight (two CTAs fit on an SM)
 // One stage: keys then values, each [2 halves of the head dim][64 keys][128 B]
 // in the 128-byte swizzle (16-byte piece b of a row at b ^ (key & 7)).
 constexpr int CL_HALF = MC * 128;
 constexpr int CL_STAGE = 2 * 2 * CL_HALF;
 constexpr unsigned long long CL_WAIT_NS = 2000000000ull;
 
-__host__ __device__ constexpr int cl_merge_bytes(int G) { return G * 16 * MHD * 4 + G * 16 * 8; }
-__host__ __device__ constexpr int cl_pg_off(int G) {
-  return ((cl_merge_bytes(G) > CL_NST * CL_STAGE ? cl_merge_bytes(G) : CL_NST * CL_STAGE) + 1023) / 1024 * 1024;
-}
-__host__ __device__ constexpr int cl_smem_bytes(int G) { return cl_pg_off(G) + MAXPG * 4 + 1024; }
+__host__ __device__ constexpr int cl_pg_off(int G) { return (void)G, CL_NST * CL_STAGE; }
+// Receive region of the merge: per (query head, token row) pair a CTA owns, one
+// slot per cluster rank of CL_RSLOT floats (the partial output's 128 dims,
+// then the running maximum and sum).
+constexpr int CL_RSLOT = MHD + 4;
+__host__ __device__ constexpr int cl_rb_off(int G) { return cl_pg_off(G) + MAXPG * 4; }
+__host__ __device__ constexpr int cl_smem_bytes(int G) { return cl_rb_off(G) + G * 16 * CL_RSLOT * 4 + 1024; }
 
 // Byte offset of (key, 16-byte piece b of the 256-byte row) in a stage's key or value tile.
 __device__ __forceinline__ uint32_t swz2(int key, int b) {
@@ -392,12 +395,46 @@ __device__ __forceinline__ float4 cl_ld4(uint32_t addr) {
                : "r"(addr));
   return v;
 }
+__device__ __forceinline__ void cl_st2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+// Arrive (release, cluster scope) on the mbarrier at `addr` in another CTA of the cluster.
+__device__ __forceinline__ void cl_remote_arrive(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ bool cl_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (acquire at cluster scope) for arrivals from other CTAs of the cluster.
+__device__ __noinline__ bool cl_wait_bar_cluster(uint32_t bar, uint32_t parity, int* err) {
+  if (cl_try_wait_cluster(bar, parity)) return true;
+  unsigned long long t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (cl_try_wait_cluster(bar, parity)) return true;
+    if ((it & 1023u) == 0) {
+      unsigned long long t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > CL_WAIT_NS) break;
+    }
+  }
+  flag_error(err, ERR_TIMEOUT);
+  return false;
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// NW warps (one per query head of a group, at least four): four-warp CTAs are
-// held to 168 registers so that three fit on an SM next to their shared memory.
+// NW warps (one per query head of a group, at least four); two four-warp CTAs
+// fit on an SM next to their shared memory.
 template <int CLA, int NW>
 __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensorMap& kvmap) {
   // The GEMM before this kernel triggers it only after its own wait (see
@@ -455,14 +492,19 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
   const __nv_bfloat16* blk = reinterpret_cast<const __nv_bfloat16*>(p.blk);
   const int PT = p.page_tokens;
   __shared__ __align__(8) uint64_t s_full[CL_NST];
+  __shared__ __align__(8) uint64_t s_merge;  // one arrival per cluster rank once its partial is here
   __shared__ int s_failed;
   if (threadIdx.x == 0) {
     for (int b2 = 0; b2 < CL_NST; ++b2) cl_mbar_init(smem_addr(&s_full[b2]));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&s_merge)), "r"(CLA) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kvmap)) : "memory");
     s_failed = 0;
   }
   __syncthreads();
+  // every rank's merge barrier is initialised before any rank arrives on it
+  // remotely (the matching wait comes after the chunks, long after this)
+  cl_arrive();
   // Stage step st into buffer buf: part 1 = the pages wholly before first_new
   // (written by earlier passes), 2 = the rest, 3 = all.  Context chunks come
   // by TMA, one 2 KB box per (page, k|v, half row), issued by thread 0; the
@@ -489,7 +531,11 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
       if (threadIdx.x == 0) cl_arrive_expect_tx(bar, 0);
       return;
     }
-    if (threadIdx.x != 0) return;
+    // warp 0: lane 0 keeps the barrier's byte count, lane 4 * pg + 2 * kv + half
+    // issues the box of (page pg, k|v, half) itself, so the chunk's boxes go out
+    // in parallel rather than one after another from a single thread
+    if (threadIdx.x >= 32) return;
+    const int ln = threadIdx.x;
     const int key0 = (j + CLA * st) * MC;
     const int npg = (min(MC, max_len - key0) + PT - 1) / PT;  // pages holding a key the tile can see
     auto wanted = [&](int pg) {
@@ -497,23 +543,21 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
       const int page = s_pg[st * ppc + pg];
       return ((old ? 1 : 2) & part) && page >= 0 && page < p.n_pages;
     };
-    uint32_t bytes = 0;
-    for (int pg = 0; pg < npg; ++pg)
-      if (wanted(pg)) bytes += 4u * (uint32_t)PT * 128u;
-    if (part == 1) {
-      if (bytes) cl_expect_tx(bar, bytes);
-    } else {
-      cl_arrive_expect_tx(bar, bytes);
+    if (ln == 0) {
+      uint32_t bytes = 0;
+      for (int pg = 0; pg < npg; ++pg)
+        if (wanted(pg)) bytes += 4u * (uint32_t)PT * 128u;
+      if (part == 1) {
+        if (bytes) cl_expect_tx(bar, bytes);
+      } else {
+        cl_arrive_expect_tx(bar, bytes);
+      }
     }
-    for (int pg = 0; pg < npg; ++pg) {
-      if (!wanted(pg)) continue;
+    const int pg = ln >> 2, kv = (ln >> 1) & 1, half = ln & 1;
+    if (pg < npg && wanted(pg)) {
       const int page = s_pg[st * ppc + pg];
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv)
-#pragma unroll
-        for (int half = 0; half < 2; ++half)
-          tma_kv(smem_addr((kv ? sV : sK) + half * CL_HALF + pg * PT * 128), &kvmap, bar, half,
-                 (page * 2 + kv) * p.Hkv + h);
+      tma_kv(smem_addr((kv ? sV : sK) + half * CL_HALF + pg * PT * 128), &kvmap, bar, half,
+             (page * 2 + kv) * p.Hkv + h);
     }
   };
   // Keys and values the staged pages do not cover (past the tile's longest
@@ -698,40 +742,53 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
   cp_async_wait_0();
   __syncthreads();
 
-  // ---- leave the partial in shared memory (over the stage buffers)
-  float* sO = reinterpret_cast<float*>(smc);
-  float2* sML = reinterpret_cast<float2*>(smc + G * 16 * MHD * 4);
-  if (active) {
+  // ---- the merge.  Pair pp = (query head g, token row r) = g * 16 + r belongs to
+  // rank pp / (pairs / CLA).  Every rank writes its partial of each pair (output,
+  // running maximum and sum) into slot j of that pair in the owner's receive
+  // region (remote stores), then arrives once on every rank's merge barrier;
+  // each rank waits for its own barrier and merges its pairs from local
+  // shared memory.  No rank reads another's shared memory, and every write into
+  // a rank lands before that rank's barrier completes, so a rank may leave as
+  // soon as it has merged.
+  const int pairs = G * 16;
+  const int per_owner = pairs / CLA;  // G * 16 is a multiple of 16, CLA divides 16
+  const uint32_t rb_s = smem_addr(smc + cl_rb_off(G));
+  // ranks without a chunk of this tile hold (-inf, 0, 0): their terms are
+  // exactly zero, so they are neither written nor read
+  const bool held_me = j < nA || (!causal && j == CLA - 1);
+  cl_wait();  // the merge barriers are initialised
+  if (active && held_me) {
 #pragma unroll
     for (int hl = 0; hl < 2; ++hl) {
       const int rr = gid + hl * 8;
-      float* dst = sO + (size_t)(warp * 16 + rr) * MHD;
+      const int pp = warp * 16 + rr;
+      const uint32_t owner = (uint32_t)(pp / per_owner);
+      const uint32_t slot = rb_s + (uint32_t)(((pp % per_owner) * CLA + j) * CL_RSLOT) * 4u;
+      const uint32_t dst = cl_map(slot, owner);
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt)
-        *reinterpret_cast<float2*>(dst + nt * 8 + tig * 2) = make_float2(o[nt][2 * hl], o[nt][2 * hl + 1]);
-      if (tig == 0) sML[warp * 16 + rr] = make_float2(hl ? m_hi : m_lo, hl ? l_hi : l_lo);
+      for (int nt = 0; nt < 16; ++nt) cl_st2(dst + (uint32_t)(nt * 8 + tig * 2) * 4u, o[nt][2 * hl], o[nt][2 * hl + 1]);
+      if (tig == 0) cl_st2(dst + (uint32_t)MHD * 4u, hl ? m_hi : m_lo, hl ? l_hi : l_lo);
     }
   }
-  cl_arrive();
-  cl_wait();
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+  __syncthreads();
+  if (threadIdx.x < CLA) cl_remote_arrive(cl_map(smem_addr(&s_merge), (uint32_t)threadIdx.x));
+  if (!cl_wait_bar_cluster(smem_addr(&s_merge), 0u, p.err)) return;
 
-  // ---- merge: this CTA's share of the (head, row) pairs, 32 threads x 4 dims per pair
-  const int pairs = G * 16;
-  const int p0 = j * pairs / CLA, p1 = (j + 1) * pairs / CLA;
-  const uint32_t sO_s = smem_addr(sO), sML_s = smem_addr(sML);
-  for (int pp = p0 + warp; pp < p1; pp += blockDim.x >> 5) {
+  // ---- merge this rank's pairs, 32 threads x 4 dims per pair, ranks in order
+  for (int lp = warp; lp < per_owner; lp += blockDim.x >> 5) {
+    const int pp = j * per_owner + lp;
     const int g = pp >> 4, rr = pp & 15;
     if (rr >= nrows || s_len[rr] < 0) continue;
+    const float* slot0 = reinterpret_cast<const float*>(smc + cl_rb_off(G)) + (size_t)lp * CLA * CL_RSLOT;
     float2 ml[CLA];
     float4 av[CLA];
-    // ranks without a chunk of this tile hold (-inf, 0, 0): their terms are
-    // exactly zero, so they are not read
 #pragma unroll
     for (int i = 0; i < CLA; ++i) {
       const bool held = i < nA || (!causal && i == CLA - 1);
-      ml[i] = held ? cl_ld2(cl_map(sML_s + (uint32_t)(g * 16 + rr) * 8u, (uint32_t)i)) : make_float2(-INFINITY, 0.f);
-      av[i] = held ? cl_ld4(cl_map(sO_s + (uint32_t)((g * 16 + rr) * MHD + lane * 4) * 4u, (uint32_t)i))
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float* sl = slot0 + (size_t)i * CL_RSLOT;
+      ml[i] = held ? *reinterpret_cast<const float2*>(sl + MHD) : make_float2(-INFINITY, 0.f);
+      av[i] = held ? *reinterpret_cast<const float4*>(sl + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float Mx = -INFINITY;
 #pragma unroll
@@ -755,12 +812,10 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
     packed.y = pack_bf16(a.z * inv, a.w * inv);
     *reinterpret_cast<uint2*>(out) = packed;
   }
-  cl_arrive();  // this CTA's reads of the other partials are done
-  cl_wait();    // and nobody leaves while another CTA may still read its partial
 }
 
 template <int CLA, int NW>
-__global__ void __launch_bounds__(NW * 32, NW == 4 ? 3 : 1)
+__global__ void __launch_bounds__(NW * 32, NW == 4 ? 2 : 1)
     attn_cl_kernel(AttnParams p, const __grid_constant__ CUtensorMap kvmap) {
   trace_entry(p.trace);
   attn_cl_body<CLA, NW>(p, kvmap);
@@ -933,7 +988,11 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(AttnParams p, const __g
       if (threadIdx.x == 0) cl_arrive_expect_tx(bar, 0);
       return;
     }
-    if (threadIdx.x != 0) return;
+    // warp 0: lane 0 keeps the barrier's byte count, lane 4 * pg + 2 * kv + half
+    // issues the box of (page pg, k|v, half) itself, so the chunk's boxes go out
+    // in parallel rather than one after another from a single thread
+    if (threadIdx.x >= 32) return;
+    const int ln = threadIdx.x;
     const int key0 = (j + CLA * st) * MC;
     const int npg = (min(MC, max_len - key0) + PT - 1) / PT;  // pages holding a key the tile can see
     auto wanted = [&](int pg) {
@@ -941,23 +1000,21 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(AttnParams p, const __g
       const int page = s_pg[st * ppc + pg];
       return ((old ? 1 : 2) & part) && page >= 0 && page < p.n_pages;
     };
-    uint32_t bytes = 0;
-    for (int pg = 0; pg < npg; ++pg)
-      if (wanted(pg)) bytes += 4u * (uint32_t)PT * 128u;
-    if (part == 1) {
-      if (bytes) cl_expect_tx(bar, bytes);
-    } else {
-      cl_arrive_expect_tx(bar, bytes);
+    if (ln == 0) {
+      uint32_t bytes = 0;
+      for (int pg = 0; pg < npg; ++pg)
+        if (wanted(pg)) bytes += 4u * (uint32_t)PT * 128u;
+      if (part == 1) {
+        if (bytes) cl_expect_tx(bar, bytes);
+      } else {
+        cl_arrive_expect_tx(bar, bytes);
+      }
     }
-    for (int pg = 0; pg < npg; ++pg) {
-      if (!wanted(pg)) continue;
+    const int pg = ln >> 2, kv = (ln >> 1) & 1, half = ln & 1;
+    if (pg < npg && wanted(pg)) {
       const int page = s_pg[st * ppc + pg];
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv)
-#pragma unroll
-        for (int half = 0; half < 2; ++half)
-          tma_kv(smem_addr((kv ? sV : sK) + half * CL_HALF + pg * PT * 128), &kvmap, bar, half,
-                 (page * 2 + kv) * p.Hkv + h);
+      tma_kv(smem_addr((kv ? sV : sK) + half * CL_HALF + pg * PT * 128), &kvmap, bar, half,
+             (page * 2 + kv) * p.Hkv + h);
     }
   };
   // Keys and values the staged pages do not cover (past the tile's longest
@@ -1217,8 +1274,13 @@ __device__ __forceinline__ void tp_arrive(uint32_t bar) {
 }
 // A bounded wait whose outcome is the same for every lane of the warp (the
 // warp-collective tensor-memory loads after it need all 32 lanes).
+// One test inline first: in the pipelined kernel most waits find the phase
+// already complete, and the bounded loop is an out-of-line call.
+__device__ __forceinline__ bool cl_wait_fast(uint32_t bar, uint32_t parity, int* err) {
+  return cl_try_wait(bar, parity) || cl_wait_bar(bar, parity, err);
+}
 __device__ __forceinline__ bool tp_wait_warp(uint32_t bar, uint32_t parity, int* err) {
-  return __all_sync(0xffffffffu, cl_wait_bar(bar, parity, err)) != 0;
+  return __all_sync(0xffffffffu, cl_wait_fast(bar, parity, err)) != 0;
 }
 
 // DUP (groups of at most four query heads): the 64 real rows of the 128-row
@@ -1272,6 +1334,7 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
   __shared__ __align__(8) uint64_t s_fk[TP_NST], s_fv[TP_NST], s_ek[TP_NST], s_ev[TP_NST];
   __shared__ __align__(8) uint64_t s_bs[2], s_bp[2], s_bpv[2], s_done;
   __shared__ int s_failed;
+  __shared__ uint8_t s_part[MAXPG];  // per chunk of this CTA: the value tile needs zeros
   __shared__ uint32_t s_tmem;
   if (threadIdx.x == 0) {
     for (int b = 0; b < TP_NST; ++b) {
@@ -1320,6 +1383,10 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
     const int kv = warp == 4 ? 0 : 1;
     uint64_t* fullb = kv ? s_fv : s_fk;
     uint64_t* emptyb = kv ? s_ev : s_ek;
+    // Called by the whole warp: lane 0 keeps the barrier's byte count, and
+    // lane 2 * pg + half issues the box of (page pg, half) itself, so a
+    // chunk's boxes go out in parallel (each issuing thread's TMA copies are
+    // served one after another, and a box here is only 2 KB).
     auto stage_tma = [&](int st, int buf, int part) {
       uint8_t* sT = smc + buf * CL_STAGE + kv * 2 * CL_HALF;
       const uint32_t bar = smem_addr(&fullb[buf]);
@@ -1330,24 +1397,23 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
         const int page = s_pg[st * ppc + pg];
         return ((old ? 1 : 2) & part) && page >= 0 && page < p.n_pages;
       };
-      uint32_t bytes = 0;
-      for (int pg = 0; pg < npg; ++pg)
-        if (wanted(pg)) bytes += 2u * (uint32_t)PT * 128u;
-      if (part == 1) {
-        if (bytes) cl_expect_tx(bar, bytes);
-      } else {
-        cl_arrive_expect_tx(bar, bytes);
+      if (lane == 0) {
+        uint32_t bytes = 0;
+        for (int pg = 0; pg < npg; ++pg)
+          if (wanted(pg)) bytes += 2u * (uint32_t)PT * 128u;
+        if (part == 1) {
+          if (bytes) cl_expect_tx(bar, bytes);
+        } else {
+          cl_arrive_expect_tx(bar, bytes);
+        }
       }
-      for (int pg = 0; pg < npg; ++pg) {
-        if (!wanted(pg)) continue;
+      const int pg = lane >> 1, half = lane & 1;
+      if (pg < npg && wanted(pg)) {
         const int page = s_pg[st * ppc + pg];
-#pragma unroll
-        for (int half = 0; half < 2; ++half)
-          tma_kv(smem_addr(sT + half * CL_HALF + pg * PT * 128), &kvmap, bar, half, (page * 2 + kv) * p.Hkv + h);
+        tma_kv(smem_addr(sT + half * CL_HALF + pg * PT * 128), &kvmap, bar, half, (page * 2 + kv) * p.Hkv + h);
       }
     };
-    if (lane == 0)
-      for (int st = 0; st < TP_NST && st < nmine; ++st) stage_tma(st, st, 1);
+    for (int st = 0; st < TP_NST && st < nmine; ++st) stage_tma(st, st, 1);
     pdl_wait();
     int issued = 0;
     for (int st = 0; st < nsteps; ++st) {
@@ -1355,7 +1421,7 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
       if (st >= TP_NST) {
         // the tile is free once chunk st - TP_NST's S (keys) or P V (values) has finished
         bool ok = true;
-        if (lane == 0) ok = cl_wait_bar(smem_addr(&emptyb[buf]), (uint32_t)((st / TP_NST) - 1) & 1u, p.err);
+        if (lane == 0) ok = cl_wait_fast(smem_addr(&emptyb[buf]), (uint32_t)((st / TP_NST) - 1) & 1u, p.err);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok || *reinterpret_cast<volatile int*>(&s_failed)) {
           s_failed = 1;
@@ -1363,7 +1429,7 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
         }
       }
       if (st < nmine) {
-        if (lane == 0) stage_tma(st, buf, st < TP_NST ? 2 : 3);
+        stage_tma(st, buf, st < TP_NST ? 2 : 3);
       } else {
         // the drafter's block rows (keys past the block read as zeros)
         uint8_t* sT = smc + buf * CL_STAGE + kv * 2 * CL_HALF;
@@ -1393,16 +1459,24 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
     // ================================================================ MMA issuer
     asm volatile("bar.sync 1, 160;" ::: "memory");  // the Q tile is in shared memory
     if (lane == 0 && nsteps > 0) {
-      const uint32_t qbase = smem_addr(smc + TP_QOFF);
+      // Shared-memory descriptors are computed once: a descriptor's start
+      // address field is the byte address / 16, so an operand at a constant
+      // offset is the base descriptor plus offset / 16 (no carry: every
+      // address is below 256 KB).
+      const uint64_t qd = tc_desc(smem_addr(smc + TP_QOFF), 16);
+      const uint64_t kd = tc_desc(smem_addr(smc), 16);
+      const uint64_t pd = tc_desc(smem_addr(smc + TP_POFF), 16);
+      const uint64_t vd = tc_desc(smem_addr(smc + 2 * CL_HALF), CL_HALF);
       auto issue_s = [&](int i) -> bool {
         const int buf = i % TP_NST;
-        if (!cl_wait_bar(smem_addr(&s_fk[buf]), (uint32_t)(i / TP_NST) & 1u, p.err)) return false;
+        if (!cl_wait_fast(smem_addr(&s_fk[buf]), (uint32_t)(i / TP_NST) & 1u, p.err)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t kbase = smem_addr(smc + buf * CL_STAGE);
+        const uint64_t kb = kd + (uint64_t)((buf * CL_STAGE) >> 4);
+        const uint32_t dst = tmem + (uint32_t)(i & 1) * 64u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma(tmem + (uint32_t)(i & 1) * 64u, tc_desc(qbase + (kk >> 2) * TC_QHALF + (kk & 3) * 32, 16),
-                 tc_desc(kbase + (kk >> 2) * CL_HALF + (kk & 3) * 32, 16), TC_IDESC_S, kk > 0 ? 1u : 0u);
+          tc_mma(dst, qd + (uint64_t)(((kk >> 2) * TC_QHALF + (kk & 3) * 32) >> 4),
+                 kb + (uint64_t)(((kk >> 2) * CL_HALF + (kk & 3) * 32) >> 4), TC_IDESC_S, kk > 0 ? 1u : 0u);
         tc_commit(smem_addr(&s_bs[i & 1]));
         tc_commit(smem_addr(&s_ek[buf]));  // the key tile is free once S_i has read it
         return true;
@@ -1410,17 +1484,17 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
       bool ok = issue_s(0);
       if (ok && nsteps > 1) ok = issue_s(1);
       for (int i = 0; ok && i < nsteps; ++i) {
-        if (!cl_wait_bar(smem_addr(&s_bp[i & 1]), (uint32_t)(i >> 1) & 1u, p.err) ||
-            !cl_wait_bar(smem_addr(&s_fv[i % TP_NST]), (uint32_t)(i / TP_NST) & 1u, p.err)) {
+        if (!cl_wait_fast(smem_addr(&s_bp[i & 1]), (uint32_t)(i >> 1) & 1u, p.err) ||
+            !cl_wait_fast(smem_addr(&s_fv[i % TP_NST]), (uint32_t)(i / TP_NST) & 1u, p.err)) {
           ok = false;
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t vbase = smem_addr(smc + (i % TP_NST) * CL_STAGE) + 2 * CL_HALF;
-        const uint32_t pbase = smem_addr(smc + TP_POFF + (i & 1) * 128 * 128);
+        const uint64_t vb = vd + (uint64_t)(((i % TP_NST) * CL_STAGE) >> 4);
+        const uint64_t pb = pd + (uint64_t)(((i & 1) * 128 * 128) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma(tmem + 128u, tc_desc(pbase + kk * 32, 16), tc_desc(vbase + kk * 2048, CL_HALF), TC_IDESC_PV,
+          tc_mma(tmem + 128u, pb + (uint64_t)((kk * 32) >> 4), vb + (uint64_t)((kk * 2048) >> 4), TC_IDESC_PV,
                  (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(smem_addr(&s_bpv[i & 1]));
         tc_commit(smem_addr(&s_ev[i % TP_NST]));  // the value tile is free once P_i V_i has read it
@@ -1449,6 +1523,18 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("bar.arrive 1, 160;" ::: "memory");
+    // which of this CTA's chunks need zeros in their value tile (keys past the
+    // tile's longest row, or a page the table does not hold), once for all
+    for (int st = threadIdx.x; st < nmine && st < MAXPG; st += 128) {
+      const int nkeys = min(MC, max_len - (j + CLA * st) * MC);
+      bool part = nkeys < MC;
+      for (int pg = 0; pg < (nkeys + PT - 1) / PT; ++pg) {
+        const int page = s_pg[st * ppc + pg];
+        part = part || page < 0 || page >= p.n_pages;
+      }
+      s_part[st] = part ? 1 : 0;
+    }
+    asm volatile("bar.sync 3, 128;" ::: "memory");
 
     const int trow = threadIdx.x;  // tensor-memory lane = MMA row
     const int half = lane >> 4;    // DUP: this thread's keys of a chunk are half * 32 + [0, 32)
@@ -1523,12 +1609,7 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
       // row, or a page the table does not hold) read as zeros in P V
       if (!is_blk) {
         const int nkeys = min(MC, max_len - key0);
-        bool partial = nkeys < MC;
-        for (int pg = 0; pg < (nkeys + PT - 1) / PT && !partial; ++pg) {
-          const int page = s_pg[i * ppc + pg];
-          partial = page < 0 || page >= p.n_pages;
-        }
-        if (partial) {
+        if (s_part[i]) {
           // the value tile has landed (its barrier cannot run ahead: the tile is refilled only after P_i V_i)
           if (!tp_wait_warp(smem_addr(&s_fv[i % TP_NST]), (uint32_t)(i / TP_NST) & 1u, p.err)) {
             failed = true;

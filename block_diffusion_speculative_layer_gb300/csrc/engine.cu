@@ -429,7 +429,7 @@ df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiPar
   ProfScope ps(H, cls, H->bf16 ? 1 : 2, gemm_bytes(H, W, M, ep), 2.0 * M * W.N * W.K);
   if (H->bf16) {
     const int splits = tc_splits(W.N, W.K, H->split_target);
-    const int wide = tc_wide_tile(M, W.N);
+    const int wide = tc_wide_tile(M, W.N, W.K, splits);
     const int nt = wide ? wide : tc_token_tile(M);
     const void* tmX = nullptr;
     CKS(xmap(H, X, W.K, nt, &tmX));
@@ -1945,7 +1945,7 @@ df_status df_op_gemm_bf16(const void* x_dev, const void* w_dev, float* y_dev, in
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int sp = splits ? splits : tc_splits(N, K, tc_split_target(sms));
   if (sp < 1 || sp > K / 64) return DF_EINVAL;
-  const int wide = token_tile < 0 ? -token_tile : (token_tile == 0 ? tc_wide_tile(M, N) : 0);
+  const int wide = token_tile < 0 ? -token_tile : (token_tile == 0 ? tc_wide_tile(M, N, K, sp) : 0);
   const int nt = wide ? wide : (token_tile ? token_tile : tc_token_tile(M));
   if (wide ? (nt != 64 && nt != 128) : (nt != 16 && nt != 32 && nt != 64 && nt != 128 && nt != 256)) return DF_EINVAL;
   Tmap tw, tx;
@@ -2030,7 +2030,7 @@ df_status df_op_lmhead_argmax_bf16(const void* x_dev, const void* wlm_dev, int32
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int sp = tc_splits(V, K, tc_split_target(sms));
-  const int wide = tc_wide_tile(M, V);  // the engine's choice of form
+  const int wide = tc_wide_tile(M, V, K, sp);  // the engine's choice of form
   const int nt = wide ? wide : tc_token_tile(M);
   Tmap tw, tx;
   if (!make_tmap_bf16(tw.b, wlm_dev, V, K, 128) || !make_tmap_bf16(tx.b, x_dev, M, K, nt)) return DF_EINVAL;
@@ -2069,7 +2069,7 @@ df_status df_op_bench_gemm_bf16(const void* x_dev, const void* w_dev, float* y_d
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int sp = splits ? splits : tc_splits(N, K, tc_split_target(sms));
   if (sp < 1 || sp > K / 64) return DF_EINVAL;
-  const int wide = token_tile < 0 ? -token_tile : (token_tile == 0 ? tc_wide_tile(M, N) : 0);
+  const int wide = token_tile < 0 ? -token_tile : (token_tile == 0 ? tc_wide_tile(M, N, K, sp) : 0);
   const int nt = wide ? wide : (token_tile ? token_tile : tc_token_tile(M));
   if (wide ? (nt != 64 && nt != 128) : (nt != 16 && nt != 32 && nt != 64 && nt != 128 && nt != 256)) return DF_EINVAL;
   Tmap tw, tx;

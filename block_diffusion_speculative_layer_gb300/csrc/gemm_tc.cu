@@ -162,9 +162,9 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int NT>
+template <int NT, int ST = 0>
 struct TcCfg {
-  static constexpr int STAGES = NT <= 16 ? 6 : NT <= 32 ? 5 : 4;
+  static constexpr int STAGES = ST ? ST : NT <= 16 ? 6 : NT <= 32 ? 5 : 4;
   static constexpr int W_BYTES = BM * BK * 2;
   static constexpr int X_BYTES = NT * BK * 2;
   static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
@@ -176,11 +176,11 @@ struct TcCfg {
   static_assert((TLD * 4) % 16 == 0, "tile rows must stay 16-byte aligned for vector copies");
 };
 
-template <int NT>
+template <int NT, int ST>
 __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUtensorMap& tmX, int M, int N, int K,
                                              int splits, float* __restrict__ ws, int* __restrict__ counters,
                                              int creduce, const EpiParams& ep) {
-  using C = TcCfg<NT>;
+  using C = TcCfg<NT, ST>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sW = smem;
@@ -230,35 +230,45 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   // at once.
   const bool late_trigger = ep.kind == EPI_QKV;
   if (!late_trigger) pdl_trigger();
-  if (warp == 0 && lane == 0) {
-    // ---- TMA producer
+  if (warp == 0 && lane < 2) {
+    // ---- TMA producers: lane 0 the weight tiles (and each stage's byte count),
+    // lane 1 the token tiles, so the two copies of a stage are issued in
+    // parallel (one thread's TMA copies are served one after another)
     const uint64_t pol_w = policy_evict_first();  // weights are read once per launch
     const uint64_t pol_x = policy_evict_last();   // activations are re-read by every weight tile
     // The weights do not depend on the kernel before this one: fill the first
     // stages with weight tiles while it drains, then wait for its outputs.
     const int pre = nk < C::STAGES ? nk : C::STAGES;
-    for (int i = 0; i < pre; ++i) {
-      mbar_expect_tx(full0 + 8 * i, C::STAGE_BYTES);
-      tma_load_2d(smem_u32(sW + i * C::W_BYTES), &tmW, full0 + 8 * i, (kb0 + i) * BK, n0, pol_w);
-    }
+    if (lane == 0)
+      for (int i = 0; i < pre; ++i) {
+        mbar_expect_tx(full0 + 8 * i, C::STAGE_BYTES);
+        tma_load_2d(smem_u32(sW + i * C::W_BYTES), &tmW, full0 + 8 * i, (kb0 + i) * BK, n0, pol_w);
+      }
     pdl_wait();
     if (late_trigger) pdl_trigger();
-    for (int i = 0; i < pre; ++i)
-      tma_load_2d(smem_u32(sX + i * C::X_BYTES), &tmX, full0 + 8 * i, (kb0 + i) * BK, m0, pol_x);
+    if (lane == 1)
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d(smem_u32(sX + i * C::X_BYTES), &tmX, full0 + 8 * i, (kb0 + i) * BK, m0, pol_x);
     int i = pre;
     for (; i < nk; ++i) {
       const int s = i % C::STAGES;
       const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
-      if (i >= C::STAGES && !mbar_wait(empty0 + 8 * s, ph ^ 1u, ep.err)) {
+      int ok = 1;
+      if (lane == 0) ok = (i < C::STAGES || mbar_wait(empty0 + 8 * s, ph ^ 1u, ep.err)) ? 1 : 0;
+      ok = __shfl_sync(0x3u, ok, 0);
+      if (!ok) {
         flags[2] = 1;
         break;
       }
-      mbar_expect_tx(full0 + 8 * s, C::STAGE_BYTES);
       const int kc = (kb0 + i) * BK;
-      tma_load_2d(smem_u32(sW + s * C::W_BYTES), &tmW, full0 + 8 * s, kc, n0, pol_w);
-      tma_load_2d(smem_u32(sX + s * C::X_BYTES), &tmX, full0 + 8 * s, kc, m0, pol_x);
+      if (lane == 0) {
+        mbar_expect_tx(full0 + 8 * s, C::STAGE_BYTES);
+        tma_load_2d(smem_u32(sW + s * C::W_BYTES), &tmW, full0 + 8 * s, kc, n0, pol_w);
+      } else {
+        tma_load_2d(smem_u32(sX + s * C::X_BYTES), &tmX, full0 + 8 * s, kc, m0, pol_x);
+      }
     }
-    flags[3] = i;
+    if (lane == 0) flags[3] = i;
   } else {
     pdl_wait();
     if (late_trigger) pdl_trigger();
@@ -423,13 +433,13 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
                                (have_pre && splits == 1) ? &pre : nullptr);
 }
 
-template <int NT>
+template <int NT, int ST = 0>
 __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                       const __grid_constant__ CUtensorMap tmX, int M, int N, int K,
                                                       int splits, float* __restrict__ ws, int* __restrict__ counters,
                                                       int creduce, EpiParams ep) {
   trace_entry(ep.trace);
-  gemm_tc_body<NT>(tmW, tmX, M, N, K, splits, ws, counters, creduce, ep);
+  gemm_tc_body<NT, ST>(tmW, tmX, M, N, K, splits, ws, counters, creduce, ep);
   trace_exit(ep.trace);
 }
 
@@ -547,33 +557,41 @@ __device__ __forceinline__ void gemm_tcw_body(const CUtensorMap& tmW, const CUte
   constexpr bool RTMEM = W::RTMEM;
   float R[RTMEM ? 1 : NT];
   if (warp == 4) {
-    if (lane == 0) {
-      // ---- TMA producer: the tile's whole K, weight tiles of the first stages before the wait
+    if (lane < 2) {
+      // ---- TMA producers, the tile's whole K: lane 0 the weight tiles (of the
+      // first stages before the wait) and the byte counts, lane 1 the token tiles
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       const int pre = nkb < STAGES ? nkb : STAGES;
-      for (int i = 0; i < pre; ++i) {
-        mbar_expect_tx(full0 + 8 * i, C::STAGE_BYTES);
-        tma_load_2d(smem_u32(sW + i * C::W_BYTES), &tmW, full0 + 8 * i, i * BK, n0, pol_w);
-      }
+      if (lane == 0)
+        for (int i = 0; i < pre; ++i) {
+          mbar_expect_tx(full0 + 8 * i, C::STAGE_BYTES);
+          tma_load_2d(smem_u32(sW + i * C::W_BYTES), &tmW, full0 + 8 * i, i * BK, n0, pol_w);
+        }
       pdl_wait();
       if (late_trigger) pdl_trigger();
-      for (int i = 0; i < pre; ++i)
-        tma_load_2d(smem_u32(sX + i * C::X_BYTES), &tmX, full0 + 8 * i, i * BK, m0, pol_x);
+      if (lane == 1)
+        for (int i = 0; i < pre; ++i)
+          tma_load_2d(smem_u32(sX + i * C::X_BYTES), &tmX, full0 + 8 * i, i * BK, m0, pol_x);
       int i = pre;
       for (; i < nkb; ++i) {
         const int s = i % STAGES;
         const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
-        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, ep.err)) {
+        int ok = 1;
+        if (lane == 0) ok = (mbar_wait(empty0 + 8 * s, ph ^ 1u, ep.err) && !flags[0]) ? 1 : 0;
+        ok = __shfl_sync(0x3u, ok, 0);
+        if (!ok) {
           flags[0] = 1;
           break;
         }
-        if (flags[0]) break;
-        mbar_expect_tx(full0 + 8 * s, C::STAGE_BYTES);
-        tma_load_2d(smem_u32(sW + s * C::W_BYTES), &tmW, full0 + 8 * s, i * BK, n0, pol_w);
-        tma_load_2d(smem_u32(sX + s * C::X_BYTES), &tmX, full0 + 8 * s, i * BK, m0, pol_x);
+        if (lane == 0) {
+          mbar_expect_tx(full0 + 8 * s, C::STAGE_BYTES);
+          tma_load_2d(smem_u32(sW + s * C::W_BYTES), &tmW, full0 + 8 * s, i * BK, n0, pol_w);
+        } else {
+          tma_load_2d(smem_u32(sX + s * C::X_BYTES), &tmX, full0 + 8 * s, i * BK, m0, pol_x);
+        }
       }
-      flags[2] = i;
+      if (lane == 0) flags[2] = i;
     } else {
       pdl_wait();
       if (late_trigger) pdl_trigger();
@@ -778,10 +796,28 @@ size_t tc_workspace_floats(int M, int N, int splits, int nt) {
 size_t tc_counter_ints(int M, int N, int nt) { return (size_t)(N / BM) * ((M + nt - 1) / nt); }
 
 bool tc_cluster_reduce(int nt, int splits);
+static bool tc_cluster_reduce_qkv16(int splits);
 
-template <int NT>
+template <int NT, int ST = 0>
 static cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<NT>::SMEM);
+  return cudaFuncSetAttribute(gemm_tc_kernel<NT, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TcCfg<NT, ST>::SMEM);
+}
+
+// Stages of the key/value GEMM at 16 token rows: 6 (the 16-token default), or
+// 4 with DF_QKV_STAGES=4 in the environment, which leaves room on every SM
+// for an attention CTA next to two GEMM CTAs so that the attention's setup
+// can run while the GEMM streams.  Measured in the decode chain the 4-stage
+// ring was slower (q|k|v 14.5 against 13.8 us, attention 13.6 against
+// 13.2 us), so 6 stays the default.
+constexpr int QKV_LEAN_STAGES = 4;
+static bool qkv_lean() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("DF_QKV_STAGES");
+    v = (e && atoi(e) == 4) ? 1 : 0;
+  }
+  return v == 1;
 }
 
 // Set every token-tile variant's shared-memory limit up front (before any
@@ -790,7 +826,9 @@ cudaError_t tc_prepare() {
   for (int nt = 16; nt <= 256; nt *= 2)
     for (int cz = 2; cz <= 8; ++cz) tc_cluster_reduce(nt, cz);
   cudaError_t e;
+  for (int cz = 2; cz <= 8; ++cz) tc_cluster_reduce_qkv16(cz);
   if ((e = set_smem_attr<16>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<16, QKV_LEAN_STAGES>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<32>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<64>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<128>()) != cudaSuccess) return e;
@@ -804,7 +842,7 @@ cudaError_t tc_prepare() {
 // Whether clusters of cz CTAs of this token-tile variant can be resident
 // (asked once per variant and size; DF_NO_CLUSTER=1 in the environment
 // turns cluster reduction off).
-template <int NT>
+template <int NT, int ST = 0>
 static bool cluster_fits(int cz) {
   static int known[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // 0 unknown, 1 yes, 2 no
   if (cz < 2 || cz > 8) return false;
@@ -812,11 +850,11 @@ static bool cluster_fits(int cz) {
     const char* env = getenv("DF_NO_CLUSTER");
     bool ok = !(env && env[0] == '1');
     if (ok) {
-      ok = set_smem_attr<NT>() == cudaSuccess;
+      ok = set_smem_attr<NT, ST>() == cudaSuccess;
       cudaLaunchConfig_t c = {};
       c.gridDim = dim3(1, 1, cz);
       c.blockDim = dim3(128);
-      c.dynamicSmemBytes = TcCfg<NT>::SMEM;
+      c.dynamicSmemBytes = TcCfg<NT, ST>::SMEM;
       cudaLaunchAttribute a[1];
       a[0].id = cudaLaunchAttributeClusterDimension;
       a[0].val.clusterDim.x = 1;
@@ -825,13 +863,15 @@ static bool cluster_fits(int cz) {
       c.attrs = a;
       c.numAttrs = 1;
       int n = 0;
-      ok = ok && cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<NT>, &c) == cudaSuccess && n > 0;
+      ok = ok && cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<NT, ST>, &c) == cudaSuccess && n > 0;
       cudaGetLastError();
     }
     known[cz] = ok ? 1 : 2;
   }
   return known[cz] == 1;
 }
+
+static bool tc_cluster_reduce_qkv16(int splits) { return cluster_fits<16, QKV_LEAN_STAGES>(splits); }
 
 bool tc_cluster_reduce(int nt, int splits) {
   switch (nt) {
@@ -844,30 +884,37 @@ bool tc_cluster_reduce(int nt, int splits) {
   }
 }
 
-template <int NT>
+template <int NT, int ST = 0>
 static cudaError_t launch_nt(const void* tmW, const void* tmX, int M, int N, int K, int splits, float* ws,
                              int* counters, const EpiParams& ep, bool creduce, cudaStream_t st) {
-  using C = TcCfg<NT>;
+  using C = TcCfg<NT, ST>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_kernel<NT, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid(N / BM, (M + NT - 1) / NT, splits);
   const int cz = (creduce && splits > 1) ? splits : 1;
-  return launch_kc(gemm_tc_kernel<NT>, grid, dim3(128), (size_t)C::SMEM, st, cz,
+  return launch_kc(gemm_tc_kernel<NT, ST>, grid, dim3(128), (size_t)C::SMEM, st, cz,
                    *reinterpret_cast<const CUtensorMap*>(tmW), *reinterpret_cast<const CUtensorMap*>(tmX), M, N, K,
                    splits, ws, counters, cz > 1 ? 1 : 0, ep);
 }
 
-// Token tile of the serial-split form for an M-row GEMM with N outputs (0:
-// the split-K form).  Beyond 128 token rows the split-K form's tiles fill an
-// SM each and its clusters run in waves; the serial-split form takes over
-// with 64-token tiles.  (At 128 rows the split-K form is as fast or faster:
-// 45 against 69 us for the 4096 x 12288 down projection.)  DF_GEMM_WIDE=0 in
-// the environment turns it off; DF_GEMM_WIDE_MIN=m moves the threshold.
-int tc_wide_tile(int M, int N) {
+// Token tile of the serial-split form for an M-row GEMM of an N x K weight
+// cut into `splits` K ranges (0: the split-K form).  Beyond 128 token rows
+// the split-K form's 256-token tiles fill an SM each and its clusters run in
+// waves; where the K ranges are short (K / splits <= 1024) that wave and
+// reduction overhead dominates and the serial-split form with 64-token tiles
+// is faster (at 256 rows: o projection 37.6 -> 28.8 us, q|k|v 31.0 -> 27.5);
+// with long ranges (the down projection, 1536 per range: 56.2 against
+// 69.4 us) or a single range (gate|up, the LM head: no cluster at all) the
+// split-K form reads each weight tile once per 256 tokens and stays.  At 128
+// rows the split-K form is as fast or faster everywhere.  DF_GEMM_WIDE=0 in
+// the environment turns the serial-split form off; DF_GEMM_WIDE_MIN=m moves
+// the row threshold.
+int tc_wide_tile(int M, int N, int K, int splits) {
   static int min_m = -1;
   if (min_m < 0) {
     const char* off = getenv("DF_GEMM_WIDE");
@@ -876,7 +923,7 @@ int tc_wide_tile(int M, int N) {
     if (min_m < 1) min_m = 1;
   }
   (void)N;
-  return M < min_m ? 0 : 64;
+  return (M >= min_m && splits > 1 && K / splits <= 1024) ? 64 : 0;
 }
 
 template <int NT>
@@ -910,7 +957,11 @@ cudaError_t launch_gemm_tc(const void* tmW, const void* tmX, int nt, int M, int 
   if (N % BM || K % BK || M < 1 || splits < 1 || splits > K / BK) return cudaErrorInvalidValue;
   if (creduce && splits > 8) return cudaErrorInvalidValue;  // a portable cluster holds at most 8 CTAs
   switch (nt) {
-    case 16: return launch_nt<16>(tmW, tmX, M, N, K, splits, ws, counters, ep, creduce, st);
+    case 16:
+      if (ep.kind == EPI_QKV && qkv_lean())  // same split, same MMA order: the same bits
+        return launch_nt<16, QKV_LEAN_STAGES>(tmW, tmX, M, N, K, splits, ws, counters, ep,
+                                              creduce && tc_cluster_reduce_qkv16(splits), st);
+      return launch_nt<16>(tmW, tmX, M, N, K, splits, ws, counters, ep, creduce, st);
     case 32: return launch_nt<32>(tmW, tmX, M, N, K, splits, ws, counters, ep, creduce, st);
     case 64: return launch_nt<64>(tmW, tmX, M, N, K, splits, ws, counters, ep, creduce, st);
     case 128: return launch_nt<128>(tmW, tmX, M, N, K, splits, ws, counters, ep, creduce, st);

@@ -70,9 +70,9 @@ cudaError_t launch_gemm_tc(const void* tmW, const void* tmX, int nt, int M, int 
                            int* counters, const EpiParams& ep, cudaStream_t st, bool cluster_reduce = false);
 // Serial-split form (one CTA per weight tile and token tile runs all `splits`
 // K ranges and adds them in split order: bitwise the split-K form's result).
-// nt is 64 or 128; the X map's box has nt rows.  tc_wide_tile(M, N) is the
-// engine's choice of nt for M token rows, 0 for the split-K form.
-int tc_wide_tile(int M, int N);
+// nt is 64 or 128; the X map's box has nt rows.  tc_wide_tile(M, N, K,
+// splits) is the engine's choice of nt for M token rows, 0 for the split-K form.
+int tc_wide_tile(int M, int N, int K, int splits);
 cudaError_t launch_gemm_tcw(const void* tmW, const void* tmX, int nt, int M, int N, int K, int splits,
                             const EpiParams& ep, cudaStream_t st);
 

@@ -142,10 +142,11 @@ def test_gemm_wide_matches_float64_and_split_k(dfl, M, N, K, splits, nt):
     np.testing.assert_array_equal(y, ref)
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 6144, 4096), (256, 4096, 12288), (144, 24576, 4096)])
+@pytest.mark.parametrize("M,N,K", [(256, 6144, 4096), (256, 4096, 4096), (256, 4096, 12288), (144, 24576, 4096)])
 def test_gemm_wide_engine_shapes_bitwise(dfl, M, N, K):
-    # the engine's own choice (token_tile 0 picks the serial-split form here) against
-    # the split-K form with 16-token tiles, on the verify pass shapes of a 16-sequence batch
+    # the engine's own choice (token_tile 0: the serial-split form for the first two
+    # shapes, the split-K form with 256-token tiles for the others) against the
+    # split-K form with 16-token tiles, on the verify pass shapes of a 16-sequence batch
     x, w = inputs(M, N, K, seed=17)
     xd, wd = dev_bf16(x), dev_bf16(w)
     a = dfl.gemm_bf16(xd, wd).cpu().numpy()
