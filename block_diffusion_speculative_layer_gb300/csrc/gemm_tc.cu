@@ -81,6 +81,11 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) 
   return false;
 }
 
+// One test inline first; the bounded loop is an out-of-line call.
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, int* err) {
+  return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, err);
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
                                             uint64_t policy) {
   asm volatile(
@@ -254,7 +259,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
       const int s = i % C::STAGES;
       const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
       int ok = 1;
-      if (lane == 0) ok = (i < C::STAGES || mbar_wait(empty0 + 8 * s, ph ^ 1u, ep.err)) ? 1 : 0;
+      if (lane == 0) ok = (i < C::STAGES || mbar_wait_fast(empty0 + 8 * s, ph ^ 1u, ep.err)) ? 1 : 0;
       ok = __shfl_sync(0x3u, ok, 0);
       if (!ok) {
         flags[2] = 1;
@@ -276,20 +281,22 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   if (warp == 1 && lane == 0) {
     // ---- MMA issuer
     constexpr uint32_t idesc = idesc_bf16(BM, NT);
+    // descriptors computed once: an operand at a constant offset is the base
+    // descriptor plus offset / 16 (the start-address field; addresses < 256 KB)
+    const uint64_t dw0 = desc_sw128(smem_u32(sW)), dx0 = desc_sw128(smem_u32(sX));
     int i = 0;
     for (; i < nk; ++i) {
       const int s = i % C::STAGES;
       const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
-      if (!mbar_wait(full0 + 8 * s, ph, ep.err)) {
+      if (!mbar_wait_fast(full0 + 8 * s, ph, ep.err)) {
         flags[2] = 1;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t aw = smem_u32(sW + s * C::W_BYTES);
-      const uint32_t ax = smem_u32(sX + s * C::X_BYTES);
+      const uint64_t dw = dw0 + (uint64_t)((s * C::W_BYTES) >> 4), dx = dx0 + (uint64_t)((s * C::X_BYTES) >> 4);
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk) {
-        mma_bf16(tmem, desc_sw128(aw + kk * 32), desc_sw128(ax + kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_bf16(tmem, dw + (uint64_t)(kk * 2), dx + (uint64_t)(kk * 2), idesc, (i > 0 || kk > 0) ? 1u : 0u);
       }
       mma_commit(empty0 + 8 * s);
     }
@@ -578,7 +585,7 @@ __device__ __forceinline__ void gemm_tcw_body(const CUtensorMap& tmW, const CUte
         const int s = i % STAGES;
         const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
         int ok = 1;
-        if (lane == 0) ok = (mbar_wait(empty0 + 8 * s, ph ^ 1u, ep.err) && !flags[0]) ? 1 : 0;
+        if (lane == 0) ok = (mbar_wait_fast(empty0 + 8 * s, ph ^ 1u, ep.err) && !flags[0]) ? 1 : 0;
         ok = __shfl_sync(0x3u, ok, 0);
         if (!ok) {
           flags[0] = 1;
@@ -602,12 +609,13 @@ __device__ __forceinline__ void gemm_tcw_body(const CUtensorMap& tmW, const CUte
     if (lane == 0) {
       // ---- MMA issuer: split q into accumulator q & 1, reused once the fold of split q - 2 is done
       constexpr uint32_t idesc = idesc_bf16(BM, NT);
+      const uint64_t dw0 = desc_sw128(smem_u32(sW)), dx0 = desc_sw128(smem_u32(sX));
       int i = 0;
       bool ok = true;
       for (int q = 0; q < splits && ok; ++q) {
         const int kb0 = (int)((long long)nkb * q / splits), kb1 = (int)((long long)nkb * (q + 1) / splits);
         const int b = q & 1;
-        if (q >= 2 && !mbar_wait(aempty0 + 8 * b, (uint32_t)((q - 2) >> 1) & 1u, ep.err)) {
+        if (q >= 2 && !mbar_wait_fast(aempty0 + 8 * b, (uint32_t)((q - 2) >> 1) & 1u, ep.err)) {
           ok = false;
           break;
         }
@@ -615,16 +623,15 @@ __device__ __forceinline__ void gemm_tcw_body(const CUtensorMap& tmW, const CUte
         for (int kb = kb0; kb < kb1; ++kb, ++i) {
           const int s = i % STAGES;
           const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
-          if (!mbar_wait(full0 + 8 * s, ph, ep.err)) {
+          if (!mbar_wait_fast(full0 + 8 * s, ph, ep.err)) {
             ok = false;
             break;
           }
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          const uint32_t aw = smem_u32(sW + s * C::W_BYTES);
-          const uint32_t ax = smem_u32(sX + s * C::X_BYTES);
+          const uint64_t dw = dw0 + (uint64_t)((s * C::W_BYTES) >> 4), dx = dx0 + (uint64_t)((s * C::X_BYTES) >> 4);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16(tmem + (uint32_t)(b * NT), desc_sw128(aw + kk * 32), desc_sw128(ax + kk * 32), idesc,
+            mma_bf16(tmem + (uint32_t)(b * NT), dw + (uint64_t)(kk * 2), dx + (uint64_t)(kk * 2), idesc,
                      (kb > kb0 || kk > 0) ? 1u : 0u);
           mma_commit(empty0 + 8 * s);
         }
@@ -642,7 +649,7 @@ __device__ __forceinline__ void gemm_tcw_body(const CUtensorMap& tmW, const CUte
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     for (int q = 0; q < splits; ++q) {
       const int b = q & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(afull0 + 8 * b, (uint32_t)(q >> 1) & 1u, ep.err))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_fast(afull0 + 8 * b, (uint32_t)(q >> 1) & 1u, ep.err))) {
         flags[0] = 1;
         break;
       }
