@@ -568,6 +568,14 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
     uint8_t* sV = sK + 2 * CL_HALF;
     const int key0 = (j + CLA * st) * MC;
     const int nkeys = min(MC, max_len - key0);
+    if (nkeys == MC) {  // a full chunk whose pages are all in the table needs nothing (the usual case)
+      bool all = true;
+      for (int pg = 0; pg < ppc; ++pg) {
+        const int page = s_pg[st * ppc + pg];
+        all = all && page >= 0 && page < p.n_pages;
+      }
+      if (all) return;
+    }
     for (int idx = threadIdx.x; idx < MC * (MHD / 8); idx += blockDim.x) {
       const int key = idx >> 4, b = idx & 15;
       const int page = s_pg[st * ppc + key / PT];
@@ -616,7 +624,9 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
   for (int st = 0; st < nsteps; ++st) {
     const int buf = st % CL_NST;
     if (st >= nmine) cp_async_wait_0();  // the block rows (this thread's copies)
-    if (!cl_wait_bar(smem_addr(&s_full[buf]), (uint32_t)(st / CL_NST) & 1u, p.err)) s_failed = 1;
+    if (!cl_try_wait(smem_addr(&s_full[buf]), (uint32_t)(st / CL_NST) & 1u) &&
+        !cl_wait_bar(smem_addr(&s_full[buf]), (uint32_t)(st / CL_NST) & 1u, p.err))
+      s_failed = 1;
     fixup(st, buf);
     __syncthreads();
     if (s_failed) break;

@@ -129,6 +129,9 @@ struct EpiParams {
   // In-situ timing (null: off): trace[0] = max over CTAs of ~(entry time),
   // trace[1] = max over CTAs of the exit time, in device-timer nanoseconds.
   unsigned long long* trace;
+  // weight tiles past the shared-memory ring prefetched into L2 before the
+  // programmatic wait (split-K form; 0 = none)
+  int l2_prefetch;
 };
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }

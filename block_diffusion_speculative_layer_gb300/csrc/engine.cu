@@ -67,6 +67,7 @@ struct df_handle {
   int sm_count = 152;
   bool attn_pipe = false;  // bf16 attention on the pipelined tcgen05 kernel (df_config.attn_kernel)
   int split_target = 253;  // CTAs a split-K GEMM aims for (DF_SPLIT_CTAS overrides tc_split_target)
+  int l2_prefetch = 0;     // weight tiles a GEMM prefetches into L2 past its ring before its wait (DF_GEMM_L2PF)
   int tap_of_layer[1024];  // zero-based layer index -> tap slot (or -1)
   int Mmax = 0;
 
@@ -435,6 +436,7 @@ df_status gemm(df_handle* H, const Linear& W, const void* X, int M, const EpiPar
     CKS(xmap(H, X, W.K, nt, &tmX));
     EpiParams e = ep;
     e.trace = ps.tp;
+    e.l2_prefetch = H->l2_prefetch;
     if (wide) {
       CK(launch_gemm_tcw(W.tm.b, tmX, nt, M, W.N, W.K, splits, e, H->st));
     } else {
@@ -1436,6 +1438,8 @@ df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_we
   {
     const char* sc = getenv("DF_SPLIT_CTAS");
     if (sc && atoi(sc) > 0) H->split_target = atoi(sc);
+    const char* pf = getenv("DF_GEMM_L2PF");
+    if (pf && atoi(pf) > 0) H->l2_prefetch = std::min(atoi(pf), 64);
   }
   if (e != cudaSuccess) {
     delete H;

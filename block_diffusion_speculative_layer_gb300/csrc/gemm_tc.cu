@@ -95,6 +95,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// L2 prefetch of one tile of a tensor map (a hint: no data reaches shared memory).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // Thread-block cluster helpers (all threads of every CTA execute the barriers).
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
@@ -244,11 +251,15 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
     // The weights do not depend on the kernel before this one: fill the first
     // stages with weight tiles while it drains, then wait for its outputs.
     const int pre = nk < C::STAGES ? nk : C::STAGES;
-    if (lane == 0)
+    if (lane == 0) {
       for (int i = 0; i < pre; ++i) {
         mbar_expect_tx(full0 + 8 * i, C::STAGE_BYTES);
         tma_load_2d(smem_u32(sW + i * C::W_BYTES), &tmW, full0 + 8 * i, (kb0 + i) * BK, n0, pol_w);
       }
+      // and up to ep.l2_prefetch further weight tiles into L2 while the kernel before drains
+      const int pf_end = min(nk, pre + ep.l2_prefetch);
+      for (int i = pre; i < pf_end; ++i) tma_prefetch_2d(&tmW, (kb0 + i) * BK, n0);
+    }
     pdl_wait();
     if (late_trigger) pdl_trigger();
     if (lane == 1)
