@@ -822,20 +822,21 @@ static cudaError_t set_smem_attr() {
                               TcCfg<NT, ST>::SMEM);
 }
 
-// Stages of the key/value GEMM at 16 token rows: 6 (the 16-token default), or
-// 4 with DF_QKV_STAGES=4 in the environment, which leaves room on every SM
-// for an attention CTA next to two GEMM CTAs so that the attention's setup
-// can run while the GEMM streams.  Measured in the decode chain the 4-stage
-// ring was slower (q|k|v 14.5 against 13.8 us, attention 13.6 against
-// 13.2 us), so 6 stays the default.
+// Stages of the 16-token GEMMs: 6 (108 KB, two CTAs per SM), or 4 (73 KB, three
+// CTAs per SM) with DF_GEMM16_STAGES=4 in the environment, so that a GEMM's
+// CTAs can become resident (and prefetch their weights) next to the CTAs of
+// the GEMM before it; DF_QKV_STAGES=4 applies the 4-stage ring to the
+// key/value GEMM alone (measured slower in the decode chain: q|k|v 14.5
+// against 13.8 us).  Same splits and MMA order either way: the same bits.
 constexpr int QKV_LEAN_STAGES = 4;
-static bool qkv_lean() {
+static int lean16_mode() {  // 0: 6 stages; 1: 4 for the key/value GEMM; 2: 4 for every 16-token GEMM
   static int v = -1;
   if (v < 0) {
-    const char* e = getenv("DF_QKV_STAGES");
-    v = (e && atoi(e) == 4) ? 1 : 0;
+    const char* a = getenv("DF_GEMM16_STAGES");
+    const char* q = getenv("DF_QKV_STAGES");
+    v = (a && atoi(a) == 4) ? 2 : (q && atoi(q) == 4) ? 1 : 0;
   }
-  return v == 1;
+  return v;
 }
 
 // Set every token-tile variant's shared-memory limit up front (before any
@@ -976,7 +977,7 @@ cudaError_t launch_gemm_tc(const void* tmW, const void* tmX, int nt, int M, int 
   if (creduce && splits > 8) return cudaErrorInvalidValue;  // a portable cluster holds at most 8 CTAs
   switch (nt) {
     case 16:
-      if (ep.kind == EPI_QKV && qkv_lean())  // same split, same MMA order: the same bits
+      if (lean16_mode() == 2 || (lean16_mode() == 1 && ep.kind == EPI_QKV))  // same split and MMA order
         return launch_nt<16, QKV_LEAN_STAGES>(tmW, tmX, M, N, K, splits, ws, counters, ep,
                                               creduce && tc_cluster_reduce_qkv16(splits), st);
       return launch_nt<16>(tmW, tmX, M, N, K, splits, ws, counters, ep, creduce, st);
