@@ -1271,7 +1271,7 @@ constexpr int TP_QOFF = TP_NST * CL_STAGE;         // Q tile: two 64-dim halves 
 constexpr int TP_POFF = TP_QOFF + 2 * TC_QHALF;    // P tiles: two buffers x 128 rows x 128 B
 constexpr int TP_PGOFF = TP_POFF + 2 * 128 * 128;  // page ids of the CTA's chunks
 constexpr int TP_SMEM = TP_PGOFF + MAXPG * 4 + 1024;
-constexpr int TP_THREADS = 224;
+constexpr int TP_THREADS = 256;
 constexpr float TP_RESCALE = ATT_RESCALE;          // lazy rescale threshold (log2 units)
 static_assert(8 * 16 * TC_OLD * 4 + 8 * 16 * 8 <= TP_NST * CL_STAGE, "partials fit over the stages");
 static_assert(TP_SMEM <= 227 * 1024, "shared memory of one CTA");
@@ -1342,7 +1342,7 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
 
   // full / empty barriers of the key (k) and value (v) tiles of each stage
   __shared__ __align__(8) uint64_t s_fk[TP_NST], s_fv[TP_NST], s_ek[TP_NST], s_ev[TP_NST];
-  __shared__ __align__(8) uint64_t s_bs[2], s_bp[2], s_bpv[2], s_done;
+  __shared__ __align__(8) uint64_t s_bs[2], s_bp[2], s_bpv[2], s_sc[2], s_done, s_done_s;
   __shared__ int s_failed;
   __shared__ uint8_t s_part[MAXPG];  // per chunk of this CTA: the value tile needs zeros
   __shared__ uint32_t s_tmem;
@@ -1358,7 +1358,9 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
       tp_mbar_init(smem_addr(&s_bp[b]), 4);  // one arrival per softmax warp
       tp_mbar_init(smem_addr(&s_bpv[b]), 1);
     }
+    for (int b = 0; b < 2; ++b) tp_mbar_init(smem_addr(&s_sc[b]), 4);  // S buffer read: one arrival per softmax warp
     tp_mbar_init(smem_addr(&s_done), 1);
+    tp_mbar_init(smem_addr(&s_done_s), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kvmap)) : "memory");
     s_failed = 0;
@@ -1465,55 +1467,64 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
       for (int st = max(0, issued - TP_NST); st < issued; ++st)
         if (st < nmine) cl_wait_bar(smem_addr(&fullb[st % TP_NST]), (uint32_t)(st / TP_NST) & 1u, p.err);
     __syncwarp();
-  } else if (warp == 5) {
-    // ================================================================ MMA issuer
-    asm volatile("bar.sync 1, 160;" ::: "memory");  // the Q tile is in shared memory
+  } else if (warp == 5 || warp == 7) {
+    // ================================================================ MMA issuers
+    // Warp 7 issues S = Q K^T of every chunk, warp 5 every O += P V: each
+    // thread's tcgen05.mma instructions take long to issue, and the two
+    // chains are independent (different tensor-memory accumulators).
+    // Shared-memory descriptors are computed once: a descriptor's start
+    // address field is the byte address / 16, so an operand at a constant
+    // offset is the base descriptor plus offset / 16 (no carry: every address
+    // is below 256 KB).
+    if (warp == 7) asm volatile("bar.sync 1, 160;" ::: "memory");  // the Q tile is in shared memory
     if (lane == 0 && nsteps > 0) {
-      // Shared-memory descriptors are computed once: a descriptor's start
-      // address field is the byte address / 16, so an operand at a constant
-      // offset is the base descriptor plus offset / 16 (no carry: every
-      // address is below 256 KB).
-      const uint64_t qd = tc_desc(smem_addr(smc + TP_QOFF), 16);
-      const uint64_t kd = tc_desc(smem_addr(smc), 16);
-      const uint64_t pd = tc_desc(smem_addr(smc + TP_POFF), 16);
-      const uint64_t vd = tc_desc(smem_addr(smc + 2 * CL_HALF), CL_HALF);
-      auto issue_s = [&](int i) -> bool {
-        const int buf = i % TP_NST;
-        if (!cl_wait_fast(smem_addr(&s_fk[buf]), (uint32_t)(i / TP_NST) & 1u, p.err)) return false;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint64_t kb = kd + (uint64_t)((buf * CL_STAGE) >> 4);
-        const uint32_t dst = tmem + (uint32_t)(i & 1) * 64u;
+      bool ok = true;
+      if (warp == 7) {
+        const uint64_t qd = tc_desc(smem_addr(smc + TP_QOFF), 16);
+        const uint64_t kd = tc_desc(smem_addr(smc), 16);
+        for (int i = 0; ok && i < nsteps; ++i) {
+          const int buf = i % TP_NST;
+          // S buffer i & 1 is free once the softmax has read S_{i-2}; the key tile has landed
+          if ((i >= 2 && !cl_wait_fast(smem_addr(&s_sc[i & 1]), (uint32_t)((i - 2) >> 1) & 1u, p.err)) ||
+              !cl_wait_fast(smem_addr(&s_fk[buf]), (uint32_t)(i / TP_NST) & 1u, p.err)) {
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint64_t kb = kd + (uint64_t)((buf * CL_STAGE) >> 4);
+          const uint32_t dst = tmem + (uint32_t)(i & 1) * 64u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma(dst, qd + (uint64_t)(((kk >> 2) * TC_QHALF + (kk & 3) * 32) >> 4),
-                 kb + (uint64_t)(((kk >> 2) * CL_HALF + (kk & 3) * 32) >> 4), TC_IDESC_S, kk > 0 ? 1u : 0u);
-        tc_commit(smem_addr(&s_bs[i & 1]));
-        tc_commit(smem_addr(&s_ek[buf]));  // the key tile is free once S_i has read it
-        return true;
-      };
-      bool ok = issue_s(0);
-      if (ok && nsteps > 1) ok = issue_s(1);
-      for (int i = 0; ok && i < nsteps; ++i) {
-        if (!cl_wait_fast(smem_addr(&s_bp[i & 1]), (uint32_t)(i >> 1) & 1u, p.err) ||
-            !cl_wait_fast(smem_addr(&s_fv[i % TP_NST]), (uint32_t)(i / TP_NST) & 1u, p.err)) {
-          ok = false;
-          break;
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma(dst, qd + (uint64_t)(((kk >> 2) * TC_QHALF + (kk & 3) * 32) >> 4),
+                   kb + (uint64_t)(((kk >> 2) * CL_HALF + (kk & 3) * 32) >> 4), TC_IDESC_S, kk > 0 ? 1u : 0u);
+          tc_commit(smem_addr(&s_bs[i & 1]));
+          tc_commit(smem_addr(&s_ek[buf]));  // the key tile is free once S_i has read it
         }
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint64_t vb = vd + (uint64_t)(((i % TP_NST) * CL_STAGE) >> 4);
-        const uint64_t pb = pd + (uint64_t)(((i & 1) * 128 * 128) >> 4);
+      } else {
+        const uint64_t pd = tc_desc(smem_addr(smc + TP_POFF), 16);
+        const uint64_t vd = tc_desc(smem_addr(smc + 2 * CL_HALF), CL_HALF);
+        for (int i = 0; ok && i < nsteps; ++i) {
+          if (!cl_wait_fast(smem_addr(&s_bp[i & 1]), (uint32_t)(i >> 1) & 1u, p.err) ||
+              !cl_wait_fast(smem_addr(&s_fv[i % TP_NST]), (uint32_t)(i / TP_NST) & 1u, p.err)) {
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint64_t vb = vd + (uint64_t)(((i % TP_NST) * CL_STAGE) >> 4);
+          const uint64_t pb = pd + (uint64_t)(((i & 1) * 128 * 128) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma(tmem + 128u, pb + (uint64_t)((kk * 32) >> 4), vb + (uint64_t)((kk * 2048) >> 4), TC_IDESC_PV,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(smem_addr(&s_bpv[i & 1]));
-        tc_commit(smem_addr(&s_ev[i % TP_NST]));  // the value tile is free once P_i V_i has read it
-        if (i + 2 < nsteps) ok = issue_s(i + 2);
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma(tmem + 128u, pb + (uint64_t)((kk * 32) >> 4), vb + (uint64_t)((kk * 2048) >> 4), TC_IDESC_PV,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_addr(&s_bpv[i & 1]));
+          tc_commit(smem_addr(&s_ev[i % TP_NST]));  // the value tile is free once P_i V_i has read it
+        }
       }
       if (!ok) s_failed = 1;
-      // every MMA issued above has finished before tensor memory is freed
-      tc_commit(smem_addr(&s_done));
-      cl_wait_bar(smem_addr(&s_done), 0u, p.err);
+      // every MMA this thread issued has finished before tensor memory is freed
+      const uint32_t done = smem_addr(warp == 7 ? &s_done_s : &s_done);
+      tc_commit(done);
+      cl_wait_bar(done, 0u, p.err);
     }
     __syncwarp();
   } else {
@@ -1571,6 +1582,10 @@ __device__ __forceinline__ void attn_tp_body(const AttnParams& p, const CUtensor
       } else {
         tc_ld64(tmem + lane_base + (uint32_t)sb * 64u, sv);
       }
+      // S_i is in registers: its buffer may take S_{i+2}
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) tp_arrive(smem_addr(&s_sc[sb]));
       const int koff = DUP ? half * 32 : 0;
       const bool is_blk = i >= nmine;
       const int key0 = is_blk ? 0 : (j + CLA * i) * MC;

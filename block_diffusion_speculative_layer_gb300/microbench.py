@@ -47,7 +47,7 @@ def drafter(a):
         d, kvd = shape.d_model, shape.kv_dim
         max_b = max(batches)
         eng = dfl.Engine(shape, syn.iter_weights(shape), max_batch=max_b, max_ctx=max(ctxs) + 2 * B,
-                         attn_kernel=_attn(a))
+                         attn_kernel=_attn(a), page_tokens=a.page_tokens)
         taps = syn.make_hidden(512, 5 * d).reshape(512, 5, d)   # N(0, 1) feature rows
         for C in ctxs:
             for nb in batches:
@@ -62,6 +62,7 @@ def drafter(a):
                 us = {"fuse": r["fuse_us"], "inject": r["inject_us"], "block_attention": r["block_attention_us"],
                       "lm_head": r["lm_head_us"]}
                 print(json.dumps({"op": "drafter_step", "block": B, "ctx": C, "batch": nb, "attn": a.attn,
+                                  "page_tokens": a.page_tokens,
                                   "us": {k: round(v, 2) for k, v in us.items()},
                                   "drafter_pass_us": round(r["drafter_pass_us"], 2),
                                   "total_us": round(sum(us.values()), 2),
@@ -95,7 +96,7 @@ def ar_proxy(a):
 
 
 def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None, sampling=None, attn=0,
-                profile=False):
+                profile=False, page_tokens=16):
     """One timed df_generate over a batch (device weights drawn on the GPU),
     after one untimed warm-up generation of 16 tokens.  block_range: (b_min,
     b_max) for df_set_block_range, or None for the configured block size.
@@ -108,7 +109,7 @@ def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None,
 
     t0 = time.time()
     eng = dfl.Engine(shape, syn.iter_weights_device(shape), max_batch=len(prompts), max_ctx=max_ctx,
-                     attn_kernel=attn)
+                     attn_kernel=attn, page_tokens=page_tokens)
     torch.cuda.empty_cache()
     setup_s = time.time() - t0
     if block_range:
@@ -144,7 +145,7 @@ def _generation(shape, prompts, n_new, max_ctx, label, config, block_range=None,
                   for k, v in pr.items() if v["launches"]}
     eng.close()
     tokens = len(prompts) * n_new
-    print(json.dumps({"op": label, "config": config, "attn_kernel": attn, "sequences": len(prompts),
+    print(json.dumps({"op": label, "config": config, "attn_kernel": attn, "page_tokens": page_tokens, "sequences": len(prompts),
                       "new_tokens_each": n_new,
                       "tokens_per_s": tokens / secs, "wall_s": secs, "cycles": s2["cycles"],
                       # the engine counts one cycle per sequence per draft + verify pass
@@ -175,7 +176,7 @@ def serving(a):
     max_ctx = ((int(max(lens)) + a.new + 16 + 2 * shape.block_size + 63) // 64) * 64
     _generation(shape, prompts, a.new, max_ctx, "serving_batch16",
                 "qwen3-8b-shape bf16, 16 sequences, prompts U[128,2048], block 16, %d new each" % a.new,
-                _block_range(a), attn=_attn(a), profile=a.profile)
+                _block_range(a), attn=_attn(a), profile=a.profile, page_tokens=a.page_tokens)
 
 
 def sampled(a):
@@ -201,7 +202,7 @@ def dense27b(a):
     max_ctx = ((8192 + a.new + 16 + 2 * shape.block_size + 63) // 64) * 64
     _generation(shape, prompts, a.new, max_ctx, "dense27b_batch4",
                 "27b-class bf16, batch 4, prompt 8192, block 16, %d new each" % a.new, _block_range(a),
-                attn=_attn(a), profile=a.profile)
+                attn=_attn(a), profile=a.profile, page_tokens=a.page_tokens)
 
 
 def profile_cycle(a):
@@ -366,6 +367,7 @@ def main():
     ap.add_argument("--ctx", default="1024,4096,16384,32768")
     ap.add_argument("--batch", default="1,4,16,32")
     ap.add_argument("--reduced", action="store_true", help="drafter: 1 drafter layer, vocab 4096")
+    ap.add_argument("--page-tokens", type=int, default=16, help="drafter/serving/dense27b: tokens per KV page")
     ap.add_argument("--M", type=int, default=16)
     ap.add_argument("--N", type=int, default=24576)
     ap.add_argument("--K", type=int, default=4096)
