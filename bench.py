@@ -317,7 +317,7 @@ def run_ours(args):
     B, P, n_new = shape.block_size, args.prompt_len, args.new_tokens
     max_ctx = ((P + n_new + 2 * B + 63) // 64) * 64
     t0 = time.time()
-    eng = dfl.Engine(shape, syn.iter_weights(shape), max_batch=1, max_ctx=max_ctx)
+    eng = dfl.Engine(shape, syn.iter_weights(shape), max_batch=1, max_ctx=max_ctx, page_tokens=args.page_tokens)
     torch.cuda.empty_cache()
     setup_s = time.time() - t0
     stream = eng.stream
@@ -468,6 +468,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": 1000.0 * secs / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": P + n_new, "parallelism": "replicas",
+                       "kv_page_tokens": args.page_tokens,
                        "l2": "inputs larger than L2 (18.5 GB of weights streamed per cycle)"},
             "cycle": {"draft_us": draft_us, "verify_us": verify_us, "cycle_us": draft_us + verify_us,
                       "mean_accept_len": tau, "cycles_per_step": st["cycles"] / args.steps,
@@ -505,6 +506,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--prompt-len", type=int, default=512)
     ap.add_argument("--new-tokens", type=int, default=512)
+    ap.add_argument("--page-tokens", type=int, default=16, help="tokens per KV-cache page")
     ap.add_argument("--no-forced", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-proxy", action="store_true")

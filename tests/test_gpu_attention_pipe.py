@@ -129,3 +129,32 @@ def test_no_flow_between_sequences(dfl):
     np.testing.assert_array_equal(res[0][0][0], res[1][0][0])
     np.testing.assert_array_equal(res[0][1][:B], res[1][1][:B])
     assert np.abs(res[0][1][B:] - res[1][1][B:]).max() > 0
+
+
+@pytest.mark.parametrize("page_tokens", [8, 32, 64])
+@pytest.mark.parametrize("kernel", ["pipe", "mma"])
+def test_lossless_other_page_sizes(dfl, page_tokens, kernel):
+    # KV pages of 8, 32 or 64 tokens (one TMA box per page half): a ragged batch
+    # decodes the GPU's own greedy stream, and a sequence alone equals itself in the batch
+    shape = G4
+    w = syn.make_weights(shape)
+    k = dfl.DF_ATTN_PIPE if kernel == "pipe" else dfl.DF_ATTN_MMA
+    with dfl.Engine(shape, w, max_batch=4, max_ctx=1024 + 128, page_tokens=page_tokens, attn_kernel=k) as eng:
+        lens = [33, 700, 5, 1000]
+        prompts = [syn.make_prompt(shape, L, stream=120 + i) for i, L in enumerate(lens)]
+        spec, _ = eng.generate(prompts, 32)
+        np.testing.assert_array_equal(spec, eng.greedy_reference(prompts, 32))
+        alone, _ = eng.generate(prompts[3:4], 32)
+        np.testing.assert_array_equal(alone[0], spec[3])
+
+
+def test_page_size_does_not_change_the_stream(dfl):
+    # the attention's arithmetic depends on chunk positions, not on the page size
+    shape = G4
+    w = syn.make_weights(shape)
+    p = syn.make_prompt(shape, 300, stream=130)
+    outs = []
+    for pt in (16, 64):
+        with dfl.Engine(shape, w, max_batch=1, max_ctx=512, page_tokens=pt, attn_kernel=dfl.DF_ATTN_PIPE) as eng:
+            outs.append(eng.generate([p], 24)[0])
+    np.testing.assert_array_equal(outs[0], outs[1])
