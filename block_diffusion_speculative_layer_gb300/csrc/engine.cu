@@ -66,6 +66,7 @@ struct df_handle {
   int d = 0, hd = 0, Hq = 0, Hkv = 0, F = 0, V = 0, L = 0, Ld = 0, B = 0, qdim = 0, kvdim = 0, qkv_n = 0;
   int sm_count = 152;
   bool attn_pipe = false;  // bf16 attention on the pipelined tcgen05 kernel (df_config.attn_kernel)
+  int attn_cla = 4;        // its cluster size (CTAs), fixed for the handle
   int split_target = 253;  // CTAs a split-K GEMM aims for (DF_SPLIT_CTAS overrides tc_split_target)
   int l2_prefetch = 0;     // weight tiles a GEMM prefetches into L2 past its ring before its wait (DF_GEMM_L2PF)
   int tap_of_layer[1024];  // zero-based layer index -> tap slot (or -1)
@@ -520,7 +521,7 @@ df_status attention(df_handle* H, int M, int R, int nseq, bool causal, const voi
                4.0 * M * H->qdim * (double)max_len);
   p.trace = ps.tp;
   p.pipelined = H->attn_pipe ? 1 : 0;
-  p.cla = DF_ATTN_PIPE_CLUSTER;
+  p.cla = H->attn_cla;
   CK(launch_attention(p, H->bf16, H->st));
   return DF_OK;
 }
@@ -1419,10 +1420,16 @@ df_status df_init(const df_config* cfg, const void* const* weights, int32_t n_we
   H->kvdim = H->Hkv * H->hd;
   H->qkv_n = H->qdim + 2 * H->kvdim;
   H->Mmax = std::max(std::min(PREFILL_CHUNK, cfg->max_ctx), cfg->max_batch * cfg->block_size);
-  // attention kernel of the handle: the pipelined tcgen05 kernel (clusters of 4) for batches of 4 or
-  // more sequences, where it streams the cache fastest; the mma.sync kernel (lowest latency) otherwise
+  // attention kernel of the handle: the pipelined tcgen05 kernel for batches of 2 or more sequences or
+  // one sequence beyond 8K positions, where it streams the cache fastest (clusters of 4, or of 8 for a
+  // single sequence, which then has only 8 KV heads to spread); the mma.sync kernel (lowest latency)
+  // for one sequence up to 8K positions.  Measured at batch 1 (one launch of the Qwen3-8B block
+  // attention): 1K 16.4 vs 20.5 us, 8K 32.8 vs 32.8, 32K 86.0 vs 71.7 (mma.sync vs pipelined, 8 CTAs);
+  // at batch 2: 1K 26.6 vs 22.5, 32K 157.7 vs 127.0 (clusters of 4).
   H->attn_pipe = H->bf16 && (cfg->attn_kernel == DF_ATTN_PIPE ||
-                             (cfg->attn_kernel == DF_ATTN_AUTO && cfg->max_batch >= DF_ATTN_PIPE_MIN_BATCH));
+                             (cfg->attn_kernel == DF_ATTN_AUTO && (cfg->max_batch >= DF_ATTN_PIPE_MIN_BATCH ||
+                                                                   cfg->max_ctx > DF_ATTN_PIPE_MIN_CTX)));
+  H->attn_cla = cfg->max_batch == 1 ? DF_ATTN_PIPE_CLUSTER_ONE : DF_ATTN_PIPE_CLUSTER;
   {
     const char* g = getenv("DF_NO_GRAPH");
     H->use_graphs = !(g && g[0] == '1');

@@ -30,6 +30,7 @@ if ROOT not in sys.path:
 def drafter(a):
     """Drafter step alone on the Qwen3-8B width: fusion, injection, block attention, LM-head argmax."""
     import numpy as np
+    import torch
 
     import block_diffusion_speculative_layer_gb300 as dfl
     import synthetic as syn
@@ -45,12 +46,14 @@ def drafter(a):
             # the same kernels on a few GB of device memory (profiling captures)
             shape = shape.replace(draft_layers=1, vocab=4096)
         d, kvd = shape.d_model, shape.kv_dim
-        max_b = max(batches)
-        eng = dfl.Engine(shape, syn.iter_weights(shape), max_batch=max_b, max_ctx=max(ctxs) + 2 * B,
-                         attn_kernel=_attn(a), page_tokens=a.page_tokens)
         taps = syn.make_hidden(512, 5 * d).reshape(512, 5, d)   # N(0, 1) feature rows
-        for C in ctxs:
-            for nb in batches:
+        # one engine per batch size, configured for that batch (the attention kernel and its
+        # cluster size are chosen per engine from max_batch and max_ctx)
+        for nb in batches:
+            eng = dfl.Engine(shape, syn.iter_weights_device(shape), max_batch=nb, max_ctx=max(ctxs) + 2 * B,
+                             attn_kernel=_attn(a), page_tokens=a.page_tokens)
+            torch.cuda.empty_cache()
+            for C in ctxs:
                 r = eng.bench_drafter_step(nb, C, taps, iters=a.iters)
                 M = nb * B
                 byts = {
@@ -68,7 +71,7 @@ def drafter(a):
                                   "total_us": round(sum(us.values()), 2),
                                   "GB/s": {k: round(byts[k] / (us[k] * 1e-6) / 1e9, 1) for k in us if us[k] > 0}}),
                       flush=True)
-        eng.close()
+            eng.close()
 
 
 def ar_proxy(a):

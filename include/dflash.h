@@ -91,15 +91,18 @@ typedef enum { DF_FP32 = 0, DF_BF16 = 1 } df_dtype;
  *                       weights and GEMM operands, fp32 accumulation,
  *                       fp32 residual stream).
  *   mask_token_id     : id embedded into the drafter's masked slots (vocab-1).
- *   attn_kernel       : bf16 attention kernel for the whole handle (fixed, so
- *                       that verification and greedy decoding stay bitwise
- *                       equal): DF_ATTN_MMA (1) the mma.sync cluster kernel
- *                       (lowest latency at batch 1-3), DF_ATTN_PIPE (2) the
- *                       warp-specialised tcgen05 kernel in clusters of
- *                       DF_ATTN_PIPE_CLUSTER CTAs (streams long contexts and
- *                       batches fastest), DF_ATTN_AUTO (0) the pipelined
- *                       kernel when max_batch >= DF_ATTN_PIPE_MIN_BATCH, else
- *                       the mma.sync kernel.  The two round differently.
+ *   attn_kernel       : bf16 attention kernel for the whole handle (fixed, with
+ *                       its cluster size, so that verification and greedy
+ *                       decoding stay bitwise equal and a sequence decodes the
+ *                       same alone or in a batch): DF_ATTN_MMA (1) the mma.sync
+ *                       cluster kernel (lowest latency for one sequence up to
+ *                       8K positions), DF_ATTN_PIPE (2) the warp-specialised
+ *                       tcgen05 kernel (streams long contexts and batches
+ *                       fastest) in clusters of DF_ATTN_PIPE_CLUSTER CTAs, or
+ *                       DF_ATTN_PIPE_CLUSTER_ONE for a handle with max_batch 1,
+ *                       DF_ATTN_AUTO (0) the pipelined kernel when max_batch >=
+ *                       DF_ATTN_PIPE_MIN_BATCH or max_ctx > DF_ATTN_PIPE_MIN_CTX,
+ *                       else the mma.sync kernel.  The two round differently.
  */
 typedef struct {
   int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim, d_ffn, vocab;
@@ -113,8 +116,10 @@ typedef struct {
 } df_config;
 
 enum { DF_ATTN_AUTO = 0, DF_ATTN_MMA = 1, DF_ATTN_PIPE = 2 };
-#define DF_ATTN_PIPE_MIN_BATCH 4 /* DF_ATTN_AUTO: the pipelined kernel from this max_batch on */
-#define DF_ATTN_PIPE_CLUSTER 4   /* the engine's pipelined-kernel cluster size (CTAs) */
+#define DF_ATTN_PIPE_MIN_BATCH 2    /* DF_ATTN_AUTO: the pipelined kernel from this max_batch on, */
+#define DF_ATTN_PIPE_MIN_CTX 8192   /* or for one sequence beyond this max_ctx */
+#define DF_ATTN_PIPE_CLUSTER 4      /* the pipelined kernel's cluster size (CTAs) */
+#define DF_ATTN_PIPE_CLUSTER_ONE 8  /* ... for a handle with max_batch 1 */
 
 /* Per-handle counters.  k = accepted drafts in a cycle; a cycle emits k+1
  * tokens, so the mean accepted length is (accepted_drafts + cycles) / cycles. */
