@@ -395,12 +395,18 @@ __device__ __forceinline__ float4 cl_ld4(uint32_t addr) {
                : "r"(addr));
   return v;
 }
-__device__ __forceinline__ void cl_st2(uint32_t addr, float a, float b) {
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+// Asynchronous stores of two or four floats into another CTA's shared memory;
+// their bytes count toward that CTA's mbarrier at `rbar` (complete-tx), so the
+// owner needs no fence or separate arrival from the writer.
+__device__ __forceinline__ void cl_st2_async(uint32_t addr, float a, float b, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "f"(a), "f"(b), "r"(rbar)
+               : "memory");
 }
-// Arrive (release, cluster scope) on the mbarrier at `addr` in another CTA of the cluster.
-__device__ __forceinline__ void cl_remote_arrive(uint32_t addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+__device__ __forceinline__ void cl_st4_async(uint32_t addr, float a, float b, float c, float d, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+               : "memory");
 }
 __device__ __forceinline__ bool cl_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -492,18 +498,22 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
   const __nv_bfloat16* blk = reinterpret_cast<const __nv_bfloat16*>(p.blk);
   const int PT = p.page_tokens;
   __shared__ __align__(8) uint64_t s_full[CL_NST];
-  __shared__ __align__(8) uint64_t s_merge;  // one arrival per cluster rank once its partial is here
+  __shared__ __align__(8) uint64_t s_merge;  // complete once every partial of this rank's pairs is here
   __shared__ int s_failed;
   if (threadIdx.x == 0) {
     for (int b2 = 0; b2 < CL_NST; ++b2) cl_mbar_init(smem_addr(&s_full[b2]));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&s_merge)), "r"(CLA) : "memory");
+    cl_mbar_init(smem_addr(&s_merge));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the merge barrier's one arrival, with the bytes the holding ranks push
+    // here: per pair of this rank, an output row and its (maximum, sum)
+    const int held = min(nA, CLA) + ((!causal && nA < CLA) ? 1 : 0);
+    cl_arrive_expect_tx(smem_addr(&s_merge), (uint32_t)(held * (G * 16 / CLA) * (MHD + 2) * 4));
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kvmap)) : "memory");
     s_failed = 0;
   }
   __syncthreads();
-  // every rank's merge barrier is initialised before any rank arrives on it
-  // remotely (the matching wait comes after the chunks, long after this)
+  // every rank's merge barrier is initialised (and expects its bytes) before
+  // any rank stores into it (the matching wait comes after the chunks)
   cl_arrive();
   // Stage step st into buffer buf: part 1 = the pages wholly before first_new
   // (written by earlier passes), 2 = the rest, 3 = all.  Context chunks come
@@ -591,6 +601,8 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
   for (int st = 0; st < CL_NST && st < nsteps; ++st) stage(st, st, 1);
 
   pdl_wait();
+  // the rest of the first stages (the pages this pass wrote), ahead of the queries
+  for (int st = 0; st < CL_NST && st < nsteps; ++st) stage(st, st, 2);
   // ---- this warp's query head and its 16 rows (A fragments straight from global)
   const bool active = warp < G;
   const int head = h * G + warp;
@@ -611,8 +623,6 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
       qa[ks][3] = vhi ? q32[base_hi + (d0 + 8) / 2] : 0u;
     }
   }
-  // the rest of the first stages
-  for (int st = 0; st < CL_NST && st < nsteps; ++st) stage(st, st, 2);
 
   // ---- online softmax over this CTA's chunks
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
@@ -755,11 +765,11 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
   // ---- the merge.  Pair pp = (query head g, token row r) = g * 16 + r belongs to
   // rank pp / (pairs / CLA).  Every rank writes its partial of each pair (output,
   // running maximum and sum) into slot j of that pair in the owner's receive
-  // region (remote stores), then arrives once on every rank's merge barrier;
-  // each rank waits for its own barrier and merges its pairs from local
-  // shared memory.  No rank reads another's shared memory, and every write into
-  // a rank lands before that rank's barrier completes, so a rank may leave as
-  // soon as it has merged.
+  // region by asynchronous remote stores whose bytes complete the owner's merge
+  // barrier; each rank waits for its own barrier and merges its pairs from
+  // local shared memory.  No rank reads another's shared memory, and every
+  // write into a rank lands before that rank's barrier completes, so a rank
+  // may leave as soon as it has merged.
   const int pairs = G * 16;
   const int per_owner = pairs / CLA;  // G * 16 is a multiple of 16, CLA divides 16
   const uint32_t rb_s = smem_addr(smc + cl_rb_off(G));
@@ -775,14 +785,25 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
       const uint32_t owner = (uint32_t)(pp / per_owner);
       const uint32_t slot = rb_s + (uint32_t)(((pp % per_owner) * CLA + j) * CL_RSLOT) * 4u;
       const uint32_t dst = cl_map(slot, owner);
+      const uint32_t rbar = cl_map(smem_addr(&s_merge), owner);
+      // 16-byte stores: for the column tiles 2q and 2q+1, lanes tig and tig^1
+      // swap one pair so the even lane holds four consecutive columns of tile
+      // 2q and the odd lane four of tile 2q+1
+      const bool odd = (tig & 1) != 0;
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) cl_st2(dst + (uint32_t)(nt * 8 + tig * 2) * 4u, o[nt][2 * hl], o[nt][2 * hl + 1]);
-      if (tig == 0) cl_st2(dst + (uint32_t)MHD * 4u, hl ? m_hi : m_lo, hl ? l_hi : l_lo);
+      for (int q = 0; q < 8; ++q) {
+        const float a0 = o[2 * q][2 * hl], a1 = o[2 * q][2 * hl + 1];
+        const float b0 = o[2 * q + 1][2 * hl], b1 = o[2 * q + 1][2 * hl + 1];
+        const float y0 = __shfl_xor_sync(0xffffffffu, odd ? a0 : b0, 1);
+        const float y1 = __shfl_xor_sync(0xffffffffu, odd ? a1 : b1, 1);
+        if (odd)
+          cl_st4_async(dst + (uint32_t)((2 * q + 1) * 8 + (tig - 1) * 2) * 4u, y0, y1, b0, b1, rbar);
+        else
+          cl_st4_async(dst + (uint32_t)(2 * q * 8 + tig * 2) * 4u, a0, a1, y0, y1, rbar);
+      }
+      if (tig == 0) cl_st2_async(dst + (uint32_t)MHD * 4u, hl ? m_hi : m_lo, hl ? l_hi : l_lo, rbar);
     }
   }
-  asm volatile("fence.acq_rel.cluster;" ::: "memory");
-  __syncthreads();
-  if (threadIdx.x < CLA) cl_remote_arrive(cl_map(smem_addr(&s_merge), (uint32_t)threadIdx.x));
   if (!cl_wait_bar_cluster(smem_addr(&s_merge), 0u, p.err)) return;
 
   // ---- merge this rank's pairs, 32 threads x 4 dims per pair, ranks in order
