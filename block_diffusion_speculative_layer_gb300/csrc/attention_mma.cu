@@ -315,12 +315,15 @@ constexpr int CL_STAGE = 2 * 2 * CL_HALF;
 constexpr unsigned long long CL_WAIT_NS = 2000000000ull;
 
 __host__ __device__ constexpr int cl_pg_off(int G) { return (void)G, CL_NST * CL_STAGE; }
-// Receive region of the merge: per (query head, token row) pair a CTA owns, one
-// slot per cluster rank of CL_RSLOT floats (the partial output's 128 dims,
-// then the running maximum and sum).
+// Receive region of the merge: one region per cluster rank, holding that
+// rank's slots of the (query head, token row) pairs this CTA owns, CL_RSLOT
+// floats each (the partial output's 128 dims, then the running maximum and
+// sum).  A rank stages its own slots of all pairs over the stage buffers.
 constexpr int CL_RSLOT = MHD + 4;
 __host__ __device__ constexpr int cl_rb_off(int G) { return cl_pg_off(G) + MAXPG * 4; }
 __host__ __device__ constexpr int cl_smem_bytes(int G) { return cl_rb_off(G) + G * 16 * CL_RSLOT * 4 + 1024; }
+static_assert(8 * 16 * CL_RSLOT * 4 <= cl_rb_off(8), "the partials' staging area ends before the receive area");
+static_assert((CL_RSLOT * 4) % 16 == 0 && cl_rb_off(8) % 16 == 0, "bulk copies move whole 16-byte units");
 
 // Byte offset of (key, 16-byte piece b of the 256-byte row) in a stage's key or value tile.
 __device__ __forceinline__ uint32_t swz2(int key, int b) {
@@ -395,17 +398,12 @@ __device__ __forceinline__ float4 cl_ld4(uint32_t addr) {
                : "r"(addr));
   return v;
 }
-// Asynchronous stores of two or four floats into another CTA's shared memory;
-// their bytes count toward that CTA's mbarrier at `rbar` (complete-tx), so the
-// owner needs no fence or separate arrival from the writer.
-__device__ __forceinline__ void cl_st2_async(uint32_t addr, float a, float b, uint32_t rbar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
-               "f"(a), "f"(b), "r"(rbar)
-               : "memory");
-}
-__device__ __forceinline__ void cl_st4_async(uint32_t addr, float a, float b, float c, float d, uint32_t rbar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
-               "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory into another CTA's; the bytes complete that CTA's
+// mbarrier at `rbar` (complete-tx).
+__device__ __forceinline__ void cl_bulk_push(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t rbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(src), "r"(bytes), "r"(rbar)
                : "memory");
 }
 __device__ __forceinline__ bool cl_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -504,10 +502,10 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
     for (int b2 = 0; b2 < CL_NST; ++b2) cl_mbar_init(smem_addr(&s_full[b2]));
     cl_mbar_init(smem_addr(&s_merge));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    // the merge barrier's one arrival, with the bytes the holding ranks push
-    // here: per pair of this rank, an output row and its (maximum, sum)
+    // the merge barrier's one arrival, with the bytes the holding ranks send
+    // here: per pair of this rank, one slot (output row, maximum and sum)
     const int held = min(nA, CLA) + ((!causal && nA < CLA) ? 1 : 0);
-    cl_arrive_expect_tx(smem_addr(&s_merge), (uint32_t)(held * (G * 16 / CLA) * (MHD + 2) * 4));
+    cl_arrive_expect_tx(smem_addr(&s_merge), (uint32_t)(held * (G * 16 / CLA) * CL_RSLOT * 4));
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kvmap)) : "memory");
     s_failed = 0;
   }
@@ -763,61 +761,55 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
   __syncthreads();
 
   // ---- the merge.  Pair pp = (query head g, token row r) = g * 16 + r belongs to
-  // rank pp / (pairs / CLA).  Every rank writes its partial of each pair (output,
-  // running maximum and sum) into slot j of that pair in the owner's receive
-  // region by asynchronous remote stores whose bytes complete the owner's merge
-  // barrier; each rank waits for its own barrier and merges its pairs from
-  // local shared memory.  No rank reads another's shared memory, and every
-  // write into a rank lands before that rank's barrier completes, so a rank
-  // may leave as soon as it has merged.
+  // rank pp / (pairs / CLA).  Every rank leaves its partial of each pair
+  // (output, running maximum and sum) in slot pp of a local staging area over
+  // the stage buffers, so the pairs of one owner are consecutive slots, and
+  // sends each owner its slots with one bulk copy into region j of the
+  // owner's receive area; the copies' bytes complete the owner's merge
+  // barrier.  Each rank waits for its own barrier and merges its pairs from
+  // local shared memory.  A copy reads its source until the destination's
+  // barrier completes, so every rank arrives on a cluster barrier once its own
+  // merge barrier has completed and waits on it before it leaves.
   const int pairs = G * 16;
   const int per_owner = pairs / CLA;  // G * 16 is a multiple of 16, CLA divides 16
   const uint32_t rb_s = smem_addr(smc + cl_rb_off(G));
   // ranks without a chunk of this tile hold (-inf, 0, 0): their terms are
-  // exactly zero, so they are neither written nor read
+  // exactly zero, so they are neither sent nor read
   const bool held_me = j < nA || (!causal && j == CLA - 1);
-  cl_wait();  // the merge barriers are initialised
   if (active && held_me) {
+    float* stg = reinterpret_cast<float*>(smc);
 #pragma unroll
     for (int hl = 0; hl < 2; ++hl) {
-      const int rr = gid + hl * 8;
-      const int pp = warp * 16 + rr;
-      const uint32_t owner = (uint32_t)(pp / per_owner);
-      const uint32_t slot = rb_s + (uint32_t)(((pp % per_owner) * CLA + j) * CL_RSLOT) * 4u;
-      const uint32_t dst = cl_map(slot, owner);
-      const uint32_t rbar = cl_map(smem_addr(&s_merge), owner);
-      // 16-byte stores: for the column tiles 2q and 2q+1, lanes tig and tig^1
-      // swap one pair so the even lane holds four consecutive columns of tile
-      // 2q and the odd lane four of tile 2q+1
-      const bool odd = (tig & 1) != 0;
+      float* slot = stg + (size_t)(warp * 16 + gid + hl * 8) * CL_RSLOT;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float a0 = o[2 * q][2 * hl], a1 = o[2 * q][2 * hl + 1];
-        const float b0 = o[2 * q + 1][2 * hl], b1 = o[2 * q + 1][2 * hl + 1];
-        const float y0 = __shfl_xor_sync(0xffffffffu, odd ? a0 : b0, 1);
-        const float y1 = __shfl_xor_sync(0xffffffffu, odd ? a1 : b1, 1);
-        if (odd)
-          cl_st4_async(dst + (uint32_t)((2 * q + 1) * 8 + (tig - 1) * 2) * 4u, y0, y1, b0, b1, rbar);
-        else
-          cl_st4_async(dst + (uint32_t)(2 * q * 8 + tig * 2) * 4u, a0, a1, y0, y1, rbar);
-      }
-      if (tig == 0) cl_st2_async(dst + (uint32_t)MHD * 4u, hl ? m_hi : m_lo, hl ? l_hi : l_lo, rbar);
+      for (int nt = 0; nt < 16; ++nt)
+        *reinterpret_cast<float2*>(slot + nt * 8 + tig * 2) = make_float2(o[nt][2 * hl], o[nt][2 * hl + 1]);
+      if (tig == 0) *reinterpret_cast<float2*>(slot + MHD) = make_float2(hl ? m_hi : m_lo, hl ? l_hi : l_lo);
     }
   }
-  if (!cl_wait_bar_cluster(smem_addr(&s_merge), 0u, p.err)) return;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes, read by the bulk copies
+  __syncthreads();
+  cl_wait();  // the merge barriers are initialised
+  if (held_me && (int)threadIdx.x < CLA) {
+    const uint32_t q = threadIdx.x, bytes = (uint32_t)(per_owner * CL_RSLOT * 4);
+    cl_bulk_push(cl_map(rb_s + (uint32_t)j * bytes, q), smem_addr(smc) + q * bytes, bytes,
+                 cl_map(smem_addr(&s_merge), q));
+  }
+  const bool merged_in = cl_wait_bar_cluster(smem_addr(&s_merge), 0u, p.err);
+  cl_arrive();  // every copy into this rank has landed
 
   // ---- merge this rank's pairs, 32 threads x 4 dims per pair, ranks in order
-  for (int lp = warp; lp < per_owner; lp += blockDim.x >> 5) {
+  for (int lp = warp; merged_in && lp < per_owner; lp += blockDim.x >> 5) {
     const int pp = j * per_owner + lp;
     const int g = pp >> 4, rr = pp & 15;
     if (rr >= nrows || s_len[rr] < 0) continue;
-    const float* slot0 = reinterpret_cast<const float*>(smc + cl_rb_off(G)) + (size_t)lp * CLA * CL_RSLOT;
+    const float* slot0 = reinterpret_cast<const float*>(smc + cl_rb_off(G)) + (size_t)lp * CL_RSLOT;
     float2 ml[CLA];
     float4 av[CLA];
 #pragma unroll
     for (int i = 0; i < CLA; ++i) {
       const bool held = i < nA || (!causal && i == CLA - 1);
-      const float* sl = slot0 + (size_t)i * CL_RSLOT;
+      const float* sl = slot0 + (size_t)i * per_owner * CL_RSLOT;
       ml[i] = held ? *reinterpret_cast<const float2*>(sl + MHD) : make_float2(-INFINITY, 0.f);
       av[i] = held ? *reinterpret_cast<const float4*>(sl + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -843,6 +835,7 @@ __device__ __forceinline__ void attn_cl_body(const AttnParams& p, const CUtensor
     packed.y = pack_bf16(a.z * inv, a.w * inv);
     *reinterpret_cast<uint2*>(out) = packed;
   }
+  cl_wait();  // and every copy out of it has landed
 }
 
 template <int CLA, int NW>
