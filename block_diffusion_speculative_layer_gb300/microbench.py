@@ -9,7 +9,7 @@
   python -m block_diffusion_speculative_layer_gb300.microbench dense27b [--new 1024]
   python -m block_diffusion_speculative_layer_gb300.microbench profile_cycle [--ctx 1024] [--batch 1] [--vocab 4096]
   python -m block_diffusion_speculative_layer_gb300.microbench attention [--ctx ...] [--batch ...] [--attn mma|pipe|auto]
-                                                                         [--causal] [--iters 5]
+                                                                         [--causal] [--iters 5] [--pages shuffled|runs]
 
 Inputs are seeded synthetic bf16 (N(0,1) activations, N(0,0.02) weights)
 drawn on the GPU by torch.  For small shapes several weight copies are used
@@ -265,7 +265,9 @@ def attention(a):
     C positions plus its 16-row block (or, with --causal, the target's causal
     attention of 16 verify rows), for each context and batch, on the
     mma.sync and/or pipelined kernel.  Keys and values are random bf16 in a
-    paged cache with shuffled pages; L2 is flushed (a 256 MB write) before
+    paged cache whose pages are a random permutation of the pool (--pages
+    shuffled) or each sequence's run of consecutive ids, as the engine's
+    allocator hands them out (--pages runs); L2 is flushed (a 256 MB write) before
     every timed launch, and each launch is timed alone with CUDA events
     (after a device-side sleep that covers the host's preparation of the
     launch, so the events bracket the kernel only)."""
@@ -285,7 +287,8 @@ def attention(a):
             ppseq = (need + PT - 1) // PT
             n_pages = nb * ppseq
             cache = torch.randn((n_pages, 2, Hkv, PT, 128), device="cuda", generator=g).to(torch.bfloat16)
-            perm = torch.randperm(n_pages, device="cuda", generator=g).to(torch.int32)
+            perm = (torch.randperm(n_pages, device="cuda", generator=g).to(torch.int32) if a.pages == "shuffled"
+                    else torch.arange(n_pages, device="cuda", dtype=torch.int32))
             table = perm.reshape(nb, ppseq).contiguous()
             q = torch.randn((nb * R, Hq * 128), device="cuda", generator=g).to(torch.bfloat16)
             blk = torch.randn((2, Hkv, nb * R, 128), device="cuda", generator=g).to(torch.bfloat16)
@@ -319,7 +322,7 @@ def attention(a):
                 assert int(err.item()) == 0, f"attention error word {int(err.item())}"
                 print(json.dumps({"op": "attention", "kernel": "pipe" if k == dfl.DF_ATTN_PIPE else "mma",
                                   "cluster_ctas": a.cla if k == dfl.DF_ATTN_PIPE else 16,
-                                  "causal": bool(a.causal), "ctx": C, "batch": nb, "rows_per_seq": R,
+                                  "causal": bool(a.causal), "ctx": C, "batch": nb, "rows_per_seq": R, "pages": a.pages,
                                   "us": round(us, 2), "algorithmic_bytes": byts,
                                   "GB/s": round(byts / (us * 1e-6) / 1e9, 1),
                                   "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / peak, 3)}), flush=True)
@@ -358,6 +361,8 @@ def main():
                                    "profile_cycle", "attention"])
     ap.add_argument("--causal", action="store_true", help="attention: the target's causal verify rows")
     ap.add_argument("--cla", type=int, default=4, help="attention: CTAs per cluster of the pipelined kernel")
+    ap.add_argument("--pages", default="shuffled", choices=["shuffled", "runs"],
+                    help="attention: page ids a random permutation of the pool, or consecutive per sequence")
     ap.add_argument("--profile", action="store_true",
                     help="serving/dense27b/sampled: also report in-situ device time per kernel class")
     ap.add_argument("--vocab", type=int, default=4096, help="profile_cycle: vocabulary")

@@ -5,8 +5,9 @@ the target's verify rows attend causally over the cache; the drafter's block
 rows attend over the injected context before their anchor and, in both
 directions, over their own block; nothing crosses sequences.
 
-Random bf16 queries, keys and values in a paged cache with shuffled pages,
-ragged context lengths; the reference is the oracle's attention (float64) on
+Random bf16 queries, keys and values in a paged cache with shuffled pages
+(and, in one test, pages in runs of consecutive ids, as the engine's
+allocator hands them out), ragged context lengths; the reference is the oracle's attention (float64) on
 the same bf16 values, gathered and masked by the rule above.  Both kernels
 (mma.sync cluster and pipelined tcgen05), query-head groups of 4, 5 and 8.
 A row computed alone must equal the same row computed inside its block, bit
@@ -43,22 +44,30 @@ def bf(x):
     return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).cuda()
 
 
-def make_case(seed, lens, R, Hq, Hkv, causal):
+def make_case(seed, lens, R, Hq, Hkv, causal, layout="shuffled"):
     """Cache holding each sequence's positions 0..len-1 (plus its block rows for
-    the causal case), shuffled pages, queries of R rows per sequence."""
+    the causal case), queries of R rows per sequence.  Pages: "shuffled" (a
+    random permutation of the pool), or "runs" (each sequence takes
+    consecutive page ids, the last sequence ending at the pool's last page,
+    and about a quarter of its 4-page chunks are shuffled inside)."""
     g = np.random.default_rng(seed)
     nseq = len(lens)
     need = [L + (R if causal else 0) for L in lens]
     pt_stride = max((n + PT - 1) // PT for n in need) + 1
     n_pages = sum((n + PT - 1) // PT for n in need) + 3
-    perm = g.permutation(n_pages)
+    perm = g.permutation(n_pages) if layout == "shuffled" else np.arange(3, n_pages)
     table = np.full((nseq, pt_stride), -1, np.int32)
     cache = g.standard_normal((n_pages, 2, Hkv, PT, HD)).astype(np.float32)
     k_seq, v_seq = [], []
     used = 0
     for i, n in enumerate(need):
         npg = (n + PT - 1) // PT
-        table[i, :npg] = perm[used:used + npg]
+        ids = perm[used:used + npg].copy()
+        if layout == "runs":
+            for c0 in range(0, npg - 3, 4):
+                if g.random() < 0.25:
+                    g.shuffle(ids[c0:c0 + 4])
+        table[i, :npg] = ids
         used += npg
         ks = cache[table[i, :npg], 0].transpose(0, 2, 1, 3).reshape(npg * PT, Hkv, HD)[:n]
         vs = cache[table[i, :npg], 1].transpose(0, 2, 1, 3).reshape(npg * PT, Hkv, HD)[:n]
@@ -142,3 +151,28 @@ def test_a_row_alone_equals_the_row_in_its_block(dfl, kernel):
         one = run(dfl, c1, lens, 1, Hkv, True, k)
         for i in range(len(lens)):
             np.testing.assert_array_equal(one[i], full[i * R + j])
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "block"])
+def test_pages_in_runs(dfl, kernel, causal):
+    # pages in runs of consecutive ids (the engine's allocation): the result
+    # matches the oracle and equals, bit for bit, the same cache contents
+    # placed by a random permutation of the pool
+    G, Hkv, R = 4, 8, 16
+    lens = [1000, 37, 2048 + 5, 700]
+    c = make_case(11, lens, R, G * Hkv, Hkv, causal, layout="runs")
+    full_chunks = sum(1 for i, L in enumerate(lens) for c0 in range(0, (L + PT - 1) // PT - 3, 4)
+                      if np.all(np.diff(c["table"][i, c0:c0 + 4]) == 1))
+    assert full_chunks >= 20  # most chunks are runs
+    got = run(dfl, c, lens, R, Hkv, causal, kernel)
+    ref = reference(c, lens, R, G * Hkv, Hkv, causal)
+    assert T.rel_err(got, ref) <= 2e-2
+    for r in range(0, got.shape[0], 9):
+        assert T.rel_err(got[r], ref[r]) <= 2e-2, r
+    perm = np.random.default_rng(5).permutation(c["cache"].shape[0])
+    moved = dict(c)
+    moved["cache"] = np.empty_like(c["cache"])
+    moved["cache"][perm] = c["cache"]  # page p's contents now sit in page perm[p]
+    moved["table"] = np.where(c["table"] >= 0, perm[np.maximum(c["table"], 0)], -1).astype(np.int32)
+    np.testing.assert_array_equal(run(dfl, moved, lens, R, Hkv, causal, kernel), got)
