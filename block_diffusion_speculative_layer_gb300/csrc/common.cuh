@@ -197,25 +197,39 @@ __device__ __forceinline__ void epilogue_stage(const EpiParams& ep, int m0, int 
 }
 
 // Global operands of the epilogue that do not depend on the accumulator (the
-// residual rows, the rotary factors), loaded before the accumulator is final
-// so that their latency overlaps the accumulator drain and the split-K
-// reduction.  Only for tiles of at most EPI_BATCH rows.
+// residual rows, the rotary factors), copied into shared memory with cp.async
+// as soon as the accumulator is complete: the copies' latency overlaps the
+// accumulator drain and the split-K reduction, and each thread waits for its
+// own copies only when the epilogue reads them.  (Loads into a register array
+// that the epilogue indexes by a run-time row would live in local memory, and
+// storing them there waits for the loads at once.)  Only for tiles of at most
+// EPI_BATCH rows.  `buf` holds EPI_PRE_FLOATS floats of shared memory: thread
+// f keeps row r's residual at buf[r * 128 + f] (EPI_RESID), or its (cosine,
+// sine) at ((float2*)buf)[r * 128 + f] (EPI_QKV).
+constexpr int EPI_PRE_FLOATS = 2 * EPI_BATCH * 128;
 struct EpiPre {
-  float a[EPI_BATCH];  // EPI_RESID: residual value; EPI_QKV: cosine
-  float b[EPI_BATCH];  // EPI_QKV: sine
+  float* buf;
 };
+__device__ __forceinline__ void cp_async_f1(float* dst, const float* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_f2(float2* dst, const float2* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_own() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Fill `pre` for rows [0, rows) of the tile at (m0, n0); all 128 threads
-// call it, thread f for feature n0 + f.  Returns whether `pre` was filled.
+// Start the copies for rows [0, rows) of the tile at (m0, n0); all 128 threads
+// call it, thread f for feature n0 + f.  Returns whether `pre` will be filled.
 __device__ __forceinline__ bool epilogue_preload(const EpiParams& ep, int n0, int m0, int rows, int M,
-                                                 const RowMeta* meta, EpiPre& pre) {
+                                                 const RowMeta* meta, const EpiPre& pre) {
   rows = min(rows, M - m0);
   if (rows > EPI_BATCH) return false;
   const int f = threadIdx.x & 127;
   const int n = n0 + f;
   if (ep.kind == EPI_RESID) {
-#pragma unroll
-    for (int i = 0; i < EPI_BATCH; ++i) pre.a[i] = (i < rows) ? ep.resid[(size_t)(m0 + i) * ep.ldr + n] : 0.f;
+    for (int i = 0; i < rows; ++i) cp_async_f1(pre.buf + i * 128 + f, ep.resid + (size_t)(m0 + i) * ep.ldr + n);
     return true;
   }
   if (ep.kind == EPI_QKV) {
@@ -226,18 +240,13 @@ __device__ __forceinline__ bool epilogue_preload(const EpiParams& ep, int n0, in
       const int r2 = (n - ep.q_dim) % (2 * ep.kv_dim);
       rotated = r2 < ep.kv_dim;
     }
-#pragma unroll
-    for (int i = 0; i < EPI_BATCH; ++i) {
-      pre.a[i] = 1.f;
-      pre.b[i] = 0.f;
-      if (i < rows && rotated) {
-        const int pos = meta[i].pos;
-        if (pos >= 0 && pos < ep.rope_rows) {
-          const float2 cs = __ldg(ep.rope + (size_t)pos * half + (dim & (half - 1)));
-          pre.a[i] = cs.x;
-          pre.b[i] = cs.y;
-        }
-      }
+    float2* cs = reinterpret_cast<float2*>(pre.buf);
+    for (int i = 0; i < rows; ++i) {
+      const int pos = meta[i].pos;
+      if (rotated && pos >= 0 && pos < ep.rope_rows)
+        cp_async_f2(cs + i * 128 + f, ep.rope + (size_t)pos * half + (dim & (half - 1)));
+      else
+        cs[i * 128 + f] = make_float2(1.f, 0.f);
     }
     return true;
   }
@@ -284,9 +293,10 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
         if (ep.ss_out) row_sumsq(nv, r, red);
       };
       if (pre) {
-        // residuals already in registers: a compact row loop
+        // residuals already on their way to shared memory: a compact row loop
+        cp_async_wait_own();
 #pragma unroll 1
-        for (int r = 0; r < rows; ++r) row(r, pre->a[r]);
+        for (int r = 0; r < rows; ++r) row(r, pre->buf[r * 128 + f]);
       } else {
         // issue EPI_BATCH residual loads together, then the rows
         for (int rb = 0; rb < rows; rb += EPI_BATCH) {
@@ -401,10 +411,12 @@ __device__ void epilogue_tile(const EpiParams& ep, const float* tile, int ld, in
         return true;
       };
       if (pre) {
-        // rotary factors already in registers: a compact row loop
+        // rotary factors already on their way to shared memory: a compact row loop
+        cp_async_wait_own();
+        const float2* cs = reinterpret_cast<const float2*>(pre->buf);
 #pragma unroll 1
         for (int r = 0; r < rows; ++r)
-          if (usable(r)) store(r, value(r, make_float2(pre->a[r], pre->b[r])));
+          if (usable(r)) store(r, value(r, cs[r * 128 + f]));
       } else {
         for (int rb = 0; rb < rows; rb += EPI_BATCH) {
           // the batch's rotary factors first (independent read-only loads)

@@ -184,7 +184,8 @@ struct TcCfg {
   static constexpr int TLD = BM + 4;  // epilogue tile row stride (floats)
   static constexpr int META_OFF = STAGES * STAGE_BYTES + 256;   // row facts staged during the mainloop
   static constexpr int SMEM = 1024 + META_OFF + NT * (int)sizeof(RowMeta);
-  static_assert(NT * TLD * 4 + NT * 16 <= STAGES * STAGE_BYTES, "epilogue tile and row sums must fit in the ring");
+  static constexpr int PRE_OFF = NT * TLD * 4 + NT * 16;  // the epilogue's operand copies, after tile and row sums
+  static_assert(PRE_OFF + EPI_PRE_FLOATS * 4 <= STAGES * STAGE_BYTES, "epilogue tile, row sums and copies fit in the ring");
   static_assert((TLD * 4) % 16 == 0, "tile rows must stay 16-byte aligned for vector copies");
 };
 
@@ -325,17 +326,19 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   if (!mbar_wait(accum_bar, 0, ep.err)) flags[2] = 1;
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   __syncthreads();
-  // The rows whose epilogue this CTA runs; their global operands are loaded
-  // now, ahead of the drain and the split-K reduction.
+  // The rows whose epilogue this CTA runs; the copies of their global
+  // operands start now (into the ring, which no MMA or load uses any more),
+  // ahead of the drain and the split-K reduction.
   const int rows = min(NT, M - m0);
   const bool cl = creduce && splits > 1;
   const int q = cl ? (int)cluster_rank() : 0;
   const int r0 = cl ? rows * q / splits : 0, r1 = cl ? rows * (q + 1) / splits : rows;
-  EpiPre pre;
-  const bool have_pre = (cl || splits == 1) && epilogue_preload(ep, n0, m0 + r0, r1 - r0, M, meta + r0, pre);
+  const bool failed = flags[2] != 0;
+  const EpiPre pre{reinterpret_cast<float*>(smem + C::PRE_OFF)};
+  const bool have_pre =
+      !failed && (cl || splits == 1) && epilogue_preload(ep, n0, m0 + r0, r1 - r0, M, meta + r0, pre);
   float* tile = reinterpret_cast<float*>(smem);
   const int f = threadIdx.x;
-  const bool failed = flags[2] != 0;
   if (!failed) {
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
 #pragma unroll 1
@@ -403,6 +406,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
     if (!failed)
       epilogue_tile<__nv_bfloat16>(ep, tile + (size_t)r0 * C::TLD, C::TLD, n0, m0 + r0, r1 - r0, M, meta + r0, red,
                                    /*staged=*/true, have_pre ? &pre : nullptr);
+    cp_async_wait_own();  // no copy into this CTA's memory outlives it
     cluster_wait();    // nobody leaves while another CTA may still read its tile
     return;
   }
