@@ -7,6 +7,10 @@ the sum of |x||w| terms: the bound used is 1e-5 of that sum.  Argmax must
 pick the float64 argmax wherever the float64 top-2 margin exceeds that bound,
 and otherwise an index whose float64 logit is within it of the maximum.
 """
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 
@@ -191,3 +195,35 @@ def test_lmhead_argmax_ties_pick_lowest_index(dfl):
     ids = dfl.lmhead_argmax_bf16(dev_bf16(x), dev_bf16(w2)).cpu().numpy()
     for m in range(M):
         assert ids[m] == min(3 + m, win[m])
+
+
+# Split-K through the cluster (each CTA reads its rows of the other CTAs'
+# partials from their shared memory) against split-K through a global
+# workspace (DF_NO_CLUSTER=1, in a child process): both add the partials in
+# split order, so the results are the same bits.
+SPLIT_K = [(16, 1024, 4096, 8, 16), (13, 640, 2560, 5, 16), (40, 256, 1024, 4, 64), (256, 384, 320, 5, 256)]
+
+_WORKSPACE_CHILD = """
+import sys
+import numpy as np
+import torch
+sys.path[:0] = [sys.argv[2], sys.argv[3]]
+import block_diffusion_speculative_layer_gb300 as dfl
+import test_gpu_gemm as t
+for i, (M, N, K, splits, nt) in enumerate(t.SPLIT_K):
+    x, w = t.inputs(M, N, K, seed=30 + i)
+    y = dfl.gemm_bf16(t.dev_bf16(x), t.dev_bf16(w), splits=splits, token_tile=nt).cpu().numpy()
+    np.save(sys.argv[1] + "/y%d.npy" % i, y)
+"""
+
+
+def test_cluster_split_k_equals_workspace_split_k(dfl, tmp_path):
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, DF_NO_CLUSTER="1")
+    subprocess.run([sys.executable, "-c", _WORKSPACE_CHILD, str(tmp_path), os.path.dirname(here), here], env=env,
+                   check=True, timeout=600)
+    for i, (M, N, K, splits, nt) in enumerate(SPLIT_K):
+        x, w = inputs(M, N, K, seed=30 + i)
+        got = dfl.gemm_bf16(dev_bf16(x), dev_bf16(w), splits=splits, token_tile=nt).cpu().numpy()
+        check_close(got, x, w)
+        np.testing.assert_array_equal(got, np.load(tmp_path / ("y%d.npy" % i)))
