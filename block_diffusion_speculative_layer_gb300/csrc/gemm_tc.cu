@@ -104,6 +104,9 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, 
 
 // Thread-block cluster helpers (all threads of every CTA execute the barriers).
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+// For an arrival that follows reads whose values are already used (it
+// publishes nothing); every thread of the CTA takes the same form.
+__device__ __forceinline__ void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -401,7 +404,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
         if (r < r1) *reinterpret_cast<float4*>(tile + r * C::TLD + 4 * c4) = acc;
       }
     }
-    cluster_arrive();  // this CTA's reads of the other partials are done
+    cluster_arrive_relaxed();  // this CTA's reads of the other partials are done
     __syncthreads();
     if (!failed)
       epilogue_tile<__nv_bfloat16>(ep, tile + (size_t)r0 * C::TLD, C::TLD, n0, m0 + r0, r1 - r0, M, meta + r0, red,
