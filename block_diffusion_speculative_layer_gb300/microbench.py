@@ -8,6 +8,7 @@
   python -m block_diffusion_speculative_layer_gb300.microbench serving [--new 1024]
   python -m block_diffusion_speculative_layer_gb300.microbench dense27b [--new 1024]
   python -m block_diffusion_speculative_layer_gb300.microbench profile_cycle [--ctx 1024] [--batch 1] [--vocab 4096]
+  python -m block_diffusion_speculative_layer_gb300.microbench offpath [--model fp32|bf16]
   python -m block_diffusion_speculative_layer_gb300.microbench attention [--ctx ...] [--batch ...] [--attn mma|pipe|auto]
                                                                          [--causal] [--iters 5] [--pages shuffled|runs]
 
@@ -330,6 +331,36 @@ def attention(a):
             torch.cuda.empty_cache()
 
 
+def offpath(a):
+    """Small generations that launch the kernels the bs1 bf16 decode path does
+    not (for ncu captures): the tiny fp32 model (greedy generation, greedy
+    reference, sampled generation), or a small bf16 model (8 layers, d 512,
+    4 / 2 heads x 128, a 300-token prompt, 16 new tokens) whose attention
+    kernel follows DF_ATTN_SPLIT / DF_ATTN_TC in the environment."""
+    import torch
+
+    import block_diffusion_speculative_layer_gb300 as dfl
+    import synthetic as syn
+
+    if a.model == "fp32":
+        shape = syn.TINY
+        w = syn.make_weights(shape)
+        prompt = syn.make_prompt(shape, 16)
+        with dfl.Engine(shape, w, max_batch=1, max_ctx=128) as eng:
+            _, st = eng.generate([prompt], 16)
+            eng.greedy_reference([prompt], 8)
+            eng.generate_sampled([prompt], 16, temperature=0.8, top_p=0.95, seed=3)
+    else:
+        shape = syn.ModelShape("offpath-bf16", n_layers=8, d_model=512, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                               d_ffn=1024, vocab=2048, draft_layers=1, block_size=8, dtype="bf16")
+        w = syn.make_weights(shape)
+        prompt = syn.make_prompt(shape, 300)
+        with dfl.Engine(shape, w, max_batch=1, max_ctx=512) as eng:
+            _, st = eng.generate([prompt], 16)
+    torch.cuda.synchronize()
+    print(json.dumps({"op": "offpath", "model": a.model, "cycles": st["cycles"], "ok": True}))
+
+
 def _hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -358,7 +389,8 @@ def main():
 
     ap = argparse.ArgumentParser()
     ap.add_argument("op", choices=["gemm", "lmhead", "drafter", "ar_proxy", "serving", "dense27b", "sampled",
-                                   "profile_cycle", "attention"])
+                                   "profile_cycle", "attention", "offpath"])
+    ap.add_argument("--model", default="fp32", choices=["fp32", "bf16"], help="offpath: which small model")
     ap.add_argument("--causal", action="store_true", help="attention: the target's causal verify rows")
     ap.add_argument("--cla", type=int, default=4, help="attention: CTAs per cluster of the pipelined kernel")
     ap.add_argument("--pages", default="shuffled", choices=["shuffled", "runs"],
@@ -396,6 +428,9 @@ def main():
         return
     if a.op == "attention":
         attention(a)
+        return
+    if a.op == "offpath":
+        offpath(a)
         return
     if a.op == "profile_cycle":
         a.ctx = int(a.ctx.split(",")[0])
